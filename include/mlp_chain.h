@@ -1,0 +1,199 @@
+/*
+ * mlp_chain.h -- C ABI of the CTA-pipelined GEMM chain library (libmlp_chain.so).
+ *
+ * What it computes.  A chain of S dependent GEMMs on one GPU,
+ *     A_0 = X,   A_{s+1} = epi_s( A_s * W_s ),   Y = A_S,
+ * with bf16 operands, fp32 accumulation and every intermediate stored as bf16.  S = 2 is the
+ * two-layer GEMM standing in for an MLP block, Y = (X*W1)*W2, the running example of
+ * "CTA-Pipelining: A Latency-Oriented Spatial Scaling Method for Multi-GPU Systems"
+ * (arXiv 2607.07862, section III: the first GEMM's output is consumed directly by the next
+ * GEMM; bf16 in/out with an fp32 accumulator, Fig. 2 set-up).  S > 2 is the multi-layer GEMM
+ * of section IV (Fig. 3-4).  epi_s is the identity, or GeLU(tanh) on the fp32 accumulator
+ * (MLP_EPI_GELU_TANH), and with `residual` the last stage also adds X before rounding.
+ *
+ * How it schedules (MLP_MODE_PIPELINED).  CTA-pipelining (section III-A and Fig. 1): every
+ * stage boundary owns a dependency array (built on the host from the static tile dataflow), a
+ * scoreboard of per-consumer-tile counters initialised from it, and a work-queue.  A producer
+ * tile stores its output, fences, and decrements the counter of every consumer tile that reads
+ * it; the decrement that reaches zero pushes that consumer's tile id onto the queue.  Consumer
+ * CTAs poll the queue in a short prologue, adopt the dequeued tile id in place of their own
+ * and run the unchanged GEMM body.  Here all stages run in ONE persistent, warp-specialised
+ * kernel on one GPU (one CTA per SM): the pages put one layer per GPU instead.
+ * MLP_MODE_SEQUENTIAL launches the same tile engine once per GEMM, back to back on one stream
+ * (the pages' "two consecutive GEMMs" baseline, section III-C).  MLP_MODE_MICROBATCH splits
+ * X into row chunks and overlaps GEMM s of chunk i with GEMM s+1 of chunk i-1 on separate
+ * streams (static micro-batching, section IV, Fig. 3).  All three modes use the same tiles in
+ * the same order of k, so Y is bit-identical across modes.
+ *
+ * Conventions for every entry point.
+ *   - Matrices are dense, row-major, bf16, with 16-byte aligned base pointers; every
+ *     dimension except M must be a multiple of 8 (one 16-byte TMA unit).
+ *   - Device pointers are CUDA device addresses on the handle's device; host pointers are
+ *     ordinary process memory (pinned memory makes the copies asynchronous).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - The caller owns X, W[], Y and the workspace.  The library owns its device state
+ *     (scoreboards, queues, tickets, status word, event log), allocated in create and freed in
+ *     destroy.
+ *   - Errors are returned, never thrown or trapped.  Device-side failures (a bounded wait that
+ *     ran out, a bad dequeued tile id) set a sticky status word that mlp_chain_check reports;
+ *     until then further runs of that handle do nothing.
+ *   - A handle is not thread-safe, and two runs of one handle must not overlap on the GPU
+ *     (they share one scoreboard).  Different handles are independent.
+ */
+#ifndef MLP_CHAIN_H_
+#define MLP_CHAIN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLP_MAX_GEMMS 4
+
+typedef enum {
+    MLP_OK = 0,
+    MLP_ERR_INVALID_ARG = 1,  /* a size, pointer, alignment or option is not acceptable      */
+    MLP_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (dtype, tile)    */
+    MLP_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                             */
+    MLP_ERR_OOM = 4,          /* device allocation failed                                      */
+    MLP_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (dependency never satisfied)    */
+    MLP_ERR_DEVICE_STATE = 6, /* the handle's device state is inconsistent (reset pending)     */
+    MLP_ERR_BAD_TILE = 7      /* a dequeued tile id was out of range                           */
+} mlp_status;
+
+typedef enum { MLP_DT_BF16 = 1, MLP_DT_F32 = 2 } mlp_dtype;
+
+typedef enum {
+    MLP_MODE_PIPELINED = 0,   /* one persistent grid, scoreboard + work-queue (CTA-pipelining) */
+    MLP_MODE_SEQUENTIAL = 1,  /* one launch per GEMM, back to back                              */
+    MLP_MODE_MICROBATCH = 2   /* row chunks, GEMM s+1 of chunk i overlaps GEMM s of chunk i+1   */
+} mlp_mode;
+
+typedef enum { MLP_EPI_NONE = 0, MLP_EPI_GELU_TANH = 1 } mlp_epilogue;
+
+/* debug_flags bits */
+#define MLP_DEBUG_EVENT_LOG 1u          /* record one mlp_event per tile (pipelined mode)        */
+#define MLP_DEBUG_DROP_DECREMENT 2u     /* fault injection, first pipelined run of the handle
+                                           only: first-stage producer tile `drop_tile` skips its
+                                           scoreboard decrements, so its consumers never become
+                                           ready and their bounded wait must end the run with
+                                           MLP_ERR_TIMEOUT                                       */
+
+typedef struct {
+    int64_t M;                          /* rows of X (any value >= 1)                           */
+    int32_t num_gemms;                  /* S, 1..MLP_MAX_GEMMS                                   */
+    int64_t dims[MLP_MAX_GEMMS + 1];    /* K, N1, N2, ...: W_s is dims[s] x dims[s+1]            */
+    mlp_dtype in_dtype, acc_dtype, h_dtype, out_dtype; /* must be BF16, F32, BF16, BF16         */
+    int32_t tile_m;                     /* 0 or 128 (rows per tile; 64 is accepted and run as a
+                                           128-row tile, which gives the same dependency array
+                                           whenever M <= 64)                                    */
+    int32_t tile_n[MLP_MAX_GEMMS];      /* per GEMM: 0 (library choice), 32, 64, 128 or 256     */
+    int32_t tile_k;                     /* 0 or 64                                               */
+    mlp_epilogue epilogue;              /* applied after every GEMM                              */
+    int32_t residual;                   /* nonzero: last stage adds X (needs dims[S] == dims[0]) */
+    mlp_mode mode;
+    int32_t microbatch_rows;            /* MICROBATCH: rows per chunk, a multiple of 128        */
+    int32_t device;                     /* CUDA device ordinal                                  */
+    uint32_t debug_flags;               /* MLP_DEBUG_* bits                                     */
+    int32_t drop_tile;                  /* with MLP_DEBUG_DROP_DECREMENT                         */
+    uint32_t timeout_us;                /* bounded device waits; 0 = 2 000 000 (2 s)             */
+    int32_t grid_ctas;                  /* 0 = one CTA per SM                                    */
+    int32_t raster_group;               /* first-stage raster: 0/1 = row panels in order; g > 1
+                                           = groups of g row panels, column-major inside a group */
+} mlp_chain_desc;
+
+/* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG).  t_* are %globaltimer ns;
+ * seq_* come from one device-wide counter, taken after the consumer's acquire (start) and
+ * before the producer's scoreboard release (end), so seq_end(p) < seq_start(c) for every
+ * dependency p -> c. */
+typedef struct {
+    int32_t stage, tile, smid, cta;
+    uint64_t t_start, t_end;
+    uint32_t seq_start, seq_end;
+} mlp_event;
+
+typedef struct {
+    int32_t num_gemms;
+    int32_t tile_m, tile_k;
+    int32_t tile_n[MLP_MAX_GEMMS];
+    int32_t tiles_m[MLP_MAX_GEMMS], tiles_n[MLP_MAX_GEMMS];
+    int32_t grid_ctas;                  /* CTAs of the pipelined launch                          */
+    int32_t num_sms;
+    int32_t pipe_stages;                /* shared-memory ring depth                               */
+    int32_t smem_bytes;                 /* dynamic shared memory per CTA                          */
+    int32_t tmem_cols;
+    int32_t launches_per_run;           /* kernels one mlp_chain_run enqueues                     */
+} mlp_chain_info;
+
+typedef struct mlp_chain *mlp_chain_t;
+
+/* Validate `desc`, build the dependency arrays, allocate the device state on desc->device.
+ * On success *out owns everything it allocated.  Errors: INVALID_ARG, UNSUPPORTED, CUDA, OOM. */
+mlp_status mlp_chain_create(const mlp_chain_desc *desc, mlp_chain_t *out);
+
+/* Bytes of device workspace run() needs for the intermediates A_1 .. A_{S-1} (0 when S = 1). */
+mlp_status mlp_chain_workspace_size(mlp_chain_t h, size_t *bytes);
+
+/* Enqueue the whole chain on `stream` (asynchronous).  X: M x dims[0]; W[s]: dims[s] x
+ * dims[s+1]; Y: M x dims[S]; workspace: >= mlp_chain_workspace_size bytes, 256-byte aligned.
+ * All device pointers.  Returns INVALID_ARG for null or misaligned pointers, CUDA if a launch
+ * fails, DEVICE_STATE if a previous device error has not been collected by mlp_chain_check. */
+mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *const *W, void *Y,
+                         void *workspace, void *stream);
+
+/* As mlp_chain_run, but X and Y are HOST buffers: enqueue the copy of X into the device
+ * staging buffer X_dev, the chain, and the copy of the result from Y_dev back into Y_host, all
+ * on `stream` (asynchronous; synchronise the stream before reading Y_host). */
+mlp_status mlp_chain_run_host(mlp_chain_t h, const void *X_host, const void *const *W,
+                              void *Y_host, void *X_dev, void *Y_dev, void *workspace,
+                              void *stream);
+
+/* Synchronise `stream`, read the device status word and clear it.  Returns OK, TIMEOUT or
+ * BAD_TILE; after a device error the handle's scoreboard, queues and tickets are re-initialised
+ * so the next run starts clean. */
+mlp_status mlp_chain_check(mlp_chain_t h, void *stream);
+
+/* The dependency array of stage boundary b (GEMM b produces, GEMM b+1 consumes), as host
+ * arrays owned by the handle: prod_off[P+1], prod_tgt[prod_off[P]] (consumer ids ascending for
+ * each producer), init_count[C].  Tile ids are row-major over each GEMM's tile grid. */
+mlp_status mlp_chain_get_deps(mlp_chain_t h, int32_t boundary, const int32_t **prod_off,
+                              const int32_t **prod_tgt, const int32_t **init_count,
+                              int32_t *P, int32_t *C);
+
+/* Copy the event log of the last pipelined run (synchronises the device) into host_buf, up to
+ * cap records; *n = records written.  INVALID_ARG without MLP_DEBUG_EVENT_LOG. */
+mlp_status mlp_chain_get_event_log(mlp_chain_t h, mlp_event *host_buf, size_t cap, size_t *n);
+
+mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info);
+
+/* Free the handle and its device state (synchronises its internal streams). */
+mlp_status mlp_chain_destroy(mlp_chain_t h);
+
+/* Host-only dependency-array builder (no GPU needed), the same routine create() uses.
+ * Producer tiles: bm_p x bn_p over an M x n_out output; consumer tiles: bm_c x bn_c over
+ * M x n_next, each reading all n_out columns of its rows.  Pass NULL arrays to query sizes:
+ * returns the number of edges (>= 0) or -1 on bad arguments / too small tgt_cap. */
+int64_t mlp_deps_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm_p, int32_t bn_p,
+                       int32_t bm_c, int32_t bn_c, int32_t *prod_off, int32_t *prod_tgt,
+                       int64_t tgt_cap, int32_t *init_count);
+
+/* Host model of the scoreboard / work-queue protocol (no GPU needed): `threads` host threads
+ * run the same ticket, decrement, push and poll steps as the kernel on std::atomic state, with
+ * seeded random delays, over a chain of `num_gemms` stages of tiles_m x tiles_n[s] tiles
+ * (consumers read whole row panels).  order_out (optional, one entry per tile of all stages)
+ * receives tiles in completion order as stage << 24 | tile.  With drop_tile >= 0 that
+ * first-stage tile withholds its decrements and the run must end in MLP_ERR_TIMEOUT after
+ * timeout_ms.  Returns OK when every tile ran exactly once after all of its producers. */
+mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
+                              int32_t threads, uint64_t seed, int32_t drop_tile,
+                              uint32_t timeout_ms, int32_t *order_out);
+
+const char *mlp_status_str(mlp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLP_CHAIN_H_ */

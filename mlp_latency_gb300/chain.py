@@ -1,0 +1,193 @@
+"""Python binding of the C ABI in include/mlp_chain.h: argument marshalling only.
+
+Every step of the chain runs in the CUDA library; this module passes device pointers
+(``tensor.data_ptr()``) and the CUDA stream handle through ctypes. torch is used only to
+obtain those pointers and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import _lib
+from ._lib import ChainDesc, ChainInfo, Event
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_DEVICE_STATE, ERR_BAD_TILE = range(8)
+DT_BF16, DT_F32 = 1, 2
+MODES = {"pipelined": 0, "sequential": 1, "microbatch": 2}
+DEBUG_EVENT_LOG, DEBUG_DROP_DECREMENT = 1, 2
+
+EVENT_DTYPE = np.dtype([("stage", np.int32), ("tile", np.int32), ("smid", np.int32), ("cta", np.int32),
+                        ("t_start", np.uint64), ("t_end", np.uint64), ("seq_start", np.uint32),
+                        ("seq_end", np.uint32)])
+
+
+class MlpChainError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        msg = _lib.load().mlp_status_str(int(status)).decode()
+        super().__init__(f"{what}: {msg} (status {status})" if what else msg)
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise MlpChainError(status, what)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+class Chain:
+    """One handle of the library: a fixed chain shape, tile shape and launch mode.
+
+    Shapes follow the header: X[M x dims[0]], W[s][dims[s] x dims[s+1]], Y[M x dims[-1]].
+    """
+
+    def __init__(self, M: int, dims: Sequence[int], *, tile_n: Optional[Sequence[int]] = None,
+                 gelu: bool = False, residual: bool = False, mode: str = "pipelined",
+                 microbatch_rows: int = 0, device: int = 0, event_log: bool = False,
+                 drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
+                 raster_group: int = 0, tile_m: int = 0):
+        lib = _lib.load()
+        d = ChainDesc()
+        d.M = int(M)
+        d.num_gemms = len(dims) - 1
+        for i, v in enumerate(dims):
+            d.dims[i] = int(v)
+        d.in_dtype, d.acc_dtype, d.h_dtype, d.out_dtype = DT_BF16, DT_F32, DT_BF16, DT_BF16
+        d.tile_m = int(tile_m)
+        for i, v in enumerate(tile_n or []):
+            d.tile_n[i] = int(v)
+        d.tile_k = 0
+        d.epilogue = 1 if gelu else 0
+        d.residual = int(bool(residual))
+        d.mode = MODES[mode]
+        d.microbatch_rows = int(microbatch_rows)
+        d.device = int(device)
+        flags = DEBUG_EVENT_LOG if event_log else 0
+        if drop_tile is not None:
+            flags |= DEBUG_DROP_DECREMENT
+            d.drop_tile = int(drop_tile)
+        d.debug_flags = flags
+        d.timeout_us = int(timeout_us)
+        d.grid_ctas = int(grid_ctas)
+        d.raster_group = int(raster_group)
+        self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
+        self._lib = lib
+        h = ctypes.c_void_p()
+        _check(lib.mlp_chain_create(ctypes.byref(d), ctypes.byref(h)), "mlp_chain_create")
+        self._h = h
+        self._wbuf = (ctypes.c_void_p * len(self.dims))()
+
+    # ------------------------------------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.mlp_chain_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # ------------------------------------------------------------------------------------
+    def workspace_size(self) -> int:
+        n = ctypes.c_size_t()
+        _check(self._lib.mlp_chain_workspace_size(self._h, ctypes.byref(n)), "workspace_size")
+        return n.value
+
+    def _wptrs(self, Ws):
+        for i, w in enumerate(Ws):
+            self._wbuf[i] = w.data_ptr() if hasattr(w, "data_ptr") else int(w)
+        return self._wbuf
+
+    def run(self, X, Ws, Y, workspace, stream=None):
+        """Enqueue the chain; X, Ws, Y, workspace are CUDA tensors (or raw device addresses)."""
+        ptr = lambda t: (t.data_ptr() if hasattr(t, "data_ptr") else int(t)) if t is not None else None
+        _check(self._lib.mlp_chain_run(self._h, ptr(X), self._wptrs(Ws), ptr(Y), ptr(workspace),
+                                       _stream_ptr(stream)), "mlp_chain_run")
+
+    def run_host(self, X_host, Ws, Y_host, X_dev, Y_dev, workspace, stream=None):
+        """Enqueue H2D copy of X_host, the chain, and D2H copy into Y_host (pinned host tensors)."""
+        ptr = lambda t: t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+        _check(self._lib.mlp_chain_run_host(self._h, ptr(X_host), self._wptrs(Ws), ptr(Y_host), ptr(X_dev),
+                                            ptr(Y_dev), ptr(workspace) if workspace is not None else None,
+                                            _stream_ptr(stream)), "mlp_chain_run_host")
+
+    def check(self, stream=None) -> int:
+        """Synchronise and return the device status (0 = OK); re-arms the handle after an error."""
+        return int(self._lib.mlp_chain_check(self._h, _stream_ptr(stream)))
+
+    def deps(self, boundary: int = 0):
+        off, tgt, init = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+        P, C = ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.mlp_chain_get_deps(self._h, boundary, ctypes.byref(off), ctypes.byref(tgt),
+                                            ctypes.byref(init), ctypes.byref(P), ctypes.byref(C)), "get_deps")
+        offa = np.ctypeslib.as_array(ctypes.cast(off, ctypes.POINTER(ctypes.c_int32)), (P.value + 1,)).copy()
+        nnz = int(offa[-1])
+        tgta = (np.ctypeslib.as_array(ctypes.cast(tgt, ctypes.POINTER(ctypes.c_int32)), (nnz,)).copy()
+                if nnz else np.zeros(0, np.int32))
+        inita = np.ctypeslib.as_array(ctypes.cast(init, ctypes.POINTER(ctypes.c_int32)), (C.value,)).copy()
+        return offa, tgta, inita
+
+    def event_log(self) -> np.ndarray:
+        info = self.info()
+        cap = sum(info["tiles_m"][s] * info["tiles_n"][s] for s in range(info["num_gemms"]))
+        buf = np.zeros(cap, dtype=EVENT_DTYPE)
+        n = ctypes.c_size_t()
+        _check(self._lib.mlp_chain_get_event_log(self._h, buf.ctypes.data, cap, ctypes.byref(n)), "event_log")
+        return buf[: n.value]
+
+    def info(self) -> dict:
+        i = ChainInfo()
+        _check(self._lib.mlp_chain_get_info(self._h, ctypes.byref(i)), "get_info")
+        S = i.num_gemms
+        return {"num_gemms": S, "tile_m": i.tile_m, "tile_k": i.tile_k, "tile_n": list(i.tile_n[:S]),
+                "tiles_m": list(i.tiles_m[:S]), "tiles_n": list(i.tiles_n[:S]), "grid_ctas": i.grid_ctas,
+                "num_sms": i.num_sms, "pipe_stages": i.pipe_stages, "smem_bytes": i.smem_bytes,
+                "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run}
+
+
+def deps_build(M: int, n_out: int, n_next: int, bm_p: int, bn_p: int, bm_c: int, bn_c: int):
+    """Host-only dependency-array builder (mlp_deps_build): (prod_off, prod_tgt, init_count)."""
+    lib = _lib.load()
+    P = -(-M // bm_p) * -(-n_out // bn_p)
+    C = -(-M // bm_c) * -(-n_next // bn_c)
+    init = np.zeros(C, dtype=np.int32)
+    nnz = lib.mlp_deps_build(M, n_out, n_next, bm_p, bn_p, bm_c, bn_c, None, None, 0, init.ctypes.data)
+    if nnz < 0:
+        raise MlpChainError(ERR_INVALID_ARG, "mlp_deps_build")
+    off = np.zeros(P + 1, dtype=np.int32)
+    tgt = np.zeros(max(nnz, 1), dtype=np.int32)
+    r = lib.mlp_deps_build(M, n_out, n_next, bm_p, bn_p, bm_c, bn_c, off.ctypes.data, tgt.ctypes.data,
+                           tgt.shape[0], init.ctypes.data)
+    if r != nnz:
+        raise MlpChainError(ERR_INVALID_ARG, "mlp_deps_build")
+    return off, tgt[:nnz], init
+
+
+def protocol_model(tiles_m: int, tiles_n: Sequence[int], threads: int = 8, seed: int = 0,
+                   drop_tile: int = -1, timeout_ms: int = 2000, return_order: bool = False):
+    """Run the host-thread protocol model (mlp_protocol_model); returns (status, order)."""
+    lib = _lib.load()
+    tn = np.ascontiguousarray(tiles_n, dtype=np.int32)
+    total = int(tiles_m * tn.sum())
+    order = np.full(total, -1, dtype=np.int32) if return_order else None
+    st = lib.mlp_protocol_model(len(tn), tiles_m, tn.ctypes.data, threads, seed, drop_tile, timeout_ms,
+                                order.ctypes.data if order is not None else None)
+    return int(st), order

@@ -1,0 +1,589 @@
+// mlp_chain.cu -- C ABI of the CTA-pipelined GEMM chain (see include/mlp_chain.h): handle
+// creation, TMA descriptor encoding, and the three launch modes (pipelined, sequential,
+// micro-batched) of the one tile engine in chain_kernel.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/mlp_chain.h"
+#include "chain_kernel.cuh"
+
+using mlpc::ChainParams;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map over a rows x cols row-major matrix, box = box_rows x box_cols.
+bool encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows, int box_cols,
+               CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceBoundary {
+    int32_t *off = nullptr, *tgt = nullptr, *init = nullptr;
+    uint32_t *count = nullptr, *tail = nullptr;
+    unsigned long long *queue = nullptr;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+struct mlp_chain {
+    mlp_chain_desc desc{};
+    int device = 0, num_sms = 0, S = 0;
+    int BN[MLP_MAX_GEMMS] = {}, tiles_m = 0, tiles_n[MLP_MAX_GEMMS] = {}, k_blocks[MLP_MAX_GEMMS] = {};
+    int b_swz[MLP_MAX_GEMMS] = {};
+    int num_pipe = 0, max_bn = 0, grid = 0;
+    uint32_t stage_bytes = 0, tmem_cols = 0;
+    size_t smem = 0;
+    std::vector<int32_t> off[MLP_MAX_GEMMS - 1], tgt[MLP_MAX_GEMMS - 1], init[MLP_MAX_GEMMS - 1];
+    void *dev_block = nullptr;
+    DeviceBoundary db[MLP_MAX_GEMMS - 1];
+    uint32_t *d_ctrl = nullptr;  // ticket, done, epoch, status, seq
+    mlpc::EventRec *d_events = nullptr;
+    size_t n_events = 0;
+    int32_t stage_base[MLP_MAX_GEMMS + 1] = {};
+    // cached launch parameters (tensor maps are re-encoded only when a pointer changes)
+    ChainParams params;
+    const void *c_X = nullptr, *c_W[MLP_MAX_GEMMS] = {}, *c_Y = nullptr, *c_ws = nullptr;
+    bool params_valid = false;
+    bool fault_armed = false;   // MLP_DEBUG_DROP_DECREMENT fires on the first run only
+    // micro-batch streams and events
+    cudaStream_t side[MLP_MAX_GEMMS] = {};
+    std::vector<cudaEvent_t> events;
+    cudaEvent_t fork = nullptr;
+    int n_chunks = 0, chunk_tiles = 0;
+};
+
+extern "C" const char *mlp_status_str(mlp_status s)
+{
+    switch (s) {
+    case MLP_OK: return "ok";
+    case MLP_ERR_INVALID_ARG: return "invalid argument";
+    case MLP_ERR_UNSUPPORTED: return "unsupported";
+    case MLP_ERR_CUDA: return "CUDA error";
+    case MLP_ERR_OOM: return "out of device memory";
+    case MLP_ERR_TIMEOUT: return "bounded device wait timed out";
+    case MLP_ERR_DEVICE_STATE: return "device state needs a reset";
+    case MLP_ERR_BAD_TILE: return "dequeued tile id out of range";
+    }
+    return "unknown status";
+}
+
+static int default_bn(int64_t tiles_m, int64_t N, int num_sms)
+{
+    // Largest tile width that still gives every SM a tile; else the narrowest.
+    const int cands[4] = {256, 128, 64, 32};
+    for (int bn : cands)
+        if (tiles_m * ((N + bn - 1) / bn) >= num_sms)
+            return bn;
+    return 32;
+}
+
+static mlp_status full_reset(mlp_chain *h)
+{
+    if (cudaSetDevice(h->device) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    if (cudaMemset(h->d_ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    for (int b = 0; b + 1 < h->S; ++b) {
+        const size_t C = h->init[b].size();
+        if (cudaMemcpy(h->db[b].count, h->db[b].init, C * sizeof(int32_t), cudaMemcpyDeviceToDevice) != cudaSuccess ||
+            cudaMemset(h->db[b].queue, 0, C * sizeof(unsigned long long)) != cudaSuccess ||
+            cudaMemset(h->db[b].tail, 0, sizeof(uint32_t)) != cudaSuccess)
+            return MLP_ERR_CUDA;
+    }
+    return cudaDeviceSynchronize() == cudaSuccess ? MLP_OK : MLP_ERR_CUDA;
+}
+
+static void release(mlp_chain *h)
+{
+    if (!h)
+        return;
+    cudaSetDevice(h->device);
+    for (auto &e : h->events)
+        if (e)
+            cudaEventDestroy(e);
+    if (h->fork)
+        cudaEventDestroy(h->fork);
+    for (auto &s : h->side)
+        if (s)
+            cudaStreamDestroy(s);
+    if (h->dev_block)
+        cudaFree(h->dev_block);
+    delete h;
+}
+
+extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out)
+{
+    if (!d || !out)
+        return MLP_ERR_INVALID_ARG;
+    *out = nullptr;
+    const int S = d->num_gemms;
+    if (S < 1 || S > MLP_MAX_GEMMS || d->M < 1 || d->M > (int64_t)1 << 30)
+        return MLP_ERR_INVALID_ARG;
+    for (int s = 0; s <= S; ++s)
+        if (d->dims[s] < 8 || d->dims[s] % 8 != 0 || d->dims[s] > (int64_t)1 << 24)
+            return MLP_ERR_INVALID_ARG;
+    if (d->in_dtype != MLP_DT_BF16 || d->acc_dtype != MLP_DT_F32 || d->h_dtype != MLP_DT_BF16 ||
+        d->out_dtype != MLP_DT_BF16)
+        return MLP_ERR_UNSUPPORTED;
+    if (!(d->tile_m == 0 || d->tile_m == 64 || d->tile_m == 128) || !(d->tile_k == 0 || d->tile_k == 64))
+        return MLP_ERR_UNSUPPORTED;
+    if (d->epilogue != MLP_EPI_NONE && d->epilogue != MLP_EPI_GELU_TANH)
+        return MLP_ERR_INVALID_ARG;
+    if (d->residual && d->dims[S] != d->dims[0])
+        return MLP_ERR_INVALID_ARG;
+    if (d->mode != MLP_MODE_PIPELINED && d->mode != MLP_MODE_SEQUENTIAL && d->mode != MLP_MODE_MICROBATCH)
+        return MLP_ERR_INVALID_ARG;
+    if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < mlpc::kBM || d->microbatch_rows % mlpc::kBM))
+        return MLP_ERR_INVALID_ARG;
+    if (d->grid_ctas < 0 || d->raster_group < 0)
+        return MLP_ERR_INVALID_ARG;
+
+    mlp_chain *h = new (std::nothrow) mlp_chain();
+    if (!h)
+        return MLP_ERR_OOM;
+    h->desc = *d;
+    h->S = S;
+    h->fault_armed = (d->debug_flags & MLP_DEBUG_DROP_DECREMENT) != 0;
+    h->device = d->device;
+    if (cudaSetDevice(h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        release(h);
+        return MLP_ERR_CUDA;
+    }
+    int cc_major = 0, cc_minor = 0, smem_optin = 0;
+    cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, h->device);
+    cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device);
+    cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+    if (cc_major != 10 || cc_minor != 3) {  // the binary is built for sm_103a only
+        release(h);
+        return MLP_ERR_UNSUPPORTED;
+    }
+
+    h->tiles_m = static_cast<int>((d->M + mlpc::kBM - 1) / mlpc::kBM);
+    for (int s = 0; s < S; ++s) {
+        int bn = d->tile_n[s] ? d->tile_n[s] : default_bn(h->tiles_m, d->dims[s + 1], h->num_sms);
+        if (bn != 32 && bn != 64 && bn != 128 && bn != 256) {
+            release(h);
+            return MLP_ERR_UNSUPPORTED;
+        }
+        h->BN[s] = bn;
+        h->b_swz[s] = bn >= 64 ? 128 : 64;
+        h->tiles_n[s] = static_cast<int>((d->dims[s + 1] + bn - 1) / bn);
+        h->k_blocks[s] = static_cast<int>((d->dims[s] + mlpc::kBK - 1) / mlpc::kBK);
+        h->max_bn = std::max(h->max_bn, bn);
+    }
+    h->stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
+    const size_t fixed = 1024 + sizeof(mlpc::Ctrl);
+    h->num_pipe = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - fixed) / h->stage_bytes));
+    if (h->num_pipe < 2) {
+        release(h);
+        return MLP_ERR_UNSUPPORTED;
+    }
+    h->smem = mlpc::chain_smem_bytes(h->num_pipe, h->stage_bytes);
+    h->tmem_cols = 32;
+    while (h->tmem_cols < static_cast<uint32_t>(2 * h->max_bn))
+        h->tmem_cols *= 2;
+    h->stage_base[0] = 0;
+    for (int s = 0; s < S; ++s)
+        h->stage_base[s + 1] = h->stage_base[s] + h->tiles_m * h->tiles_n[s];
+    const int total = h->stage_base[S];
+    h->grid = d->grid_ctas ? d->grid_ctas : std::min(h->num_sms, total);
+    if (d->mode == MLP_MODE_PIPELINED && h->grid > h->num_sms) {
+        release(h);  // the pipelined grid must be co-resident (one CTA per SM)
+        return MLP_ERR_INVALID_ARG;
+    }
+
+    // dependency arrays (host), then one device block for all library-owned state
+    size_t bytes = 8 * sizeof(uint32_t);
+    for (int b = 0; b + 1 < S; ++b) {
+        const int64_t nnz = mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], mlpc::kBM, h->BN[b], mlpc::kBM,
+                                           h->BN[b + 1], nullptr, nullptr, 0, nullptr);
+        if (nnz < 0) {
+            release(h);
+            return MLP_ERR_INVALID_ARG;
+        }
+        h->off[b].resize(static_cast<size_t>(h->tiles_m) * h->tiles_n[b] + 1);
+        h->tgt[b].resize(static_cast<size_t>(std::max<int64_t>(nnz, 1)));
+        h->init[b].resize(static_cast<size_t>(h->tiles_m) * h->tiles_n[b + 1]);
+        mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], mlpc::kBM, h->BN[b], mlpc::kBM, h->BN[b + 1],
+                       h->off[b].data(), h->tgt[b].data(), nnz, h->init[b].data());
+        h->tgt[b].resize(static_cast<size_t>(nnz));
+        bytes = align_up(bytes, 256) + h->off[b].size() * 4;
+        bytes = align_up(bytes, 256) + std::max<size_t>(h->tgt[b].size(), 1) * 4;
+        bytes = align_up(bytes, 256) + h->init[b].size() * 4;      // init
+        bytes = align_up(bytes, 256) + h->init[b].size() * 4;      // count
+        bytes = align_up(bytes, 256) + h->init[b].size() * 8;      // queue
+        bytes = align_up(bytes, 256) + 4;                          // tail
+    }
+    if (d->debug_flags & MLP_DEBUG_EVENT_LOG) {
+        h->n_events = static_cast<size_t>(total);
+        bytes = align_up(bytes, 256) + h->n_events * sizeof(mlpc::EventRec);
+    }
+    if (cudaMalloc(&h->dev_block, bytes) != cudaSuccess) {
+        h->dev_block = nullptr;
+        release(h);
+        return MLP_ERR_OOM;
+    }
+    uint8_t *p = static_cast<uint8_t *>(h->dev_block);
+    size_t o = 0;
+    h->d_ctrl = reinterpret_cast<uint32_t *>(p);
+    o = 8 * sizeof(uint32_t);
+    bool ok = true;
+    for (int b = 0; b + 1 < S; ++b) {
+        auto take = [&](size_t n) {
+            o = align_up(o, 256);
+            void *r = p + o;
+            o += n;
+            return r;
+        };
+        h->db[b].off = static_cast<int32_t *>(take(h->off[b].size() * 4));
+        h->db[b].tgt = static_cast<int32_t *>(take(std::max<size_t>(h->tgt[b].size(), 1) * 4));
+        h->db[b].init = static_cast<int32_t *>(take(h->init[b].size() * 4));
+        h->db[b].count = static_cast<uint32_t *>(take(h->init[b].size() * 4));
+        h->db[b].queue = static_cast<unsigned long long *>(take(h->init[b].size() * 8));
+        h->db[b].tail = static_cast<uint32_t *>(take(4));
+        ok = ok && cudaMemcpy(h->db[b].off, h->off[b].data(), h->off[b].size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+        if (!h->tgt[b].empty())
+            ok = ok && cudaMemcpy(h->db[b].tgt, h->tgt[b].data(), h->tgt[b].size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+        ok = ok && cudaMemcpy(h->db[b].init, h->init[b].data(), h->init[b].size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+    }
+    if (h->n_events) {
+        o = align_up(o, 256);
+        h->d_events = reinterpret_cast<mlpc::EventRec *>(p + o);
+        ok = ok && cudaMemset(h->d_events, 0, h->n_events * sizeof(mlpc::EventRec)) == cudaSuccess;
+    }
+    if (!ok || full_reset(h) != MLP_OK) {
+        release(h);
+        return MLP_ERR_CUDA;
+    }
+    // The device maximum, so that handles with different ring depths can share the kernel.
+    if (cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
+        cudaSuccess) {
+        release(h);
+        return MLP_ERR_CUDA;
+    }
+    if (d->mode == MLP_MODE_MICROBATCH) {
+        const int rows_tiles = d->microbatch_rows / mlpc::kBM;
+        h->chunk_tiles = rows_tiles;
+        h->n_chunks = (h->tiles_m + rows_tiles - 1) / rows_tiles;
+        h->events.assign(static_cast<size_t>(h->n_chunks) * S, nullptr);
+        for (auto &e : h->events)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                ok = false;
+        if (cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) != cudaSuccess)
+            ok = false;
+        for (int s = 1; s < S; ++s)
+            if (cudaStreamCreateWithFlags(&h->side[s], cudaStreamNonBlocking) != cudaSuccess)
+                ok = false;
+        if (!ok) {
+            release(h);
+            return MLP_ERR_CUDA;
+        }
+    }
+    *out = h;
+    return MLP_OK;
+}
+
+extern "C" mlp_status mlp_chain_workspace_size(mlp_chain_t h, size_t *bytes)
+{
+    if (!h || !bytes)
+        return MLP_ERR_INVALID_ARG;
+    size_t b = 0;
+    for (int s = 1; s < h->S; ++s)
+        b = align_up(b, 256) + static_cast<size_t>(h->desc.M) * h->desc.dims[s] * 2;
+    *bytes = b;
+    return MLP_OK;
+}
+
+static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const *W, void *Y, void *ws)
+{
+    bool same = h->params_valid && X == h->c_X && Y == h->c_Y && ws == h->c_ws;
+    for (int s = 0; s < h->S && same; ++s)
+        same = W[s] == h->c_W[s];
+    if (same)
+        return MLP_OK;
+    ChainParams &P = h->params;
+    std::memset(&P, 0, sizeof(P));
+    const mlp_chain_desc &d = h->desc;
+    size_t wo = 0;
+    const void *a_ptr = X;
+    for (int s = 0; s < h->S; ++s) {
+        void *out_ptr;
+        if (s + 1 < h->S) {
+            wo = align_up(wo, 256);
+            out_ptr = static_cast<uint8_t *>(ws) + wo;
+            wo += static_cast<size_t>(d.M) * d.dims[s + 1] * 2;
+        } else {
+            out_ptr = Y;
+        }
+        if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&P.mapB[s], W[s], d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
+                       h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+            return MLP_ERR_CUDA;
+        mlpc::StageParams &sp = P.st[s];
+        sp.M = static_cast<int32_t>(d.M);
+        sp.K = static_cast<int32_t>(d.dims[s]);
+        sp.N = static_cast<int32_t>(d.dims[s + 1]);
+        sp.BN = h->BN[s];
+        sp.tiles_m = h->tiles_m;
+        sp.tiles_n = h->tiles_n[s];
+        sp.k_blocks = h->k_blocks[s];
+        sp.b_swz = h->b_swz[s];
+        sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
+        sp.gelu = d.epilogue == MLP_EPI_GELU_TANH;
+        sp.residual = (d.residual && s + 1 == h->S) ? static_cast<const __nv_bfloat16 *>(X) : nullptr;
+        a_ptr = out_ptr;
+    }
+    for (int b = 0; b + 1 < h->S; ++b) {
+        P.bd[b].prod_off = h->db[b].off;
+        P.bd[b].prod_tgt = h->db[b].tgt;
+        P.bd[b].init_count = h->db[b].init;
+        P.bd[b].count = h->db[b].count;
+        P.bd[b].queue = h->db[b].queue;
+        P.bd[b].tail = h->db[b].tail;
+    }
+    P.num_stages = h->S;
+    for (int s = 0; s <= h->S; ++s)
+        P.stage_base[s] = h->stage_base[s];
+    P.raster_group = d.raster_group;
+    P.num_pipe = h->num_pipe;
+    P.stage_bytes = h->stage_bytes;
+    P.tmem_cols = h->tmem_cols;
+    P.acc_stride = h->max_bn;
+    P.drop_tile = -1;
+    P.timeout_ns = static_cast<uint64_t>(d.timeout_us ? d.timeout_us : 2000000u) * 1000ull;
+    P.ticket = h->d_ctrl + 0;
+    P.done = h->d_ctrl + 1;
+    P.epoch = h->d_ctrl + 2;
+    P.status = h->d_ctrl + 3;
+    P.seq = h->d_ctrl + 4;
+    P.events = h->d_events;
+    h->c_X = X;
+    h->c_Y = Y;
+    h->c_ws = ws;
+    for (int s = 0; s < h->S; ++s)
+        h->c_W[s] = W[s];
+    h->params_valid = true;
+    return MLP_OK;
+}
+
+static bool launch(const ChainParams &P, int grid, size_t smem, cudaStream_t st)
+{
+    mlpc::chain_kernel<<<grid, mlpc::kThreads, smem, st>>>(P);
+    return cudaGetLastError() == cudaSuccess;
+}
+
+extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *const *W, void *Y, void *workspace,
+                                    void *stream)
+{
+    if (!h || !X || !W || !Y)
+        return MLP_ERR_INVALID_ARG;
+    if (h->S > 1 && !workspace)
+        return MLP_ERR_INVALID_ARG;
+    auto misaligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+    if (misaligned(X) || misaligned(Y) || (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return MLP_ERR_INVALID_ARG;
+    for (int s = 0; s < h->S; ++s)
+        if (!W[s] || misaligned(W[s]))
+            return MLP_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->device) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    const mlp_status ps = prepare_params(h, X, W, Y, workspace);
+    if (ps != MLP_OK)
+        return ps;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ChainParams P = h->params;
+    if (h->desc.mode == MLP_MODE_PIPELINED) {
+        P.pipelined = 1;
+        if (h->fault_armed) {
+            P.drop_tile = h->desc.drop_tile;
+            h->fault_armed = false;
+        }
+        P.first_stage = 0;
+        P.m_tile_begin = 0;
+        P.m_tile_end = h->tiles_m;
+        return launch(P, h->grid, h->smem, st) ? MLP_OK : MLP_ERR_CUDA;
+    }
+    P.pipelined = 0;
+    if (h->desc.mode == MLP_MODE_SEQUENTIAL) {
+        for (int s = 0; s < h->S; ++s) {
+            P.first_stage = s;
+            P.m_tile_begin = 0;
+            P.m_tile_end = h->tiles_m;
+            const int tiles = h->tiles_m * h->tiles_n[s];
+            const int g = h->desc.grid_ctas ? h->desc.grid_ctas : std::min(h->num_sms, tiles);
+            if (!launch(P, g, h->smem, st))
+                return MLP_ERR_CUDA;
+        }
+        return MLP_OK;
+    }
+    // micro-batch: stage s of chunk i runs on stream s after stage s-1 of chunk i
+    if (cudaEventRecord(h->fork, st) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    for (int s = 1; s < h->S; ++s)
+        if (cudaStreamWaitEvent(h->side[s], h->fork, 0) != cudaSuccess)
+            return MLP_ERR_CUDA;
+    for (int i = 0; i < h->n_chunks; ++i) {
+        P.m_tile_begin = i * h->chunk_tiles;
+        P.m_tile_end = std::min(h->tiles_m, (i + 1) * h->chunk_tiles);
+        for (int s = 0; s < h->S; ++s) {
+            cudaStream_t ss = s == 0 ? st : h->side[s];
+            if (s > 0 && cudaStreamWaitEvent(ss, h->events[static_cast<size_t>(i) * h->S + s - 1], 0) != cudaSuccess)
+                return MLP_ERR_CUDA;
+            P.first_stage = s;
+            const int tiles = (P.m_tile_end - P.m_tile_begin) * h->tiles_n[s];
+            const int g = h->desc.grid_ctas ? h->desc.grid_ctas : std::min(h->num_sms, tiles);
+            if (!launch(P, g, h->smem, ss))
+                return MLP_ERR_CUDA;
+            if (cudaEventRecord(h->events[static_cast<size_t>(i) * h->S + s], ss) != cudaSuccess)
+                return MLP_ERR_CUDA;
+        }
+    }
+    // join: the last stage of the last chunk follows every other launch
+    if (h->S > 1 &&
+        cudaStreamWaitEvent(st, h->events[static_cast<size_t>(h->n_chunks - 1) * h->S + h->S - 1], 0) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    return MLP_OK;
+}
+
+extern "C" mlp_status mlp_chain_run_host(mlp_chain_t h, const void *X_host, const void *const *W, void *Y_host,
+                                         void *X_dev, void *Y_dev, void *workspace, void *stream)
+{
+    if (!h || !X_host || !Y_host || !X_dev || !Y_dev)
+        return MLP_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t xb = static_cast<size_t>(h->desc.M) * h->desc.dims[0] * 2;
+    const size_t yb = static_cast<size_t>(h->desc.M) * h->desc.dims[h->S] * 2;
+    if (cudaSetDevice(h->device) != cudaSuccess ||
+        cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    const mlp_status r = mlp_chain_run(h, X_dev, W, Y_dev, workspace, stream);
+    if (r != MLP_OK)
+        return r;
+    return cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, st) == cudaSuccess ? MLP_OK : MLP_ERR_CUDA;
+}
+
+extern "C" mlp_status mlp_chain_check(mlp_chain_t h, void *stream)
+{
+    if (!h)
+        return MLP_ERR_INVALID_ARG;
+    if (cudaSetDevice(h->device) != cudaSuccess ||
+        cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    for (auto &s : h->side)
+        if (s && cudaStreamSynchronize(s) != cudaSuccess)
+            return MLP_ERR_CUDA;
+    uint32_t status = 0;
+    if (cudaMemcpy(&status, h->d_ctrl + 3, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    if (status == 0)
+        return MLP_OK;
+    const mlp_status r = full_reset(h);
+    if (r != MLP_OK)
+        return r;
+    return status == MLP_ERR_BAD_TILE ? MLP_ERR_BAD_TILE : MLP_ERR_TIMEOUT;
+}
+
+extern "C" mlp_status mlp_chain_get_deps(mlp_chain_t h, int32_t b, const int32_t **off, const int32_t **tgt,
+                                         const int32_t **init, int32_t *P, int32_t *C)
+{
+    if (!h || b < 0 || b + 1 >= h->S)
+        return MLP_ERR_INVALID_ARG;
+    if (off)
+        *off = h->off[b].data();
+    if (tgt)
+        *tgt = h->tgt[b].data();
+    if (init)
+        *init = h->init[b].data();
+    if (P)
+        *P = static_cast<int32_t>(h->off[b].size() - 1);
+    if (C)
+        *C = static_cast<int32_t>(h->init[b].size());
+    return MLP_OK;
+}
+
+extern "C" mlp_status mlp_chain_get_event_log(mlp_chain_t h, mlp_event *buf, size_t cap, size_t *n)
+{
+    if (!h || !buf || !n || !h->d_events)
+        return MLP_ERR_INVALID_ARG;
+    static_assert(sizeof(mlp_event) == sizeof(mlpc::EventRec), "event record layout");
+    if (cudaSetDevice(h->device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return MLP_ERR_CUDA;
+    const size_t k = std::min(cap, h->n_events);
+    if (cudaMemcpy(buf, h->d_events, k * sizeof(mlp_event), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    *n = k;
+    return MLP_OK;
+}
+
+extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
+{
+    if (!h || !info)
+        return MLP_ERR_INVALID_ARG;
+    std::memset(info, 0, sizeof(*info));
+    info->num_gemms = h->S;
+    info->tile_m = mlpc::kBM;
+    info->tile_k = mlpc::kBK;
+    for (int s = 0; s < h->S; ++s) {
+        info->tile_n[s] = h->BN[s];
+        info->tiles_m[s] = h->tiles_m;
+        info->tiles_n[s] = h->tiles_n[s];
+    }
+    info->grid_ctas = h->grid;
+    info->num_sms = h->num_sms;
+    info->pipe_stages = h->num_pipe;
+    info->smem_bytes = static_cast<int32_t>(h->smem);
+    info->tmem_cols = static_cast<int32_t>(h->tmem_cols);
+    info->launches_per_run = h->desc.mode == MLP_MODE_PIPELINED ? 1
+                             : h->desc.mode == MLP_MODE_SEQUENTIAL ? h->S
+                                                                   : h->S * h->n_chunks;
+    return MLP_OK;
+}
+
+extern "C" mlp_status mlp_chain_destroy(mlp_chain_t h)
+{
+    if (!h)
+        return MLP_ERR_INVALID_ARG;
+    cudaSetDevice(h->device);
+    for (auto &s : h->side)
+        if (s)
+            cudaStreamSynchronize(s);
+    release(h);
+    return MLP_OK;
+}

@@ -1,0 +1,145 @@
+"""CPU-only checks of the C ABI library: it builds, loads, exports every declared symbol, and
+its host logic (dependency-array builder, protocol model, argument validation) is right.
+No call here touches a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import mlp_latency_gb300 as mc
+from mlp_latency_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mc.build()
+    return mc.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "mlp_chain.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mlp_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"{n} has no binding"
+
+
+def test_struct_layouts_match_the_c_compiler(tmp_path):
+    """Offsets of every ctypes field equal the C compiler's offsetof for the header's structs."""
+    structs = {"mlp_chain_desc": _lib.ChainDesc, "mlp_event": _lib.Event, "mlp_chain_info": _lib.ChainInfo}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "mlp_chain.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{cname}.{f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    out = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                          check=True).stdout.split("\n") if l)
+    for cname, cls in structs.items():
+        assert int(out[cname]) == ctypes.sizeof(cls), cname
+        for f, _ in cls._fields_:
+            assert int(out[f"{cname}.{f}"]) == getattr(cls, f).offset, f"{cname}.{f}"
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.mlp_status_str(s)
+
+
+SHAPES = [
+    (64, 256, 256, 64, 64, 64, 64),
+    (64, 256, 256, 128, 64, 128, 64),
+    (128, 4096, 4096, 128, 32, 128, 32),
+    (300, 192, 160, 128, 64, 128, 32),
+    (300, 200, 100, 64, 48, 128, 64),
+    (257, 96, 64, 128, 32, 64, 64),
+    (1, 64, 64, 128, 64, 128, 64),
+    (513, 128, 384, 128, 128, 128, 256),
+    (2048, 1024, 512, 128, 256, 128, 128),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_deps_builder_matches_oracle_enumeration(lib, oracle_mod, shape):
+    off, tgt, init = mc.deps_build(*shape)
+    o_off, o_tgt, o_init = oracle_mod.deps(*shape)
+    assert np.array_equal(off, o_off)
+    assert np.array_equal(tgt, o_tgt)
+    assert np.array_equal(init, o_init)
+
+
+def test_tiny_config_has_four_producers_per_consumer(lib):
+    # 64 rows, 64x64 tiles: one row panel, 4 producer and 4 consumer tiles
+    off, tgt, init = mc.deps_build(64, 256, 256, 128, 64, 128, 64)
+    assert init.tolist() == [4, 4, 4, 4]
+    assert off.tolist() == [0, 4, 8, 12, 16]
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n,threads,seed", [
+    (1, [4, 4], 4, 0), (4, [8, 3], 8, 1), (3, [5, 7, 2, 4], 6, 2), (6, [2, 9], 16, 3), (2, [1, 1], 3, 4),
+])
+def test_protocol_model_orders_every_tile(lib, tiles_m, tiles_n, threads, seed):
+    st, order = mc.protocol_model(tiles_m, tiles_n, threads=threads, seed=seed, return_order=True)
+    assert st == mc.OK
+    total = tiles_m * sum(tiles_n)
+    assert sorted(order.tolist()) == sorted((s << 24) | t for s in range(len(tiles_n))
+                                            for t in range(tiles_m * tiles_n[s]))
+
+
+def test_protocol_model_dropped_decrement_times_out(lib):
+    st, _ = mc.protocol_model(2, [4, 4], threads=4, seed=5, drop_tile=1, timeout_ms=200)
+    assert st == mc.ERR_TIMEOUT
+
+
+def _desc(**kw):
+    d = _lib.ChainDesc()
+    d.M, d.num_gemms = 128, 2
+    for i, v in enumerate((256, 256, 256)):
+        d.dims[i] = v
+    d.in_dtype, d.acc_dtype, d.h_dtype, d.out_dtype = 1, 2, 1, 1
+    for k, v in kw.items():
+        if k == "dims":
+            for i, x in enumerate(v):
+                d.dims[i] = x
+        else:
+            setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("kw,expect", [
+    ({"num_gemms": 0}, mc.ERR_INVALID_ARG),
+    ({"num_gemms": 5}, mc.ERR_INVALID_ARG),
+    ({"M": 0}, mc.ERR_INVALID_ARG),
+    ({"dims": (256, 100, 256)}, mc.ERR_INVALID_ARG),
+    ({"in_dtype": 2}, mc.ERR_UNSUPPORTED),
+    ({"tile_m": 96}, mc.ERR_UNSUPPORTED),
+    ({"residual": 1, "dims": (256, 256, 512)}, mc.ERR_INVALID_ARG),
+    ({"mode": 2, "microbatch_rows": 100}, mc.ERR_INVALID_ARG),
+    ({"mode": 7}, mc.ERR_INVALID_ARG),
+])
+def test_create_rejects_bad_descriptors_before_touching_cuda(lib, kw, expect):
+    h = ctypes.c_void_p()
+    assert lib.mlp_chain_create(ctypes.byref(_desc(**kw)), ctypes.byref(h)) == expect
+    assert not h.value
+
+
+def test_null_arguments(lib):
+    assert lib.mlp_chain_create(None, None) == mc.ERR_INVALID_ARG
+    assert lib.mlp_chain_run(None, None, None, None, None, None) == mc.ERR_INVALID_ARG
+    assert lib.mlp_chain_check(None, None) == mc.ERR_INVALID_ARG
+    assert lib.mlp_chain_destroy(None) == mc.ERR_INVALID_ARG

@@ -1,0 +1,232 @@
+"""GPU parity of the CUDA chain (through the C ABI) against the CPU oracle.
+
+Bar: Y within |d| <= 1e-2 (|ref| + 1) per element of the oracle; bit-exact on integer-valued
+inputs and closed forms; bit-identical across the pipelined, sequential and micro-batched
+launch modes (same tiles, same k order); the event log shows no consumer tile starting before
+all of its producer tiles finished.
+"""
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+
+
+@pytest.fixture(scope="module")
+def mc():
+    import mlp_latency_gb300
+    mlp_latency_gb300.build()
+    mlp_latency_gb300.load()
+    return mlp_latency_gb300
+
+
+DEV = torch.device("cuda:0")
+
+
+def run_chain(mc, X, Ws, mode="pipelined", reps=1, **kw):
+    M, dims = X.shape[0], [X.shape[1]] + [w.shape[1] for w in Ws]
+    Xd = X.to(DEV)
+    Wd = [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, mode=mode, **kw) as ch:
+        ws = torch.empty(max(ch.workspace_size(), 256), dtype=torch.uint8, device=DEV)
+        Y = torch.full((M, dims[-1]), float("nan"), dtype=torch.bfloat16, device=DEV)
+        outs = []
+        for _ in range(reps):
+            Y.fill_(float("nan"))
+            ch.run(Xd, Wd, Y, ws)
+            st = ch.check()
+            assert st == 0, f"device status {st}"
+            outs.append(Y.cpu().clone())
+        H = ws[: M * dims[1] * 2].view(torch.bfloat16).view(M, dims[1]).cpu() if len(Ws) > 1 else None
+        info = ch.info()
+    return outs if reps > 1 else outs[0], H, info
+
+
+def assert_close_to_oracle(got, ref_bits):
+    ref = (ref_bits.astype(np.uint32) << 16).view(np.float32)
+    g = got.float().numpy()
+    err = np.abs(g - ref)
+    bad = ~(err <= TOL * (np.abs(ref) + 1))
+    assert not bad.any(), (f"{int(bad.sum())}/{bad.size} outside tolerance; worst {float(err.max())} "
+                           f"at {np.unravel_index(np.argmax(err), err.shape)}")
+
+
+def bits(t):
+    return si.bits(t)
+
+
+# ----------------------------------------------------------------------------- tiny chain --
+def test_tiny_pipelined_matches_oracle(mc, oracle_mod):
+    w = si.WORKLOADS["tiny_m64_d256"]
+    X, Ws = si.draw(w, seed=0)
+    Y, H, info = run_chain(mc, X, Ws, tile_n=[64, 64])
+    assert info["tiles_n"] == [4, 4] and info["launches_per_run"] == 1
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(H, Ho)
+    assert_close_to_oracle(Y, Yo)
+
+
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
+def test_every_tile_width_matches_oracle(mc, oracle_mod, bn):
+    w = si.make_workload("t", 200, (320, 512, 264))
+    X, Ws = si.draw(w, seed=1)
+    Y, H, _ = run_chain(mc, X, Ws, tile_n=[bn, bn])
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(H, Ho)
+    assert_close_to_oracle(Y, Yo)
+
+
+@pytest.mark.parametrize("M,dims", [(1, (64, 64, 64)), (130, (72, 136, 40)), (257, (1000, 328, 96)),
+                                    (384, (128, 2048, 128))])
+def test_ragged_shapes_match_oracle(mc, oracle_mod, M, dims):
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=2)
+    Y, H, _ = run_chain(mc, X, Ws)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(H, Ho)
+    assert_close_to_oracle(Y, Yo)
+
+
+def test_integer_valued_inputs_are_bit_exact(mc, oracle_mod):
+    X, Ws = si.draw_integer(300, (1024, 1024, 512), seed=11)
+    Y, H, _ = run_chain(mc, X, Ws, tile_n=[128, 64])
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert np.array_equal(bits(H), Ho)
+    assert np.array_equal(bits(Y), Yo)
+
+
+def test_identity_and_permutation_closed_forms(mc):
+    M, d = 192, 256
+    X, _ = si.draw(si.make_workload("t", M, (d, d, d)), seed=7)
+    I = torch.eye(d, dtype=torch.bfloat16)
+    P, perm = si.permutation_matrix(d, seed=3)
+    Y, _, _ = run_chain(mc, X, [I, P], tile_n=[64, 128])
+    expect = torch.empty_like(X)
+    expect[:, perm] = X
+    assert torch.equal(Y.view(torch.int16), expect.view(torch.int16))
+
+
+# ------------------------------------------------------------------------------ the modes --
+@pytest.mark.parametrize("M,dims,tn", [(512, (512, 1024, 256), [128, 64]), (300, (256, 384, 512), [64, 128]),
+                                       (1024, (256, 256, 256), [256, 32])])
+def test_modes_are_bit_identical(mc, M, dims, tn):
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=4)
+    Yp, _, _ = run_chain(mc, X, Ws, tile_n=tn)
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=tn)
+    assert torch.equal(Yp.view(torch.int16), Ys.view(torch.int16))
+    for rows in (128, 256):
+        if rows < M:
+            Ym, _, info = run_chain(mc, X, Ws, mode="microbatch", microbatch_rows=rows, tile_n=tn)
+            assert info["launches_per_run"] == 2 * -(-M // rows)
+            assert torch.equal(Yp.view(torch.int16), Ym.view(torch.int16))
+
+
+def test_repeated_runs_of_one_handle_are_identical(mc):
+    X, Ws = si.draw(si.make_workload("t", 640, (256, 512, 256)), seed=6)
+    outs, _, _ = run_chain(mc, X, Ws, reps=5, tile_n=[64, 64])
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_small_grid_still_completes(mc, oracle_mod):
+    # fewer CTAs than tiles: every CTA loops over producer and consumer tickets
+    X, Ws = si.draw(si.make_workload("t", 512, (256, 512, 256)), seed=8)
+    Y, _, _ = run_chain(mc, X, Ws, tile_n=[64, 64], grid_ctas=3)
+    assert_close_to_oracle(Y, oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
+
+
+def test_grouped_raster_matches(mc):
+    X, Ws = si.draw(si.make_workload("t", 1024, (256, 512, 256)), seed=9)
+    Ya, _, _ = run_chain(mc, X, Ws, tile_n=[64, 64])
+    Yb, _, _ = run_chain(mc, X, Ws, tile_n=[64, 64], raster_group=3)
+    assert torch.equal(Ya.view(torch.int16), Yb.view(torch.int16))
+
+
+# ------------------------------------------------------------------------ the protocol log --
+def test_event_log_respects_every_dependency(mc):
+    M, dims, tn = 640, (256, 512, 384), [64, 128]
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=10)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=tn, event_log=True) as ch:
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        for _ in range(2):   # the second run checks the re-armed scoreboard
+            ch.run(Xd, Wd, Y, ws)
+            assert ch.check() == 0
+            log = ch.event_log()
+            off, tgt, init = ch.deps(0)
+            info = ch.info()
+            P = info["tiles_m"][0] * info["tiles_n"][0]
+            C = info["tiles_m"][1] * info["tiles_n"][1]
+            assert len(log) == P + C
+            prod, cons = log[:P], log[P:]
+            assert np.array_equal(prod["stage"], np.zeros(P)) and np.array_equal(prod["tile"], np.arange(P))
+            assert np.array_equal(cons["stage"], np.ones(C)) and np.array_equal(cons["tile"], np.arange(C))
+            seqs = np.concatenate([log["seq_start"], log["seq_end"][:P]])
+            assert len(set(seqs.tolist())) == len(seqs)
+            for p in range(P):
+                for c in tgt[off[p]:off[p + 1]]:
+                    assert prod["seq_end"][p] < cons["seq_start"][c]
+                    assert prod["t_end"][p] <= cons["t_start"][c]
+            assert np.all(init == info["tiles_n"][0])
+
+
+def test_dropped_decrement_times_out_then_recovers(mc):
+    M, dims = 256, (256, 256, 256)
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=12)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=[64, 64], drop_tile=1, timeout_us=20000) as ch:
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        ch.run(Xd, Wd, Y, ws)                    # tile 1 withholds its decrements
+        assert ch.check() == mc.ERR_TIMEOUT      # ... so its consumers' bounded wait ran out
+        ch.run(Xd, Wd, Y, ws)                    # the fault fires once; check() re-armed the handle
+        assert ch.check() == 0
+        Y2 = Y.cpu()
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=[64, 64])
+    assert torch.equal(Y2.view(torch.int16), Ys.view(torch.int16))
+
+
+def test_invalid_pointers_are_rejected(mc):
+    with mc.Chain(128, (256, 256, 256)) as ch:
+        X = torch.zeros(128, 256, dtype=torch.bfloat16, device=DEV)
+        W = [torch.zeros(256, 256, dtype=torch.bfloat16, device=DEV)] * 2
+        Y = torch.zeros(128, 256, dtype=torch.bfloat16, device=DEV)
+        ws = torch.empty(ch.workspace_size() + 512, dtype=torch.uint8, device=DEV)
+        with pytest.raises(mc.MlpChainError):
+            ch.run(X, W, Y, None)
+        with pytest.raises(mc.MlpChainError):
+            ch.run(X.view(-1)[1:], W, Y, ws)          # misaligned X
+        with pytest.raises(mc.MlpChainError):
+            ch.run(X, W, Y, ws[16:])                  # misaligned workspace
+
+
+# ---------------------------------------------------------------------- GeLU + residual --
+def test_gelu_residual_four_gemm_chain(mc, oracle_mod):
+    w = si.make_workload("t", 300, (512,) * 5, gelu=True, residual=True)
+    X, Ws = si.draw(w, seed=14)
+    Y, _, _ = run_chain(mc, X, Ws, gelu=True, residual=True, tile_n=[64, 128, 64, 128])
+    Yo = oracle_mod.chain(bits(X), [bits(t) for t in Ws], gelu=True, residual=True)
+    assert_close_to_oracle(Y, Yo)
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", gelu=True, residual=True, tile_n=[64, 128, 64, 128])
+    assert torch.equal(Y.view(torch.int16), Ys.view(torch.int16))
+    Ym, _, _ = run_chain(mc, X, Ws, mode="microbatch", microbatch_rows=128, gelu=True, residual=True,
+                         tile_n=[64, 128, 64, 128])
+    assert torch.equal(Y.view(torch.int16), Ym.view(torch.int16))
+
+
+# ------------------------------------------------------------------ full-size workloads --
+@pytest.mark.parametrize("name", ["decode_m128_d4096", "llama_m256_4096_14336", "prefill_m2048_d8192",
+                                  "gelu4_m512_d8192"])
+def test_full_size_workloads_sampled_rows(mc, oracle_mod, name):
+    w = si.WORKLOADS[name]
+    X, Ws = si.draw(w, seed=0)
+    Y, _, info = run_chain(mc, X, Ws, gelu=w.gelu, residual=w.residual)
+    rows = si.sample_rows(w.M, 32, seed=1)
+    Yo = oracle_mod.chain(bits(X), [bits(t) for t in Ws], gelu=w.gelu, residual=w.residual, rows=rows)
+    assert_close_to_oracle(Y[torch.from_numpy(rows)], Yo)
+    # properties that hold at any size: every element finite and written
+    assert torch.isfinite(Y.float()).all()
