@@ -1,0 +1,512 @@
+#!/usr/bin/env python3
+"""Latency / throughput of the CTA-pipelined GEMM chain on one GB300 (or N replicas).
+
+One step = one pass of the whole chain (every GEMM, the scoreboard / work-queue hand-off, all
+epilogues) over one batch of seeded synthetic inputs, launched as one CUDA graph replay.  The
+L2 cache is flushed (a write of twice its size) between timed steps, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Rank 0 prints one JSON line.  Under torchrun every rank runs its own replica of the workload
+(weak scaling, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "single-batch 2-layer GEMM latency (µs) and TFLOP/s vs roofline on 1 GB300"
+DEFAULT_WORKLOAD = "decode_m128_d4096"
+# tile widths per GEMM chosen by a sweep on GB300 (bench.py --sweep)
+TUNED_TILES = {
+    "tiny_m64_d256": [64, 64],
+    "decode_m128_d4096": [32, 32],
+    "prefill_m2048_d8192": [256, 256],
+    "llama_m256_4096_14336": [128, 32],
+    "gelu4_m512_d8192": [128, 128, 128, 128],
+}
+KERNEL_SOURCES = ["mlp_latency_gb300/csrc/chain_kernel.cuh", "mlp_latency_gb300/csrc/ptx.cuh",
+                  "mlp_latency_gb300/csrc/protocol.h"]
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(PROFILE_DIR, f"chain_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only) on a thread."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                return
+            m = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self._reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _sample(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c)) == 0 and \
+                self._reasons_fn(self.h, ctypes.byref(r)) == 0:
+            self.samples.append((c.value, r.value))
+
+    def start(self):
+        self.samples = []
+        self._stop = threading.Event()
+
+        def loop():
+            while not self._stop.is_set():
+                self._sample()
+                time.sleep(self.period)
+        if self.ok:
+            self._t = threading.Thread(target=loop, daemon=True)
+            self._t.start()
+
+    def stop(self):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+            self._sample()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml unavailable"}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = [name for b, name in self.REASONS.items() if bits & b]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(mhz), "source": "nvml"}
+
+    @staticmethod
+    def rejected(summary) -> bool:
+        bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+        if bad & set(summary["reasons"]):
+            return True
+        if summary["sm_mhz"] and summary["sm_max_mhz"] and summary["sm_mhz"] < 0.6 * summary["sm_max_mhz"] \
+                and not summary["reasons"]:
+            return True
+        return False
+
+
+# --------------------------------------------------------------------------- distributed --
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- timing --
+def time_steps(step_fn, flush_fn, steps: int, stream):
+    """Per-step device time (ms) with CUDA events on `stream`; L2 flushed between steps."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_fn()
+        starts[i].record(stream)
+        step_fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def pct(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]
+
+
+# ------------------------------------------------------------------------- cpu baseline --
+def cpu_oracle_baseline(w, X, Ws, budget_s: float, Y_gpu=None):
+    """Time the CPU oracle (as it stands) on a bounded row sample of the workload."""
+    import oracle  # the one place the bench runs the oracle (plus the reference arm)
+    threads = oracle.default_threads()
+    per_row_flops = w.flops / w.M
+    xb, wb = si.bits(X), [si.bits(t) for t in Ws]
+    # pick a row count that takes about budget_s / 3 per call, then repeat within the budget
+    rows = si.sample_rows(w.M, min(w.M, 8), seed=3)
+    t0 = time.perf_counter()
+    oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+    per_row = (time.perf_counter() - t0) / len(rows)
+    n = int(max(1, min(w.M, (budget_s / 3) / max(per_row, 1e-9))))
+    rows = np.arange(w.M, dtype=np.int64) if n >= w.M else si.sample_rows(w.M, n, seed=4)
+    total_rows, total_t, calls = 0, 0.0, 0
+    parity = None
+    while total_t < budget_s or calls == 0:
+        t0 = time.perf_counter()
+        Yo = oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+        total_t += time.perf_counter() - t0
+        total_rows += len(rows)
+        calls += 1
+        if calls == 1 and Y_gpu is not None:
+            ref = oracle.bf16_to_f32(Yo)
+            got = Y_gpu[rows].astype(np.float32)
+            parity = bool(np.all(np.abs(got - ref) <= 1e-2 * (np.abs(ref) + 1)))
+        if calls >= 50:
+            break
+    value = per_row_flops * total_rows / total_t / 1e12
+    sample = (f"{len(rows)} of {w.M} rows of {w.name} per call (rows are independent), "
+              f"{calls} calls, {total_t:.1f} s wall")
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+            "cpu": cpu_model()}, parity, total_t / calls, len(rows)
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+# ----------------------------------------------------------------------------- reference --
+def run_reference(args, w):
+    """The oracle on the host cores, as the reference arm: same workload, metric and unit."""
+    import torch
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    X, Ws = si.draw(w, seed=0)
+    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    import oracle
+    xb, wb = si.bits(X), [si.bits(t) for t in Ws]
+    threads = oracle.default_threads()
+    rows = si.sample_rows(w.M, min(w.M, 4), seed=3)
+    t0 = time.perf_counter()
+    oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+    per_row = (time.perf_counter() - t0) / len(rows)
+    n = int(max(1, min(w.M, budget / max(per_row, 1e-9))))
+    rows = np.arange(w.M, dtype=np.int64) if n >= w.M else si.sample_rows(w.M, n, seed=4)
+    for _ in range(args.warmup):
+        oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+        times.append(time.perf_counter() - t0)
+    step_s = statistics.mean(times)
+    flops = w.flops / w.M * len(rows)
+    value = flops / step_s / 1e12
+    sample = f"{len(rows)} of {w.M} rows of {w.name} per step (rows are independent)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
+                   "residual": w.residual, "what": "CPU oracle, plain C, fp32 accumulate"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tile-n", default=None, help="comma-separated tile widths per GEMM")
+    ap.add_argument("--mode", default="pipelined", choices=["pipelined", "sequential", "microbatch"])
+    ap.add_argument("--microbatch-rows", type=int, default=0)
+    ap.add_argument("--raster-group", type=int, default=0)
+    ap.add_argument("--no-baselines", action="store_true", help="skip sequential/micro-batch/cuBLAS lines")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="only run this many graph replays after warm-up (for ncu); prints nothing")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = si.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import mlp_latency_gb300 as mc
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    mc.load()  # raises if the CUDA library was not built: no fallback
+
+    tiles = [int(t) for t in args.tile_n.split(",")] if args.tile_n else TUNED_TILES.get(w.name)
+    X, Ws = si.draw(w, seed=0)
+    Xd, Wd = X.to(dev), [t.to(dev) for t in Ws]
+    Y = torch.empty(w.M, w.dims[-1], dtype=torch.bfloat16, device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def make(mode, rows=0):
+        return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
+                        microbatch_rows=rows, device=local, raster_group=args.raster_group)
+
+    chain = make(args.mode, args.microbatch_rows)
+    info = chain.info()
+    ws = torch.empty(max(chain.workspace_size(), 256), dtype=torch.uint8, device=dev)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()  # eager once (also encodes the TMA descriptors)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        torch.cuda.synchronize()
+        return g
+
+    with torch.cuda.stream(stream):
+        g_main = capture(lambda: chain.run(Xd, Wd, Y, ws, stream=stream))
+        status = chain.check(stream)
+        if status != 0:
+            raise RuntimeError(f"device status {status} after the first run")
+
+        def flush():
+            flush_buf.zero_()
+
+        for _ in range(args.warmup):
+            flush()
+            g_main.replay()
+        torch.cuda.synchronize()
+        if args.profile_steps:
+            for _ in range(args.profile_steps):
+                flush()
+                g_main.replay()
+            torch.cuda.synchronize()
+            return
+
+        uuid = "GPU-" + str(getattr(props, "uuid", "")) if getattr(props, "uuid", None) else ""
+        sampler = ClockSampler(uuid)
+        remeasured = False
+        for attempt in range(2):
+            barrier(world)
+            torch.cuda.synchronize()
+            sampler.start()
+            ms = time_steps(g_main.replay, flush, args.steps, stream)
+            sampler.stop()
+            torch.cuda.synchronize()
+            barrier(world)
+            clocks = sampler.summary()
+            if not ClockSampler.rejected(clocks) or attempt == 1:
+                break
+            remeasured = True
+        if chain.check(stream) != 0:
+            raise RuntimeError("device status set during the timed region")
+
+        mean_ms = statistics.mean(ms)
+        mean_ms_all = max_over_ranks(mean_ms, world, dev)
+        value = world * w.flops / (mean_ms_all * 1e-3) / 1e12
+        lat_us = statistics.median(ms) * 1e3
+
+        # ---- baselines on this GPU: sequential launches, micro-batching sweep, cuBLAS --------
+        baselines = {}
+        k_base = min(args.steps, 300)
+        if not args.no_baselines:
+            for mode in ("sequential", "pipelined"):
+                if mode == args.mode:
+                    continue
+                ch = make(mode)
+                g = capture(lambda ch=ch: ch.run(Xd, Wd, Y, ws, stream=stream))
+                for _ in range(args.warmup):
+                    flush(); g.replay()
+                baselines[f"{mode}_us"] = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
+                ch.close()
+            best = None
+            rows = 128
+            while rows <= w.M // 2:
+                ch = make("microbatch", rows)
+                g = capture(lambda ch=ch: ch.run(Xd, Wd, Y, ws, stream=stream))
+                for _ in range(args.warmup):
+                    flush(); g.replay()
+                t = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
+                baselines[f"microbatch_{rows}_us"] = t
+                if best is None or t < best[1]:
+                    best = (rows, t)
+                ch.close()
+                rows *= 2
+            baselines["microbatch_best_us"] = best[1] if best else None
+            baselines["microbatch_best_rows"] = best[0] if best else None
+            if not w.gelu and not w.residual:
+                def torch_chain():
+                    h = Xd
+                    for t in Wd:
+                        h = torch.matmul(h, t)
+                    Y.copy_(h)
+                g = capture(torch_chain)
+                for _ in range(args.warmup):
+                    flush(); g.replay()
+                baselines["torch_matmul_us"] = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
+
+        # ---- end to end through the host-buffer C-ABI call ------------------------------------
+        Xh = X.pin_memory()
+        Yh = torch.empty(w.M, w.dims[-1], dtype=torch.bfloat16).pin_memory()
+        Xs = torch.empty_like(Xd)
+        for _ in range(args.warmup):
+            chain.run_host(Xh, Wd, Yh, Xs, Y, ws, stream=stream)
+        torch.cuda.synchronize()
+        e2e_ms = time_steps(lambda: chain.run_host(Xh, Wd, Yh, Xs, Y, ws, stream=stream), flush,
+                            args.steps, stream)
+        e2e_mean = max_over_ranks(statistics.mean(e2e_ms), world, dev)
+        e2e_value = world * w.flops / (e2e_mean * 1e-3) / 1e12
+        if chain.check(stream) != 0:
+            raise RuntimeError("device status set during the e2e loop")
+        Y_host = Y.float().cpu().numpy()
+
+    # ---- roofline of the dominant kernel (the one chain kernel of the pipelined step) ----------
+    peaks = load_peaks()
+    t_hbm = w.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = w.flops / (peaks["bf16_tflops"] * 1e12)
+    launches = info["launches_per_run"]
+    launch_s = mean_ms * 1e-3 / launches
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": w.algorithmic_bytes / launches / launch_s / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": w.flops / launches / launch_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(w.name) if args.mode == "pipelined" and tiles == TUNED_TILES.get(w.name) else None
+    roof["peak_source"] = f"{peaks['source']} (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
+    roof["t_roof_us"] = max(t_hbm, t_tc) * 1e6
+    roof["latency_frac_of_roof"] = max(t_hbm, t_tc) * 1e6 / (mean_ms * 1e3)
+    roof["algorithmic_bytes"] = w.algorithmic_bytes
+    roof["flops"] = w.flops
+
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu, parity, _, _ = cpu_oracle_baseline(w, X, Ws, args.cpu_budget, Y_host)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
+                       "residual": w.residual, "mode": args.mode, "tile_m": 128, "tile_n": info["tile_n"],
+                       "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
+                       "graph": "one CUDA graph replay per step",
+                       "l2": f"flushed between steps (write of {2 * l2 >> 20} MiB, outside the timed events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "latency_us": {"median": lat_us, "mean": mean_ms * 1e3, "p10": pct(ms, 0.1) * 1e3,
+                           "p90": pct(ms, 0.9) * 1e3},
+            "baselines": baselines,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "parity_vs_oracle_sample": parity,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": X.numel() * 2,
+                    "d2h_bytes_per_step": Y.numel() * 2, "latency_us": statistics.median(e2e_ms) * 1e3,
+                    "what": "mlp_chain_run_host: pinned X -> device, chain, Y -> pinned host, per step"},
+            "gpu_launches": args.steps * launches,
+            "clocks": {**clocks, "remeasured": remeasured},
+            "kernel_source_sha256": kernel_source_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    chain.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

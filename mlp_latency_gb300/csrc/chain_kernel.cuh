@@ -31,6 +31,7 @@ constexpr int kBK = 64;           // 64 bf16 = 128 bytes = one 128B-swizzle row
 constexpr int kThreads = 256;
 constexpr int kSchedDepth = 4;
 constexpr int kMaxPipe = 16;
+constexpr int kTicketLead = 4;    // k-blocks before the end of a tile at which the next ticket is taken
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 
 // Device status codes (match mlp_status).
@@ -95,6 +96,7 @@ struct __align__(8) Ctrl {
     uint64_t sfull[kSchedDepth], sempty[kSchedDepth];
     uint64_t drain;
     uint64_t epi_sync;
+    uint64_t want_next;   // TMA -> scheduler: take the next ticket now
     int32_t item_stage[kSchedDepth], item_tile[kSchedDepth];
     uint32_t tmem_base;
     volatile int32_t abort_flag;
@@ -162,6 +164,10 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
         const int32_t slot = it % kSchedDepth;
         const uint32_t ph = (it / kSchedDepth) & 1;
         if (!wait_bar(&c->sempty[slot], ph ^ 1, c, p))
+            return;
+        // Take tickets just in time: a ticket taken early would sit in this CTA while other
+        // CTAs idle, so wait until the TMA warp is about to finish its current tile.
+        if (it > 0 && !wait_bar(&c->want_next, (it - 1) & 1, c, p))
             return;
         int32_t stage = -1, tile = 0;
         if (p.pipelined) {
@@ -264,8 +270,11 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const uint32_t box_bytes = kBK * sp.b_swz;
         const int32_t nbox = sp.BN / box_cols;
         const uint32_t bytes = kABytes + static_cast<uint32_t>(kBK * sp.BN * 2);
+        const int32_t lead_kb = sp.k_blocks > kTicketLead ? sp.k_blocks - kTicketLead : 0;
         bool ok = true;
         for (int32_t kb = 0; kb < sp.k_blocks; ++kb) {
+            if (kb == lead_kb)
+                mbar_arrive(&c->want_next);
             if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
                 ok = false;
                 break;
@@ -500,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
         mbar_init(&c->drain, 1);
         mbar_init(&c->epi_sync, 4);
+        mbar_init(&c->want_next, 1);
         c->abort_flag = 0;
         c->skip = ld_relaxed_gpu_u32(p.status) != 0;   // sticky error: do nothing
         c->epoch = p.pipelined ? ld_relaxed_gpu_u32(p.epoch) : 0u;
