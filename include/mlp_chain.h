@@ -190,6 +190,32 @@ mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t 
                               int32_t threads, uint64_t seed, int32_t drop_tile,
                               uint32_t timeout_ms, int32_t *order_out);
 
+/* Allocation-free run of the two-GEMM chain (the paper has no counterpart to this entry point).
+ *
+ * For callers that cannot allocate device memory when they run the chain: code running inside
+ * an allocator or memory-pool callback, runtimes that reserve all device memory up front and
+ * forbid further cudaMalloc, or embeddings that must not go through the host framework's
+ * caching allocator.  It needs no handle: it runs Y = (X*W1)*W2 (X: M x K, W1: K x N1,
+ * W2: N1 x N2, Y: M x N2; bf16, device pointers, 16-byte aligned, K, N1, N2 multiples of 8) in
+ * pipelined mode with the library's default tiles, and keeps every byte of scratch -- the
+ * intermediate H, the dependency array, scoreboard, work-queue, tickets and status word -- in one
+ * static device array of MLP_NOALLOC_SCRATCH_BYTES that each GPU loading the library holds until
+ * the process exits.  It calls no cudaMalloc/cudaFree or other allocating routine.
+ *   - Limit: shapes whose scratch (mainly M*N1*2 bytes of H) exceeds the array are rejected
+ *     with MLP_ERR_INVALID_ARG before anything is enqueued.
+ *   - The first call on a device (the current device) looks up the array's device address and
+ *     sets the kernel's shared-memory limit; make that first call before any stream capture.
+ *   - Every call shares the one array: each call first re-initialises all of its state on
+ *     `stream` (a small set-up kernel, then the chain kernel), so nothing of the previous call
+ *     leaks in, but calls whose execution overlaps on the GPU (different streams, threads or
+ *     processes sharing the device context) race and give wrong results.
+ *   - With sync_check != 0 the call synchronises `stream` and returns MLP_ERR_TIMEOUT or
+ *     MLP_ERR_BAD_TILE if the device reported one; with 0 it returns after enqueueing. */
+#define MLP_NOALLOC_SCRATCH_BYTES (16u << 20)
+mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, int64_t N2, const void *X,
+                                 const void *W1, const void *W2, void *Y, int32_t sync_check,
+                                 void *stream);
+
 const char *mlp_status_str(mlp_status s);
 
 #ifdef __cplusplus

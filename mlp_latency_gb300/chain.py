@@ -191,3 +191,17 @@ def protocol_model(tiles_m: int, tiles_n: Sequence[int], threads: int = 8, seed:
     st = lib.mlp_protocol_model(len(tn), tiles_m, tn.ctypes.data, threads, seed, drop_tile, timeout_ms,
                                 order.ctypes.data if order is not None else None)
     return int(st), order
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def run_noalloc(X, W1, W2, Y, sync_check: bool = True, stream=None):
+    """mlp_chain_run_noalloc: the two-GEMM chain with no device allocation (all scratch in the
+    library's static device array). For callers that may not allocate device memory while they
+    run; overlapping calls race. Raises MlpChainError on a non-OK status."""
+    lib = _lib.load()
+    M, K = X.shape
+    N1, N2 = W1.shape[1], W2.shape[1]
+    _check(lib.mlp_chain_run_noalloc(M, K, N1, N2, X.data_ptr(), W1.data_ptr(), W2.data_ptr(), Y.data_ptr(),
+                                     int(bool(sync_check)), _stream_ptr(stream)), "mlp_chain_run_noalloc")

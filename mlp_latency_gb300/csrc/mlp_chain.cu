@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -586,4 +587,216 @@ extern "C" mlp_status mlp_chain_destroy(mlp_chain_t h)
             cudaStreamSynchronize(s);
     release(h);
     return MLP_OK;
+}
+
+// ============================================================================================
+// Allocation-free entry point.
+//
+// Some callers cannot allocate device memory at the point where they run the chain: code that
+// runs inside a custom allocator or memory-pool callback, a runtime that reserves every byte of
+// device memory up front and forbids further cudaMalloc, or an embedding that must not touch
+// the CUDA caching allocator of the host framework.  mlp_chain_run_noalloc serves them: it runs
+// the two-GEMM chain in pipelined mode with all of its scratch (the intermediate H, the
+// dependency array, scoreboard, work-queue, tickets and status word) inside the file-scope
+// array below, which every GPU that loads this library holds until the process exits.
+// ============================================================================================
+namespace {
+
+__device__ __align__(256) static uint8_t g_noalloc_scratch[MLP_NOALLOC_SCRATCH_BYTES];
+
+struct NoallocDevice {
+    bool ready = false;
+    uint8_t *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+};
+NoallocDevice g_noalloc_dev[64];
+std::mutex g_noalloc_mutex;
+
+struct NoallocLayout {
+    size_t ctrl, off, tgt, init, count, queue, tail, h, total;
+};
+
+NoallocLayout noalloc_layout(int64_t M, int64_t N1, int P, int C, int64_t nnz)
+{
+    NoallocLayout L{};
+    size_t o = 0;
+    L.ctrl = o;  o += 8 * sizeof(uint32_t);
+    o = align_up(o, 256); L.off = o;   o += static_cast<size_t>(P + 1) * 4;
+    o = align_up(o, 256); L.tgt = o;   o += static_cast<size_t>(nnz) * 4;
+    o = align_up(o, 256); L.init = o;  o += static_cast<size_t>(C) * 4;
+    o = align_up(o, 256); L.count = o; o += static_cast<size_t>(C) * 4;
+    o = align_up(o, 256); L.queue = o; o += static_cast<size_t>(C) * 8;
+    o = align_up(o, 256); L.tail = o;  o += 4;
+    o = align_up(o, 256); L.h = o;     o += static_cast<size_t>(M) * N1 * 2;
+    L.total = o;
+    return L;
+}
+
+// Writes the whole protocol state of one run into the scratch: control words cleared, the
+// dependency array of equal-height row tiles (producer tile (m, n) feeds every consumer tile of
+// row panel m, and each consumer needs all Pn producer tiles of its panel), counters armed,
+// queue slots emptied.  Nothing of a previous call survives.
+__global__ void noalloc_setup_kernel(uint8_t *base, NoallocLayout L, int Pn, int Cn, int tiles_m)
+{
+    const int P = tiles_m * Pn, C = tiles_m * Cn;
+    const long long nnz = static_cast<long long>(P) * Cn;
+    uint32_t *ctrl = reinterpret_cast<uint32_t *>(base + L.ctrl);
+    int32_t *off = reinterpret_cast<int32_t *>(base + L.off);
+    int32_t *tgt = reinterpret_cast<int32_t *>(base + L.tgt);
+    int32_t *init = reinterpret_cast<int32_t *>(base + L.init);
+    uint32_t *count = reinterpret_cast<uint32_t *>(base + L.count);
+    unsigned long long *queue = reinterpret_cast<unsigned long long *>(base + L.queue);
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (long long i = i0; i < 8; i += stride)
+        ctrl[i] = 0;
+    if (i0 == 0)
+        *reinterpret_cast<uint32_t *>(base + L.tail) = 0;
+    for (long long i = i0; i <= P; i += stride)
+        off[i] = static_cast<int32_t>(i * Cn);
+    for (long long e = i0; e < nnz; e += stride) {
+        const long long p = e / Cn;
+        tgt[e] = static_cast<int32_t>((p / Pn) * Cn + e % Cn);
+    }
+    for (long long c = i0; c < C; c += stride) {
+        init[c] = Pn;
+        count[c] = static_cast<uint32_t>(Pn);
+        queue[c] = 0;
+    }
+}
+
+}  // namespace
+
+extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, int64_t N2, const void *X,
+                                            const void *W1, const void *W2, void *Y, int32_t sync_check,
+                                            void *stream)
+{
+    if (M < 1 || M > (int64_t)1 << 30 || !X || !W1 || !W2 || !Y)
+        return MLP_ERR_INVALID_ARG;
+    const int64_t dims[3] = {K, N1, N2};
+    for (int64_t d : dims)
+        if (d < 8 || d % 8 != 0 || d > (int64_t)1 << 24)
+            return MLP_ERR_INVALID_ARG;
+    auto misaligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
+    if (misaligned(X) || misaligned(W1) || misaligned(W2) || misaligned(Y))
+        return MLP_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return MLP_ERR_CUDA;
+
+    NoallocDevice nd;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        NoallocDevice &slot = g_noalloc_dev[dev];
+        if (!slot.ready) {
+            // One-time set-up on this device (the current one): the scratch array's device
+            // address, the SM count and the kernel's shared-memory limit.
+            int major = 0, minor = 0, smem_optin = 0;
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+            if (major != 10 || minor != 3)
+                return MLP_ERR_UNSUPPORTED;
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+                return MLP_ERR_CUDA;
+            if (cudaDeviceGetAttribute(&slot.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+                cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
+                    cudaSuccess)
+                return MLP_ERR_CUDA;
+            slot.scratch = static_cast<uint8_t *>(ptr);
+            slot.ready = true;
+        }
+        nd = slot;
+    }
+
+    // Tiling: the same choices mlp_chain_create makes for this shape.
+    const int tiles_m = static_cast<int>((M + mlpc::kBM - 1) / mlpc::kBM);
+    const int bn[2] = {default_bn(tiles_m, N1, nd.num_sms), default_bn(tiles_m, N2, nd.num_sms)};
+    const int tn[2] = {static_cast<int>((N1 + bn[0] - 1) / bn[0]), static_cast<int>((N2 + bn[1] - 1) / bn[1])};
+    const int P = tiles_m * tn[0], C = tiles_m * tn[1];
+    const int64_t nnz = static_cast<int64_t>(P) * tn[1];
+    const NoallocLayout L = noalloc_layout(M, N1, P, C, nnz);
+    if (L.total > MLP_NOALLOC_SCRATCH_BYTES)
+        return MLP_ERR_INVALID_ARG;   // this shape needs more scratch than the static array holds
+
+    const int max_bn = std::max(bn[0], bn[1]);
+    const uint32_t stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * max_bn * 2);
+    int smem_optin = 0;
+    cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    const int num_pipe =
+        static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - 1024 - sizeof(mlpc::Ctrl)) / stage_bytes));
+    if (num_pipe < 2)
+        return MLP_ERR_UNSUPPORTED;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>(2 * max_bn))
+        tmem_cols *= 2;
+
+    uint8_t *base = nd.scratch;
+    void *H = base + L.h;
+    ChainParams P_;
+    std::memset(&P_, 0, sizeof(P_));
+    const void *a_ptr[2] = {X, H};
+    const void *w_ptr[2] = {W1, W2};
+    void *o_ptr[2] = {H, Y};
+    for (int s = 0; s < 2; ++s) {
+        const int b_swz = bn[s] >= 64 ? 128 : 64;
+        if (!encode_2d(&P_.mapA[s], a_ptr[s], M, dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&P_.mapB[s], w_ptr[s], dims[s], dims[s + 1], mlpc::kBK, b_swz / 2,
+                       b_swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+            return MLP_ERR_CUDA;
+        mlpc::StageParams &sp = P_.st[s];
+        sp.M = static_cast<int32_t>(M);
+        sp.K = static_cast<int32_t>(dims[s]);
+        sp.N = static_cast<int32_t>(dims[s + 1]);
+        sp.BN = bn[s];
+        sp.tiles_m = tiles_m;
+        sp.tiles_n = tn[s];
+        sp.k_blocks = static_cast<int32_t>((dims[s] + mlpc::kBK - 1) / mlpc::kBK);
+        sp.b_swz = b_swz;
+        sp.out = static_cast<__nv_bfloat16 *>(o_ptr[s]);
+    }
+    P_.bd[0].prod_off = reinterpret_cast<const int32_t *>(base + L.off);
+    P_.bd[0].prod_tgt = reinterpret_cast<const int32_t *>(base + L.tgt);
+    P_.bd[0].init_count = reinterpret_cast<const int32_t *>(base + L.init);
+    P_.bd[0].count = reinterpret_cast<uint32_t *>(base + L.count);
+    P_.bd[0].queue = reinterpret_cast<unsigned long long *>(base + L.queue);
+    P_.bd[0].tail = reinterpret_cast<uint32_t *>(base + L.tail);
+    P_.num_stages = 2;
+    P_.pipelined = 1;
+    P_.m_tile_end = tiles_m;
+    P_.stage_base[0] = 0;
+    P_.stage_base[1] = P;
+    P_.stage_base[2] = P + C;
+    P_.num_pipe = num_pipe;
+    P_.stage_bytes = stage_bytes;
+    P_.tmem_cols = tmem_cols;
+    P_.acc_stride = max_bn;
+    P_.drop_tile = -1;
+    P_.timeout_ns = 2000000000ull;
+    uint32_t *ctrl = reinterpret_cast<uint32_t *>(base + L.ctrl);
+    P_.ticket = ctrl + 0;
+    P_.done = ctrl + 1;
+    P_.epoch = ctrl + 2;
+    P_.status = ctrl + 3;
+    P_.seq = ctrl + 4;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long work = std::max<long long>(nnz, std::max(C, P + 1));
+    const int setup_blocks = static_cast<int>(std::min<long long>(1024, (work + 255) / 256));
+    noalloc_setup_kernel<<<setup_blocks, 256, 0, st>>>(base, L, tn[0], tn[1], tiles_m);
+    if (cudaGetLastError() != cudaSuccess)
+        return MLP_ERR_CUDA;
+    const int grid = std::min(nd.num_sms, P + C);
+    if (!launch(P_, grid, mlpc::chain_smem_bytes(num_pipe, stage_bytes), st))
+        return MLP_ERR_CUDA;
+    if (!sync_check)
+        return MLP_OK;
+    uint32_t status = 0;
+    if (cudaMemcpyAsync(&status, ctrl + 3, sizeof(status), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    if (status == 0)
+        return MLP_OK;
+    return status == MLP_ERR_BAD_TILE ? MLP_ERR_BAD_TILE : MLP_ERR_TIMEOUT;
 }
