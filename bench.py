@@ -41,7 +41,7 @@ TUNED_TILES = {
     "gelu4_m512_d8192": [128, 128, 128, 128],
 }
 KERNEL_SOURCES = ["mlp_latency_gb300/csrc/chain_kernel.cuh", "mlp_latency_gb300/csrc/ptx.cuh",
-                  "mlp_latency_gb300/csrc/protocol.h"]
+                  "mlp_latency_gb300/csrc/protocol.h", "mlp_latency_gb300/csrc/dep_groups.h"]
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -303,6 +303,10 @@ def main():
     ap.add_argument("--mode", default="pipelined", choices=["pipelined", "sequential", "microbatch"])
     ap.add_argument("--microbatch-rows", type=int, default=0)
     ap.add_argument("--raster-group", type=int, default=0)
+    ap.add_argument("--pipe-stages", type=int, default=0)
+    ap.add_argument("--acc-split", type=int, default=0)
+    ap.add_argument("--weight-layout", default="kn", choices=["kn", "nk"],
+                    help="nk: weights stored transposed (nn.Linear layout)")
     ap.add_argument("--no-baselines", action="store_true", help="skip sequential/micro-batch/cuBLAS lines")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
@@ -330,7 +334,9 @@ def main():
 
     tiles = [int(t) for t in args.tile_n.split(",")] if args.tile_n else TUNED_TILES.get(w.name)
     X, Ws = si.draw(w, seed=0)
-    Xd, Wd = X.to(dev), [t.to(dev) for t in Ws]
+    Xd = X.to(dev)
+    # the library reads W_s as stored; "nk" stores each weight transposed (same values)
+    Wd = [(t.t().contiguous() if args.weight_layout == "nk" else t).to(dev) for t in Ws]
     Y = torch.empty(w.M, w.dims[-1], dtype=torch.bfloat16, device=dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
@@ -339,7 +345,9 @@ def main():
 
     def make(mode, rows=0):
         return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
-                        microbatch_rows=rows, device=local, raster_group=args.raster_group)
+                        microbatch_rows=rows, device=local, raster_group=args.raster_group,
+                        pipe_stages=args.pipe_stages, acc_split=args.acc_split,
+                        weight_layout=args.weight_layout)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()
@@ -427,9 +435,11 @@ def main():
             baselines["microbatch_best_us"] = best[1] if best else None
             baselines["microbatch_best_rows"] = best[0] if best else None
             if not w.gelu and not w.residual:
+                Wd_kn = [t.t() for t in Wd] if args.weight_layout == "nk" else Wd
+
                 def torch_chain():
                     h = Xd
-                    for t in Wd:
+                    for t in Wd_kn:
                         h = torch.matmul(h, t)
                     Y.copy_(h)
                 g = capture(torch_chain)

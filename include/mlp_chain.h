@@ -102,6 +102,14 @@ typedef struct {
     int32_t grid_ctas;                  /* 0 = one CTA per SM                                    */
     int32_t raster_group;               /* first-stage raster: 0/1 = row panels in order; g > 1
                                            = groups of g row panels, column-major inside a group */
+    int32_t pipe_stages;                /* shared-memory ring depth: 0 = as deep as fits         */
+    int32_t weight_layout;              /* 0: W_s stored dims[s] x dims[s+1] row-major (K x N);
+                                           1: stored transposed, dims[s+1] x dims[s] row-major
+                                           (N x K, the layout of nn.Linear.weight)             */
+    int32_t acc_split;                  /* 0/1: one fp32 accumulator per tile; 2: 16-deep k steps
+                                           alternate between two accumulators that the epilogue
+                                           adds (even + odd), so consecutive MMAs do not depend on
+                                           each other; needs 4 * tile_n <= 512                    */
 } mlp_chain_desc;
 
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG).  t_* are %globaltimer ns;

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libmlp_chain.so")
 SOURCES = [os.path.join(CSRC, "mlp_chain.cu"), os.path.join(CSRC, "host_protocol.cpp")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("chain_kernel.cuh", "ptx.cuh", "protocol.h")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("chain_kernel.cuh", "ptx.cuh", "protocol.h", "dep_groups.h")] + [
     os.path.join(INCLUDE, "mlp_chain.h")]
 
 NVCC_FLAGS = [
@@ -60,7 +60,8 @@ class ChainDesc(ctypes.Structure):
         ("out_dtype", ctypes.c_int), ("tile_m", i32), ("tile_n", i32 * MAX_GEMMS), ("tile_k", i32),
         ("epilogue", ctypes.c_int), ("residual", i32), ("mode", ctypes.c_int),
         ("microbatch_rows", i32), ("device", i32), ("debug_flags", u32), ("drop_tile", i32),
-        ("timeout_us", u32), ("grid_ctas", i32), ("raster_group", i32),
+        ("timeout_us", u32), ("grid_ctas", i32), ("raster_group", i32), ("pipe_stages", i32),
+        ("weight_layout", i32), ("acc_split", i32),
     ]
 
 

@@ -48,14 +48,16 @@ def _stream_ptr(stream) -> Optional[int]:
 class Chain:
     """One handle of the library: a fixed chain shape, tile shape and launch mode.
 
-    Shapes follow the header: X[M x dims[0]], W[s][dims[s] x dims[s+1]], Y[M x dims[-1]].
+    Shapes follow the header: X[M x dims[0]], W[s][dims[s] x dims[s+1]] (weight_layout "kn") or
+    W[s][dims[s+1] x dims[s]] ("nk", nn.Linear's layout), Y[M x dims[-1]].
     """
 
     def __init__(self, M: int, dims: Sequence[int], *, tile_n: Optional[Sequence[int]] = None,
                  gelu: bool = False, residual: bool = False, mode: str = "pipelined",
                  microbatch_rows: int = 0, device: int = 0, event_log: bool = False,
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
-                 raster_group: int = 0, tile_m: int = 0):
+                 raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
+                 weight_layout: str = "kn"):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -80,6 +82,9 @@ class Chain:
         d.timeout_us = int(timeout_us)
         d.grid_ctas = int(grid_ctas)
         d.raster_group = int(raster_group)
+        d.pipe_stages = int(pipe_stages)
+        d.acc_split = int(acc_split)
+        d.weight_layout = {"kn": 0, "nk": 1}[weight_layout]
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
         self._lib = lib
         h = ctypes.c_void_p()

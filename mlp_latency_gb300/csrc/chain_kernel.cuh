@@ -47,15 +47,19 @@ struct StageParams {
     __nv_bfloat16 *out;    // M x N row-major
     const __nv_bfloat16 *residual;  // M x N (the chain input) or null
     int32_t gelu;
-    int32_t pad_;
+    int32_t b_kmajor;      // 1: weights stored N x K, B tile is K-major (one box of BN rows)
 };
 
-struct BoundaryParams {    // stage s -> stage s+1
-    const int32_t *prod_off;
-    const int32_t *prod_tgt;
-    const int32_t *init_count;
-    uint32_t *count;
-    unsigned long long *queue;
+// Stage boundary s -> s+1.  The scoreboard holds one counter per group of consumer tiles with
+// identical producer sets (a row panel for GEMM chains); see dep_groups.h.
+struct BoundaryParams {
+    const int32_t *pg_off;     // producer tile -> groups it feeds (CSR)
+    const int32_t *pg_tgt;
+    const int32_t *grp_off;    // group -> member consumer tiles (CSR)
+    const int32_t *grp_mem;
+    const int32_t *grp_init;   // producers each group waits for
+    uint32_t *count;           // one counter per group
+    unsigned long long *queue; // one slot per consumer tile
     uint32_t *tail;
 };
 
@@ -79,7 +83,9 @@ struct ChainParams {
     int32_t num_pipe;                    // shared-memory ring depth
     uint32_t stage_bytes;                // bytes of one ring slot (A + B)
     uint32_t tmem_cols;
-    int32_t acc_stride;                  // TMEM columns between the two accumulators
+    int32_t acc_stride;                  // TMEM columns between the two accumulator buffers
+    int32_t acc_split;                   // 1, or 2: k16 steps alternate between two sub-accumulators
+    int32_t sub_stride;                  // TMEM columns between the sub-accumulators of a buffer
     int32_t drop_tile;                   // fault injection (-1: off)
     uint64_t timeout_ns;
     uint32_t *ticket;
@@ -283,8 +289,12 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             uint8_t *b = a + kABytes;
             mbar_arrive_expect_tx(&c->full[ps], bytes);
             tma_load_2d(a, &p.mapA[s], &c->full[ps], kb * kBK, m0, pol_act);
-            for (int32_t j = 0; j < nbox; ++j)
-                tma_load_2d(b + j * box_bytes, &p.mapB[s], &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
+            if (sp.b_kmajor) {
+                tma_load_2d(b, &p.mapB[s], &c->full[ps], kb * kBK, n0, pol_w);
+            } else {
+                for (int32_t j = 0; j < nbox; ++j)
+                    tma_load_2d(b + j * box_bytes, &p.mapB[s], &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
+            }
             ++fills[ps];
             if (++ps == p.num_pipe) {
                 ps = 0;
@@ -324,16 +334,18 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(p.acc_stride);
-        const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(sp.BN), 1u);
+        const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(sp.BN), sp.b_kmajor ? 0u : 1u);
         const uint32_t b_swz = static_cast<uint32_t>(sp.b_swz);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
+        const bool split2 = p.acc_split == 2;
         bool ok = true;
         for (int32_t kb = 0; kb < sp.k_blocks; ++kb) {
+            // TMA fills and tcgen05.mma reads are both async-proxy operations ordered by the
+            // mbarrier's transaction count: no tcgen05 fence is needed per k block.
             if (!wait_bar(&c->full[ps], pph, c, p)) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
             const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(ps) * p.stage_bytes);
             const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
@@ -342,8 +354,15 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                 const uint64_t ad = smem_desc(a_addr + kk * 32u, 16u, 1024u, 2u);
                 // B: MN-major; a 16-deep k step is 16 rows of b_swz bytes.  LBO: next block of
                 // b_swz/2 columns (one TMA box of 64 rows); SBO: next group of 8 rows.
-                const uint64_t bd = smem_desc(b_addr + kk * 16u * b_swz, kBK * b_swz, 8u * b_swz, b_code);
-                mma_bf16_ss(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                // B stored N x K: K-major like A, BN rows of 128 bytes.
+                const uint64_t bd = sp.b_kmajor
+                                        ? smem_desc(b_addr + kk * 32u, 16u, 1024u, 2u)
+                                        : smem_desc(b_addr + kk * 16u * b_swz, kBK * b_swz, 8u * b_swz, b_code);
+                // k step j goes to sub-accumulator j % acc_split; its first step overwrites.
+                const uint32_t j = static_cast<uint32_t>(kb) * (kBK / 16) + kk;
+                const uint32_t sub = split2 ? (j & 1u) : 0u;
+                mma_bf16_ss(d_tmem + sub * static_cast<uint32_t>(p.sub_stride), ad, bd, idesc,
+                            j >= (split2 ? 2u : 1u) ? 1u : 0u);
             }
             issued = true;
             mma_commit(&c->empty[ps]);  // frees the ring slot once these MMAs have read it
@@ -434,7 +453,16 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         for (int32_t c0 = 0; c0 < sp.BN; c0 += 32) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(taddr + c0, r);
-            tmem_ld_wait();
+            if (p.acc_split == 2) {
+                uint32_t r2[32];
+                tmem_ld_32x32b_x32(taddr + p.sub_stride + c0, r2);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e)   // even k steps + odd k steps, in that order
+                    r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+            } else {
+                tmem_ld_wait();
+            }
             store_chunk(sp, m, n0 + c0, r);
         }
         tc_fence_before();
@@ -465,17 +493,37 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 const bool dropped = (s == 0 && tile == p.drop_tile);
                 if (producer && !dropped) {
                     const BoundaryParams &bd = p.bd[s];
-                    const int32_t e0 = bd.prod_off[tile], e1 = bd.prod_off[tile + 1];
-                    for (int32_t e = e0 + lane; e < e1; e += 32) {
-                        const int32_t cons = bd.prod_tgt[e];
-                        fence_acq_rel_gpu();
-                        const uint32_t old = atom_add_acq_rel_gpu(bd.count + cons, 0xffffffffu);
-                        if (old == 1u) {
-                            // Last producer of `cons`: re-arm its counter for the next run and
-                            // push it.  No other producer touches this counter again this run.
-                            bd.count[cons] = static_cast<uint32_t>(bd.init_count[cons]);
-                            const uint32_t q = atom_add_relaxed_gpu(bd.tail, 1u);
-                            st_release_gpu_u64(bd.queue + q, queue_entry(c->epoch, cons));
+                    const int32_t e0 = bd.pg_off[tile], e1 = bd.pg_off[tile + 1];
+                    for (int32_t eb = e0; eb < e1; eb += 32) {
+                        const int32_t e = eb + lane;
+                        int32_t g = -1;
+                        bool fire = false;
+                        if (e < e1) {
+                            g = bd.pg_tgt[e];
+                            fence_acq_rel_gpu();
+                            const uint32_t old = atom_add_acq_rel_gpu(bd.count + g, 0xffffffffu);
+                            fire = (old == 1u);
+                            if (fire)   // re-arm for the next run; no producer touches it again
+                                bd.count[g] = static_cast<uint32_t>(bd.grp_init[g]);
+                        }
+                        // Every group this warp completed is published by the whole warp: the
+                        // lane whose acq_rel decrement reached zero acquired every earlier
+                        // producer's release; __syncwarp orders that before each lane's release
+                        // fence, which makes its relaxed queue stores carry the release.
+                        uint32_t todo = __ballot_sync(0xffffffffu, fire);
+                        while (todo) {
+                            const int32_t src = __ffs(todo) - 1;
+                            todo &= todo - 1;
+                            const int32_t gg = __shfl_sync(0xffffffffu, g, src);
+                            const int32_t m0 = bd.grp_off[gg], n = bd.grp_off[gg + 1] - m0;
+                            uint32_t q0 = 0;
+                            if (lane == src)
+                                q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(n));
+                            q0 = __shfl_sync(0xffffffffu, q0, src);
+                            __syncwarp();
+                            fence_acq_rel_gpu();
+                            for (int32_t i = lane; i < n; i += 32)
+                                st_relaxed_gpu_u64(bd.queue + q0 + i, queue_entry(c->epoch, bd.grp_mem[m0 + i]));
                         }
                     }
                 }

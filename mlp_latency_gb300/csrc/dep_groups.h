@@ -1,0 +1,26 @@
+// dep_groups.h -- host-side compression of a dependency array into scoreboard groups.
+//
+// Consumer tiles whose producer sets are identical become ready at the same moment, so they
+// can share one scoreboard counter: the counter of a group starts at the group's in-degree,
+// each producer decrements every group it feeds once, and the decrement that reaches zero
+// pushes all members of the group onto the work-queue.  Readiness is exactly that of one
+// counter per consumer tile (section III-A of the CTA-pipelining paper), with O(P) instead of
+// O(P * consumers-per-panel) atomics.  For a GEMM chain with equal row tiles a group is the set
+// of consumer tiles of one row panel.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+namespace mlpc {
+
+struct DepGroups {
+    std::vector<int32_t> pg_off, pg_tgt;    // producer -> groups it feeds (ascending)
+    std::vector<int32_t> grp_off, grp_mem;  // group -> member consumer tiles (ascending)
+    std::vector<int32_t> grp_init;          // producers each group waits for
+};
+
+// prod_off[P+1] / prod_tgt: producer -> consumers CSR (consumer ids ascending per producer).
+DepGroups build_groups(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C);
+
+}  // namespace mlpc

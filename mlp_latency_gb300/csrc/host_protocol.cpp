@@ -11,11 +11,13 @@
 #include <atomic>
 #include <chrono>
 #include <cstdint>
+#include <map>
 #include <random>
 #include <thread>
 #include <vector>
 
 #include "../../include/mlp_chain.h"
+#include "dep_groups.h"
 #include "protocol.h"
 
 extern "C" int64_t mlp_deps_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm_p, int32_t bn_p,
@@ -57,6 +59,49 @@ extern "C" int64_t mlp_deps_build(int64_t M, int64_t n_out, int64_t n_next, int3
     return e;
 }
 
+mlpc::DepGroups mlpc::build_groups(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C)
+{
+    // producers of each consumer, ascending (producers are visited in ascending order)
+    std::vector<std::vector<int32_t>> in(static_cast<size_t>(C));
+    for (int32_t p = 0; p < P; ++p)
+        for (int32_t e = prod_off[p]; e < prod_off[p + 1]; ++e)
+            in[static_cast<size_t>(prod_tgt[e])].push_back(p);
+    std::map<std::vector<int32_t>, int32_t> id;
+    std::vector<int32_t> group_of(static_cast<size_t>(C));
+    std::vector<std::vector<int32_t>> members;
+    DepGroups g;
+    for (int32_t c = 0; c < C; ++c) {
+        auto it = id.find(in[c]);
+        int32_t gid;
+        if (it == id.end()) {
+            gid = static_cast<int32_t>(members.size());
+            id.emplace(in[c], gid);
+            members.emplace_back();
+            g.grp_init.push_back(static_cast<int32_t>(in[c].size()));
+        } else {
+            gid = it->second;
+        }
+        group_of[c] = gid;
+        members[gid].push_back(c);
+    }
+    g.grp_off.push_back(0);
+    for (auto &m : members) {
+        g.grp_mem.insert(g.grp_mem.end(), m.begin(), m.end());
+        g.grp_off.push_back(static_cast<int32_t>(g.grp_mem.size()));
+    }
+    g.pg_off.push_back(0);
+    for (int32_t p = 0; p < P; ++p) {
+        std::vector<int32_t> gs;
+        for (int32_t e = prod_off[p]; e < prod_off[p + 1]; ++e)
+            gs.push_back(group_of[prod_tgt[e]]);
+        std::sort(gs.begin(), gs.end());
+        gs.erase(std::unique(gs.begin(), gs.end()), gs.end());
+        g.pg_tgt.insert(g.pg_tgt.end(), gs.begin(), gs.end());
+        g.pg_off.push_back(static_cast<int32_t>(g.pg_tgt.size()));
+    }
+    return g;
+}
+
 // ------------------------------------------------------------------------------------------
 // Host model of the protocol: `threads` host threads play the persistent CTAs.  Each takes
 // tickets in stage order; first-stage tickets map to tiles through raster_tile(); later-stage
@@ -69,7 +114,8 @@ namespace {
 
 struct ModelBoundary {
     std::vector<int32_t> off, tgt, init;
-    std::vector<std::atomic<uint32_t>> count;
+    mlpc::DepGroups grp;
+    std::vector<std::atomic<uint32_t>> count;   // one per group
     std::vector<std::atomic<uint64_t>> queue;
     std::atomic<uint32_t> tail{0};
 };
@@ -101,12 +147,15 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
         bd[b].init.resize(static_cast<size_t>(tiles_m) * tiles_n[b + 1]);
         mlp_deps_build(tiles_m, tiles_n[b], tiles_n[b + 1], 1, 1, 1, 1, bd[b].off.data(), bd[b].tgt.data(), nnz,
                        bd[b].init.data());
-        bd[b].count = std::vector<std::atomic<uint32_t>>(bd[b].init.size());
+        bd[b].grp = mlpc::build_groups(bd[b].off.data(), bd[b].tgt.data(),
+                                       static_cast<int32_t>(bd[b].off.size() - 1),
+                                       static_cast<int32_t>(bd[b].init.size()));
+        bd[b].count = std::vector<std::atomic<uint32_t>>(bd[b].grp.grp_init.size());
         bd[b].queue = std::vector<std::atomic<uint64_t>>(bd[b].init.size());
-        for (size_t i = 0; i < bd[b].init.size(); ++i) {
-            bd[b].count[i].store(static_cast<uint32_t>(bd[b].init[i]));
+        for (size_t i = 0; i < bd[b].grp.grp_init.size(); ++i)
+            bd[b].count[i].store(static_cast<uint32_t>(bd[b].grp.grp_init[i]));
+        for (size_t i = 0; i < bd[b].init.size(); ++i)
             bd[b].queue[i].store(0);
-        }
     }
 
     std::atomic<uint32_t> ticket{0}, seq{0}, status{0};
@@ -164,13 +213,17 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                     order_out[order_pos.fetch_add(1)] = (s << 24) | tile;
                 if (s + 1 < S && !(s == 0 && tile == drop_tile)) {
                     ModelBoundary &b = bd[s];
-                    for (int32_t e = b.off[tile]; e < b.off[tile + 1]; ++e) {
-                        const int32_t c = b.tgt[e];
-                        const uint32_t old = b.count[c].fetch_sub(1, std::memory_order_acq_rel);
+                    const mlpc::DepGroups &G = b.grp;
+                    for (int32_t e = G.pg_off[tile]; e < G.pg_off[tile + 1]; ++e) {
+                        const int32_t g = G.pg_tgt[e];
+                        const uint32_t old = b.count[g].fetch_sub(1, std::memory_order_acq_rel);
                         if (old == 1u) {
-                            b.count[c].store(static_cast<uint32_t>(b.init[c]), std::memory_order_relaxed);
-                            const uint32_t slot = b.tail.fetch_add(1, std::memory_order_relaxed);
-                            b.queue[slot].store(mlpc::queue_entry(epoch, c), std::memory_order_release);
+                            b.count[g].store(static_cast<uint32_t>(G.grp_init[g]), std::memory_order_relaxed);
+                            const int32_t n = G.grp_off[g + 1] - G.grp_off[g];
+                            const uint32_t slot0 = b.tail.fetch_add(static_cast<uint32_t>(n), std::memory_order_relaxed);
+                            for (int32_t i = 0; i < n; ++i)
+                                b.queue[slot0 + i].store(mlpc::queue_entry(epoch, G.grp_mem[G.grp_off[g] + i]),
+                                                         std::memory_order_release);
                         }
                     }
                 }

@@ -13,6 +13,7 @@
 
 #include "../../include/mlp_chain.h"
 #include "chain_kernel.cuh"
+#include "dep_groups.h"
 
 using mlpc::ChainParams;
 
@@ -53,9 +54,10 @@ bool encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, in
 }
 
 struct DeviceBoundary {
-    int32_t *off = nullptr, *tgt = nullptr, *init = nullptr;
+    int32_t *pg_off = nullptr, *pg_tgt = nullptr, *grp_off = nullptr, *grp_mem = nullptr, *grp_init = nullptr;
     uint32_t *count = nullptr, *tail = nullptr;
     unsigned long long *queue = nullptr;
+    size_t groups = 0, consumers = 0;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -67,10 +69,11 @@ struct mlp_chain {
     int device = 0, num_sms = 0, S = 0;
     int BN[MLP_MAX_GEMMS] = {}, tiles_m = 0, tiles_n[MLP_MAX_GEMMS] = {}, k_blocks[MLP_MAX_GEMMS] = {};
     int b_swz[MLP_MAX_GEMMS] = {};
-    int num_pipe = 0, max_bn = 0, grid = 0;
+    int num_pipe = 0, max_bn = 0, grid = 0, acc_split = 1;
     uint32_t stage_bytes = 0, tmem_cols = 0;
     size_t smem = 0;
     std::vector<int32_t> off[MLP_MAX_GEMMS - 1], tgt[MLP_MAX_GEMMS - 1], init[MLP_MAX_GEMMS - 1];
+    mlpc::DepGroups grp[MLP_MAX_GEMMS - 1];
     void *dev_block = nullptr;
     DeviceBoundary db[MLP_MAX_GEMMS - 1];
     uint32_t *d_ctrl = nullptr;  // ticket, done, epoch, status, seq
@@ -121,9 +124,9 @@ static mlp_status full_reset(mlp_chain *h)
     if (cudaMemset(h->d_ctrl, 0, 8 * sizeof(uint32_t)) != cudaSuccess)
         return MLP_ERR_CUDA;
     for (int b = 0; b + 1 < h->S; ++b) {
-        const size_t C = h->init[b].size();
-        if (cudaMemcpy(h->db[b].count, h->db[b].init, C * sizeof(int32_t), cudaMemcpyDeviceToDevice) != cudaSuccess ||
-            cudaMemset(h->db[b].queue, 0, C * sizeof(unsigned long long)) != cudaSuccess ||
+        const DeviceBoundary &db = h->db[b];
+        if (cudaMemcpy(db.count, db.grp_init, db.groups * sizeof(int32_t), cudaMemcpyDeviceToDevice) != cudaSuccess ||
+            cudaMemset(db.queue, 0, db.consumers * sizeof(unsigned long long)) != cudaSuccess ||
             cudaMemset(h->db[b].tail, 0, sizeof(uint32_t)) != cudaSuccess)
             return MLP_ERR_CUDA;
     }
@@ -172,7 +175,9 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_INVALID_ARG;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < mlpc::kBM || d->microbatch_rows % mlpc::kBM))
         return MLP_ERR_INVALID_ARG;
-    if (d->grid_ctas < 0 || d->raster_group < 0)
+    if (d->grid_ctas < 0 || d->raster_group < 0 || d->pipe_stages < 0 || d->pipe_stages == 1 ||
+        d->pipe_stages > mlpc::kMaxPipe || d->acc_split < 0 || d->acc_split > 2 || d->weight_layout < 0 ||
+        d->weight_layout > 1)
         return MLP_ERR_INVALID_ARG;
 
     mlp_chain *h = new (std::nothrow) mlp_chain();
@@ -212,13 +217,20 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     h->stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
     const size_t fixed = 1024 + sizeof(mlpc::Ctrl);
     h->num_pipe = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - fixed) / h->stage_bytes));
+    if (d->pipe_stages)
+        h->num_pipe = std::min(h->num_pipe, d->pipe_stages);
+    h->acc_split = d->acc_split == 2 ? 2 : 1;
+    if (h->acc_split * 2 * h->max_bn > 512) {
+        release(h);
+        return MLP_ERR_UNSUPPORTED;
+    }
     if (h->num_pipe < 2) {
         release(h);
         return MLP_ERR_UNSUPPORTED;
     }
     h->smem = mlpc::chain_smem_bytes(h->num_pipe, h->stage_bytes);
     h->tmem_cols = 32;
-    while (h->tmem_cols < static_cast<uint32_t>(2 * h->max_bn))
+    while (h->tmem_cols < static_cast<uint32_t>(2 * h->acc_split * h->max_bn))
         h->tmem_cols *= 2;
     h->stage_base[0] = 0;
     for (int s = 0; s < S; ++s)
@@ -245,10 +257,15 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], mlpc::kBM, h->BN[b], mlpc::kBM, h->BN[b + 1],
                        h->off[b].data(), h->tgt[b].data(), nnz, h->init[b].data());
         h->tgt[b].resize(static_cast<size_t>(nnz));
-        bytes = align_up(bytes, 256) + h->off[b].size() * 4;
-        bytes = align_up(bytes, 256) + std::max<size_t>(h->tgt[b].size(), 1) * 4;
-        bytes = align_up(bytes, 256) + h->init[b].size() * 4;      // init
-        bytes = align_up(bytes, 256) + h->init[b].size() * 4;      // count
+        h->grp[b] = mlpc::build_groups(h->off[b].data(), h->tgt[b].data(), static_cast<int32_t>(h->off[b].size() - 1),
+                                       static_cast<int32_t>(h->init[b].size()));
+        const mlpc::DepGroups &G = h->grp[b];
+        bytes = align_up(bytes, 256) + G.pg_off.size() * 4;
+        bytes = align_up(bytes, 256) + std::max<size_t>(G.pg_tgt.size(), 1) * 4;
+        bytes = align_up(bytes, 256) + G.grp_off.size() * 4;
+        bytes = align_up(bytes, 256) + G.grp_mem.size() * 4;
+        bytes = align_up(bytes, 256) + G.grp_init.size() * 4;      // init
+        bytes = align_up(bytes, 256) + G.grp_init.size() * 4;      // count
         bytes = align_up(bytes, 256) + h->init[b].size() * 8;      // queue
         bytes = align_up(bytes, 256) + 4;                          // tail
     }
@@ -273,16 +290,27 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
             o += n;
             return r;
         };
-        h->db[b].off = static_cast<int32_t *>(take(h->off[b].size() * 4));
-        h->db[b].tgt = static_cast<int32_t *>(take(std::max<size_t>(h->tgt[b].size(), 1) * 4));
-        h->db[b].init = static_cast<int32_t *>(take(h->init[b].size() * 4));
-        h->db[b].count = static_cast<uint32_t *>(take(h->init[b].size() * 4));
-        h->db[b].queue = static_cast<unsigned long long *>(take(h->init[b].size() * 8));
-        h->db[b].tail = static_cast<uint32_t *>(take(4));
-        ok = ok && cudaMemcpy(h->db[b].off, h->off[b].data(), h->off[b].size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
-        if (!h->tgt[b].empty())
-            ok = ok && cudaMemcpy(h->db[b].tgt, h->tgt[b].data(), h->tgt[b].size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
-        ok = ok && cudaMemcpy(h->db[b].init, h->init[b].data(), h->init[b].size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+        const mlpc::DepGroups &G = h->grp[b];
+        DeviceBoundary &db = h->db[b];
+        db.groups = G.grp_init.size();
+        db.consumers = h->init[b].size();
+        db.pg_off = static_cast<int32_t *>(take(G.pg_off.size() * 4));
+        db.pg_tgt = static_cast<int32_t *>(take(std::max<size_t>(G.pg_tgt.size(), 1) * 4));
+        db.grp_off = static_cast<int32_t *>(take(G.grp_off.size() * 4));
+        db.grp_mem = static_cast<int32_t *>(take(G.grp_mem.size() * 4));
+        db.grp_init = static_cast<int32_t *>(take(G.grp_init.size() * 4));
+        db.count = static_cast<uint32_t *>(take(G.grp_init.size() * 4));
+        db.queue = static_cast<unsigned long long *>(take(db.consumers * 8));
+        db.tail = static_cast<uint32_t *>(take(4));
+        auto up = [&](int32_t *dst, const std::vector<int32_t> &v) {
+            if (!v.empty())
+                ok = ok && cudaMemcpy(dst, v.data(), v.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
+        };
+        up(db.pg_off, G.pg_off);
+        up(db.pg_tgt, G.pg_tgt);
+        up(db.grp_off, G.grp_off);
+        up(db.grp_mem, G.grp_mem);
+        up(db.grp_init, G.grp_init);
     }
     if (h->n_events) {
         o = align_up(o, 256);
@@ -353,9 +381,14 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         } else {
             out_ptr = Y;
         }
-        if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&P.mapB[s], W[s], d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
-                       h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+        if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MLP_ERR_CUDA;
+        const bool w_ok = d.weight_layout == 1
+                              ? encode_2d(&P.mapB[s], W[s], d.dims[s + 1], d.dims[s], h->BN[s], mlpc::kBK,
+                                          CU_TENSOR_MAP_SWIZZLE_128B)
+                              : encode_2d(&P.mapB[s], W[s], d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
+                                          h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        if (!w_ok)
             return MLP_ERR_CUDA;
         mlpc::StageParams &sp = P.st[s];
         sp.M = static_cast<int32_t>(d.M);
@@ -366,15 +399,18 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.tiles_n = h->tiles_n[s];
         sp.k_blocks = h->k_blocks[s];
         sp.b_swz = h->b_swz[s];
+        sp.b_kmajor = d.weight_layout == 1;
         sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
         sp.gelu = d.epilogue == MLP_EPI_GELU_TANH;
         sp.residual = (d.residual && s + 1 == h->S) ? static_cast<const __nv_bfloat16 *>(X) : nullptr;
         a_ptr = out_ptr;
     }
     for (int b = 0; b + 1 < h->S; ++b) {
-        P.bd[b].prod_off = h->db[b].off;
-        P.bd[b].prod_tgt = h->db[b].tgt;
-        P.bd[b].init_count = h->db[b].init;
+        P.bd[b].pg_off = h->db[b].pg_off;
+        P.bd[b].pg_tgt = h->db[b].pg_tgt;
+        P.bd[b].grp_off = h->db[b].grp_off;
+        P.bd[b].grp_mem = h->db[b].grp_mem;
+        P.bd[b].grp_init = h->db[b].grp_init;
         P.bd[b].count = h->db[b].count;
         P.bd[b].queue = h->db[b].queue;
         P.bd[b].tail = h->db[b].tail;
@@ -386,7 +422,9 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     P.num_pipe = h->num_pipe;
     P.stage_bytes = h->stage_bytes;
     P.tmem_cols = h->tmem_cols;
-    P.acc_stride = h->max_bn;
+    P.acc_stride = h->acc_split * h->max_bn;
+    P.acc_split = h->acc_split;
+    P.sub_stride = h->max_bn;
     P.drop_tile = -1;
     P.timeout_ns = static_cast<uint64_t>(d.timeout_us ? d.timeout_us : 2000000u) * 1000ull;
     P.ticket = h->d_ctrl + 0;
@@ -613,18 +651,21 @@ NoallocDevice g_noalloc_dev[64];
 std::mutex g_noalloc_mutex;
 
 struct NoallocLayout {
-    size_t ctrl, off, tgt, init, count, queue, tail, h, total;
+    size_t ctrl, pg_off, pg_tgt, grp_off, grp_mem, grp_init, count, queue, tail, h, total;
 };
 
-NoallocLayout noalloc_layout(int64_t M, int64_t N1, int P, int C, int64_t nnz)
+// Groups are the row panels (tiles_m of them); every producer feeds exactly its own panel.
+NoallocLayout noalloc_layout(int64_t M, int64_t N1, int P, int C, int G)
 {
     NoallocLayout L{};
     size_t o = 0;
     L.ctrl = o;  o += 8 * sizeof(uint32_t);
-    o = align_up(o, 256); L.off = o;   o += static_cast<size_t>(P + 1) * 4;
-    o = align_up(o, 256); L.tgt = o;   o += static_cast<size_t>(nnz) * 4;
-    o = align_up(o, 256); L.init = o;  o += static_cast<size_t>(C) * 4;
-    o = align_up(o, 256); L.count = o; o += static_cast<size_t>(C) * 4;
+    o = align_up(o, 256); L.pg_off = o;   o += static_cast<size_t>(P + 1) * 4;
+    o = align_up(o, 256); L.pg_tgt = o;   o += static_cast<size_t>(P) * 4;
+    o = align_up(o, 256); L.grp_off = o;  o += static_cast<size_t>(G + 1) * 4;
+    o = align_up(o, 256); L.grp_mem = o;  o += static_cast<size_t>(C) * 4;
+    o = align_up(o, 256); L.grp_init = o; o += static_cast<size_t>(G) * 4;
+    o = align_up(o, 256); L.count = o; o += static_cast<size_t>(G) * 4;
     o = align_up(o, 256); L.queue = o; o += static_cast<size_t>(C) * 8;
     o = align_up(o, 256); L.tail = o;  o += 4;
     o = align_up(o, 256); L.h = o;     o += static_cast<size_t>(M) * N1 * 2;
@@ -633,34 +674,40 @@ NoallocLayout noalloc_layout(int64_t M, int64_t N1, int P, int C, int64_t nnz)
 }
 
 // Writes the whole protocol state of one run into the scratch: control words cleared, the
-// dependency array of equal-height row tiles (producer tile (m, n) feeds every consumer tile of
-// row panel m, and each consumer needs all Pn producer tiles of its panel), counters armed,
-// queue slots emptied.  Nothing of a previous call survives.
+// grouped dependency array of equal-height row tiles (producer tile (m, n) feeds row panel m;
+// panel m holds consumer tiles m*Cn .. m*Cn+Cn-1 and waits for its Pn producer tiles),
+// counters armed, queue slots emptied.  Nothing of a previous call survives.
 __global__ void noalloc_setup_kernel(uint8_t *base, NoallocLayout L, int Pn, int Cn, int tiles_m)
 {
-    const int P = tiles_m * Pn, C = tiles_m * Cn;
-    const long long nnz = static_cast<long long>(P) * Cn;
+    const int P = tiles_m * Pn, C = tiles_m * Cn, G = tiles_m;
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(base + L.ctrl);
-    int32_t *off = reinterpret_cast<int32_t *>(base + L.off);
-    int32_t *tgt = reinterpret_cast<int32_t *>(base + L.tgt);
-    int32_t *init = reinterpret_cast<int32_t *>(base + L.init);
+    int32_t *pg_off = reinterpret_cast<int32_t *>(base + L.pg_off);
+    int32_t *pg_tgt = reinterpret_cast<int32_t *>(base + L.pg_tgt);
+    int32_t *grp_off = reinterpret_cast<int32_t *>(base + L.grp_off);
+    int32_t *grp_mem = reinterpret_cast<int32_t *>(base + L.grp_mem);
+    int32_t *grp_init = reinterpret_cast<int32_t *>(base + L.grp_init);
     uint32_t *count = reinterpret_cast<uint32_t *>(base + L.count);
     unsigned long long *queue = reinterpret_cast<unsigned long long *>(base + L.queue);
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    const long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (long long i = i0; i < 8; i += stride)
+    const int stride = gridDim.x * blockDim.x;
+    const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
+    for (int i = i0; i < 8; i += stride)
         ctrl[i] = 0;
     if (i0 == 0)
         *reinterpret_cast<uint32_t *>(base + L.tail) = 0;
-    for (long long i = i0; i <= P; i += stride)
-        off[i] = static_cast<int32_t>(i * Cn);
-    for (long long e = i0; e < nnz; e += stride) {
-        const long long p = e / Cn;
-        tgt[e] = static_cast<int32_t>((p / Pn) * Cn + e % Cn);
+    for (int i = i0; i <= P; i += stride) {
+        pg_off[i] = i;
+        if (i < P)
+            pg_tgt[i] = i / Pn;
     }
-    for (long long c = i0; c < C; c += stride) {
-        init[c] = Pn;
-        count[c] = static_cast<uint32_t>(Pn);
+    for (int g = i0; g <= G; g += stride) {
+        grp_off[g] = g * Cn;
+        if (g < G) {
+            grp_init[g] = Pn;
+            count[g] = static_cast<uint32_t>(Pn);
+        }
+    }
+    for (int c = i0; c < C; c += stride) {
+        grp_mem[c] = c;
         queue[c] = 0;
     }
 }
@@ -715,8 +762,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     const int bn[2] = {default_bn(tiles_m, N1, nd.num_sms), default_bn(tiles_m, N2, nd.num_sms)};
     const int tn[2] = {static_cast<int>((N1 + bn[0] - 1) / bn[0]), static_cast<int>((N2 + bn[1] - 1) / bn[1])};
     const int P = tiles_m * tn[0], C = tiles_m * tn[1];
-    const int64_t nnz = static_cast<int64_t>(P) * tn[1];
-    const NoallocLayout L = noalloc_layout(M, N1, P, C, nnz);
+    const NoallocLayout L = noalloc_layout(M, N1, P, C, tiles_m);
     if (L.total > MLP_NOALLOC_SCRATCH_BYTES)
         return MLP_ERR_INVALID_ARG;   // this shape needs more scratch than the static array holds
 
@@ -756,9 +802,11 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
         sp.b_swz = b_swz;
         sp.out = static_cast<__nv_bfloat16 *>(o_ptr[s]);
     }
-    P_.bd[0].prod_off = reinterpret_cast<const int32_t *>(base + L.off);
-    P_.bd[0].prod_tgt = reinterpret_cast<const int32_t *>(base + L.tgt);
-    P_.bd[0].init_count = reinterpret_cast<const int32_t *>(base + L.init);
+    P_.bd[0].pg_off = reinterpret_cast<const int32_t *>(base + L.pg_off);
+    P_.bd[0].pg_tgt = reinterpret_cast<const int32_t *>(base + L.pg_tgt);
+    P_.bd[0].grp_off = reinterpret_cast<const int32_t *>(base + L.grp_off);
+    P_.bd[0].grp_mem = reinterpret_cast<const int32_t *>(base + L.grp_mem);
+    P_.bd[0].grp_init = reinterpret_cast<const int32_t *>(base + L.grp_init);
     P_.bd[0].count = reinterpret_cast<uint32_t *>(base + L.count);
     P_.bd[0].queue = reinterpret_cast<unsigned long long *>(base + L.queue);
     P_.bd[0].tail = reinterpret_cast<uint32_t *>(base + L.tail);
@@ -772,6 +820,8 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     P_.stage_bytes = stage_bytes;
     P_.tmem_cols = tmem_cols;
     P_.acc_stride = max_bn;
+    P_.acc_split = 1;
+    P_.sub_stride = max_bn;
     P_.drop_tile = -1;
     P_.timeout_ns = 2000000000ull;
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(base + L.ctrl);
@@ -782,7 +832,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     P_.seq = ctrl + 4;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const long long work = std::max<long long>(nnz, std::max(C, P + 1));
+    const long long work = std::max(C, P + 1);
     const int setup_blocks = static_cast<int>(std::min<long long>(1024, (work + 255) / 256));
     noalloc_setup_kernel<<<setup_blocks, 256, 0, st>>>(base, L, tn[0], tn[1], tiles_m);
     if (cudaGetLastError() != cudaSuccess)

@@ -28,7 +28,8 @@ DEV = torch.device("cuda:0")
 
 
 def run_chain(mc, X, Ws, mode="pipelined", reps=1, **kw):
-    M, dims = X.shape[0], [X.shape[1]] + [w.shape[1] for w in Ws]
+    col = 0 if kw.get("weight_layout") == "nk" else 1
+    M, dims = X.shape[0], [X.shape[1]] + [w.shape[col] for w in Ws]
     Xd = X.to(DEV)
     Wd = [w.to(DEV) for w in Ws]
     with mc.Chain(M, dims, mode=mode, **kw) as ch:
@@ -230,3 +231,36 @@ def test_full_size_workloads_sampled_rows(mc, oracle_mod, name):
     assert_close_to_oracle(Y[torch.from_numpy(rows)], Yo)
     # properties that hold at any size: every element finite and written
     assert torch.isfinite(Y.float()).all()
+
+
+# --------------------------------------------------------------------- tuning knobs --
+@pytest.mark.parametrize("bn,split,stages", [(32, 2, 0), (128, 2, 3), (64, 1, 2), (256, 1, 2)])
+def test_split_accumulators_and_ring_depth(mc, oracle_mod, bn, split, stages):
+    X, Ws = si.draw(si.make_workload("t", 384, (1024, 512, 320)), seed=15)
+    Y, H, _ = run_chain(mc, X, Ws, tile_n=[bn, bn], acc_split=split, pipe_stages=stages)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(H, Ho)
+    assert_close_to_oracle(Y, Yo)
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=[bn, bn], acc_split=split, pipe_stages=stages)
+    assert torch.equal(Y.view(torch.int16), Ys.view(torch.int16))
+
+
+def test_split_accumulators_integer_inputs_exact(mc, oracle_mod):
+    X, Ws = si.draw_integer(200, (1024, 512, 256), seed=16)
+    Y, H, _ = run_chain(mc, X, Ws, tile_n=[64, 32], acc_split=2)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert np.array_equal(bits(H), Ho)
+    assert np.array_equal(bits(Y), Yo)
+
+
+@pytest.mark.parametrize("bn", [32, 64, 128, 256])
+def test_transposed_weight_layout(mc, oracle_mod, bn):
+    # weights stored N x K (nn.Linear layout): B is K-major in shared memory
+    X, Ws = si.draw(si.make_workload("t", 272, (640, 384, 264)), seed=17)
+    Wt = [w.t().contiguous() for w in Ws]
+    Y, H, _ = run_chain(mc, X, Wt, tile_n=[bn, bn], weight_layout="nk")
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(H, Ho)
+    assert_close_to_oracle(Y, Yo)
+    Ys, _, _ = run_chain(mc, X, Wt, mode="sequential", tile_n=[bn, bn], weight_layout="nk")
+    assert torch.equal(Y.view(torch.int16), Ys.view(torch.int16))
