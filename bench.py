@@ -35,11 +35,12 @@ DEFAULT_WORKLOAD = "decode_m128_d4096"
 # tile widths per GEMM chosen by a sweep on GB300 (bench.py --sweep)
 TUNED_TILES = {
     "tiny_m64_d256": [64, 64],
-    "decode_m128_d4096": [32, 32],
+    "decode_m128_d4096": [0, 0],
     "prefill_m2048_d8192": [256, 256],
-    "llama_m256_4096_14336": [128, 32],
+    "llama_m256_4096_14336": [0, 0],
     "gelu4_m512_d8192": [128, 128, 128, 128],
 }
+TUNED_SPLIT = {}
 KERNEL_SOURCES = ["mlp_latency_gb300/csrc/chain_kernel.cuh", "mlp_latency_gb300/csrc/ptx.cuh",
                   "mlp_latency_gb300/csrc/protocol.h", "mlp_latency_gb300/csrc/dep_groups.h"]
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -299,7 +300,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--tile-n", default=None, help="comma-separated tile widths per GEMM")
+    ap.add_argument("--tile-n", default=None, help="comma-separated tile widths per GEMM (0 = library choice)")
+    ap.add_argument("--k-split", default=None, help="comma-separated split-K factors per GEMM (0 = library choice)")
     ap.add_argument("--mode", default="pipelined", choices=["pipelined", "sequential", "microbatch"])
     ap.add_argument("--microbatch-rows", type=int, default=0)
     ap.add_argument("--raster-group", type=int, default=0)
@@ -332,7 +334,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     mc.load()  # raises if the CUDA library was not built: no fallback
 
-    tiles = [int(t) for t in args.tile_n.split(",")] if args.tile_n else TUNED_TILES.get(w.name)
+    tiles = [int(t) for t in args.tile_n.split(",")][: w.num_gemms] if args.tile_n else TUNED_TILES.get(w.name)
+    ksplit = [int(t) for t in args.k_split.split(",")][: w.num_gemms] if args.k_split else TUNED_SPLIT.get(w.name)
     X, Ws = si.draw(w, seed=0)
     Xd = X.to(dev)
     # the library reads W_s as stored; "nk" stores each weight transposed (same values)
@@ -347,7 +350,7 @@ def main():
         return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
                         microbatch_rows=rows, device=local, raster_group=args.raster_group,
                         pipe_stages=args.pipe_stages, acc_split=args.acc_split,
-                        weight_layout=args.weight_layout)
+                        weight_layout=args.weight_layout, k_split=ksplit)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()
@@ -494,6 +497,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
                        "residual": w.residual, "mode": args.mode, "tile_m": 128, "tile_n": info["tile_n"],
+                       "k_split": info["k_split"], "cluster_size": info["cluster_size"],
                        "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",
                        "l2": f"flushed between steps (write of {2 * l2 >> 20} MiB, outside the timed events)",

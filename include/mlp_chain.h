@@ -106,6 +106,11 @@ typedef struct {
     int32_t weight_layout;              /* 0: W_s stored dims[s] x dims[s+1] row-major (K x N);
                                            1: stored transposed, dims[s+1] x dims[s] row-major
                                            (N x K, the layout of nn.Linear.weight)             */
+    int32_t k_split[MLP_MAX_GEMMS];     /* per GEMM: CTAs sharing one tile along its reduction
+                                           dimension (split-K inside a thread-block cluster):
+                                           0 = library choice, else 1, 2, 4 or 8 with
+                                           tile_n / k_split >= 32; partial sums are added in a
+                                           fixed order, so results stay deterministic            */
     int32_t acc_split;                  /* 0/1: one fp32 accumulator per tile; 2: 16-deep k steps
                                            alternate between two accumulators that the epilogue
                                            adds (even + odd), so consecutive MMAs do not depend on
@@ -120,6 +125,7 @@ typedef struct {
     int32_t stage, tile, smid, cta;
     uint64_t t_start, t_end;
     uint32_t seq_start, seq_end;
+    uint64_t t_acc;                     /* accumulator complete (split tiles: slice 0)           */
 } mlp_event;
 
 typedef struct {
@@ -133,6 +139,8 @@ typedef struct {
     int32_t smem_bytes;                 /* dynamic shared memory per CTA                          */
     int32_t tmem_cols;
     int32_t launches_per_run;           /* kernels one mlp_chain_run enqueues                     */
+    int32_t cluster_size;               /* CTAs per thread-block cluster                          */
+    int32_t k_split[MLP_MAX_GEMMS];
 } mlp_chain_info;
 
 typedef struct mlp_chain *mlp_chain_t;

@@ -61,13 +61,13 @@ class ChainDesc(ctypes.Structure):
         ("epilogue", ctypes.c_int), ("residual", i32), ("mode", ctypes.c_int),
         ("microbatch_rows", i32), ("device", i32), ("debug_flags", u32), ("drop_tile", i32),
         ("timeout_us", u32), ("grid_ctas", i32), ("raster_group", i32), ("pipe_stages", i32),
-        ("weight_layout", i32), ("acc_split", i32),
+        ("weight_layout", i32), ("k_split", i32 * MAX_GEMMS), ("acc_split", i32),
     ]
 
 
 class Event(ctypes.Structure):
     _fields_ = [("stage", i32), ("tile", i32), ("smid", i32), ("cta", i32), ("t_start", u64),
-                ("t_end", u64), ("seq_start", u32), ("seq_end", u32)]
+                ("t_end", u64), ("seq_start", u32), ("seq_end", u32), ("t_acc", u64)]
 
 
 class ChainInfo(ctypes.Structure):
@@ -75,7 +75,7 @@ class ChainInfo(ctypes.Structure):
         ("num_gemms", i32), ("tile_m", i32), ("tile_k", i32), ("tile_n", i32 * MAX_GEMMS),
         ("tiles_m", i32 * MAX_GEMMS), ("tiles_n", i32 * MAX_GEMMS), ("grid_ctas", i32),
         ("num_sms", i32), ("pipe_stages", i32), ("smem_bytes", i32), ("tmem_cols", i32),
-        ("launches_per_run", i32),
+        ("launches_per_run", i32), ("cluster_size", i32), ("k_split", i32 * MAX_GEMMS),
     ]
 
 

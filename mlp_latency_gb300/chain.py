@@ -21,7 +21,7 @@ DEBUG_EVENT_LOG, DEBUG_DROP_DECREMENT = 1, 2
 
 EVENT_DTYPE = np.dtype([("stage", np.int32), ("tile", np.int32), ("smid", np.int32), ("cta", np.int32),
                         ("t_start", np.uint64), ("t_end", np.uint64), ("seq_start", np.uint32),
-                        ("seq_end", np.uint32)])
+                        ("seq_end", np.uint32), ("t_acc", np.uint64)])
 
 
 class MlpChainError(RuntimeError):
@@ -57,7 +57,7 @@ class Chain:
                  microbatch_rows: int = 0, device: int = 0, event_log: bool = False,
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
-                 weight_layout: str = "kn"):
+                 weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -85,6 +85,8 @@ class Chain:
         d.pipe_stages = int(pipe_stages)
         d.acc_split = int(acc_split)
         d.weight_layout = {"kn": 0, "nk": 1}[weight_layout]
+        for i, v in enumerate(k_split or []):
+            d.k_split[i] = int(v)
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
         self._lib = lib
         h = ctypes.c_void_p()
@@ -165,7 +167,8 @@ class Chain:
         return {"num_gemms": S, "tile_m": i.tile_m, "tile_k": i.tile_k, "tile_n": list(i.tile_n[:S]),
                 "tiles_m": list(i.tiles_m[:S]), "tiles_n": list(i.tiles_n[:S]), "grid_ctas": i.grid_ctas,
                 "num_sms": i.num_sms, "pipe_stages": i.pipe_stages, "smem_bytes": i.smem_bytes,
-                "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run}
+                "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run,
+                "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S])}
 
 
 def deps_build(M: int, n_out: int, n_next: int, bm_p: int, bn_p: int, bm_c: int, bn_c: int):

@@ -2,20 +2,26 @@
 // with the CTA-pipelining protocol of "CTA-Pipelining: A Latency-Oriented Spatial Scaling
 // Method for Multi-GPU Systems" (arXiv 2607.07862).
 //
-// Warp roles (256 threads, one CTA per SM):
-//   warp 0      TMA producer: streams A (activations, K-major) and B (weights, MN-major) tiles
-//               into an NS-deep shared-memory ring.
+// The kernel runs as clusters of `cs` CTAs (cs = 1, 2, 4 or 8), one CTA per SM.  A cluster
+// takes one work item at a time: cs/S tiles of a stage, each tile shared by S CTAs that split
+// its reduction dimension (split-K, S = 1 .. cs).  Rank r works on tile r / S, k-slice r % S.
+//
+// Warp roles (256 threads per CTA):
+//   warp 0      TMA producer: streams A (activations, K-major) and B (weights) tiles of its
+//               k-slice into an NS-deep shared-memory ring.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma into a double-buffered TMEM
 //               accumulator; warp 1 also owns the TMEM allocation.
-//   warp 2      scheduler: takes tickets and, for consumer stages, polls the work-queue (the
-//               injected prologue of section III-A, Fig. 1; "fetch the work-queue value and
-//               broadcast it" of section III-C, Fig. 2b, here a shared-memory ring + mbarrier).
-//   warps 4-7   epilogue: TMEM -> registers -> (GeLU) -> bf16 -> global, then the injected
-//               epilogue: fence, scoreboard decrements and queue pushes (section III-A; the
-//               fence placement follows the memory-consistency discussion of section V).
-// Because the scheduler and epilogue warps would otherwise wait at pipeline barriers, the
-// protocol work overlaps the next tile's mainloop, which is how the pages hide it in
-// warp-specialised persistent kernels (section III-C, Fig. 2b).
+//   warp 2      scheduler (rank 0 of each cluster only): takes a ticket per cluster item and,
+//               for consumer stages, polls the work-queue (the injected prologue of section
+//               III-A, Fig. 1), then broadcasts the item to every CTA of the cluster through
+//               distributed shared memory (the scheduler warp's CGA broadcast of section III-C,
+//               Fig. 2b).
+//   warps 4-7   epilogue: TMEM -> registers -> (split-K reduction) -> (GeLU / residual) ->
+//               bf16 -> global, then the injected epilogue: fence, scoreboard decrements and
+//               queue pushes (section III-A; fence placement per the memory-consistency
+//               discussion of section V).
+// The scheduler and epilogue warps would otherwise wait at pipeline barriers, so the protocol
+// work overlaps the next tile's mainloop: the hiding of section III-C, Fig. 2b.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -26,12 +32,13 @@
 namespace mlpc {
 
 constexpr int kMaxStages = 4;
+constexpr int kMaxCluster = 8;
 constexpr int kBM = 128;          // rows per tile = TMEM lanes
 constexpr int kBK = 64;           // 64 bf16 = 128 bytes = one 128B-swizzle row
 constexpr int kThreads = 256;
 constexpr int kSchedDepth = 4;
 constexpr int kMaxPipe = 16;
-constexpr int kTicketLead = 4;    // k-blocks before the end of a tile at which the next ticket is taken
+constexpr int kTicketLead = 4;    // k-blocks before the end of a slice at which the next ticket is taken
 constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
 
 // Device status codes (match mlp_status).
@@ -40,14 +47,20 @@ constexpr uint32_t kStatusBadTile = 7;
 
 struct StageParams {
     int32_t M, K, N;
-    int32_t BN;            // tile width (32, 64, 128, 256)
+    int32_t BN;             // tile width (32, 64, 128, 256)
     int32_t tiles_m, tiles_n;
     int32_t k_blocks;
-    int32_t b_swz;         // bytes of one B swizzle row: 128 (BN >= 64) or 64 (BN = 32)
-    __nv_bfloat16 *out;    // M x N row-major
+    int32_t b_swz;          // bytes of one B swizzle row: 128 (BN >= 64) or 64 (BN = 32)
+    __nv_bfloat16 *out;     // M x N row-major
     const __nv_bfloat16 *residual;  // M x N (the chain input) or null
     int32_t gelu;
-    int32_t b_kmajor;      // 1: weights stored N x K, B tile is K-major (one box of BN rows)
+    int32_t b_kmajor;       // 1: weights stored N x K, B tile is K-major (one box of BN rows)
+    int32_t split;          // S: CTAs sharing one tile along k (divides the cluster size)
+    int32_t kb_per_split;   // k blocks of each slice (the last one may get fewer)
+    int32_t tiles_per_item; // cluster size / S
+    int32_t items;          // cluster items of this stage
+    float *partials;        // split-K: one 128 x BN fp32 buffer per CTA ([chunk][row][32])
+    int32_t pad_;
 };
 
 // Stage boundary s -> s+1.  The scoreboard holds one counter per group of consumer tiles with
@@ -67,6 +80,7 @@ struct EventRec {
     int32_t stage, tile, smid, cta;
     uint64_t t_start, t_end;
     uint32_t seq_start, seq_end;
+    uint64_t t_acc;   // accumulator complete (split tiles: the split-0 slice)
 };
 
 struct ChainParams {
@@ -78,7 +92,9 @@ struct ChainParams {
     int32_t pipelined;
     int32_t first_stage;                 // non-pipelined launches run this single stage
     int32_t m_tile_begin, m_tile_end;    // ... over these row tiles
-    int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket of each stage
+    int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
+    int32_t tile_base[kMaxStages + 1];   // first event-log record of each stage
+    int32_t cs;                          // cluster size
     int32_t raster_group;
     int32_t num_pipe;                    // shared-memory ring depth
     uint32_t stage_bytes;                // bytes of one ring slot (A + B)
@@ -86,6 +102,7 @@ struct ChainParams {
     int32_t acc_stride;                  // TMEM columns between the two accumulator buffers
     int32_t acc_split;                   // 1, or 2: k16 steps alternate between two sub-accumulators
     int32_t sub_stride;                  // TMEM columns between the sub-accumulators of a buffer
+    int32_t partial_floats;              // floats per CTA partial buffer (128 x max tile width)
     int32_t drop_tile;                   // fault injection (-1: off)
     uint64_t timeout_ns;
     uint32_t *ticket;
@@ -103,16 +120,25 @@ struct __align__(8) Ctrl {
     uint64_t drain;
     uint64_t epi_sync;
     uint64_t want_next;   // TMA -> scheduler: take the next ticket now
-    int32_t item_stage[kSchedDepth], item_tile[kSchedDepth];
+    uint64_t red_bar;     // split-K: every sibling's partial is written
+    uint64_t done_bar;    // split-K: every sibling has read the partials and stored its slice
+    int32_t item_stage[kSchedDepth], item_tile[kSchedDepth], item_split[kSchedDepth];
     uint32_t tmem_base;
     volatile int32_t abort_flag;
     int32_t skip;
     uint32_t epoch;
 };
 
-__host__ __device__ inline uint32_t ctrl_offset(int num_pipe, uint32_t stage_bytes)
+constexpr uint32_t kEpiStageBytes = 32 * 64;   // per epilogue warp: 32 rows x 32 bf16 columns
+
+__host__ __device__ inline uint32_t staging_offset(int num_pipe, uint32_t stage_bytes)
 {
     return static_cast<uint32_t>(num_pipe) * stage_bytes;
+}
+
+__host__ __device__ inline uint32_t ctrl_offset(int num_pipe, uint32_t stage_bytes)
+{
+    return staging_offset(num_pipe, stage_bytes) + 4 * kEpiStageBytes;
 }
 
 __host__ inline size_t chain_smem_bytes(int num_pipe, uint32_t stage_bytes)
@@ -124,16 +150,18 @@ __host__ inline size_t chain_smem_bytes(int num_pipe, uint32_t stage_bytes)
 // Every wait has a deadline.  On expiry the waiter records kStatusTimeout (first error wins)
 // and raises the CTA's abort flag so the other roles stop too.  Returns false on abort.
 // Drain waits (after an abort, for this CTA's own copies and MMAs in flight) ignore the abort
-// flag and use a short fixed limit.
+// flag and use a short fixed limit.  Waits on phases completed by other CTAs of the cluster
+// acquire at cluster scope.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctrl *c, const ChainParams &p,
-                                         bool honor_abort = true)
+                                         bool honor_abort = true, bool cluster_scope = false)
 {
-    if (mbar_try_wait(bar, parity))
+    auto probe = [&]() { return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (probe())
         return true;
     const uint64_t t0 = globaltimer_ns();
     const uint64_t limit = honor_abort ? 2 * p.timeout_ns + 1000000000ull : 200000000ull;
     while (true) {
-        if (mbar_try_wait(bar, parity))
+        if (probe())
             return true;
         if (honor_abort && c->abort_flag)
             return false;
@@ -146,11 +174,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Ctrl *c
 }
 
 // Warp-collective wait: lane 0 waits, the result is broadcast so the warp stays converged.
-__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Ctrl *c, const ChainParams &p)
+__device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Ctrl *c, const ChainParams &p,
+                                              bool cluster_scope = false)
 {
     uint32_t ok = 0;
     if ((threadIdx.x & 31) == 0)
-        ok = wait_bar(bar, parity, c, p) ? 1u : 0u;
+        ok = wait_bar(bar, parity, c, p, true, cluster_scope) ? 1u : 0u;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     return ok != 0;
 }
@@ -162,32 +191,50 @@ __device__ __forceinline__ float gelu_tanh_f32(float x)
     return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
 }
 
+// Arrive on the same mbarrier in CTA `rank` of this cluster, `count` times.
+__device__ __forceinline__ void arrive_rank(uint64_t *bar, uint32_t rank, uint32_t count)
+{
+    const uint32_t a = map_to_rank(bar, rank);
+    if (count == 1)
+        mbar_arrive_cluster(a);
+    else
+        asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(a), "r"(count)
+                     : "memory");
+}
+
 // ------------------------------------------------------------------------------ scheduler --
+// Rank 0 of each cluster: obtain the next cluster item and broadcast it.
 __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
 {
     const int32_t total = p.pipelined ? p.stage_base[p.num_stages] : 0;
+    const int32_t cs = p.cs;
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
         const uint32_t ph = (it / kSchedDepth) & 1;
-        if (!wait_bar(&c->sempty[slot], ph ^ 1, c, p))
+        if (!wait_bar(&c->sempty[slot], ph ^ 1, c, p, true, true))
             return;
-        // Take tickets just in time: a ticket taken early would sit in this CTA while other
-        // CTAs idle, so wait until the TMA warp is about to finish its current tile.
+        // Take tickets just in time: a ticket taken early would sit in this cluster while
+        // others idle, so wait until the TMA warp is about to finish its current slice.
         if (it > 0 && !wait_bar(&c->want_next, (it - 1) & 1, c, p))
             return;
-        int32_t stage = -1, tile = 0;
+        int32_t stage = -1, ntiles = 0;
+        int32_t tiles[kMaxCluster];
         if (p.pipelined) {
             const int32_t t = static_cast<int32_t>(atom_add_relaxed_gpu(p.ticket, 1u));
             if (t < total) {
-                int32_t s = 0;
-                s = stage_of_ticket(p.stage_base, t);
-                const int32_t local = t - p.stage_base[s];
-                if (s == 0) {
-                    tile = raster_tile(local, p.st[0].tiles_m, p.st[0].tiles_n, p.raster_group);
-                    stage = 0;
-                } else {
-                    // Consumer prologue: poll queue slot `local` until this run's entry lands.
-                    const unsigned long long *q = p.bd[s - 1].queue + local;
+                const int32_t s = stage_of_ticket(p.stage_base, t);
+                const StageParams &sp = p.st[s];
+                const int32_t ntile_stage = sp.tiles_m * sp.tiles_n;
+                const int32_t first = (t - p.stage_base[s]) * sp.tiles_per_item;
+                ntiles = min(sp.tiles_per_item, ntile_stage - first);
+                bool ok = true;
+                for (int32_t j = 0; j < ntiles && ok; ++j) {
+                    if (s == 0) {
+                        tiles[j] = raster_tile(first + j, sp.tiles_m, sp.tiles_n, p.raster_group);
+                        continue;
+                    }
+                    // Consumer prologue: poll queue slot first+j until this run's entry lands.
+                    const unsigned long long *q = p.bd[s - 1].queue + first + j;
                     uint64_t v = ld_acquire_gpu_u64(q);
                     if (!queue_entry_ready(v, c->epoch)) {
                         const uint64_t t0 = globaltimer_ns();
@@ -199,57 +246,90 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
                             if (queue_entry_ready(v, c->epoch))
                                 break;
                             if (ld_relaxed_gpu_u32(p.status) != 0 || c->abort_flag) {
-                                v = 0;
+                                ok = false;
                                 break;
                             }
                             if (globaltimer_ns() - t0 > p.timeout_ns) {
                                 atomicCAS(p.status, 0u, kStatusTimeout);
-                                v = 0;
+                                ok = false;
                                 break;
                             }
                         }
                     }
-                    if (queue_entry_ready(v, c->epoch)) {
-                        tile = queue_entry_tile(v);
-                        if (tile < 0 || tile >= p.st[s].tiles_m * p.st[s].tiles_n) {
-                            atomicCAS(p.status, 0u, kStatusBadTile);
-                        } else {
-                            stage = s;
-                            // Later TMA (async proxy) reads of the producers' output must not
-                            // be ordered before this acquire.
-                            fence_proxy_async_global();
+                    if (!ok)
+                        break;
+                    tiles[j] = queue_entry_tile(v);
+                    if (tiles[j] < 0 || tiles[j] >= ntile_stage) {
+                        atomicCAS(p.status, 0u, kStatusBadTile);
+                        ok = false;
+                    }
+                }
+                if (ok) {
+                    stage = s;
+                    // Later TMA (async proxy) reads of the producers' output must not be
+                    // ordered before the acquires above.
+                    if (s > 0)
+                        fence_proxy_async_global();
+                    if (p.events) {
+                        for (int32_t j = 0; j < ntiles; ++j) {
+                            EventRec *e = p.events + p.tile_base[s] + tiles[j];
+                            e->stage = s;
+                            e->tile = tiles[j];
+                            e->smid = static_cast<int32_t>(smid());
+                            e->cta = static_cast<int32_t>(blockIdx.x);
+                            e->seq_start = atom_add_relaxed_gpu(p.seq, 1u);
+                            e->t_start = globaltimer_ns();
                         }
                     }
                 }
-                if (stage >= 0 && p.events) {
-                    EventRec *e = p.events + p.stage_base[stage] + tile;
-                    e->stage = stage;
-                    e->tile = tile;
-                    e->smid = static_cast<int32_t>(smid());
-                    e->cta = static_cast<int32_t>(blockIdx.x);
-                    e->seq_start = atom_add_relaxed_gpu(p.seq, 1u);
-                    e->t_start = globaltimer_ns();
-                }
             }
         } else {
-            const int32_t tn = p.st[p.first_stage].tiles_n;
-            const int32_t n_local = (p.m_tile_end - p.m_tile_begin) * tn;
-            const int32_t local = static_cast<int32_t>(blockIdx.x) + it * static_cast<int32_t>(gridDim.x);
-            if (local < n_local) {
+            const StageParams &sp = p.st[p.first_stage];
+            const int32_t n_local = (p.m_tile_end - p.m_tile_begin) * sp.tiles_n;
+            const int32_t item = static_cast<int32_t>(cluster_id_x()) + it * static_cast<int32_t>(num_clusters_x());
+            const int32_t first = item * sp.tiles_per_item;
+            if (first < n_local) {
                 stage = p.first_stage;
-                tile = p.m_tile_begin * tn + local;
+                ntiles = min(sp.tiles_per_item, n_local - first);
+                for (int32_t j = 0; j < ntiles; ++j)
+                    tiles[j] = p.m_tile_begin * sp.tiles_n + first + j;
             }
         }
-        c->item_stage[slot] = stage;
-        c->item_tile[slot] = tile;
-        mbar_arrive(&c->sfull[slot]);
+        // Broadcast: rank r gets tile r / S of the item (or none) and k-slice r % S.
+        const int32_t S = stage >= 0 ? p.st[stage].split : 1;
+        for (int32_t r = 0; r < cs; ++r) {
+            const int32_t j = r / S;
+            const int32_t tile = (stage >= 0 && j < ntiles) ? tiles[j] : -1;
+            st_cluster_s32(map_to_rank(&c->item_stage[slot], r), stage);
+            st_cluster_s32(map_to_rank(&c->item_tile[slot], r), tile);
+            st_cluster_s32(map_to_rank(&c->item_split[slot], r), r % S);
+            arrive_rank(&c->sfull[slot], r, 1);
+        }
         if (stage < 0)
             return;
     }
 }
 
+// Read the item of ring slot `slot` (after its sfull wait) and release the slot to rank 0.
+struct Item {
+    int32_t stage, tile, split;
+};
+
+__device__ __forceinline__ Item take_item(Ctrl *c, int32_t slot)
+{
+    Item it{c->item_stage[slot], c->item_tile[slot], c->item_split[slot]};
+    arrive_rank(&c->sempty[slot], 0, 1);
+    return it;
+}
+
+__device__ __forceinline__ void slice_range(const StageParams &sp, int32_t split, int32_t &kb0, int32_t &kb1)
+{
+    kb0 = split * sp.kb_per_split;
+    kb1 = min(sp.k_blocks, kb0 + sp.kb_per_split);
+}
+
 // ---------------------------------------------------------------------------- TMA producer --
-__device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t *ring)
+__device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t *ring, bool leader)
 {
     const uint64_t pol_act = policy_evict_last();    // activations are re-read by many tiles
     const uint64_t pol_w = policy_evict_first();     // each weight tile is read by one row panel
@@ -260,26 +340,29 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         fills[i] = 0;
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
-        if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p))
+        if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true, true))
             break;
-        const int32_t s = c->item_stage[slot];
-        const int32_t tile = c->item_tile[slot];
-        mbar_arrive(&c->sempty[slot]);
-        if (s < 0)
+        const Item item = take_item(c, slot);
+        if (item.stage < 0)
             break;
+        if (item.tile < 0)
+            continue;
+        const int32_t s = item.stage;
         if (s > 0)
             fence_proxy_async_global();
         const StageParams &sp = p.st[s];
-        const int32_t m0 = (tile / sp.tiles_n) * kBM;
-        const int32_t n0 = (tile % sp.tiles_n) * sp.BN;
+        const int32_t m0 = (item.tile / sp.tiles_n) * kBM;
+        const int32_t n0 = (item.tile % sp.tiles_n) * sp.BN;
         const int32_t box_cols = sp.b_swz / 2;
         const uint32_t box_bytes = kBK * sp.b_swz;
         const int32_t nbox = sp.BN / box_cols;
         const uint32_t bytes = kABytes + static_cast<uint32_t>(kBK * sp.BN * 2);
-        const int32_t lead_kb = sp.k_blocks > kTicketLead ? sp.k_blocks - kTicketLead : 0;
+        int32_t kb0, kb1;
+        slice_range(sp, item.split, kb0, kb1);
+        const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
         bool ok = true;
-        for (int32_t kb = 0; kb < sp.k_blocks; ++kb) {
-            if (kb == lead_kb)
+        for (int32_t kb = kb0; kb < kb1; ++kb) {
+            if (leader && kb == lead_kb)
                 mbar_arrive(&c->want_next);
             if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
                 ok = false;
@@ -321,13 +404,14 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
     bool issued = false;
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
-        if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p))
+        if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true, true))
             break;
-        const int32_t s = c->item_stage[slot];
-        mbar_arrive(&c->sempty[slot]);
-        if (s < 0)
+        const Item item = take_item(c, slot);
+        if (item.stage < 0)
             break;
-        const StageParams &sp = p.st[s];
+        if (item.tile < 0)
+            continue;
+        const StageParams &sp = p.st[item.stage];
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
         if (!wait_bar(&c->tempty[acc], acc_ph ^ 1, c, p))
@@ -338,8 +422,10 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         const uint32_t b_swz = static_cast<uint32_t>(sp.b_swz);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
         const bool split2 = p.acc_split == 2;
+        int32_t kb0, kb1;
+        slice_range(sp, item.split, kb0, kb1);
         bool ok = true;
-        for (int32_t kb = 0; kb < sp.k_blocks; ++kb) {
+        for (int32_t kb = kb0; kb < kb1; ++kb) {
             // TMA fills and tcgen05.mma reads are both async-proxy operations ordered by the
             // mbarrier's transaction count: no tcgen05 fence is needed per k block.
             if (!wait_bar(&c->full[ps], pph, c, p)) {
@@ -352,14 +438,15 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
                 // A: K-major, 128B swizzle; a 16-wide k step is 32 bytes along the row.
                 const uint64_t ad = smem_desc(a_addr + kk * 32u, 16u, 1024u, 2u);
-                // B: MN-major; a 16-deep k step is 16 rows of b_swz bytes.  LBO: next block of
-                // b_swz/2 columns (one TMA box of 64 rows); SBO: next group of 8 rows.
+                // B stored K x N: MN-major; a 16-deep k step is 16 rows of b_swz bytes.  LBO: next
+                // block of b_swz/2 columns (one TMA box of 64 rows); SBO: next group of 8 rows.
                 // B stored N x K: K-major like A, BN rows of 128 bytes.
                 const uint64_t bd = sp.b_kmajor
                                         ? smem_desc(b_addr + kk * 32u, 16u, 1024u, 2u)
                                         : smem_desc(b_addr + kk * 16u * b_swz, kBK * b_swz, 8u * b_swz, b_code);
-                // k step j goes to sub-accumulator j % acc_split; its first step overwrites.
-                const uint32_t j = static_cast<uint32_t>(kb) * (kBK / 16) + kk;
+                // k step j of the slice goes to sub-accumulator j % acc_split; its first step
+                // overwrites.
+                const uint32_t j = static_cast<uint32_t>(kb - kb0) * (kBK / 16) + kk;
                 const uint32_t sub = split2 ? (j & 1u) : 0u;
                 mma_bf16_ss(d_tmem + sub * static_cast<uint32_t>(p.sub_stride), ad, bd, idesc,
                             j >= (split2 ? 2u : 1u) ? 1u : 0u);
@@ -383,152 +470,297 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
 }
 
 // -------------------------------------------------------------------------------- epilogue --
-__device__ __forceinline__ void store_chunk(const StageParams &sp, int32_t m, int32_t n, const uint32_t (&r)[32])
+// Byte offset of 16-byte segment `seg` (0..3) of row `row` (0..31) in a warp's staging buffer;
+// the XOR keeps the eight rows a quarter-warp touches on distinct banks.
+__device__ __forceinline__ uint32_t stage_off(int row, int seg)
 {
-    if (m >= sp.M)
-        return;
-    const __nv_bfloat16 *res = sp.residual ? sp.residual + static_cast<size_t>(m) * sp.N + n : nullptr;
-    __nv_bfloat16 *dst = sp.out + static_cast<size_t>(m) * sp.N + n;
+    return static_cast<uint32_t>(row * 64 + ((seg ^ ((row >> 1) & 3)) * 16));
+}
+
+// One warp stores a 32-row x 32-column chunk of the output.  Lane l holds the fp32 values of
+// row row0 + l (TMEM hands each thread one row); the chunk goes through the warp's staging
+// buffer so that global stores and residual loads touch whole 64-byte row segments.
+__device__ __forceinline__ void store_chunk_warp(const StageParams &sp, int32_t row0, int32_t n, const uint32_t (&r)[32],
+                                                 uint8_t *stage, int32_t lane)
+{
+    float v[32];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (n + 8 * j >= sp.N)
-            break;
-        float v[8];
+    for (int e = 0; e < 32; ++e) {
+        v[e] = __uint_as_float(r[e]);
+        if (sp.gelu)
+            v[e] = gelu_tanh_f32(v[e]);
+    }
+    if (sp.residual) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            v[e] = __uint_as_float(r[8 * j + e]);
-            if (sp.gelu)
-                v[e] = gelu_tanh_f32(v[e]);
+        for (int it = 0; it < 4; ++it) {
+            const int rr = it * 8 + (lane >> 2), sg = lane & 3;
+            const int32_t gm = row0 + rr, gn = n + sg * 8;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (gm < sp.M && gn < sp.N)
+                x = *reinterpret_cast<const uint4 *>(sp.residual + static_cast<size_t>(gm) * sp.N + gn);
+            *reinterpret_cast<uint4 *>(stage + stage_off(rr, sg)) = x;
         }
-        if (res) {
-            const uint4 rv = *reinterpret_cast<const uint4 *>(res + 8 * j);
-            const __nv_bfloat162 *rb = reinterpret_cast<const __nv_bfloat162 *>(&rv);
+        __syncwarp();
+#pragma unroll
+        for (int sg = 0; sg < 4; ++sg) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(stage + stage_off(lane, sg));
+            const __nv_bfloat162 *xb = reinterpret_cast<const __nv_bfloat162 *>(&x);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(rb[e]);
-                v[2 * e] += f.x;
-                v[2 * e + 1] += f.y;
+                const float2 f = __bfloat1622float2(xb[e]);
+                v[sg * 8 + 2 * e] += f.x;
+                v[sg * 8 + 2 * e + 1] += f.y;
             }
         }
+        __syncwarp();
+    }
+#pragma unroll
+    for (int sg = 0; sg < 4; ++sg) {
         uint4 o;
         __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            ob[e] = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-        *reinterpret_cast<uint4 *>(dst + 8 * j) = o;
+            ob[e] = __floats2bfloat162_rn(v[sg * 8 + 2 * e], v[sg * 8 + 2 * e + 1]);
+        *reinterpret_cast<uint4 *>(stage + stage_off(lane, sg)) = o;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rr = it * 8 + (lane >> 2), sg = lane & 3;
+        const int32_t gm = row0 + rr, gn = n + sg * 8;
+        if (gm < sp.M && gn < sp.N)   // N is a multiple of 8: a segment is all in or all out
+            *reinterpret_cast<uint4 *>(sp.out + static_cast<size_t>(gm) * sp.N + gn) =
+                *reinterpret_cast<const uint4 *>(stage + stage_off(rr, sg));
+    }
+    __syncwarp();
+}
+
+// 32 accumulator columns of this thread's TMEM lane (sub-accumulators summed, even + odd).
+__device__ __forceinline__ void load_acc(const ChainParams &p, uint32_t taddr, uint32_t (&r)[32])
+{
+    tmem_ld_32x32b_x32(taddr, r);
+    if (p.acc_split == 2) {
+        uint32_t r2[32];
+        tmem_ld_32x32b_x32(taddr + p.sub_stride, r2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+    } else {
+        tmem_ld_wait();
     }
 }
 
-__device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uint32_t tmem_base)
+// Producer side of the protocol for a finished tile: decrement every group counter the tile
+// feeds; the decrement that reaches zero re-arms the counter and publishes the group's members
+// on the work-queue.  Called by one whole warp after the tile's stores were released.
+__device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, int32_t lane)
+{
+    const BoundaryParams &bd = p.bd[s];
+    const int32_t e0 = bd.pg_off[tile], e1 = bd.pg_off[tile + 1];
+    for (int32_t eb = e0; eb < e1; eb += 32) {
+        const int32_t e = eb + lane;
+        int32_t g = -1;
+        bool fire = false;
+        if (e < e1) {
+            g = bd.pg_tgt[e];
+            fence_acq_rel_gpu();
+            const uint32_t old = atom_add_acq_rel_gpu(bd.count + g, 0xffffffffu);
+            fire = (old == 1u);
+            if (fire)   // re-arm for the next run; no producer touches it again
+                bd.count[g] = static_cast<uint32_t>(bd.grp_init[g]);
+        }
+        // Every group this warp completed is published by the whole warp: the lane whose
+        // acq_rel decrement reached zero acquired every earlier producer's release; __syncwarp
+        // orders that before each lane's release fence, which makes its relaxed queue stores
+        // carry the release.
+        uint32_t todo = __ballot_sync(0xffffffffu, fire);
+        while (todo) {
+            const int32_t src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const int32_t gg = __shfl_sync(0xffffffffu, g, src);
+            const int32_t m0 = bd.grp_off[gg], n = bd.grp_off[gg + 1] - m0;
+            uint32_t q0 = 0;
+            if (lane == src)
+                q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(n));
+            q0 = __shfl_sync(0xffffffffu, q0, src);
+            __syncwarp();
+            fence_acq_rel_gpu();
+            for (int32_t i = lane; i < n; i += 32)
+                st_relaxed_gpu_u64(bd.queue + q0 + i, queue_entry(c->epoch, bd.grp_mem[m0 + i]));
+        }
+    }
+}
+
+__device__ __forceinline__ void log_end(const ChainParams &p, int32_t s, int32_t tile)
+{
+    EventRec *e = p.events + p.tile_base[s] + tile;
+    e->seq_end = atom_add_relaxed_gpu(p.seq, 1u);
+    e->t_end = globaltimer_ns();
+}
+
+__device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uint32_t tmem_base, uint32_t rank,
+                                              uint8_t *staging)
 {
     const int32_t warp = threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     const int32_t quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
     const int32_t row = quad * 32 + lane;
+    uint8_t *stage = staging + quad * kEpiStageBytes;
     uint32_t local_tiles = 0;
     uint32_t epi_phase = 0;
+    uint32_t nsplit = 0;                        // split-K tiles this CTA took part in
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
-        if (!warp_wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p))
+        if (!warp_wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true))
             break;
-        int32_t s = 0, tile = 0;
-        if (lane == 0) {
-            s = c->item_stage[slot];
-            tile = c->item_tile[slot];
-            mbar_arrive(&c->sempty[slot]);
-        }
-        s = __shfl_sync(0xffffffffu, s, 0);
-        tile = __shfl_sync(0xffffffffu, tile, 0);
-        if (s < 0)
+        Item item{0, 0, 0};
+        if (lane == 0)
+            item = take_item(c, slot);
+        item.stage = __shfl_sync(0xffffffffu, item.stage, 0);
+        item.tile = __shfl_sync(0xffffffffu, item.tile, 0);
+        item.split = __shfl_sync(0xffffffffu, item.split, 0);
+        if (item.stage < 0)
             break;
+        if (item.tile < 0)
+            continue;
+        const int32_t s = item.stage, tile = item.tile;
         const StageParams &sp = p.st[s];
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
         if (!warp_wait_bar(&c->tfull[acc], acc_ph, c, p))
             break;
         tc_fence_after();
-        const int32_t m = (tile / sp.tiles_n) * kBM + row;
+        if (p.events && warp == 4 && lane == 0 && item.split == 0)
+            p.events[p.tile_base[s] + tile].t_acc = globaltimer_ns();
+        const int32_t row0 = (tile / sp.tiles_n) * kBM + quad * 32;   // this warp's first row
         const int32_t n0 = (tile % sp.tiles_n) * sp.BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * p.acc_stride;
+        const bool producer = p.pipelined && s + 1 < p.num_stages;
+
+        if (sp.split == 1) {
+            for (int32_t c0 = 0; c0 < sp.BN; c0 += 32) {
+                uint32_t r[32];
+                load_acc(p, taddr + c0, r);
+                store_chunk_warp(sp, row0, n0 + c0, r, stage, lane);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c->tempty[acc]);   // the MMA warp may reuse this accumulator
+            ++local_tiles;
+            if (producer || (p.pipelined && p.events)) {
+                // Injected epilogue: every thread orders its stores, the four warps meet (a
+                // bounded mbarrier rather than bar.sync, so an aborting warp cannot strand the
+                // others), then one warp releases and decrements the scoreboard.
+                fence_acq_rel_gpu();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&c->epi_sync);
+                if (!warp_wait_bar(&c->epi_sync, epi_phase, c, p))
+                    break;
+                epi_phase ^= 1;
+                if (warp == 4) {
+                    if (lane == 0 && p.events)
+                        log_end(p, s, tile);
+                    __syncwarp();
+                    if (producer && !(s == 0 && tile == p.drop_tile))
+                        release_tile(p, c, s, tile, lane);
+                }
+            }
+            continue;
+        }
+
+        // ---- split-K tile: S siblings (ranks g0 .. g0+S-1) each hold a k-slice partial ----
+        const int32_t S = sp.split;
+        const uint32_t g0 = rank - static_cast<uint32_t>(item.split);      // first sibling
+        const uint32_t weight = static_cast<uint32_t>(p.cs / S);           // arrivals per sibling warp
+        const size_t cbase = static_cast<size_t>(cluster_id_x()) * p.cs;
+        // Partial layout: [BN/32 chunks][8 vectors][128 rows][4 floats]: for a fixed vector the
+        // warp's 32 lanes (rows) touch 512 contiguous bytes, so stores and loads coalesce.
+        float *mine = sp.partials + (cbase + rank) * p.partial_floats;
+        // my previous partial must have been read by every sibling of that tile
+        if (nsplit > 0 && !warp_wait_bar(&c->done_bar, (nsplit - 1) & 1, c, p, true))
+            break;
         for (int32_t c0 = 0; c0 < sp.BN; c0 += 32) {
             uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + c0, r);
-            if (p.acc_split == 2) {
-                uint32_t r2[32];
-                tmem_ld_32x32b_x32(taddr + p.sub_stride + c0, r2);
-                tmem_ld_wait();
+            load_acc(p, taddr + c0, r);
+            float4 *dst = reinterpret_cast<float4 *>(mine) + (c0 / 32) * 8 * kBM + row;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)   // even k steps + odd k steps, in that order
-                    r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
-            } else {
-                tmem_ld_wait();
-            }
-            store_chunk(sp, m, n0 + c0, r);
+            for (int v = 0; v < 8; ++v)
+                dst[v * kBM] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                           __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(&c->tempty[acc]);   // the MMA warp may reuse this accumulator
+            mbar_arrive(&c->tempty[acc]);
         ++local_tiles;
-
-        const bool producer = p.pipelined && s + 1 < p.num_stages;
-        if (producer || (p.pipelined && p.events)) {
-            // Injected epilogue: every thread orders its stores, the four warps meet (a bounded
-            // mbarrier rather than bar.sync, so an aborting warp cannot strand the others), then
-            // one warp releases and decrements the scoreboard.
-            fence_acq_rel_gpu();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&c->epi_sync);
-            if (!warp_wait_bar(&c->epi_sync, epi_phase, c, p))
-                break;
-            epi_phase ^= 1;
-            if (warp == 4) {
-                if (lane == 0 && p.events) {
-                    EventRec *e = p.events + p.stage_base[s] + tile;
-                    e->seq_end = atom_add_relaxed_gpu(p.seq, 1u);
-                    e->t_end = globaltimer_ns();
-                }
-                __syncwarp();
-                const bool dropped = (s == 0 && tile == p.drop_tile);
-                if (producer && !dropped) {
-                    const BoundaryParams &bd = p.bd[s];
-                    const int32_t e0 = bd.pg_off[tile], e1 = bd.pg_off[tile + 1];
-                    for (int32_t eb = e0; eb < e1; eb += 32) {
-                        const int32_t e = eb + lane;
-                        int32_t g = -1;
-                        bool fire = false;
-                        if (e < e1) {
-                            g = bd.pg_tgt[e];
-                            fence_acq_rel_gpu();
-                            const uint32_t old = atom_add_acq_rel_gpu(bd.count + g, 0xffffffffu);
-                            fire = (old == 1u);
-                            if (fire)   // re-arm for the next run; no producer touches it again
-                                bd.count[g] = static_cast<uint32_t>(bd.grp_init[g]);
-                        }
-                        // Every group this warp completed is published by the whole warp: the
-                        // lane whose acq_rel decrement reached zero acquired every earlier
-                        // producer's release; __syncwarp orders that before each lane's release
-                        // fence, which makes its relaxed queue stores carry the release.
-                        uint32_t todo = __ballot_sync(0xffffffffu, fire);
-                        while (todo) {
-                            const int32_t src = __ffs(todo) - 1;
-                            todo &= todo - 1;
-                            const int32_t gg = __shfl_sync(0xffffffffu, g, src);
-                            const int32_t m0 = bd.grp_off[gg], n = bd.grp_off[gg + 1] - m0;
-                            uint32_t q0 = 0;
-                            if (lane == src)
-                                q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(n));
-                            q0 = __shfl_sync(0xffffffffu, q0, src);
-                            __syncwarp();
-                            fence_acq_rel_gpu();
-                            for (int32_t i = lane; i < n; i += 32)
-                                st_relaxed_gpu_u64(bd.queue + q0 + i, queue_entry(c->epoch, bd.grp_mem[m0 + i]));
+        fence_acq_rel_cluster();
+        __syncwarp();
+        if (lane == 0)
+            for (int32_t q = 0; q < S; ++q)
+                arrive_rank(&c->red_bar, g0 + q, weight);
+        if (!warp_wait_bar(&c->red_bar, nsplit & 1, c, p, true))
+            break;
+        // Reduce my column slice over the S partials in rank order, then the epilogue.  Loads of
+        // up to four partials are issued before any of them is added.
+        const int32_t slice = sp.BN / S;
+        const int32_t col0 = item.split * slice;
+        for (int32_t c0 = col0; c0 < col0 + slice; c0 += 32) {
+            float acc_v[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                acc_v[e] = 0.0f;
+            const size_t off = static_cast<size_t>((c0 / 32) * 8 * kBM + row);   // in float4
+            for (int32_t qb = 0; qb < S; qb += 4) {
+                float4 v[4][8];
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    if (qb + qq < S) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                                                sp.partials + (cbase + g0 + qb + qq) * p.partial_floats) + off;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            v[qq][i] = __ldcg(src + i * kBM);
+                    }
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    if (qb + qq < S) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            acc_v[4 * i] += v[qq][i].x;
+                            acc_v[4 * i + 1] += v[qq][i].y;
+                            acc_v[4 * i + 2] += v[qq][i].z;
+                            acc_v[4 * i + 3] += v[qq][i].w;
                         }
                     }
-                }
+            }
+            uint32_t r[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                r[e] = __float_as_uint(acc_v[e]);
+            store_chunk_warp(sp, row0, n0 + c0, r, stage, lane);
+        }
+        fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
+        __syncwarp();
+        if (lane == 0)
+            for (int32_t q = 0; q < S; ++q)
+                arrive_rank(&c->done_bar, g0 + q, weight);
+        if (item.split == 0 && (producer || (p.pipelined && p.events))) {
+            // the tile is complete once every sibling stored its slice
+            if (!warp_wait_bar(&c->done_bar, nsplit & 1, c, p, true))
+                break;
+            if (warp == 4) {
+                fence_acq_rel_gpu();
+                if (lane == 0 && p.events)
+                    log_end(p, s, tile);
+                __syncwarp();
+                if (producer && !(s == 0 && tile == p.drop_tile))
+                    release_tile(p, c, s, tile, lane);
             }
         }
+        ++nsplit;
     }
 }
 
@@ -541,6 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     Ctrl *c = reinterpret_cast<Ctrl *>(ring + ctrl_offset(p.num_pipe, p.stage_bytes));
     const int32_t warp = threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.num_pipe; ++i) {
@@ -553,11 +786,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
         for (int i = 0; i < kSchedDepth; ++i) {
             mbar_init(&c->sfull[i], 1);
-            mbar_init(&c->sempty[i], 6);   // TMA + MMA + 4 epilogue warps
+            mbar_init(&c->sempty[i], 6 * p.cs);   // TMA + MMA + 4 epilogue warps of every rank
         }
         mbar_init(&c->drain, 1);
         mbar_init(&c->epi_sync, 4);
         mbar_init(&c->want_next, 1);
+        mbar_init(&c->red_bar, 4 * p.cs);          // 4 warps x S siblings, each arriving cs/S times
+        mbar_init(&c->done_bar, 4 * p.cs);
         c->abort_flag = 0;
         c->skip = ld_relaxed_gpu_u32(p.status) != 0;   // sticky error: do nothing
         c->epoch = p.pipelined ? ld_relaxed_gpu_u32(p.epoch) : 0u;
@@ -572,23 +807,23 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();   // every barrier of the cluster is initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = c->tmem_base;
 
     if (!c->skip) {
         if (warp == 0) {
             if (lane == 0)
-                role_tma(p, c, ring);
+                role_tma(p, c, ring, rank == 0);
         } else if (warp == 1) {
             if (lane == 0)
                 role_mma(p, c, ring, tmem_base);
             __syncwarp();
         } else if (warp == 2) {
-            if (lane == 0)
+            if (lane == 0 && rank == 0)
                 role_scheduler(p, c);
         } else if (warp >= 4) {
-            role_epilogue(p, c, tmem_base);
+            role_epilogue(p, c, tmem_base, rank, ring + staging_offset(p.num_pipe, p.stage_bytes));
         }
     }
     tc_fence_before();
@@ -612,6 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             fence_acq_rel_gpu();
         }
     }
+    cluster_sync_all();   // no CTA leaves while a peer may still write to its shared memory
 }
 
 }  // namespace mlpc

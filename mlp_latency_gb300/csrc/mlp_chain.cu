@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -70,6 +71,10 @@ struct mlp_chain {
     int BN[MLP_MAX_GEMMS] = {}, tiles_m = 0, tiles_n[MLP_MAX_GEMMS] = {}, k_blocks[MLP_MAX_GEMMS] = {};
     int b_swz[MLP_MAX_GEMMS] = {};
     int num_pipe = 0, max_bn = 0, grid = 0, acc_split = 1;
+    int cs = 1, max_clusters = 0;
+    int split[MLP_MAX_GEMMS] = {}, kb_per_split[MLP_MAX_GEMMS] = {}, items[MLP_MAX_GEMMS] = {};
+    int32_t tile_base[MLP_MAX_GEMMS + 1] = {};
+    float *partials[MLP_MAX_GEMMS] = {};
     uint32_t stage_bytes = 0, tmem_cols = 0;
     size_t smem = 0;
     std::vector<int32_t> off[MLP_MAX_GEMMS - 1], tgt[MLP_MAX_GEMMS - 1], init[MLP_MAX_GEMMS - 1];
@@ -107,14 +112,51 @@ extern "C" const char *mlp_status_str(mlp_status s)
     return "unknown status";
 }
 
-static int default_bn(int64_t tiles_m, int64_t N, int num_sms)
+// Tile width and split-K factor of one stage, from a cost model of this kernel on one SM:
+// one tcgen05.mma (M = 128, K = 16) costs about the same for any N <= 256 (~140 cycles), a TMA
+// box row (64 or 128 bytes) costs ~1.2 ns, a split tile pays ~1.5 us for its fp32 reduction,
+// and a stage cannot beat the HBM time of its weights.  clusters[i] = co-resident clusters of
+// 2^i CTAs.  Candidates with idle k slices or reduction slices narrower than 32 columns are
+// skipped.  Returns the estimated microseconds.
+static double choose_tiles(int64_t tiles_m, int64_t K, int64_t N, const int clusters[4], int fixed_bn,
+                           int fixed_split, int *bn_out, int *split_out)
 {
-    // Largest tile width that still gives every SM a tile; else the narrowest.
-    const int cands[4] = {256, 128, 64, 32};
-    for (int bn : cands)
-        if (tiles_m * ((N + bn - 1) / bn) >= num_sms)
-            return bn;
-    return 32;
+    const int k_blocks = static_cast<int>((K + 63) / 64);
+    double best = 1e30;
+    *bn_out = 256;
+    *split_out = 1;
+    const int bns[4] = {256, 128, 64, 32};
+    for (int bn : bns) {
+        if (fixed_bn && bn != fixed_bn)
+            continue;
+        if (!fixed_bn && bn < 128 && N > bn)   // narrow tiles only to cover narrow outputs
+            continue;
+        if (!fixed_bn && bn > 32 && N <= bn / 2)
+            continue;
+        for (int li = 0; li < 4; ++li) {
+            const int S = 1 << li;
+            if (fixed_split && S != fixed_split)
+                continue;
+            const int kbps = (k_blocks + S - 1) / S;
+            if (bn / S < 32 || bn % S || (S - 1) * kbps >= k_blocks || clusters[li] < 1)
+                continue;
+            const double tiles = static_cast<double>(tiles_m) * ((N + bn - 1) / bn);
+            const double slots = static_cast<double>(clusters[li]) * S;
+            const double waves = std::ceil(tiles * S / slots);
+            const double rows = 128.0 + (bn >= 64 ? bn : 64);
+            const double t_mma = kbps * 4 * 140.0 / 1900.0;          // us
+            const double t_tma = kbps * rows * 1.2e-3;               // us
+            const double t_unit = std::max(t_mma, t_tma) + 1.0 + (S > 1 ? 1.5 : 0.0);
+            const double t_hbm = static_cast<double>(K) * N * 2 / 6.5e6;
+            const double t = std::max(waves * t_unit, t_hbm);
+            if (t < best * 0.999) {
+                best = t;
+                *bn_out = bn;
+                *split_out = S;
+            }
+        }
+    }
+    return best;
 }
 
 static mlp_status full_reset(mlp_chain *h)
@@ -202,20 +244,59 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     }
 
     h->tiles_m = static_cast<int>((d->M + mlpc::kBM - 1) / mlpc::kBM);
+    // The device maximum, so that handles with different ring depths can share the kernel.
+    if (cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
+        cudaSuccess) {
+        release(h);
+        return MLP_ERR_CUDA;
+    }
+    // Co-resident clusters of 1, 2, 4, 8 CTAs (one CTA per SM; a cluster stays within a GPC).
+    int clusters[4] = {h->num_sms, 0, 0, 0};
+    for (int li = 1; li < 4; ++li) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1u << li;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3((1u << li) * 8, 1, 1);
+        cfg.blockDim = dim3(mlpc::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem_optin);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters[li], mlpc::chain_kernel, &cfg) != cudaSuccess)
+            clusters[li] = 0;
+    }
+    cudaGetLastError();
     for (int s = 0; s < S; ++s) {
-        int bn = d->tile_n[s] ? d->tile_n[s] : default_bn(h->tiles_m, d->dims[s + 1], h->num_sms);
-        if (bn != 32 && bn != 64 && bn != 128 && bn != 256) {
+        const int tn = d->tile_n[s], ks = d->k_split[s];
+        if ((tn != 0 && tn != 32 && tn != 64 && tn != 128 && tn != 256) ||
+            (ks != 0 && ks != 1 && ks != 2 && ks != 4 && ks != 8)) {
             release(h);
-            return MLP_ERR_UNSUPPORTED;
+            return tn != 0 && tn != 32 && tn != 64 && tn != 128 && tn != 256 ? MLP_ERR_UNSUPPORTED
+                                                                             : MLP_ERR_INVALID_ARG;
+        }
+        int bn = 0, split = 0;
+        if (choose_tiles(h->tiles_m, d->dims[s], d->dims[s + 1], clusters, tn, ks, &bn, &split) >= 1e29) {
+            release(h);
+            return MLP_ERR_UNSUPPORTED;   // no valid tile / split for this request
         }
         h->BN[s] = bn;
         h->b_swz[s] = bn >= 64 ? 128 : 64;
         h->tiles_n[s] = static_cast<int>((d->dims[s + 1] + bn - 1) / bn);
         h->k_blocks[s] = static_cast<int>((d->dims[s] + mlpc::kBK - 1) / mlpc::kBK);
         h->max_bn = std::max(h->max_bn, bn);
+        h->split[s] = split;
+        h->kb_per_split[s] = (h->k_blocks[s] + split - 1) / split;
+        h->cs = std::max(h->cs, split);
+    }
+    for (int s = 0; s < S; ++s) {
+        const int tpi = h->cs / h->split[s];
+        const int tiles = h->tiles_m * h->tiles_n[s];
+        h->items[s] = (tiles + tpi - 1) / tpi;
     }
     h->stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
-    const size_t fixed = 1024 + sizeof(mlpc::Ctrl);
+    const size_t fixed = 1024 + 4 * mlpc::kEpiStageBytes + sizeof(mlpc::Ctrl);
     h->num_pipe = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - fixed) / h->stage_bytes));
     if (d->pipe_stages)
         h->num_pipe = std::min(h->num_pipe, d->pipe_stages);
@@ -233,12 +314,29 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     while (h->tmem_cols < static_cast<uint32_t>(2 * h->acc_split * h->max_bn))
         h->tmem_cols *= 2;
     h->stage_base[0] = 0;
-    for (int s = 0; s < S; ++s)
-        h->stage_base[s + 1] = h->stage_base[s] + h->tiles_m * h->tiles_n[s];
-    const int total = h->stage_base[S];
-    h->grid = d->grid_ctas ? d->grid_ctas : std::min(h->num_sms, total);
-    if (d->mode == MLP_MODE_PIPELINED && h->grid > h->num_sms) {
-        release(h);  // the pipelined grid must be co-resident (one CTA per SM)
+    h->tile_base[0] = 0;
+    for (int s = 0; s < S; ++s) {
+        h->stage_base[s + 1] = h->stage_base[s] + h->items[s];
+        h->tile_base[s + 1] = h->tile_base[s] + h->tiles_m * h->tiles_n[s];
+    }
+    const int total = h->tile_base[S];
+    const int total_items = h->stage_base[S];
+    h->max_clusters = clusters[h->cs == 1 ? 0 : h->cs == 2 ? 1 : h->cs == 4 ? 2 : 3];
+    if (h->max_clusters < 1) {
+        release(h);
+        return MLP_ERR_UNSUPPORTED;
+    }
+    if (d->grid_ctas) {
+        if (d->grid_ctas % h->cs) {
+            release(h);
+            return MLP_ERR_INVALID_ARG;
+        }
+        h->grid = d->grid_ctas;
+    } else {
+        h->grid = std::min(h->max_clusters, total_items) * h->cs;
+    }
+    if (d->mode == MLP_MODE_PIPELINED && h->grid / h->cs > h->max_clusters) {
+        release(h);  // the pipelined grid must be co-resident
         return MLP_ERR_INVALID_ARG;
     }
 
@@ -273,6 +371,12 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->n_events = static_cast<size_t>(total);
         bytes = align_up(bytes, 256) + h->n_events * sizeof(mlpc::EventRec);
     }
+    // split-K partial sums: per stage that splits, one 128 x max_bn fp32 buffer per CTA slot
+    const int cta_slots = std::max(h->grid, h->max_clusters * h->cs);
+    const size_t partial_bytes = static_cast<size_t>(cta_slots) * mlpc::kBM * h->max_bn * sizeof(float);
+    for (int s = 0; s < S; ++s)
+        if (h->split[s] > 1)
+            bytes = align_up(bytes, 256) + partial_bytes;
     if (cudaMalloc(&h->dev_block, bytes) != cudaSuccess) {
         h->dev_block = nullptr;
         release(h);
@@ -316,14 +420,15 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         o = align_up(o, 256);
         h->d_events = reinterpret_cast<mlpc::EventRec *>(p + o);
         ok = ok && cudaMemset(h->d_events, 0, h->n_events * sizeof(mlpc::EventRec)) == cudaSuccess;
+        o += h->n_events * sizeof(mlpc::EventRec);
     }
+    for (int s = 0; s < S; ++s)
+        if (h->split[s] > 1) {
+            o = align_up(o, 256);
+            h->partials[s] = reinterpret_cast<float *>(p + o);
+            o += partial_bytes;
+        }
     if (!ok || full_reset(h) != MLP_OK) {
-        release(h);
-        return MLP_ERR_CUDA;
-    }
-    // The device maximum, so that handles with different ring depths can share the kernel.
-    if (cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
-        cudaSuccess) {
         release(h);
         return MLP_ERR_CUDA;
     }
@@ -400,6 +505,11 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.k_blocks = h->k_blocks[s];
         sp.b_swz = h->b_swz[s];
         sp.b_kmajor = d.weight_layout == 1;
+        sp.split = h->split[s];
+        sp.kb_per_split = h->kb_per_split[s];
+        sp.tiles_per_item = h->cs / h->split[s];
+        sp.items = h->items[s];
+        sp.partials = h->partials[s];
         sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
         sp.gelu = d.epilogue == MLP_EPI_GELU_TANH;
         sp.residual = (d.residual && s + 1 == h->S) ? static_cast<const __nv_bfloat16 *>(X) : nullptr;
@@ -416,8 +526,12 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.bd[b].tail = h->db[b].tail;
     }
     P.num_stages = h->S;
-    for (int s = 0; s <= h->S; ++s)
+    for (int s = 0; s <= h->S; ++s) {
         P.stage_base[s] = h->stage_base[s];
+        P.tile_base[s] = h->tile_base[s];
+    }
+    P.cs = h->cs;
+    P.partial_floats = mlpc::kBM * h->max_bn;
     P.raster_group = d.raster_group;
     P.num_pipe = h->num_pipe;
     P.stage_bytes = h->stage_bytes;
@@ -444,8 +558,31 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
 
 static bool launch(const ChainParams &P, int grid, size_t smem, cudaStream_t st)
 {
-    mlpc::chain_kernel<<<grid, mlpc::kThreads, smem, st>>>(P);
-    return cudaGetLastError() == cudaSuccess;
+    if (P.cs == 1) {
+        mlpc::chain_kernel<<<grid, mlpc::kThreads, smem, st>>>(P);
+        return cudaGetLastError() == cudaSuccess;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(P.cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(mlpc::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mlpc::chain_kernel, P) == cudaSuccess && cudaGetLastError() == cudaSuccess;
+}
+
+// CTAs of a non-pipelined launch over `items` cluster items.
+static int static_grid(const mlp_chain *h, int items)
+{
+    if (h->desc.grid_ctas)
+        return h->desc.grid_ctas;
+    return std::min(h->max_clusters, std::max(items, 1)) * h->cs;
 }
 
 extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *const *W, void *Y, void *workspace,
@@ -485,9 +622,7 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
             P.first_stage = s;
             P.m_tile_begin = 0;
             P.m_tile_end = h->tiles_m;
-            const int tiles = h->tiles_m * h->tiles_n[s];
-            const int g = h->desc.grid_ctas ? h->desc.grid_ctas : std::min(h->num_sms, tiles);
-            if (!launch(P, g, h->smem, st))
+            if (!launch(P, static_grid(h, h->items[s]), h->smem, st))
                 return MLP_ERR_CUDA;
         }
         return MLP_OK;
@@ -507,8 +642,8 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
                 return MLP_ERR_CUDA;
             P.first_stage = s;
             const int tiles = (P.m_tile_end - P.m_tile_begin) * h->tiles_n[s];
-            const int g = h->desc.grid_ctas ? h->desc.grid_ctas : std::min(h->num_sms, tiles);
-            if (!launch(P, g, h->smem, ss))
+            const int tpi = h->cs / h->split[s];
+            if (!launch(P, static_grid(h, (tiles + tpi - 1) / tpi), h->smem, ss))
                 return MLP_ERR_CUDA;
             if (cudaEventRecord(h->events[static_cast<size_t>(i) * h->S + s], ss) != cudaSuccess)
                 return MLP_ERR_CUDA;
@@ -612,6 +747,9 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->launches_per_run = h->desc.mode == MLP_MODE_PIPELINED ? 1
                              : h->desc.mode == MLP_MODE_SEQUENTIAL ? h->S
                                                                    : h->S * h->n_chunks;
+    info->cluster_size = h->cs;
+    for (int s = 0; s < h->S; ++s)
+        info->k_split[s] = h->split[s];
     return MLP_OK;
 }
 
@@ -759,7 +897,10 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
 
     // Tiling: the same choices mlp_chain_create makes for this shape.
     const int tiles_m = static_cast<int>((M + mlpc::kBM - 1) / mlpc::kBM);
-    const int bn[2] = {default_bn(tiles_m, N1, nd.num_sms), default_bn(tiles_m, N2, nd.num_sms)};
+    const int no_clusters[4] = {nd.num_sms, 0, 0, 0};   // this entry point runs without clusters
+    int bn[2] = {256, 256}, unused = 1;
+    choose_tiles(tiles_m, K, N1, no_clusters, 0, 1, &bn[0], &unused);
+    choose_tiles(tiles_m, N1, N2, no_clusters, 0, 1, &bn[1], &unused);
     const int tn[2] = {static_cast<int>((N1 + bn[0] - 1) / bn[0]), static_cast<int>((N2 + bn[1] - 1) / bn[1])};
     const int P = tiles_m * tn[0], C = tiles_m * tn[1];
     const NoallocLayout L = noalloc_layout(M, N1, P, C, tiles_m);
@@ -770,8 +911,8 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     const uint32_t stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * max_bn * 2);
     int smem_optin = 0;
     cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    const int num_pipe =
-        static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - 1024 - sizeof(mlpc::Ctrl)) / stage_bytes));
+    const int num_pipe = static_cast<int>(std::min<size_t>(
+        mlpc::kMaxPipe, (smem_optin - 1024 - 4 * mlpc::kEpiStageBytes - sizeof(mlpc::Ctrl)) / stage_bytes));
     if (num_pipe < 2)
         return MLP_ERR_UNSUPPORTED;
     uint32_t tmem_cols = 32;
@@ -801,6 +942,10 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
         sp.k_blocks = static_cast<int32_t>((dims[s] + mlpc::kBK - 1) / mlpc::kBK);
         sp.b_swz = b_swz;
         sp.out = static_cast<__nv_bfloat16 *>(o_ptr[s]);
+        sp.split = 1;
+        sp.kb_per_split = sp.k_blocks;
+        sp.tiles_per_item = 1;
+        sp.items = tiles_m * tn[s];
     }
     P_.bd[0].pg_off = reinterpret_cast<const int32_t *>(base + L.pg_off);
     P_.bd[0].pg_tgt = reinterpret_cast<const int32_t *>(base + L.pg_tgt);
@@ -816,6 +961,11 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     P_.stage_base[0] = 0;
     P_.stage_base[1] = P;
     P_.stage_base[2] = P + C;
+    P_.tile_base[0] = 0;
+    P_.tile_base[1] = P;
+    P_.tile_base[2] = P + C;
+    P_.cs = 1;
+    P_.partial_floats = mlpc::kBM * max_bn;
     P_.num_pipe = num_pipe;
     P_.stage_bytes = stage_bytes;
     P_.tmem_cols = tmem_cols;

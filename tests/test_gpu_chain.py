@@ -132,10 +132,12 @@ def test_repeated_runs_of_one_handle_are_identical(mc):
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
 
 
-def test_small_grid_still_completes(mc, oracle_mod):
-    # fewer CTAs than tiles: every CTA loops over producer and consumer tickets
+@pytest.mark.parametrize("grid,ks,tn", [(3, [1, 1], [64, 64]), (4, [2, 2], [64, 64]), (8, [4, 1], [128, 64])])
+def test_small_grid_still_completes(mc, oracle_mod, grid, ks, tn):
+    # fewer CTAs than tiles: every cluster loops over producer and consumer tickets
     X, Ws = si.draw(si.make_workload("t", 512, (256, 512, 256)), seed=8)
-    Y, _, _ = run_chain(mc, X, Ws, tile_n=[64, 64], grid_ctas=3)
+    Y, _, info = run_chain(mc, X, Ws, tile_n=tn, grid_ctas=grid, k_split=ks)
+    assert info["grid_ctas"] == grid
     assert_close_to_oracle(Y, oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
 
 
@@ -264,3 +266,74 @@ def test_transposed_weight_layout(mc, oracle_mod, bn):
     assert_close_to_oracle(Y, Yo)
     Ys, _, _ = run_chain(mc, X, Wt, mode="sequential", tile_n=[bn, bn], weight_layout="nk")
     assert torch.equal(Y.view(torch.int16), Ys.view(torch.int16))
+
+
+# --------------------------------------------------------------------------- split-K --
+@pytest.mark.parametrize("M,dims,tn,ks", [
+    (128, (2048, 1024, 2048), [256, 256], [8, 8]),
+    (300, (1024, 512, 384), [128, 64], [4, 2]),
+    (200, (512, 768, 256), [256, 256], [2, 1]),
+    (128, (4096, 512, 256), [64, 32], [2, 1]),
+    (257, (1000, 328, 96), None, None),          # library choice: mixed splits in one cluster
+])
+def test_split_k_matches_oracle_and_modes(mc, oracle_mod, M, dims, tn, ks):
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=18)
+    Y, H, info = run_chain(mc, X, Ws, tile_n=tn, k_split=ks)
+    if ks:
+        assert info["k_split"] == ks and info["cluster_size"] == max(ks)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(H, Ho)
+    assert_close_to_oracle(Y, Yo)
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=tn, k_split=ks)
+    assert torch.equal(Y.view(torch.int16), Ys.view(torch.int16))
+    if M > 128:
+        Ym, _, _ = run_chain(mc, X, Ws, mode="microbatch", microbatch_rows=128, tile_n=tn, k_split=ks)
+        assert torch.equal(Y.view(torch.int16), Ym.view(torch.int16))
+
+
+def test_split_k_integer_inputs_exact(mc, oracle_mod):
+    X, Ws = si.draw_integer(256, (2048, 512, 1024), seed=19)
+    Y, H, _ = run_chain(mc, X, Ws, tile_n=[128, 256], k_split=[4, 8])
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert np.array_equal(bits(H), Ho)
+    assert np.array_equal(bits(Y), Yo)
+
+
+def test_split_k_event_log_and_repeat(mc):
+    M, dims, tn, ks = 384, (2048, 1024, 512), [256, 128], [4, 2]
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=20)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=tn, k_split=ks, event_log=True) as ch:
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        first = None
+        for _ in range(3):
+            ch.run(Xd, Wd, Y, ws)
+            assert ch.check() == 0
+            if first is None:
+                first = Y.clone()
+            assert torch.equal(Y.view(torch.int16), first.view(torch.int16))
+            log = ch.event_log()
+            off, tgt, _ = ch.deps(0)
+            P = len(off) - 1
+            prod, cons = log[:P], log[P:]
+            assert np.array_equal(prod["tile"], np.arange(P)) and np.array_equal(cons["tile"], np.arange(len(cons)))
+            for p in range(P):
+                for c in tgt[off[p]:off[p + 1]]:
+                    assert prod["seq_end"][p] < cons["seq_start"][c]
+
+
+def test_split_k_dropped_decrement_times_out_then_recovers(mc):
+    M, dims = 256, (1024, 512, 512)
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=22)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=[128, 128], k_split=[4, 2], drop_tile=0, timeout_us=20000) as ch:
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        ch.run(Xd, Wd, Y, ws)
+        assert ch.check() == mc.ERR_TIMEOUT
+        ch.run(Xd, Wd, Y, ws)
+        assert ch.check() == 0
+        Y2 = Y.cpu()
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=[128, 128], k_split=[4, 2])
+    assert torch.equal(Y2.view(torch.int16), Ys.view(torch.int16))
