@@ -322,15 +322,20 @@ __device__ __forceinline__ Item take_item(Ctrl *c, int32_t slot)
     return it;
 }
 
-__device__ __forceinline__ void slice_range(const StageParams &sp, int32_t split, int32_t &kb0, int32_t &kb1)
+__device__ __forceinline__ void slice_range(int32_t k_blocks, int32_t kb_per_split, int32_t split, int32_t &kb0,
+                                            int32_t &kb1)
 {
-    kb0 = split * sp.kb_per_split;
-    kb1 = min(sp.k_blocks, kb0 + sp.kb_per_split);
+    kb0 = split * kb_per_split;
+    kb1 = min(k_blocks, kb0 + kb_per_split);
 }
 
 // ---------------------------------------------------------------------------- TMA producer --
 __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t *ring, bool leader)
 {
+    // Kernel parameters live in constant memory behind a generic pointer; every asm statement
+    // with a memory clobber would force them to be re-read, so the loop works from registers.
+    const int32_t num_pipe = p.num_pipe;
+    const uint32_t stage_bytes = p.stage_bytes;
     const uint64_t pol_act = policy_evict_last();    // activations are re-read by many tiles
     const uint64_t pol_w = policy_evict_first();     // each weight tile is read by one row panel
     int32_t ps = 0;
@@ -350,15 +355,19 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t s = item.stage;
         if (s > 0)
             fence_proxy_async_global();
-        const StageParams &sp = p.st[s];
-        const int32_t m0 = (item.tile / sp.tiles_n) * kBM;
-        const int32_t n0 = (item.tile % sp.tiles_n) * sp.BN;
-        const int32_t box_cols = sp.b_swz / 2;
-        const uint32_t box_bytes = kBK * sp.b_swz;
-        const int32_t nbox = sp.BN / box_cols;
-        const uint32_t bytes = kABytes + static_cast<uint32_t>(kBK * sp.BN * 2);
+        const StageParams &spr = p.st[s];
+        const int32_t tiles_n = spr.tiles_n, BN = spr.BN, b_swz = spr.b_swz, b_kmajor = spr.b_kmajor;
+        const int32_t k_blocks = spr.k_blocks, kbps = spr.kb_per_split;
+        const CUtensorMap *mapA = &p.mapA[s];
+        const CUtensorMap *mapB = &p.mapB[s];
+        const int32_t m0 = (item.tile / tiles_n) * kBM;
+        const int32_t n0 = (item.tile % tiles_n) * BN;
+        const int32_t box_cols = b_swz / 2;
+        const uint32_t box_bytes = kBK * b_swz;
+        const int32_t nbox = BN / box_cols;
+        const uint32_t bytes = kABytes + static_cast<uint32_t>(kBK * BN * 2);
         int32_t kb0, kb1;
-        slice_range(sp, item.split, kb0, kb1);
+        slice_range(k_blocks, kbps, item.split, kb0, kb1);
         const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
         bool ok = true;
         for (int32_t kb = kb0; kb < kb1; ++kb) {
@@ -368,18 +377,18 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                 ok = false;
                 break;
             }
-            uint8_t *a = ring + static_cast<size_t>(ps) * p.stage_bytes;
+            uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
             uint8_t *b = a + kABytes;
             mbar_arrive_expect_tx(&c->full[ps], bytes);
-            tma_load_2d(a, &p.mapA[s], &c->full[ps], kb * kBK, m0, pol_act);
-            if (sp.b_kmajor) {
-                tma_load_2d(b, &p.mapB[s], &c->full[ps], kb * kBK, n0, pol_w);
+            tma_load_2d(a, mapA, &c->full[ps], kb * kBK, m0, pol_act);
+            if (b_kmajor) {
+                tma_load_2d(b, mapB, &c->full[ps], kb * kBK, n0, pol_w);
             } else {
                 for (int32_t j = 0; j < nbox; ++j)
-                    tma_load_2d(b + j * box_bytes, &p.mapB[s], &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
+                    tma_load_2d(b + j * box_bytes, mapB, &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
             }
             ++fills[ps];
-            if (++ps == p.num_pipe) {
+            if (++ps == num_pipe) {
                 ps = 0;
                 pph ^= 1;
             }
@@ -389,7 +398,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     }
     if (c->abort_flag) {
         // Let every copy this thread issued land before the CTA's shared memory goes away.
-        for (int32_t i = 0; i < p.num_pipe; ++i)
+        for (int32_t i = 0; i < num_pipe; ++i)
             if (fills[i] > 0)
                 wait_bar(&c->full[i], (fills[i] - 1) & 1, c, p, false);
     }
@@ -398,6 +407,11 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
 // ------------------------------------------------------------------------------ MMA issuer --
 __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t *ring, uint32_t tmem_base)
 {
+    const int32_t num_pipe = p.num_pipe;
+    const uint32_t stage_bytes = p.stage_bytes;
+    const uint32_t acc_stride = static_cast<uint32_t>(p.acc_stride);
+    const uint32_t sub_stride = static_cast<uint32_t>(p.sub_stride);
+    const bool split2 = p.acc_split == 2;
     int32_t ps = 0;
     uint32_t pph = 0;
     uint32_t local_tiles = 0;
@@ -411,19 +425,20 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             break;
         if (item.tile < 0)
             continue;
-        const StageParams &sp = p.st[item.stage];
+        const StageParams &spr = p.st[item.stage];
+        const uint32_t BN = static_cast<uint32_t>(spr.BN);
+        const bool b_kmajor = spr.b_kmajor != 0;
+        const uint32_t b_swz = static_cast<uint32_t>(spr.b_swz);
+        int32_t kb0, kb1;
+        slice_range(spr.k_blocks, spr.kb_per_split, item.split, kb0, kb1);
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
         if (!wait_bar(&c->tempty[acc], acc_ph ^ 1, c, p))
             break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * static_cast<uint32_t>(p.acc_stride);
-        const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(sp.BN), sp.b_kmajor ? 0u : 1u);
-        const uint32_t b_swz = static_cast<uint32_t>(sp.b_swz);
+        const uint32_t d_tmem = tmem_base + acc * acc_stride;
+        const uint32_t idesc = idesc_bf16_f32(kBM, BN, b_kmajor ? 0u : 1u);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
-        const bool split2 = p.acc_split == 2;
-        int32_t kb0, kb1;
-        slice_range(sp, item.split, kb0, kb1);
         bool ok = true;
         for (int32_t kb = kb0; kb < kb1; ++kb) {
             // TMA fills and tcgen05.mma reads are both async-proxy operations ordered by the
@@ -432,7 +447,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                 ok = false;
                 break;
             }
-            const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(ps) * p.stage_bytes);
+            const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(ps) * stage_bytes);
             const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
             for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
@@ -441,19 +456,17 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                 // B stored K x N: MN-major; a 16-deep k step is 16 rows of b_swz bytes.  LBO: next
                 // block of b_swz/2 columns (one TMA box of 64 rows); SBO: next group of 8 rows.
                 // B stored N x K: K-major like A, BN rows of 128 bytes.
-                const uint64_t bd = sp.b_kmajor
-                                        ? smem_desc(b_addr + kk * 32u, 16u, 1024u, 2u)
-                                        : smem_desc(b_addr + kk * 16u * b_swz, kBK * b_swz, 8u * b_swz, b_code);
+                const uint64_t bd = b_kmajor ? smem_desc(b_addr + kk * 32u, 16u, 1024u, 2u)
+                                             : smem_desc(b_addr + kk * 16u * b_swz, kBK * b_swz, 8u * b_swz, b_code);
                 // k step j of the slice goes to sub-accumulator j % acc_split; its first step
                 // overwrites.
                 const uint32_t j = static_cast<uint32_t>(kb - kb0) * (kBK / 16) + kk;
                 const uint32_t sub = split2 ? (j & 1u) : 0u;
-                mma_bf16_ss(d_tmem + sub * static_cast<uint32_t>(p.sub_stride), ad, bd, idesc,
-                            j >= (split2 ? 2u : 1u) ? 1u : 0u);
+                mma_bf16_ss(d_tmem + sub * sub_stride, ad, bd, idesc, j >= (split2 ? 2u : 1u) ? 1u : 0u);
             }
             issued = true;
             mma_commit(&c->empty[ps]);  // frees the ring slot once these MMAs have read it
-            if (++ps == p.num_pipe) {
+            if (++ps == num_pipe) {
                 ps = 0;
                 pph ^= 1;
             }
@@ -470,6 +483,17 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
 }
 
 // -------------------------------------------------------------------------------- epilogue --
+// Two fp32 values to packed bf16 (lo in the low half), round to nearest even on the bit
+// pattern: add half an ulp of the kept part plus its lowest kept bit, keep the upper 16 bits;
+// NaN stays a (quiet) NaN.
+__device__ __forceinline__ uint32_t pack_bf16x2_rne(float lo, float hi)
+{
+    uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
+    const uint32_t ra = ((a & 0x7fffffffu) > 0x7f800000u) ? (a | 0x00400000u) : a + 0x7fffu + ((a >> 16) & 1u);
+    const uint32_t rb = ((b & 0x7fffffffu) > 0x7f800000u) ? (b | 0x00400000u) : b + 0x7fffu + ((b >> 16) & 1u);
+    return __byte_perm(ra, rb, 0x7632);   // high halves: ra[31:16] low, rb[31:16] high
+}
+
 // Byte offset of 16-byte segment `seg` (0..3) of row `row` (0..31) in a warp's staging buffer;
 // the XOR keeps the eight rows a quarter-warp touches on distinct banks.
 __device__ __forceinline__ uint32_t stage_off(int row, int seg)
@@ -480,14 +504,24 @@ __device__ __forceinline__ uint32_t stage_off(int row, int seg)
 // One warp stores a 32-row x 32-column chunk of the output.  Lane l holds the fp32 values of
 // row row0 + l (TMEM hands each thread one row); the chunk goes through the warp's staging
 // buffer so that global stores and residual loads touch whole 64-byte row segments.
-__device__ __forceinline__ void store_chunk_warp(const StageParams &sp, int32_t row0, int32_t n, const uint32_t (&r)[32],
-                                                 uint8_t *stage, int32_t lane)
+// Output of a stage, copied into registers once per tile.
+struct OutDesc {
+    __nv_bfloat16 *out;
+    const __nv_bfloat16 *residual;
+    int32_t M, N, gelu;
+};
+
+template <bool kGelu>
+__device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row0, int32_t n, const uint32_t (&r)[32],
+                                                   uint8_t *stage, int32_t lane)
 {
     float v[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
+    for (int e = 0; e < 32; ++e)
         v[e] = __uint_as_float(r[e]);
-        if (sp.gelu)
+    if (kGelu) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
             v[e] = gelu_tanh_f32(v[e]);
     }
     if (sp.residual) {
@@ -516,11 +550,9 @@ __device__ __forceinline__ void store_chunk_warp(const StageParams &sp, int32_t 
     }
 #pragma unroll
     for (int sg = 0; sg < 4; ++sg) {
-        uint4 o;
-        __nv_bfloat162 *ob = reinterpret_cast<__nv_bfloat162 *>(&o);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            ob[e] = __floats2bfloat162_rn(v[sg * 8 + 2 * e], v[sg * 8 + 2 * e + 1]);
+        const uint4 o = make_uint4(pack_bf16x2_rne(v[sg * 8], v[sg * 8 + 1]), pack_bf16x2_rne(v[sg * 8 + 2], v[sg * 8 + 3]),
+                                   pack_bf16x2_rne(v[sg * 8 + 4], v[sg * 8 + 5]),
+                                   pack_bf16x2_rne(v[sg * 8 + 6], v[sg * 8 + 7]));
         *reinterpret_cast<uint4 *>(stage + stage_off(lane, sg)) = o;
     }
     __syncwarp();
@@ -535,13 +567,24 @@ __device__ __forceinline__ void store_chunk_warp(const StageParams &sp, int32_t 
     __syncwarp();
 }
 
+// GeLU is chosen once per call by a uniform branch, so the plain path carries no tanh code
+// (a per-element test inside the unrolled loop could be if-converted into evaluating it always).
+__device__ __forceinline__ void store_chunk_warp(const OutDesc sp, int32_t row0, int32_t n, const uint32_t (&r)[32],
+                                                 uint8_t *stage, int32_t lane)
+{
+    if (sp.gelu)
+        store_chunk_warp_t<true>(sp, row0, n, r, stage, lane);
+    else
+        store_chunk_warp_t<false>(sp, row0, n, r, stage, lane);
+}
+
 // 32 accumulator columns of this thread's TMEM lane (sub-accumulators summed, even + odd).
-__device__ __forceinline__ void load_acc(const ChainParams &p, uint32_t taddr, uint32_t (&r)[32])
+__device__ __forceinline__ void load_acc(bool split2, uint32_t sub_stride, uint32_t taddr, uint32_t (&r)[32])
 {
     tmem_ld_32x32b_x32(taddr, r);
-    if (p.acc_split == 2) {
+    if (split2) {
         uint32_t r2[32];
-        tmem_ld_32x32b_x32(taddr + p.sub_stride, r2);
+        tmem_ld_32x32b_x32(taddr + sub_stride, r2);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 32; ++e)
@@ -607,6 +650,17 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
     const int32_t quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
     const int32_t row = quad * 32 + lane;
     uint8_t *stage = staging + quad * kEpiStageBytes;
+    // kernel-uniform parameters in registers (see role_tma)
+    const uint32_t acc_stride = static_cast<uint32_t>(p.acc_stride);
+    const uint32_t sub_stride = static_cast<uint32_t>(p.sub_stride);
+    const bool split2 = p.acc_split == 2;
+    const int32_t cs = p.cs;
+    const size_t partial_floats = static_cast<size_t>(p.partial_floats);
+    const bool pipelined = p.pipelined != 0;
+    const int32_t num_stages = p.num_stages;
+    const bool logging = p.events != nullptr;
+    const int32_t drop_tile = p.drop_tile;
+    const size_t cbase = static_cast<size_t>(cluster_id_x()) * cs;
     uint32_t local_tiles = 0;
     uint32_t epi_phase = 0;
     uint32_t nsplit = 0;                        // split-K tiles this CTA took part in
@@ -625,31 +679,34 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         if (item.tile < 0)
             continue;
         const int32_t s = item.stage, tile = item.tile;
-        const StageParams &sp = p.st[s];
+        const StageParams &spr = p.st[s];
+        const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = spr.split;
+        float *const partials = spr.partials;
+        const OutDesc od{spr.out, spr.residual, spr.M, spr.N, spr.gelu};
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
         if (!warp_wait_bar(&c->tfull[acc], acc_ph, c, p))
             break;
         tc_fence_after();
-        if (p.events && warp == 4 && lane == 0 && item.split == 0)
+        if (logging && warp == 4 && lane == 0 && item.split == 0)
             p.events[p.tile_base[s] + tile].t_acc = globaltimer_ns();
-        const int32_t row0 = (tile / sp.tiles_n) * kBM + quad * 32;   // this warp's first row
-        const int32_t n0 = (tile % sp.tiles_n) * sp.BN;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * p.acc_stride;
-        const bool producer = p.pipelined && s + 1 < p.num_stages;
+        const int32_t row0 = (tile / tiles_n) * kBM + quad * 32;   // this warp's first row
+        const int32_t n0 = (tile % tiles_n) * BN;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * acc_stride;
+        const bool producer = pipelined && s + 1 < num_stages;
 
-        if (sp.split == 1) {
-            for (int32_t c0 = 0; c0 < sp.BN; c0 += 32) {
+        if (S == 1) {
+            for (int32_t c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
-                load_acc(p, taddr + c0, r);
-                store_chunk_warp(sp, row0, n0 + c0, r, stage, lane);
+                load_acc(split2, sub_stride, taddr + c0, r);
+                store_chunk_warp(od, row0, n0 + c0, r, stage, lane);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&c->tempty[acc]);   // the MMA warp may reuse this accumulator
             ++local_tiles;
-            if (producer || (p.pipelined && p.events)) {
+            if (producer || (pipelined && logging)) {
                 // Injected epilogue: every thread orders its stores, the four warps meet (a
                 // bounded mbarrier rather than bar.sync, so an aborting warp cannot strand the
                 // others), then one warp releases and decrements the scoreboard.
@@ -661,10 +718,10 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                     break;
                 epi_phase ^= 1;
                 if (warp == 4) {
-                    if (lane == 0 && p.events)
+                    if (lane == 0 && logging)
                         log_end(p, s, tile);
                     __syncwarp();
-                    if (producer && !(s == 0 && tile == p.drop_tile))
+                    if (producer && !(s == 0 && tile == drop_tile))
                         release_tile(p, c, s, tile, lane);
                 }
             }
@@ -672,19 +729,17 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         }
 
         // ---- split-K tile: S siblings (ranks g0 .. g0+S-1) each hold a k-slice partial ----
-        const int32_t S = sp.split;
         const uint32_t g0 = rank - static_cast<uint32_t>(item.split);      // first sibling
-        const uint32_t weight = static_cast<uint32_t>(p.cs / S);           // arrivals per sibling warp
-        const size_t cbase = static_cast<size_t>(cluster_id_x()) * p.cs;
+        const uint32_t weight = static_cast<uint32_t>(cs / S);             // arrivals per sibling warp
         // Partial layout: [BN/32 chunks][8 vectors][128 rows][4 floats]: for a fixed vector the
         // warp's 32 lanes (rows) touch 512 contiguous bytes, so stores and loads coalesce.
-        float *mine = sp.partials + (cbase + rank) * p.partial_floats;
+        float *mine = partials + (cbase + rank) * partial_floats;
         // my previous partial must have been read by every sibling of that tile
         if (nsplit > 0 && !warp_wait_bar(&c->done_bar, (nsplit - 1) & 1, c, p, true))
             break;
-        for (int32_t c0 = 0; c0 < sp.BN; c0 += 32) {
+        for (int32_t c0 = 0; c0 < BN; c0 += 32) {
             uint32_t r[32];
-            load_acc(p, taddr + c0, r);
+            load_acc(split2, sub_stride, taddr + c0, r);
             float4 *dst = reinterpret_cast<float4 *>(mine) + (c0 / 32) * 8 * kBM + row;
 #pragma unroll
             for (int v = 0; v < 8; ++v)
@@ -705,7 +760,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             break;
         // Reduce my column slice over the S partials in rank order, then the epilogue.  Loads of
         // up to four partials are issued before any of them is added.
-        const int32_t slice = sp.BN / S;
+        const int32_t slice = BN / S;
         const int32_t col0 = item.split * slice;
         for (int32_t c0 = col0; c0 < col0 + slice; c0 += 32) {
             float acc_v[32];
@@ -718,8 +773,8 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq)
                     if (qb + qq < S) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                                                sp.partials + (cbase + g0 + qb + qq) * p.partial_floats) + off;
+                        const float4 *src =
+                            reinterpret_cast<const float4 *>(partials + (cbase + g0 + qb + qq) * partial_floats) + off;
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             v[qq][i] = __ldcg(src + i * kBM);
@@ -740,23 +795,23 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 r[e] = __float_as_uint(acc_v[e]);
-            store_chunk_warp(sp, row0, n0 + c0, r, stage, lane);
+            store_chunk_warp(od, row0, n0 + c0, r, stage, lane);
         }
         fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
         __syncwarp();
         if (lane == 0)
             for (int32_t q = 0; q < S; ++q)
                 arrive_rank(&c->done_bar, g0 + q, weight);
-        if (item.split == 0 && (producer || (p.pipelined && p.events))) {
+        if (item.split == 0 && (producer || (pipelined && logging))) {
             // the tile is complete once every sibling stored its slice
             if (!warp_wait_bar(&c->done_bar, nsplit & 1, c, p, true))
                 break;
             if (warp == 4) {
                 fence_acq_rel_gpu();
-                if (lane == 0 && p.events)
+                if (lane == 0 && logging)
                     log_end(p, s, tile);
                 __syncwarp();
-                if (producer && !(s == 0 && tile == p.drop_tile))
+                if (producer && !(s == 0 && tile == drop_tile))
                     release_tile(p, c, s, tile, lane);
             }
         }

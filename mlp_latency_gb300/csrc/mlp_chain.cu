@@ -114,7 +114,7 @@ extern "C" const char *mlp_status_str(mlp_status s)
 
 // Tile width and split-K factor of one stage, from a cost model of this kernel on one SM:
 // one tcgen05.mma (M = 128, K = 16) costs about the same for any N <= 256 (~140 cycles), a TMA
-// box row (64 or 128 bytes) costs ~1.2 ns, a split tile pays ~1.5 us for its fp32 reduction,
+// box row (64 or 128 bytes) costs ~1.2 ns, a split tile pays ~4 us for its fp32 reduction,
 // and a stage cannot beat the HBM time of its weights.  clusters[i] = co-resident clusters of
 // 2^i CTAs.  Candidates with idle k slices or reduction slices narrower than 32 columns are
 // skipped.  Returns the estimated microseconds.
@@ -142,11 +142,13 @@ static double choose_tiles(int64_t tiles_m, int64_t K, int64_t N, const int clus
                 continue;
             const double tiles = static_cast<double>(tiles_m) * ((N + bn - 1) / bn);
             const double slots = static_cast<double>(clusters[li]) * S;
-            const double waves = std::ceil(tiles * S / slots);
+            const double units = tiles * S;
+            // a persistent grid quantises into whole waves only while units are few
+            const double waves = units <= 2 * slots ? std::ceil(units / slots) : units / slots;
             const double rows = 128.0 + (bn >= 64 ? bn : 64);
             const double t_mma = kbps * 4 * 140.0 / 1900.0;          // us
             const double t_tma = kbps * rows * 1.2e-3;               // us
-            const double t_unit = std::max(t_mma, t_tma) + 1.0 + (S > 1 ? 1.5 : 0.0);
+            const double t_unit = std::max(t_mma, t_tma) + 1.0 + (S > 1 ? 4.0 : 0.0);
             const double t_hbm = static_cast<double>(K) * N * 2 / 6.5e6;
             const double t = std::max(waves * t_unit, t_hbm);
             if (t < best * 0.999) {
