@@ -100,8 +100,9 @@ typedef struct {
     int32_t drop_tile;                  /* with MLP_DEBUG_DROP_DECREMENT                         */
     uint32_t timeout_us;                /* bounded device waits; 0 = 2 000 000 (2 s)             */
     int32_t grid_ctas;                  /* 0 = one CTA per SM                                    */
-    int32_t raster_group;               /* first-stage raster: 0/1 = row panels in order; g > 1
-                                           = groups of g row panels, column-major inside a group */
+    int32_t raster_group;               /* first-stage raster: 1 = row panels in order; g > 1 =
+                                           groups of g row panels, column-major inside a group;
+                                           0 = library choice (4 when there are >= 8 panels)     */
     int32_t pipe_stages;                /* shared-memory ring depth: 0 = as deep as fits         */
     int32_t weight_layout;              /* 0: W_s stored dims[s] x dims[s+1] row-major (K x N);
                                            1: stored transposed, dims[s+1] x dims[s] row-major

@@ -59,8 +59,8 @@ struct StageParams {
     int32_t kb_per_split;   // k blocks of each slice (the last one may get fewer)
     int32_t tiles_per_item; // cluster size / S
     int32_t items;          // cluster items of this stage
-    float *partials;        // split-K: one 128 x BN fp32 buffer per CTA ([chunk][row][32])
-    int32_t pad_;
+    float *partials;        // split-K through global memory: one 128 x BN fp32 buffer per CTA
+    int32_t dsmem_reduce;   // split-K through the owners' shared memory (BN * 512 <= recv_bytes)
 };
 
 // Stage boundary s -> s+1.  The scoreboard holds one counter per group of consumer tiles with
@@ -103,6 +103,7 @@ struct ChainParams {
     int32_t acc_split;                   // 1, or 2: k16 steps alternate between two sub-accumulators
     int32_t sub_stride;                  // TMEM columns between the sub-accumulators of a buffer
     int32_t partial_floats;              // floats per CTA partial buffer (128 x max tile width)
+    uint32_t recv_bytes;                 // split-K receive buffer in shared memory (0: none)
     int32_t drop_tile;                   // fault injection (-1: off)
     uint64_t timeout_ns;
     uint32_t *ticket;
@@ -130,20 +131,28 @@ struct __align__(8) Ctrl {
 };
 
 constexpr uint32_t kEpiStageBytes = 32 * 64;   // per epilogue warp: 32 rows x 32 bf16 columns
+constexpr uint32_t kRecvBytes = 64 * 1024;     // split-K receive buffer: S parts of a 128 x 128/S slice
 
+// Shared memory: [ring: num_pipe x stage_bytes][4 x epilogue staging][split-K receive buffer]
+// [Ctrl], the ring 1024-byte aligned.
 __host__ __device__ inline uint32_t staging_offset(int num_pipe, uint32_t stage_bytes)
 {
     return static_cast<uint32_t>(num_pipe) * stage_bytes;
 }
 
-__host__ __device__ inline uint32_t ctrl_offset(int num_pipe, uint32_t stage_bytes)
+__host__ __device__ inline uint32_t recv_offset(int num_pipe, uint32_t stage_bytes)
 {
     return staging_offset(num_pipe, stage_bytes) + 4 * kEpiStageBytes;
 }
 
-__host__ inline size_t chain_smem_bytes(int num_pipe, uint32_t stage_bytes)
+__host__ __device__ inline uint32_t ctrl_offset(int num_pipe, uint32_t stage_bytes, uint32_t recv_bytes)
 {
-    return 1024 + ctrl_offset(num_pipe, stage_bytes) + sizeof(Ctrl);
+    return recv_offset(num_pipe, stage_bytes) + recv_bytes;
+}
+
+__host__ inline size_t chain_smem_bytes(int num_pipe, uint32_t stage_bytes, uint32_t recv_bytes)
+{
+    return 1024 + ctrl_offset(num_pipe, stage_bytes, recv_bytes) + sizeof(Ctrl);
 }
 
 // ------------------------------------------------------------------------ bounded waits --
@@ -241,7 +250,7 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
                         uint32_t backoff = 32;
                         while (true) {
                             __nanosleep(backoff);
-                            backoff = backoff < 256 ? backoff * 2 : 256;
+                            backoff = backoff < 64 ? backoff * 2 : 64;
                             v = ld_acquire_gpu_u64(q);
                             if (queue_entry_ready(v, c->epoch))
                                 break;
@@ -607,7 +616,9 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
         bool fire = false;
         if (e < e1) {
             g = bd.pg_tgt[e];
-            fence_acq_rel_gpu();
+            // acq_rel: releases, cumulatively, every store the epilogue's meeting ordered before
+            // this point (each writer fenced at gpu scope before it arrived), and acquires the
+            // earlier producers' releases when this decrement is the last.
             const uint32_t old = atom_add_acq_rel_gpu(bd.count + g, 0xffffffffu);
             fire = (old == 1u);
             if (fire)   // re-arm for the next run; no producer touches it again
@@ -643,8 +654,9 @@ __device__ __forceinline__ void log_end(const ChainParams &p, int32_t s, int32_t
 }
 
 __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uint32_t tmem_base, uint32_t rank,
-                                              uint8_t *staging)
+                                              uint8_t *staging, uint8_t *recv)
 {
+    const uint32_t recv_u32 = smem_u32(recv);
     const int32_t warp = threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     const int32_t quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
@@ -681,6 +693,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         const int32_t s = item.stage, tile = item.tile;
         const StageParams &spr = p.st[s];
         const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = spr.split;
+        const bool dsmem = spr.dsmem_reduce != 0;
         float *const partials = spr.partials;
         const OutDesc od{spr.out, spr.residual, spr.M, spr.N, spr.gelu};
         const uint32_t acc = local_tiles & 1;
@@ -731,6 +744,79 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         // ---- split-K tile: S siblings (ranks g0 .. g0+S-1) each hold a k-slice partial ----
         const uint32_t g0 = rank - static_cast<uint32_t>(item.split);      // first sibling
         const uint32_t weight = static_cast<uint32_t>(cs / S);             // arrivals per sibling warp
+        if (dsmem) {
+            // Sibling q owns columns [q*BN/S, (q+1)*BN/S).  Every CTA sends each owner its part of
+            // that slice straight from TMEM into the owner's receive buffer, laid out
+            // [source split][chunk of the slice][vector][128 rows][4 floats] (a warp writes 512
+            // contiguous bytes), then the owner adds the S parts in source order.
+            const int32_t cpo = BN / S / 32;   // 32-column chunks per owner
+            if (nsplit > 0 && !warp_wait_bar(&c->done_bar, (nsplit - 1) & 1, c, p, true))
+                break;   // every owner has finished reading its buffer from the previous tile
+            for (int32_t ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                load_acc(split2, sub_stride, taddr + ch * 32, r);
+                const int32_t owner = ch / cpo, oc = ch % cpo;
+                const uint32_t dst = map_to_rank(recv, g0 + owner) +
+                                     static_cast<uint32_t>((((item.split * cpo + oc) * 8) * kBM + row) * 16);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    st_cluster_v4_f32(dst + v * kBM * 16, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c->tempty[acc]);
+            ++local_tiles;
+            fence_acq_rel_cluster();
+            __syncwarp();
+            if (lane == 0)
+                for (int32_t q = 0; q < S; ++q)
+                    arrive_rank(&c->red_bar, g0 + q, weight);
+            if (!warp_wait_bar(&c->red_bar, nsplit & 1, c, p, true))
+                break;
+            for (int32_t oc = 0; oc < cpo; ++oc) {
+                float acc_v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    acc_v[e] = 0.0f;
+                for (int32_t q = 0; q < S; ++q) {
+                    const uint32_t src = recv_u32 + static_cast<uint32_t>((((q * cpo + oc) * 8) * kBM + row) * 16);
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        const float4 x = ld_shared_v4_f32(src + v * kBM * 16);
+                        acc_v[4 * v] += x.x;
+                        acc_v[4 * v + 1] += x.y;
+                        acc_v[4 * v + 2] += x.z;
+                        acc_v[4 * v + 3] += x.w;
+                    }
+                }
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    r[e] = __float_as_uint(acc_v[e]);
+                store_chunk_warp(od, row0, n0 + (item.split * cpo + oc) * 32, r, stage, lane);
+            }
+            fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
+            __syncwarp();
+            if (lane == 0)
+                for (int32_t q = 0; q < S; ++q)
+                    arrive_rank(&c->done_bar, g0 + q, weight);
+            if (item.split == 0 && (producer || (pipelined && logging))) {
+                if (!warp_wait_bar(&c->done_bar, nsplit & 1, c, p, true))
+                    break;
+                if (warp == 4) {
+                    fence_acq_rel_gpu();
+                    if (lane == 0 && logging)
+                        log_end(p, s, tile);
+                    __syncwarp();
+                    if (producer && !(s == 0 && tile == drop_tile))
+                        release_tile(p, c, s, tile, lane);
+                }
+            }
+            ++nsplit;
+            continue;
+        }
         // Partial layout: [BN/32 chunks][8 vectors][128 rows][4 floats]: for a fixed vector the
         // warp's 32 lanes (rows) touch 512 contiguous bytes, so stores and loads coalesce.
         float *mine = partials + (cbase + rank) * partial_floats;
@@ -759,7 +845,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         if (!warp_wait_bar(&c->red_bar, nsplit & 1, c, p, true))
             break;
         // Reduce my column slice over the S partials in rank order, then the epilogue.  Loads of
-        // up to four partials are issued before any of them is added.
+        // two partials are issued before either is added.
         const int32_t slice = BN / S;
         const int32_t col0 = item.split * slice;
         for (int32_t c0 = col0; c0 < col0 + slice; c0 += 32) {
@@ -768,10 +854,10 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             for (int e = 0; e < 32; ++e)
                 acc_v[e] = 0.0f;
             const size_t off = static_cast<size_t>((c0 / 32) * 8 * kBM + row);   // in float4
-            for (int32_t qb = 0; qb < S; qb += 4) {
-                float4 v[4][8];
+            for (int32_t qb = 0; qb < S; qb += 2) {
+                float4 v[2][8];
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
+                for (int qq = 0; qq < 2; ++qq)
                     if (qb + qq < S) {
                         const float4 *src =
                             reinterpret_cast<const float4 *>(partials + (cbase + g0 + qb + qq) * partial_floats) + off;
@@ -780,7 +866,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                             v[qq][i] = __ldcg(src + i * kBM);
                     }
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
+                for (int qq = 0; qq < 2; ++qq)
                     if (qb + qq < S) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
@@ -825,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     uint8_t *ring = smem_raw + (((base + 1023u) & ~1023u) - base);
-    Ctrl *c = reinterpret_cast<Ctrl *>(ring + ctrl_offset(p.num_pipe, p.stage_bytes));
+    Ctrl *c = reinterpret_cast<Ctrl *>(ring + ctrl_offset(p.num_pipe, p.stage_bytes, p.recv_bytes));
     const int32_t warp = threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -878,7 +964,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             if (lane == 0 && rank == 0)
                 role_scheduler(p, c);
         } else if (warp >= 4) {
-            role_epilogue(p, c, tmem_base, rank, ring + staging_offset(p.num_pipe, p.stage_bytes));
+            role_epilogue(p, c, tmem_base, rank, ring + staging_offset(p.num_pipe, p.stage_bytes),
+                          ring + recv_offset(p.num_pipe, p.stage_bytes));
         }
     }
     tc_fence_before();

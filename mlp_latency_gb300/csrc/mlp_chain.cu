@@ -72,6 +72,7 @@ struct mlp_chain {
     int b_swz[MLP_MAX_GEMMS] = {};
     int num_pipe = 0, max_bn = 0, grid = 0, acc_split = 1;
     int cs = 1, max_clusters = 0;
+    uint32_t recv_bytes = 0;
     int split[MLP_MAX_GEMMS] = {}, kb_per_split[MLP_MAX_GEMMS] = {}, items[MLP_MAX_GEMMS] = {};
     int32_t tile_base[MLP_MAX_GEMMS + 1] = {};
     float *partials[MLP_MAX_GEMMS] = {};
@@ -298,7 +299,11 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->items[s] = (tiles + tpi - 1) / tpi;
     }
     h->stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
-    const size_t fixed = 1024 + 4 * mlpc::kEpiStageBytes + sizeof(mlpc::Ctrl);
+    // split tiles up to 128 wide reduce through shared memory (distributed, within the cluster)
+    for (int s = 0; s < S; ++s)
+        if (h->split[s] > 1 && h->BN[s] * 512u <= mlpc::kRecvBytes)
+            h->recv_bytes = mlpc::kRecvBytes;
+    const size_t fixed = 1024 + 4 * mlpc::kEpiStageBytes + h->recv_bytes + sizeof(mlpc::Ctrl);
     h->num_pipe = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - fixed) / h->stage_bytes));
     if (d->pipe_stages)
         h->num_pipe = std::min(h->num_pipe, d->pipe_stages);
@@ -311,7 +316,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         release(h);
         return MLP_ERR_UNSUPPORTED;
     }
-    h->smem = mlpc::chain_smem_bytes(h->num_pipe, h->stage_bytes);
+    h->smem = mlpc::chain_smem_bytes(h->num_pipe, h->stage_bytes, h->recv_bytes);
     h->tmem_cols = 32;
     while (h->tmem_cols < static_cast<uint32_t>(2 * h->acc_split * h->max_bn))
         h->tmem_cols *= 2;
@@ -376,8 +381,9 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     // split-K partial sums: per stage that splits, one 128 x max_bn fp32 buffer per CTA slot
     const int cta_slots = std::max(h->grid, h->max_clusters * h->cs);
     const size_t partial_bytes = static_cast<size_t>(cta_slots) * mlpc::kBM * h->max_bn * sizeof(float);
+    auto global_partials = [&](int s) { return h->split[s] > 1 && !(h->recv_bytes && h->BN[s] * 512u <= h->recv_bytes); };
     for (int s = 0; s < S; ++s)
-        if (h->split[s] > 1)
+        if (global_partials(s))
             bytes = align_up(bytes, 256) + partial_bytes;
     if (cudaMalloc(&h->dev_block, bytes) != cudaSuccess) {
         h->dev_block = nullptr;
@@ -425,7 +431,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         o += h->n_events * sizeof(mlpc::EventRec);
     }
     for (int s = 0; s < S; ++s)
-        if (h->split[s] > 1) {
+        if (global_partials(s)) {
             o = align_up(o, 256);
             h->partials[s] = reinterpret_cast<float *>(p + o);
             o += partial_bytes;
@@ -512,6 +518,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.tiles_per_item = h->cs / h->split[s];
         sp.items = h->items[s];
         sp.partials = h->partials[s];
+        sp.dsmem_reduce = h->split[s] > 1 && h->recv_bytes && h->BN[s] * 512u <= h->recv_bytes;
         sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
         sp.gelu = d.epilogue == MLP_EPI_GELU_TANH;
         sp.residual = (d.residual && s + 1 == h->S) ? static_cast<const __nv_bfloat16 *>(X) : nullptr;
@@ -534,7 +541,10 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     }
     P.cs = h->cs;
     P.partial_floats = mlpc::kBM * h->max_bn;
-    P.raster_group = d.raster_group;
+    P.recv_bytes = h->recv_bytes;
+    // Default first-stage raster: groups of 4 row panels once there are enough panels, so a
+    // weight column slab is reused from L2 by 4 panels instead of being streamed again per panel.
+    P.raster_group = d.raster_group ? d.raster_group : (h->tiles_m >= 8 ? 4 : 1);
     P.num_pipe = h->num_pipe;
     P.stage_bytes = h->stage_bytes;
     P.tmem_cols = h->tmem_cols;
@@ -914,7 +924,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     int smem_optin = 0;
     cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int num_pipe = static_cast<int>(std::min<size_t>(
-        mlpc::kMaxPipe, (smem_optin - 1024 - 4 * mlpc::kEpiStageBytes - sizeof(mlpc::Ctrl)) / stage_bytes));
+        mlpc::kMaxPipe, (smem_optin - 1024 - 4 * mlpc::kEpiStageBytes - sizeof(mlpc::Ctrl)) / stage_bytes));   // no split: no receive buffer
     if (num_pipe < 2)
         return MLP_ERR_UNSUPPORTED;
     uint32_t tmem_cols = 32;
@@ -990,7 +1000,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     if (cudaGetLastError() != cudaSuccess)
         return MLP_ERR_CUDA;
     const int grid = std::min(nd.num_sms, P + C);
-    if (!launch(P_, grid, mlpc::chain_smem_bytes(num_pipe, stage_bytes), st))
+    if (!launch(P_, grid, mlpc::chain_smem_bytes(num_pipe, stage_bytes, 0), st))
         return MLP_ERR_CUDA;
     if (!sync_check)
         return MLP_OK;

@@ -81,6 +81,20 @@ __device__ __forceinline__ uint32_t map_to_rank(const void *local, uint32_t rank
     return r;
 }
 
+__device__ __forceinline__ void st_cluster_v4_f32(uint32_t cluster_addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_v4_f32(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr, int32_t v)
 {
     asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
