@@ -32,13 +32,13 @@ import seeded_inputs as si  # noqa: E402
 
 METRIC = "single-batch 2-layer GEMM latency (µs) and TFLOP/s vs roofline on 1 GB300"
 DEFAULT_WORKLOAD = "decode_m128_d4096"
-# tile widths per GEMM chosen by a sweep on GB300 (bench.py --sweep)
+# tile widths per GEMM measured best on GB300 (0: the library cost model chooses)
 TUNED_TILES = {
     "tiny_m64_d256": [64, 64],
     "decode_m128_d4096": [0, 0],
     "prefill_m2048_d8192": [256, 256],
     "llama_m256_4096_14336": [0, 0],
-    "gelu4_m512_d8192": [128, 128, 128, 128],
+    "gelu4_m512_d8192": [0, 0, 0, 0],
 }
 TUNED_SPLIT = {}
 KERNEL_SOURCES = ["mlp_latency_gb300/csrc/chain_kernel.cuh", "mlp_latency_gb300/csrc/ptx.cuh",

@@ -7,15 +7,17 @@
 // its reduction dimension (split-K, S = 1 .. cs).  Rank r works on tile r / S, k-slice r % S.
 //
 // Warp roles (256 threads per CTA):
-//   warp 0      TMA producer: streams A (activations, K-major) and B (weights) tiles of its
-//               k-slice into an NS-deep shared-memory ring.
+//   warp 0      TMA producer: for a consumer item, first polls the item's work-queue slot
+//               (the injected prologue of section III-A, Fig. 1) to learn its tile; then
+//               streams A (activations, K-major) and B (weights) tiles of its k-slice into an
+//               NS-deep shared-memory ring.
 //   warp 1      MMA issuer: one thread issues tcgen05.mma into a double-buffered TMEM
 //               accumulator; warp 1 also owns the TMEM allocation.
-//   warp 2      scheduler (rank 0 of each cluster only): takes a ticket per cluster item and,
-//               for consumer stages, polls the work-queue (the injected prologue of section
-//               III-A, Fig. 1), then broadcasts the item to every CTA of the cluster through
-//               distributed shared memory (the scheduler warp's CGA broadcast of section III-C,
-//               Fig. 2b).
+//   warp 2      scheduler (rank 0 of each cluster only): takes a ticket per cluster item and
+//               broadcasts it (stage, tile or queue slot, k-slice) to every CTA of the cluster
+//               through distributed shared memory (the scheduler warp's CGA broadcast of
+//               section III-C, Fig. 2b).
+//   warp 3      pulls the protocol's counters, queues and dependency tables into L2 at launch.
 //   warps 4-7   epilogue: TMEM -> registers -> (split-K reduction) -> (GeLU / residual) ->
 //               bf16 -> global, then the injected epilogue: fence, scoreboard decrements and
 //               queue pushes (section III-A; fence placement per the memory-consistency
@@ -70,7 +72,7 @@ struct BoundaryParams {
     const int32_t *pg_tgt;
     const int32_t *grp_off;    // group -> member consumer tiles (CSR)
     const int32_t *grp_mem;
-    const int32_t *grp_init;   // producers each group waits for
+    const int32_t *grp_init;   // releases each group waits for: producer tiles x split
     uint32_t *count;           // one counter per group
     unsigned long long *queue; // one slot per consumer tile
     uint32_t *tail;
@@ -112,6 +114,8 @@ struct ChainParams {
     uint32_t *status;
     uint32_t *seq;
     EventRec *events;                    // null: no event log
+    const uint8_t *meta;                 // protocol state (counters, queues, dependency tables) ...
+    uint32_t meta_bytes;                 // ... prefetched into L2 at launch (0: none)
 };
 
 struct __align__(8) Ctrl {
@@ -122,7 +126,7 @@ struct __align__(8) Ctrl {
     uint64_t epi_sync;
     uint64_t want_next;   // TMA -> scheduler: take the next ticket now
     uint64_t red_bar;     // split-K: every sibling's partial is written
-    uint64_t done_bar;    // split-K: every sibling has read the partials and stored its slice
+    uint64_t done_bar;    // split-K: every sibling has read its parts of my partial
     int32_t item_stage[kSchedDepth], item_tile[kSchedDepth], item_split[kSchedDepth];
     uint32_t tmem_base;
     volatile int32_t abort_flag;
@@ -200,6 +204,13 @@ __device__ __forceinline__ float gelu_tanh_f32(float x)
     return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
 }
 
+// Arrive on the same mbarrier in CTA `rank` of this cluster, `count` times, without release
+// semantics (the caller fences once before a batch of these).
+__device__ __forceinline__ void arrive_rank_relaxed(uint64_t *bar, uint32_t rank, uint32_t count)
+{
+    mbar_arrive_relaxed_cluster(map_to_rank(bar, rank), count);
+}
+
 // Arrive on the same mbarrier in CTA `rank` of this cluster, `count` times.
 __device__ __forceinline__ void arrive_rank(uint64_t *bar, uint32_t rank, uint32_t count)
 {
@@ -236,61 +247,12 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
                 const int32_t ntile_stage = sp.tiles_m * sp.tiles_n;
                 const int32_t first = (t - p.stage_base[s]) * sp.tiles_per_item;
                 ntiles = min(sp.tiles_per_item, ntile_stage - first);
-                bool ok = true;
-                for (int32_t j = 0; j < ntiles && ok; ++j) {
-                    if (s == 0) {
-                        tiles[j] = raster_tile(first + j, sp.tiles_m, sp.tiles_n, p.raster_group);
-                        continue;
-                    }
-                    // Consumer prologue: poll queue slot first+j until this run's entry lands.
-                    const unsigned long long *q = p.bd[s - 1].queue + first + j;
-                    uint64_t v = ld_acquire_gpu_u64(q);
-                    if (!queue_entry_ready(v, c->epoch)) {
-                        const uint64_t t0 = globaltimer_ns();
-                        uint32_t backoff = 32;
-                        while (true) {
-                            __nanosleep(backoff);
-                            backoff = backoff < 64 ? backoff * 2 : 64;
-                            v = ld_acquire_gpu_u64(q);
-                            if (queue_entry_ready(v, c->epoch))
-                                break;
-                            if (ld_relaxed_gpu_u32(p.status) != 0 || c->abort_flag) {
-                                ok = false;
-                                break;
-                            }
-                            if (globaltimer_ns() - t0 > p.timeout_ns) {
-                                atomicCAS(p.status, 0u, kStatusTimeout);
-                                ok = false;
-                                break;
-                            }
-                        }
-                    }
-                    if (!ok)
-                        break;
-                    tiles[j] = queue_entry_tile(v);
-                    if (tiles[j] < 0 || tiles[j] >= ntile_stage) {
-                        atomicCAS(p.status, 0u, kStatusBadTile);
-                        ok = false;
-                    }
-                }
-                if (ok) {
-                    stage = s;
-                    // Later TMA (async proxy) reads of the producers' output must not be
-                    // ordered before the acquires above.
-                    if (s > 0)
-                        fence_proxy_async_global();
-                    if (p.events) {
-                        for (int32_t j = 0; j < ntiles; ++j) {
-                            EventRec *e = p.events + p.tile_base[s] + tiles[j];
-                            e->stage = s;
-                            e->tile = tiles[j];
-                            e->smid = static_cast<int32_t>(smid());
-                            e->cta = static_cast<int32_t>(blockIdx.x);
-                            e->seq_start = atom_add_relaxed_gpu(p.seq, 1u);
-                            e->t_start = globaltimer_ns();
-                        }
-                    }
-                }
+                // Stage 0 tiles follow the raster order; a consumer item carries work-queue slots
+                // (first + j), which the CTAs that run it poll themselves (resolve_queue_slot), so
+                // the broadcast below is off the path from a queue push to the first load.
+                for (int32_t j = 0; j < ntiles; ++j)
+                    tiles[j] = s == 0 ? raster_tile(first + j, sp.tiles_m, sp.tiles_n, p.raster_group) : first + j;
+                stage = s;
             }
         } else {
             const StageParams &sp = p.st[p.first_stage];
@@ -304,7 +266,9 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
                     tiles[j] = p.m_tile_begin * sp.tiles_n + first + j;
             }
         }
-        // Broadcast: rank r gets tile r / S of the item (or none) and k-slice r % S.
+        // Broadcast: rank r gets tile r / S of the item (or none) and k-slice r % S.  All items
+        // are written first and released by one fence: a release arrive per rank would cost a
+        // round trip each and start the last rank's slice that much later than the first's.
         const int32_t S = stage >= 0 ? p.st[stage].split : 1;
         for (int32_t r = 0; r < cs; ++r) {
             const int32_t j = r / S;
@@ -312,22 +276,78 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
             st_cluster_s32(map_to_rank(&c->item_stage[slot], r), stage);
             st_cluster_s32(map_to_rank(&c->item_tile[slot], r), tile);
             st_cluster_s32(map_to_rank(&c->item_split[slot], r), r % S);
-            arrive_rank(&c->sfull[slot], r, 1);
         }
+        fence_acq_rel_cluster();
+        for (int32_t r = 0; r < cs; ++r)
+            arrive_rank_relaxed(&c->sfull[slot], r, 1);
         if (stage < 0)
             return;
     }
 }
 
-// Read the item of ring slot `slot` (after its sfull wait) and release the slot to rank 0.
+// The item of ring slot `slot`: stage, tile (in a pipelined run's consumer stages: the
+// work-queue slot that names the tile) and k-slice.
 struct Item {
     int32_t stage, tile, split;
 };
 
+// Consumer prologue (the injected prologue of section III-A, Fig. 1): poll work-queue slot
+// `qslot` of the boundary before stage s until this run's entry lands, with back-off and a
+// deadline.  Returns the consumer tile it names, or -1 after an error (status recorded, this
+// CTA's abort flag raised).  The caller orders its later TMA reads with a proxy fence.
+__device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl *c, int32_t s, int32_t qslot)
+{
+    // Relaxed polls (an acquire load costs a fence per iteration); the fence after the loop
+    // turns the load that saw the entry into the acquire.
+    const unsigned long long *q = p.bd[s - 1].queue + qslot;
+    uint64_t v = ld_relaxed_gpu_u64(q);
+    if (!queue_entry_ready(v, c->epoch)) {
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t backoff = 32;
+        while (true) {
+            __nanosleep(backoff);
+            backoff = backoff < 64 ? backoff * 2 : 64;
+            v = ld_relaxed_gpu_u64(q);
+            if (queue_entry_ready(v, c->epoch))
+                break;
+            if (c->abort_flag)
+                return -1;
+            if (ld_relaxed_gpu_u32(p.status) != 0) {
+                c->abort_flag = 1;
+                return -1;
+            }
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                atomicCAS(p.status, 0u, kStatusTimeout);
+                c->abort_flag = 1;
+                return -1;
+            }
+        }
+    }
+    fence_acq_rel_gpu();
+    const int32_t tile = queue_entry_tile(v);
+    if (tile < 0 || tile >= p.st[s].tiles_m * p.st[s].tiles_n) {
+        atomicCAS(p.status, 0u, kStatusBadTile);
+        c->abort_flag = 1;
+        return -1;
+    }
+    return tile;
+}
+
+__device__ __forceinline__ Item read_item(Ctrl *c, int32_t slot)
+{
+    return Item{c->item_stage[slot], c->item_tile[slot], c->item_split[slot]};
+}
+
+// Hand ring slot `slot` back to the scheduler (a release: the item's reads come first).
+__device__ __forceinline__ void free_item_slot(Ctrl *c, int32_t slot)
+{
+    arrive_rank(&c->sempty[slot], 0, 1);
+}
+
 __device__ __forceinline__ Item take_item(Ctrl *c, int32_t slot)
 {
-    Item it{c->item_stage[slot], c->item_tile[slot], c->item_split[slot]};
-    arrive_rank(&c->sempty[slot], 0, 1);
+    const Item it = read_item(c, slot);
+    free_item_slot(c, slot);
     return it;
 }
 
@@ -347,6 +367,8 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint32_t stage_bytes = p.stage_bytes;
     const uint64_t pol_act = policy_evict_last();    // activations are re-read by many tiles
     const uint64_t pol_w = policy_evict_first();     // each weight tile is read by one row panel
+    const bool pipelined = p.pipelined != 0;
+    EventRec *const events = pipelined ? p.events : nullptr;
     int32_t ps = 0;
     uint32_t pph = 0;
     uint32_t fills[kMaxPipe];
@@ -356,21 +378,42 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t slot = it % kSchedDepth;
         if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true, true))
             break;
-        const Item item = take_item(c, slot);
-        if (item.stage < 0)
-            break;
-        if (item.tile < 0)
+        // The slot goes back to the scheduler only after this item's loads are issued: the
+        // release round trip then stays off the path to the first load.
+        const Item item = read_item(c, slot);
+        if (item.stage < 0 || item.tile < 0) {
+            free_item_slot(c, slot);
+            if (item.stage < 0)
+                break;
             continue;
+        }
         const int32_t s = item.stage;
-        if (s > 0)
+        int32_t tile = item.tile;
+        if (pipelined && s > 0) {
+            tile = resolve_queue_slot(p, c, s, item.tile);
+            if (tile < 0) {
+                free_item_slot(c, slot);
+                break;
+            }
+        }
+        if (s > 0)   // TMA (async proxy) reads of a producer's output come after the acquire
             fence_proxy_async_global();
+        if (events && item.split == 0) {
+            EventRec *e = events + p.tile_base[s] + tile;
+            e->stage = s;
+            e->tile = tile;
+            e->smid = static_cast<int32_t>(smid());
+            e->cta = static_cast<int32_t>(blockIdx.x);
+            e->seq_start = atom_add_relaxed_gpu(p.seq, 1u);
+            e->t_start = globaltimer_ns();
+        }
         const StageParams &spr = p.st[s];
         const int32_t tiles_n = spr.tiles_n, BN = spr.BN, b_swz = spr.b_swz, b_kmajor = spr.b_kmajor;
         const int32_t k_blocks = spr.k_blocks, kbps = spr.kb_per_split;
         const CUtensorMap *mapA = &p.mapA[s];
         const CUtensorMap *mapB = &p.mapB[s];
-        const int32_t m0 = (item.tile / tiles_n) * kBM;
-        const int32_t n0 = (item.tile % tiles_n) * BN;
+        const int32_t m0 = (tile / tiles_n) * kBM;
+        const int32_t n0 = (tile % tiles_n) * BN;
         const int32_t box_cols = b_swz / 2;
         const uint32_t box_bytes = kBK * b_swz;
         const int32_t nbox = BN / box_cols;
@@ -402,6 +445,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                 pph ^= 1;
             }
         }
+        free_item_slot(c, slot);
         if (!ok)
             break;
     }
@@ -603,12 +647,72 @@ __device__ __forceinline__ void load_acc(bool split2, uint32_t sub_stride, uint3
     }
 }
 
-// Producer side of the protocol for a finished tile: decrement every group counter the tile
-// feeds; the decrement that reaches zero re-arms the counter and publishes the group's members
-// on the work-queue.  Called by one whole warp after the tile's stores were released.
-__device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, int32_t lane)
+// What the release of one producer tile reads from the dependency tables, loaded while the
+// tile's mainloop still runs so that the release itself is a decrement, one queue reservation
+// and the stores.  Filled in full when the tile feeds exactly one group (a GEMM chain's row
+// panel); `ne` is the number of groups it feeds.  Lane i holds members i and 32 + i.
+struct ReleasePlan {
+    int32_t ne, g, init, m0, n, mem0, mem1;
+};
+
+__device__ __forceinline__ ReleasePlan plan_release(const ChainParams &p, int32_t s, int32_t tile, int32_t lane)
 {
     const BoundaryParams &bd = p.bd[s];
+    ReleasePlan r{0, -1, 0, 0, 0, -1, -1};
+    const int32_t e0 = bd.pg_off[tile];
+    r.ne = bd.pg_off[tile + 1] - e0;
+    if (r.ne == 1) {
+        r.g = bd.pg_tgt[e0];
+        r.init = bd.grp_init[r.g];
+        r.m0 = bd.grp_off[r.g];
+        r.n = bd.grp_off[r.g + 1] - r.m0;
+        if (lane < r.n)
+            r.mem0 = bd.grp_mem[r.m0 + lane];
+        if (lane + 32 < r.n)
+            r.mem1 = bd.grp_mem[r.m0 + 32 + lane];
+    }
+    return r;
+}
+
+// Producer side of the protocol for a finished tile (or one split-K slice of it: a split tile
+// decrements once per slice and its counters start at producers x S): decrement every group
+// counter the tile feeds; the decrement that reaches zero re-arms the counter and publishes the
+// group's members on the work-queue.  Called by one whole warp right after a fence.acq_rel.gpu
+// that follows the tile's stores.
+__device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, int32_t lane,
+                                             const ReleasePlan &pl)
+{
+    const BoundaryParams &bd = p.bd[s];
+    if (pl.ne == 1) {
+        // One group: lane 0 decrements (the caller's fence and this relaxed decrement are the
+        // release); the last decrement re-arms the counter and reserves the group's queue slots.
+        uint32_t q0 = 0, fire = 0;
+        if (lane == 0) {
+            const uint32_t old = atom_add_relaxed_gpu(bd.count + pl.g, 0xffffffffu);
+            if (old == 1u) {
+                fire = 1;
+                q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(pl.n));
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, fire, 0))
+            return;
+        q0 = __shfl_sync(0xffffffffu, q0, 0);
+        // Lane 0's decrement saw every other producer's release; the syncwarp and each lane's
+        // fence turn that into an acquire for the whole warp and release the pushes below.
+        __syncwarp();
+        fence_acq_rel_gpu();
+        if (lane < pl.n)
+            st_relaxed_gpu_u64(bd.queue + q0 + lane, queue_entry(c->epoch, pl.mem0));
+        if (lane + 32 < pl.n)
+            st_relaxed_gpu_u64(bd.queue + q0 + 32 + lane, queue_entry(c->epoch, pl.mem1));
+        for (int32_t i = lane + 64; i < pl.n; i += 32)
+            st_relaxed_gpu_u64(bd.queue + q0 + i, queue_entry(c->epoch, bd.grp_mem[pl.m0 + i]));
+        // Re-arm for the next run (no producer of this run touches the counter again); after
+        // the pushes, so the fence above does not wait for it.
+        if (lane == 0)
+            bd.count[pl.g] = static_cast<uint32_t>(pl.init);
+        return;
+    }
     const int32_t e0 = bd.pg_off[tile], e1 = bd.pg_off[tile + 1];
     for (int32_t eb = e0; eb < e1; eb += 32) {
         const int32_t e = eb + lane;
@@ -616,16 +720,16 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
         bool fire = false;
         if (e < e1) {
             g = bd.pg_tgt[e];
-            // acq_rel: releases, cumulatively, every store the epilogue's meeting ordered before
-            // this point (each writer fenced at gpu scope before it arrived), and acquires the
-            // earlier producers' releases when this decrement is the last.
-            const uint32_t old = atom_add_acq_rel_gpu(bd.count + g, 0xffffffffu);
+            // The caller's fence.acq_rel.gpu and this relaxed decrement form the release of every
+            // store the epilogue's meeting ordered before it (each writer fenced before it
+            // arrived); the last decrement's acquire is the fence below, before the pushes.
+            const uint32_t old = atom_add_relaxed_gpu(bd.count + g, 0xffffffffu);
             fire = (old == 1u);
             if (fire)   // re-arm for the next run; no producer touches it again
                 bd.count[g] = static_cast<uint32_t>(bd.grp_init[g]);
         }
         // Every group this warp completed is published by the whole warp: the lane whose
-        // acq_rel decrement reached zero acquired every earlier producer's release; __syncwarp
+        // decrement reached zero saw every earlier producer's release; __syncwarp
         // orders that before each lane's release fence, which makes its relaxed queue stores
         // carry the release.
         uint32_t todo = __ballot_sync(0xffffffffu, fire);
@@ -653,6 +757,31 @@ __device__ __forceinline__ void log_end(const ChainParams &p, int32_t s, int32_t
     e->t_end = globaltimer_ns();
 }
 
+// Injected epilogue of a finished tile or split-K slice: every epilogue thread has fenced its
+// own stores at gpu scope; the four warps meet (a bounded mbarrier rather than bar.sync, so an
+// aborting warp cannot strand the others), then warp 4 fences once more, which makes the
+// meeting's stores cumulative, logs the tile and decrements the scoreboard.
+__device__ __forceinline__ bool publish(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, bool log_it,
+                                        bool producer, int32_t warp, int32_t lane, uint32_t &epi_phase,
+                                        const ReleasePlan &pl)
+{
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(&c->epi_sync);
+    if (!warp_wait_bar(&c->epi_sync, epi_phase, c, p))
+        return false;
+    epi_phase ^= 1;
+    if (warp == 4) {
+        fence_acq_rel_gpu();
+        if (lane == 0 && log_it)
+            log_end(p, s, tile);
+        __syncwarp();
+        if (producer && !(s == 0 && tile == p.drop_tile))
+            release_tile(p, c, s, tile, lane, pl);
+    }
+    return true;
+}
+
 __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uint32_t tmem_base, uint32_t rank,
                                               uint8_t *staging, uint8_t *recv)
 {
@@ -671,7 +800,6 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
     const bool pipelined = p.pipelined != 0;
     const int32_t num_stages = p.num_stages;
     const bool logging = p.events != nullptr;
-    const int32_t drop_tile = p.drop_tile;
     const size_t cbase = static_cast<size_t>(cluster_id_x()) * cs;
     uint32_t local_tiles = 0;
     uint32_t epi_phase = 0;
@@ -690,7 +818,16 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             break;
         if (item.tile < 0)
             continue;
-        const int32_t s = item.stage, tile = item.tile;
+        const int32_t s = item.stage;
+        int32_t tile = item.tile;
+        if (pipelined && s > 0) {   // the TMA warp of this CTA polled the same slot first
+            int32_t t = 0;
+            if (lane == 0)
+                t = resolve_queue_slot(p, c, s, item.tile);
+            tile = __shfl_sync(0xffffffffu, t, 0);
+            if (tile < 0)
+                break;
+        }
         const StageParams &spr = p.st[s];
         const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = spr.split;
         const bool dsmem = spr.dsmem_reduce != 0;
@@ -698,6 +835,10 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         const OutDesc od{spr.out, spr.residual, spr.M, spr.N, spr.gelu};
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
+        const bool producer = pipelined && s + 1 < num_stages;
+        ReleasePlan pl{0, -1, 0, 0, 0, -1, -1};
+        if (producer && warp == 4)
+            pl = plan_release(p, s, tile, lane);
         if (!warp_wait_bar(&c->tfull[acc], acc_ph, c, p))
             break;
         tc_fence_after();
@@ -706,7 +847,6 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         const int32_t row0 = (tile / tiles_n) * kBM + quad * 32;   // this warp's first row
         const int32_t n0 = (tile % tiles_n) * BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * acc_stride;
-        const bool producer = pipelined && s + 1 < num_stages;
 
         if (S == 1) {
             for (int32_t c0 = 0; c0 < BN; c0 += 32) {
@@ -720,23 +860,9 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 mbar_arrive(&c->tempty[acc]);   // the MMA warp may reuse this accumulator
             ++local_tiles;
             if (producer || (pipelined && logging)) {
-                // Injected epilogue: every thread orders its stores, the four warps meet (a
-                // bounded mbarrier rather than bar.sync, so an aborting warp cannot strand the
-                // others), then one warp releases and decrements the scoreboard.
-                fence_acq_rel_gpu();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&c->epi_sync);
-                if (!warp_wait_bar(&c->epi_sync, epi_phase, c, p))
+                fence_acq_rel_gpu();   // this thread's stores, released at gpu scope for the consumers
+                if (!publish(p, c, s, tile, logging, producer, warp, lane, epi_phase, pl))
                     break;
-                epi_phase ^= 1;
-                if (warp == 4) {
-                    if (lane == 0 && logging)
-                        log_end(p, s, tile);
-                    __syncwarp();
-                    if (producer && !(s == 0 && tile == drop_tile))
-                        release_tile(p, c, s, tile, lane);
-                }
             }
             continue;
         }
@@ -772,7 +898,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             __syncwarp();
             if (lane == 0)
                 for (int32_t q = 0; q < S; ++q)
-                    arrive_rank(&c->red_bar, g0 + q, weight);
+                    arrive_rank_relaxed(&c->red_bar, g0 + q, weight);
             if (!warp_wait_bar(&c->red_bar, nsplit & 1, c, p, true))
                 break;
             for (int32_t oc = 0; oc < cpo; ++oc) {
@@ -799,22 +925,14 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             }
             fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0)         // my receive buffer is read: siblings may send the next tile
                 for (int32_t q = 0; q < S; ++q)
-                    arrive_rank(&c->done_bar, g0 + q, weight);
-            if (item.split == 0 && (producer || (pipelined && logging))) {
-                if (!warp_wait_bar(&c->done_bar, nsplit & 1, c, p, true))
-                    break;
-                if (warp == 4) {
-                    fence_acq_rel_gpu();
-                    if (lane == 0 && logging)
-                        log_end(p, s, tile);
-                    __syncwarp();
-                    if (producer && !(s == 0 && tile == drop_tile))
-                        release_tile(p, c, s, tile, lane);
-                }
-            }
+                    arrive_rank_relaxed(&c->done_bar, g0 + q, weight);
             ++nsplit;
+            // Each sibling publishes its own column slice; the tile's consumers wait for all S.
+            if ((producer || (pipelined && logging)) &&
+                !publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, epi_phase, pl))
+                break;
             continue;
         }
         // Partial layout: [BN/32 chunks][8 vectors][128 rows][4 floats]: for a fixed vector the
@@ -841,7 +959,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         __syncwarp();
         if (lane == 0)
             for (int32_t q = 0; q < S; ++q)
-                arrive_rank(&c->red_bar, g0 + q, weight);
+                arrive_rank_relaxed(&c->red_bar, g0 + q, weight);
         if (!warp_wait_bar(&c->red_bar, nsplit & 1, c, p, true))
             break;
         // Reduce my column slice over the S partials in rank order, then the epilogue.  Loads of
@@ -885,23 +1003,13 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         }
         fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
         __syncwarp();
-        if (lane == 0)
+        if (lane == 0)         // the siblings' partials are read: they may overwrite them
             for (int32_t q = 0; q < S; ++q)
-                arrive_rank(&c->done_bar, g0 + q, weight);
-        if (item.split == 0 && (producer || (pipelined && logging))) {
-            // the tile is complete once every sibling stored its slice
-            if (!warp_wait_bar(&c->done_bar, nsplit & 1, c, p, true))
-                break;
-            if (warp == 4) {
-                fence_acq_rel_gpu();
-                if (lane == 0 && logging)
-                    log_end(p, s, tile);
-                __syncwarp();
-                if (producer && !(s == 0 && tile == drop_tile))
-                    release_tile(p, c, s, tile, lane);
-            }
-        }
+                arrive_rank_relaxed(&c->done_bar, g0 + q, weight);
         ++nsplit;
+        if ((producer || (pipelined && logging)) &&
+            !publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, epi_phase, pl))
+            break;
     }
 }
 
@@ -940,8 +1048,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&p.mapA[0]);
-        prefetch_tensormap(&p.mapB[0]);
+        for (int i = 0; i < p.num_stages; ++i) {
+            prefetch_tensormap(&p.mapA[i]);
+            prefetch_tensormap(&p.mapB[i]);
+        }
     }
     if (warp == 1) {
         tmem_alloc(&c->tmem_base, p.tmem_cols);
@@ -963,6 +1073,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         } else if (warp == 2) {
             if (lane == 0 && rank == 0)
                 role_scheduler(p, c);
+        } else if (warp == 3) {
+            // The protocol's few kilobytes of state are cold after whatever ran before (the
+            // release and the consumer prologue would each pay HBM misses in sequence), so the
+            // otherwise idle warp pulls them into L2 now, spread over the grid.
+            const uint32_t step = gridDim.x * 32u * 128u;
+            for (uint32_t off = (blockIdx.x * 32u + static_cast<uint32_t>(lane)) * 128u; off < p.meta_bytes; off += step)
+                prefetch_l2_keep(p.meta + off);
         } else if (warp >= 4) {
             role_epilogue(p, c, tmem_base, rank, ring + staging_offset(p.num_pipe, p.stage_bytes),
                           ring + recv_offset(p.num_pipe, p.stage_bytes));

@@ -71,6 +71,7 @@ struct mlp_chain {
     int BN[MLP_MAX_GEMMS] = {}, tiles_m = 0, tiles_n[MLP_MAX_GEMMS] = {}, k_blocks[MLP_MAX_GEMMS] = {};
     int b_swz[MLP_MAX_GEMMS] = {};
     int num_pipe = 0, max_bn = 0, grid = 0, acc_split = 1;
+    size_t meta_bytes = 0;   // bytes from d_ctrl through the last boundary's tables
     int cs = 1, max_clusters = 0;
     uint32_t recv_bytes = 0;
     int split[MLP_MAX_GEMMS] = {}, kb_per_split[MLP_MAX_GEMMS] = {}, items[MLP_MAX_GEMMS] = {};
@@ -422,8 +423,13 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         up(db.pg_tgt, G.pg_tgt);
         up(db.grp_off, G.grp_off);
         up(db.grp_mem, G.grp_mem);
-        up(db.grp_init, G.grp_init);
+        // A split producer tile is released slice by slice, so its groups count S releases.
+        std::vector<int32_t> releases(G.grp_init);
+        for (int32_t &v : releases)
+            v *= h->split[b];
+        up(db.grp_init, releases);
     }
+    h->meta_bytes = o;
     if (h->n_events) {
         o = align_up(o, 256);
         h->d_events = reinterpret_cast<mlpc::EventRec *>(p + o);
@@ -559,6 +565,8 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     P.status = h->d_ctrl + 3;
     P.seq = h->d_ctrl + 4;
     P.events = h->d_events;
+    P.meta = reinterpret_cast<const uint8_t *>(h->d_ctrl);
+    P.meta_bytes = static_cast<uint32_t>(h->meta_bytes);
     h->c_X = X;
     h->c_Y = Y;
     h->c_ws = ws;

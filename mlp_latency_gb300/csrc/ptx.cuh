@@ -107,6 +107,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive `count` times on an mbarrier of any CTA in the cluster, ordering nothing by itself.  A
+// caller that publishes data issues one fence.acq_rel (cluster or gpu scope) first: the fence and
+// this arrive form the release, so several remote arrives share one fence instead of each
+// paying a release round trip.
+__device__ __forceinline__ void mbar_arrive_relaxed_cluster(uint32_t cluster_addr, uint32_t count)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr), "r"(count)
+                 : "memory");
+}
+
 // try_wait with acquire at cluster scope (for phases completed by other CTAs' arrivals).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
 {
@@ -131,6 +141,12 @@ __device__ __forceinline__ void cluster_sync_all()
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Bring one line of global memory into L2 with the evict-last priority.
+__device__ __forceinline__ void prefetch_l2_keep(const void *p)
+{
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
 }
 
 // 2-D tiled load: box at coordinates (c0 = innermost, c1) into shared memory, completion
@@ -265,6 +281,13 @@ __device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const unsigned long long 
 {
     uint64_t v;
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const unsigned long long *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
 
