@@ -38,6 +38,7 @@ constexpr int kMaxCluster = 8;
 constexpr int kBM = 128;          // rows per tile = TMEM lanes
 constexpr int kBK = 64;           // 64 bf16 = 128 bytes = one 128B-swizzle row
 constexpr int kThreads = 256;
+constexpr int kEpiWarps = 4;      // epilogue warps; each releases its own rows of a tile
 constexpr int kSchedDepth = 4;
 constexpr int kMaxPipe = 16;
 constexpr int kTicketLead = 4;    // k-blocks before the end of a slice at which the next ticket is taken
@@ -72,7 +73,7 @@ struct BoundaryParams {
     const int32_t *pg_tgt;
     const int32_t *grp_off;    // group -> member consumer tiles (CSR)
     const int32_t *grp_mem;
-    const int32_t *grp_init;   // releases each group waits for: producer tiles x split
+    const int32_t *grp_init;   // releases each group waits for: producer tiles x split x kEpiWarps
     uint32_t *count;           // one counter per group
     unsigned long long *queue; // one slot per consumer tile
     uint32_t *tail;
@@ -123,7 +124,6 @@ struct __align__(8) Ctrl {
     uint64_t tfull[2], tempty[2];
     uint64_t sfull[kSchedDepth], sempty[kSchedDepth];
     uint64_t drain;
-    uint64_t epi_sync;
     uint64_t want_next;   // TMA -> scheduler: take the next ticket now
     uint64_t red_bar;     // split-K: every sibling's partial is written
     uint64_t done_bar;    // split-K: every sibling has read its parts of my partial
@@ -674,11 +674,11 @@ __device__ __forceinline__ ReleasePlan plan_release(const ChainParams &p, int32_
     return r;
 }
 
-// Producer side of the protocol for a finished tile (or one split-K slice of it: a split tile
-// decrements once per slice and its counters start at producers x S): decrement every group
-// counter the tile feeds; the decrement that reaches zero re-arms the counter and publishes the
-// group's members on the work-queue.  Called by one whole warp right after a fence.acq_rel.gpu
-// that follows the tile's stores.
+// Producer side of the protocol for the rows one epilogue warp stored of a finished tile (or of
+// one split-K slice of it): decrement every group counter the tile feeds (a group waits for
+// kEpiWarps x S decrements per producer tile); the decrement that reaches zero re-arms the
+// counter and publishes the group's members on the work-queue.  Called by the whole warp right
+// after a fence.acq_rel.gpu that follows its stores.
 __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, int32_t lane,
                                              const ReleasePlan &pl)
 {
@@ -757,29 +757,19 @@ __device__ __forceinline__ void log_end(const ChainParams &p, int32_t s, int32_t
     e->t_end = globaltimer_ns();
 }
 
-// Injected epilogue of a finished tile or split-K slice: every epilogue thread has fenced its
-// own stores at gpu scope; the four warps meet (a bounded mbarrier rather than bar.sync, so an
-// aborting warp cannot strand the others), then warp 4 fences once more, which makes the
-// meeting's stores cumulative, logs the tile and decrements the scoreboard.
-__device__ __forceinline__ bool publish(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, bool log_it,
-                                        bool producer, int32_t warp, int32_t lane, uint32_t &epi_phase,
-                                        const ReleasePlan &pl)
+// Injected epilogue of a finished tile or split-K slice, run by each epilogue warp for the 32
+// rows it stored.  The caller has fenced the warp's stores at gpu scope (after the warp's last
+// __syncwarp, so the fence is cumulative over all its lanes); that fence and the relaxed
+// decrement in release_tile form the release.  Each of the four warps of each of the S slices
+// decrements once (counters start at producer tiles x S x 4), so no warp waits for another.
+__device__ __forceinline__ void publish(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, bool log_it,
+                                        bool producer, int32_t warp, int32_t lane, const ReleasePlan &pl)
 {
+    if (log_it && warp == 4 && lane == 0)
+        log_end(p, s, tile);
     __syncwarp();
-    if (lane == 0)
-        mbar_arrive(&c->epi_sync);
-    if (!warp_wait_bar(&c->epi_sync, epi_phase, c, p))
-        return false;
-    epi_phase ^= 1;
-    if (warp == 4) {
-        fence_acq_rel_gpu();
-        if (lane == 0 && log_it)
-            log_end(p, s, tile);
-        __syncwarp();
-        if (producer && !(s == 0 && tile == p.drop_tile))
-            release_tile(p, c, s, tile, lane, pl);
-    }
-    return true;
+    if (producer && !(s == 0 && tile == p.drop_tile))
+        release_tile(p, c, s, tile, lane, pl);
 }
 
 __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uint32_t tmem_base, uint32_t rank,
@@ -802,7 +792,6 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
     const bool logging = p.events != nullptr;
     const size_t cbase = static_cast<size_t>(cluster_id_x()) * cs;
     uint32_t local_tiles = 0;
-    uint32_t epi_phase = 0;
     uint32_t nsplit = 0;                        // split-K tiles this CTA took part in
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
@@ -837,7 +826,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
         const bool producer = pipelined && s + 1 < num_stages;
         ReleasePlan pl{0, -1, 0, 0, 0, -1, -1};
-        if (producer && warp == 4)
+        if (producer)
             pl = plan_release(p, s, tile, lane);
         if (!warp_wait_bar(&c->tfull[acc], acc_ph, c, p))
             break;
@@ -860,9 +849,8 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 mbar_arrive(&c->tempty[acc]);   // the MMA warp may reuse this accumulator
             ++local_tiles;
             if (producer || (pipelined && logging)) {
-                fence_acq_rel_gpu();   // this thread's stores, released at gpu scope for the consumers
-                if (!publish(p, c, s, tile, logging, producer, warp, lane, epi_phase, pl))
-                    break;
+                fence_acq_rel_gpu();   // this warp's stores, released at gpu scope for the consumers
+                publish(p, c, s, tile, logging, producer, warp, lane, pl);
             }
             continue;
         }
@@ -930,9 +918,8 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                     arrive_rank_relaxed(&c->done_bar, g0 + q, weight);
             ++nsplit;
             // Each sibling publishes its own column slice; the tile's consumers wait for all S.
-            if ((producer || (pipelined && logging)) &&
-                !publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, epi_phase, pl))
-                break;
+            if (producer || (pipelined && logging))
+                publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, pl);
             continue;
         }
         // Partial layout: [BN/32 chunks][8 vectors][128 rows][4 floats]: for a fixed vector the
@@ -1007,9 +994,8 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             for (int32_t q = 0; q < S; ++q)
                 arrive_rank_relaxed(&c->done_bar, g0 + q, weight);
         ++nsplit;
-        if ((producer || (pipelined && logging)) &&
-            !publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, epi_phase, pl))
-            break;
+        if (producer || (pipelined && logging))
+            publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, pl);
     }
 }
 
@@ -1038,7 +1024,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             mbar_init(&c->sempty[i], 6 * p.cs);   // TMA + MMA + 4 epilogue warps of every rank
         }
         mbar_init(&c->drain, 1);
-        mbar_init(&c->epi_sync, 4);
         mbar_init(&c->want_next, 1);
         mbar_init(&c->red_bar, 4 * p.cs);          // 4 warps x S siblings, each arriving cs/S times
         mbar_init(&c->done_bar, 4 * p.cs);

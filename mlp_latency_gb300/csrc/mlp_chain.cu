@@ -423,10 +423,10 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         up(db.pg_tgt, G.pg_tgt);
         up(db.grp_off, G.grp_off);
         up(db.grp_mem, G.grp_mem);
-        // A split producer tile is released slice by slice, so its groups count S releases.
+        // A producer tile is released by each epilogue warp of each of its S split-K slices.
         std::vector<int32_t> releases(G.grp_init);
         for (int32_t &v : releases)
-            v *= h->split[b];
+            v *= h->split[b] * mlpc::kEpiWarps;
         up(db.grp_init, releases);
     }
     h->meta_bytes = o;
@@ -860,8 +860,8 @@ __global__ void noalloc_setup_kernel(uint8_t *base, NoallocLayout L, int Pn, int
     for (int g = i0; g <= G; g += stride) {
         grp_off[g] = g * Cn;
         if (g < G) {
-            grp_init[g] = Pn;
-            count[g] = static_cast<uint32_t>(Pn);
+            grp_init[g] = Pn * mlpc::kEpiWarps;   // each epilogue warp of a tile releases its rows
+            count[g] = static_cast<uint32_t>(Pn * mlpc::kEpiWarps);
         }
     }
     for (int c = i0; c < C; c += stride) {
