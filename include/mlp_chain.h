@@ -22,8 +22,13 @@
  * MLP_MODE_SEQUENTIAL launches the same tile engine once per GEMM, back to back on one stream
  * (the pages' "two consecutive GEMMs" baseline, section III-C).  MLP_MODE_MICROBATCH splits
  * X into row chunks and overlaps GEMM s of chunk i with GEMM s+1 of chunk i-1 on separate
- * streams (static micro-batching, section IV, Fig. 3).  All three modes use the same tiles in
- * the same order of k, so Y is bit-identical across modes.
+ * streams (static micro-batching, section IV, Fig. 3).  MLP_MODE_PIPELINED_KWAIT is the same
+ * persistent grid with a finer dependency: a consumer tile takes its place in raster order (no
+ * work-queue) and, before loading k block kb of its input, waits only for the producer tiles
+ * that wrote those 64 columns, each counted ready once all of its epilogue warps released their
+ * rows (the tile-granular dependency of section III-A refined to the consumer's k loop; its
+ * weight tiles are requested before the wait).  Every mode uses the same tiles in the same
+ * order of k, so Y is bit-identical across modes.
  *
  * Conventions for every entry point.
  *   - Matrices are dense, row-major, bf16, with 16-byte aligned base pointers; every
@@ -68,7 +73,8 @@ typedef enum { MLP_DT_BF16 = 1, MLP_DT_F32 = 2 } mlp_dtype;
 typedef enum {
     MLP_MODE_PIPELINED = 0,   /* one persistent grid, scoreboard + work-queue (CTA-pipelining) */
     MLP_MODE_SEQUENTIAL = 1,  /* one launch per GEMM, back to back                              */
-    MLP_MODE_MICROBATCH = 2   /* row chunks, GEMM s+1 of chunk i overlaps GEMM s of chunk i+1   */
+    MLP_MODE_MICROBATCH = 2,  /* row chunks, GEMM s+1 of chunk i overlaps GEMM s of chunk i+1   */
+    MLP_MODE_PIPELINED_KWAIT = 3  /* one persistent grid, per-k-block producer waits, no queue  */
 } mlp_mode;
 
 typedef enum { MLP_EPI_NONE = 0, MLP_EPI_GELU_TANH = 1 } mlp_epilogue;
@@ -121,7 +127,8 @@ typedef struct {
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG).  t_* are %globaltimer ns;
  * seq_* come from one device-wide counter, taken after the consumer's acquire (start) and
  * before the producer's scoreboard release (end), so seq_end(p) < seq_start(c) for every
- * dependency p -> c. */
+ * dependency p -> c.  In MLP_MODE_PIPELINED_KWAIT a consumer starts before its producers end
+ * (it waits per k block), so start is when its CTA took the tile and that order need not hold. */
 typedef struct {
     int32_t stage, tile, smid, cta;
     uint64_t t_start, t_end;

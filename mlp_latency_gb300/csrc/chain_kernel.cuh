@@ -77,6 +77,10 @@ struct BoundaryParams {
     uint32_t *count;           // one counter per group
     unsigned long long *queue; // one slot per consumer tile
     uint32_t *tail;
+    // K-granular mode: per producer tile, the releases seen so far (ready_quota per run,
+    // accumulated over the handle's runs and compared against the run's epoch).
+    uint32_t *ready;
+    uint32_t ready_quota;      // releases of one producer tile in one run: split x kEpiWarps
 };
 
 struct EventRec {
@@ -93,6 +97,7 @@ struct ChainParams {
     BoundaryParams bd[kMaxStages - 1];
     int32_t num_stages;
     int32_t pipelined;
+    int32_t kwait;                       // pipelined with per-k-block producer waits, no work-queue
     int32_t first_stage;                 // non-pipelined launches run this single stage
     int32_t m_tile_begin, m_tile_end;    // ... over these row tiles
     int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
@@ -247,11 +252,13 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
                 const int32_t ntile_stage = sp.tiles_m * sp.tiles_n;
                 const int32_t first = (t - p.stage_base[s]) * sp.tiles_per_item;
                 ntiles = min(sp.tiles_per_item, ntile_stage - first);
-                // Stage 0 tiles follow the raster order; a consumer item carries work-queue slots
+                // Stage 0 tiles (and every stage's in the K-granular mode) follow the raster order;
+                // a consumer item of the queue protocol carries work-queue slots
                 // (first + j), which the CTAs that run it poll themselves (resolve_queue_slot), so
                 // the broadcast below is off the path from a queue push to the first load.
                 for (int32_t j = 0; j < ntiles; ++j)
-                    tiles[j] = s == 0 ? raster_tile(first + j, sp.tiles_m, sp.tiles_n, p.raster_group) : first + j;
+                    tiles[j] = (s == 0 || p.kwait) ? raster_tile(first + j, sp.tiles_m, sp.tiles_n, p.raster_group)
+                                                   : first + j;
                 stage = s;
             }
         } else {
@@ -351,6 +358,61 @@ __device__ __forceinline__ Item take_item(Ctrl *c, int32_t slot)
     return it;
 }
 
+// K-granular consumer wait: block until every epilogue warp of every split-K slice of producer
+// tile `ptile` (the stage before s) has released its rows in this run.  Relaxed polls with
+// back-off and a deadline; the caller fences once after the last wait of a k-block.  Returns
+// false after an error (status recorded, abort raised).
+__device__ __forceinline__ bool wait_producer(const ChainParams &p, Ctrl *c, int32_t s, int32_t ptile)
+{
+    const BoundaryParams &bd = p.bd[s - 1];
+    const uint32_t want = bd.ready_quota * (c->epoch + 1u);
+    const uint32_t *r = bd.ready + ptile;
+    if (static_cast<int32_t>(ld_relaxed_gpu_u32(r) - want) >= 0)
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t backoff = 32;
+    while (true) {
+        __nanosleep(backoff);
+        backoff = backoff < 64 ? backoff * 2 : 64;
+        if (static_cast<int32_t>(ld_relaxed_gpu_u32(r) - want) >= 0)
+            return true;
+        if (c->abort_flag)
+            return false;
+        if (ld_relaxed_gpu_u32(p.status) != 0) {
+            c->abort_flag = 1;
+            return false;
+        }
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicCAS(p.status, 0u, kStatusTimeout);
+            c->abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Producer column tiles hi+1, hi+2, ... (up to `last`) of the row panel at `pbase` that have
+// already released in this run, taken in batches of relaxed loads issued together; returns the
+// last column tile of the unbroken ready run starting at hi.
+__device__ __forceinline__ int32_t scan_ready(const ChainParams &p, const Ctrl *c, int32_t s, int32_t pbase,
+                                              int32_t hi, int32_t last)
+{
+    const BoundaryParams &bd = p.bd[s - 1];
+    const uint32_t want = bd.ready_quota * (c->epoch + 1u);
+    while (hi < last) {
+        uint32_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = hi + 1 + j <= last ? ld_relaxed_gpu_u32(bd.ready + pbase + hi + 1 + j) : 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (hi + 1 + j > last || static_cast<int32_t>(v[j] - want) < 0)
+                return hi + j;
+        }
+        hi += 8;
+    }
+    return hi;
+}
+
 __device__ __forceinline__ void slice_range(int32_t k_blocks, int32_t kb_per_split, int32_t split, int32_t &kb0,
                                             int32_t &kb1)
 {
@@ -368,6 +430,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint64_t pol_act = policy_evict_last();    // activations are re-read by many tiles
     const uint64_t pol_w = policy_evict_first();     // each weight tile is read by one row panel
     const bool pipelined = p.pipelined != 0;
+    const bool kwait = pipelined && p.kwait != 0;
     EventRec *const events = pipelined ? p.events : nullptr;
     int32_t ps = 0;
     uint32_t pph = 0;
@@ -389,14 +452,15 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         }
         const int32_t s = item.stage;
         int32_t tile = item.tile;
-        if (pipelined && s > 0) {
+        const bool kwait_s = kwait && s > 0;
+        if (pipelined && s > 0 && !kwait) {
             tile = resolve_queue_slot(p, c, s, item.tile);
             if (tile < 0) {
                 free_item_slot(c, slot);
                 break;
             }
         }
-        if (s > 0)   // TMA (async proxy) reads of a producer's output come after the acquire
+        if (s > 0 && !kwait_s)   // TMA (async proxy) reads of a producer's output come after the acquire
             fence_proxy_async_global();
         if (events && item.split == 0) {
             EventRec *e = events + p.tile_base[s] + tile;
@@ -421,6 +485,14 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         int32_t kb0, kb1;
         slice_range(k_blocks, kbps, item.split, kb0, kb1);
         const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
+        // K-granular mode: the A tile of k block kb reads columns [kb*64, kb*64+64) of the
+        // previous stage's output, written by producer tiles kb*64/pBN .. (kb*64+63)/pBN of the
+        // same row panel; ready_hi is the last producer column tile known released.
+        const int32_t pBN = kwait_s ? p.st[s - 1].BN : 1;
+        const int32_t ptn = kwait_s ? p.st[s - 1].tiles_n : 1;
+        const int32_t pbase = kwait_s ? (tile / tiles_n) * ptn : 0;
+        int32_t ready_hi = -1;
+        const int32_t slice_last = kwait_s ? min(((kb1 - 1) * kBK + kBK - 1) / pBN, ptn - 1) : 0;
         bool ok = true;
         for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (leader && kb == lead_kb)
@@ -432,18 +504,37 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
             uint8_t *b = a + kABytes;
             mbar_arrive_expect_tx(&c->full[ps], bytes);
-            tma_load_2d(a, mapA, &c->full[ps], kb * kBK, m0, pol_act);
+            // Weights first: they depend on nothing, so in the K-granular mode they are in
+            // flight while this k block's producers finish.
             if (b_kmajor) {
                 tma_load_2d(b, mapB, &c->full[ps], kb * kBK, n0, pol_w);
             } else {
                 for (int32_t j = 0; j < nbox; ++j)
                     tma_load_2d(b + j * box_bytes, mapB, &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
             }
+            if (kwait_s) {
+                const int32_t hi = min((kb * kBK + kBK - 1) / pBN, ptn - 1);
+                if (hi > ready_hi) {
+                    for (int32_t n1 = max(ready_hi + 1, (kb * kBK) / pBN); n1 <= hi && ok; ++n1)
+                        ok = wait_producer(p, c, s, pbase + n1);
+                    // The acquire fence below is the expensive part (it waits for this SM's
+                    // copies in flight), so first take in, without waiting, every later producer
+                    // of this slice that is already done: one fence then covers them all.
+                    ready_hi = ok ? scan_ready(p, c, s, pbase, hi, slice_last) : hi;
+                    fence_acq_rel_gpu();          // acquire the producers' releases ...
+                    fence_proxy_async_global();   // ... and order the TMA reads after them
+                }
+            }
+            // (after a failed wait the load still goes out, so that the slot's transaction
+            // count completes and the drain below accounts for every copy in flight)
+            tma_load_2d(a, mapA, &c->full[ps], kb * kBK, m0, pol_act);
             ++fills[ps];
             if (++ps == num_pipe) {
                 ps = 0;
                 pph ^= 1;
             }
+            if (!ok)
+                break;
         }
         free_item_slot(c, slot);
         if (!ok)
@@ -768,8 +859,14 @@ __device__ __forceinline__ void publish(const ChainParams &p, Ctrl *c, int32_t s
     if (log_it && warp == 4 && lane == 0)
         log_end(p, s, tile);
     __syncwarp();
-    if (producer && !(s == 0 && tile == p.drop_tile))
-        release_tile(p, c, s, tile, lane, pl);
+    if (!producer || (s == 0 && tile == p.drop_tile))
+        return;
+    if (p.kwait) {   // K-granular mode: count this warp's release on the producer tile itself
+        if (lane == 0)
+            red_add_relaxed_gpu(p.bd[s].ready + tile, 1u);
+        return;
+    }
+    release_tile(p, c, s, tile, lane, pl);
 }
 
 __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uint32_t tmem_base, uint32_t rank,
@@ -788,6 +885,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
     const int32_t cs = p.cs;
     const size_t partial_floats = static_cast<size_t>(p.partial_floats);
     const bool pipelined = p.pipelined != 0;
+    const bool kwait = pipelined && p.kwait != 0;
     const int32_t num_stages = p.num_stages;
     const bool logging = p.events != nullptr;
     const size_t cbase = static_cast<size_t>(cluster_id_x()) * cs;
@@ -809,7 +907,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             continue;
         const int32_t s = item.stage;
         int32_t tile = item.tile;
-        if (pipelined && s > 0) {   // the TMA warp of this CTA polled the same slot first
+        if (pipelined && s > 0 && !kwait) {   // the TMA warp of this CTA polled the same slot first
             int32_t t = 0;
             if (lane == 0)
                 t = resolve_queue_slot(p, c, s, item.tile);
@@ -826,7 +924,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
         const bool producer = pipelined && s + 1 < num_stages;
         ReleasePlan pl{0, -1, 0, 0, 0, -1, -1};
-        if (producer)
+        if (producer && !kwait)
             pl = plan_release(p, s, tile, lane);
         if (!warp_wait_bar(&c->tfull[acc], acc_ph, c, p))
             break;

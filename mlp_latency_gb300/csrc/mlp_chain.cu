@@ -56,12 +56,15 @@ bool encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, in
 
 struct DeviceBoundary {
     int32_t *pg_off = nullptr, *pg_tgt = nullptr, *grp_off = nullptr, *grp_mem = nullptr, *grp_init = nullptr;
-    uint32_t *count = nullptr, *tail = nullptr;
+    uint32_t *count = nullptr, *tail = nullptr, *ready = nullptr;
     unsigned long long *queue = nullptr;
-    size_t groups = 0, consumers = 0;
+    size_t groups = 0, consumers = 0, producers = 0;
 };
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Both pipelined modes run one persistent, co-resident grid over all stages.
+bool is_pipelined(int mode) { return mode == MLP_MODE_PIPELINED || mode == MLP_MODE_PIPELINED_KWAIT; }
 
 }  // namespace
 
@@ -173,7 +176,8 @@ static mlp_status full_reset(mlp_chain *h)
         const DeviceBoundary &db = h->db[b];
         if (cudaMemcpy(db.count, db.grp_init, db.groups * sizeof(int32_t), cudaMemcpyDeviceToDevice) != cudaSuccess ||
             cudaMemset(db.queue, 0, db.consumers * sizeof(unsigned long long)) != cudaSuccess ||
-            cudaMemset(h->db[b].tail, 0, sizeof(uint32_t)) != cudaSuccess)
+            cudaMemset(h->db[b].tail, 0, sizeof(uint32_t)) != cudaSuccess ||
+            cudaMemset(db.ready, 0, db.producers * sizeof(uint32_t)) != cudaSuccess)
             return MLP_ERR_CUDA;
     }
     return cudaDeviceSynchronize() == cudaSuccess ? MLP_OK : MLP_ERR_CUDA;
@@ -217,7 +221,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_INVALID_ARG;
     if (d->residual && d->dims[S] != d->dims[0])
         return MLP_ERR_INVALID_ARG;
-    if (d->mode != MLP_MODE_PIPELINED && d->mode != MLP_MODE_SEQUENTIAL && d->mode != MLP_MODE_MICROBATCH)
+    if (!is_pipelined(d->mode) && d->mode != MLP_MODE_SEQUENTIAL && d->mode != MLP_MODE_MICROBATCH)
         return MLP_ERR_INVALID_ARG;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < mlpc::kBM || d->microbatch_rows % mlpc::kBM))
         return MLP_ERR_INVALID_ARG;
@@ -343,7 +347,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     } else {
         h->grid = std::min(h->max_clusters, total_items) * h->cs;
     }
-    if (d->mode == MLP_MODE_PIPELINED && h->grid / h->cs > h->max_clusters) {
+    if (is_pipelined(d->mode) && h->grid / h->cs > h->max_clusters) {
         release(h);  // the pipelined grid must be co-resident
         return MLP_ERR_INVALID_ARG;
     }
@@ -374,6 +378,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         bytes = align_up(bytes, 256) + G.grp_init.size() * 4;      // count
         bytes = align_up(bytes, 256) + h->init[b].size() * 8;      // queue
         bytes = align_up(bytes, 256) + 4;                          // tail
+        bytes = align_up(bytes, 256) + (h->off[b].size() - 1) * 4; // ready (K-granular mode)
     }
     if (d->debug_flags & MLP_DEBUG_EVENT_LOG) {
         h->n_events = static_cast<size_t>(total);
@@ -415,6 +420,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         db.count = static_cast<uint32_t *>(take(G.grp_init.size() * 4));
         db.queue = static_cast<unsigned long long *>(take(db.consumers * 8));
         db.tail = static_cast<uint32_t *>(take(4));
+        db.producers = h->off[b].size() - 1;
+        db.ready = static_cast<uint32_t *>(take(db.producers * 4));
         auto up = [&](int32_t *dst, const std::vector<int32_t> &v) {
             if (!v.empty())
                 ok = ok && cudaMemcpy(dst, v.data(), v.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess;
@@ -539,6 +546,8 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.bd[b].count = h->db[b].count;
         P.bd[b].queue = h->db[b].queue;
         P.bd[b].tail = h->db[b].tail;
+        P.bd[b].ready = h->db[b].ready;
+        P.bd[b].ready_quota = static_cast<uint32_t>(h->split[b] * mlpc::kEpiWarps);
     }
     P.num_stages = h->S;
     for (int s = 0; s <= h->S; ++s) {
@@ -625,8 +634,9 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
         return ps;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ChainParams P = h->params;
-    if (h->desc.mode == MLP_MODE_PIPELINED) {
+    if (is_pipelined(h->desc.mode)) {
         P.pipelined = 1;
+        P.kwait = h->desc.mode == MLP_MODE_PIPELINED_KWAIT;
         if (h->fault_armed) {
             P.drop_tile = h->desc.drop_tile;
             h->fault_armed = false;
@@ -764,7 +774,7 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->pipe_stages = h->num_pipe;
     info->smem_bytes = static_cast<int32_t>(h->smem);
     info->tmem_cols = static_cast<int32_t>(h->tmem_cols);
-    info->launches_per_run = h->desc.mode == MLP_MODE_PIPELINED ? 1
+    info->launches_per_run = is_pipelined(h->desc.mode) ? 1
                              : h->desc.mode == MLP_MODE_SEQUENTIAL ? h->S
                                                                    : h->S * h->n_chunks;
     info->cluster_size = h->cs;

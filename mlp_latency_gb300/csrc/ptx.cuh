@@ -315,6 +315,11 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
+__device__ __forceinline__ void red_add_relaxed_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v)
 {
     uint32_t old;
