@@ -258,7 +258,8 @@ def run_reference(args, w):
     if rank != 0:
         return
     X, Ws = si.draw(w, seed=0)
-    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    # each step is a row sample sized so that the whole run stays near two minutes of CPU time
+    budget = min(20.0, 120.0 / max(1, args.steps + args.warmup))
     import oracle
     xb, wb = si.bits(X), [si.bits(t) for t in Ws]
     threads = oracle.default_threads()
