@@ -293,6 +293,80 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------- sequence-length sweep --
+def run_sweep(args):
+    """Latency of the 2-GEMM chain against the row count M (the input sequence length) with
+    fixed d x d weights, per launch mode, with the micro-batch chunk size swept at every M: the
+    single-GPU analogue of the paper's sequence-length study (section IV, Fig. 5).  One JSON
+    line per M; Y is checked bit-identical across the modes."""
+    import torch
+    import mlp_latency_gb300 as mc
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mc.load()
+    d = args.sweep_d
+    ms_list = [int(v) for v in args.sweep_m.split(",")]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    for M in ms_list:
+        w = si.make_workload(f"sweep_m{M}_d{d}", M, (d, d, d))
+        X, Ws = si.draw(w, seed=0)
+        Xd, Wd = X.to(dev), [t.to(dev) for t in Ws]
+        Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        ref = None
+        line = {"sweep": "sequence length", "M": M, "dims": [d, d, d], "flops": w.flops,
+                "l2": "flushed between steps", "graph": "one CUDA graph replay per step"}
+
+        def timed(mode, rows=0):
+            nonlocal ref
+            with mc.Chain(M, w.dims, mode=mode, microbatch_rows=rows, device=local) as ch:
+                ws = torch.empty(max(ch.workspace_size(), 256), dtype=torch.uint8, device=dev)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    ch.run(Xd, Wd, Y, ws, stream=stream)
+                    torch.cuda.synchronize()
+                    if ch.check(stream) != 0:
+                        raise RuntimeError(f"device status set ({mode}, M={M})")
+                    with torch.cuda.graph(g, stream=stream):
+                        ch.run(Xd, Wd, Y, ws, stream=stream)
+                    torch.cuda.synchronize()
+                    for _ in range(args.warmup):
+                        flush_buf.zero_()
+                        g.replay()
+                    t_est = max(1e-6, w.flops / 1.0e15)          # rough time per step, for the step count
+                    steps = int(max(10, min(args.steps, 0.3 / t_est)))
+                    med = statistics.median(time_steps(g.replay, flush_buf.zero_, steps, stream)) * 1e3
+                    if ch.check(stream) != 0:
+                        raise RuntimeError(f"device status set ({mode}, M={M})")
+                y = Y.view(torch.int16).clone()
+                if ref is None:
+                    ref = y
+                elif not torch.equal(ref, y):
+                    raise RuntimeError(f"{mode} (rows {rows}) differs from the first mode at M={M}")
+                return med
+
+        for mode in ("sequential", "pipelined", "pipelined_kwait"):
+            line[f"{mode}_us"] = timed(mode)
+        best = None
+        rows = 128
+        while rows <= M // 2:
+            t = timed("microbatch", rows)
+            line[f"microbatch_{rows}_us"] = t
+            if best is None or t < best[1]:
+                best = (rows, t)
+            rows *= 2
+        line["microbatch_best_us"] = best[1] if best else None
+        line["microbatch_best_rows"] = best[0] if best else None
+        line["bit_identical_across_modes"] = True
+        print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------------- main --
 def main():
     ap = argparse.ArgumentParser()
@@ -315,10 +389,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="only run this many graph replays after warm-up (for ncu); prints nothing")
+    ap.add_argument("--sweep-m", default=None,
+                    help="comma-separated row counts: time the 2-GEMM chain with d x d weights at each "
+                         "(one JSON line per M) instead of the bench step")
+    ap.add_argument("--sweep-d", type=int, default=8192)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = si.WORKLOADS[args.workload]
+    if args.sweep_m:
+        run_sweep(args)
+        return
 
     if args.impl == "reference":
         run_reference(args, w)
