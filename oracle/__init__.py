@@ -50,7 +50,9 @@ def _load():
             lib = ctypes.CDLL(build())
             i64, i32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
             lib.oracle_chain.restype = ctypes.c_int
-            lib.oracle_chain.argtypes = [i64, i32, vp, vp, vp, i32, i32, vp, i64, vp, vp, i32]
+            lib.oracle_chain.argtypes = [i64, i32, vp, vp, vp, i32, i32, i32, vp, i64, vp, vp, i32]
+            lib.oracle_silu.restype = ctypes.c_double
+            lib.oracle_silu.argtypes = [ctypes.c_double]
             lib.oracle_deps.restype = i64
             lib.oracle_deps.argtypes = [i64, i64, i64, i32, i32, i32, i32, vp, vp, i64, vp]
             lib.oracle_gelu_tanh.restype = ctypes.c_double
@@ -77,18 +79,22 @@ def default_threads() -> int:
 
 def chain(X, Ws: Sequence, gelu: bool = False, residual: bool = False,
           rows: Optional[np.ndarray] = None, threads: Optional[int] = None,
-          return_h: bool = False):
+          return_h: bool = False, gated: bool = False):
     """Y (and optionally the first intermediate H) of the chain, for all rows or ``rows``.
 
-    X: M x d0 bf16 bits; Ws[s]: d_s x d_{s+1} bf16 bits. Returns uint16 arrays
-    (len(rows) or M) x d_S, and (..) x d_1 for H.
+    X: M x d0 bf16 bits; Ws[s]: d_s x d_{s+1} bf16 bits. With ``gated`` the first stage takes
+    two matrices, Ws[0] (gate) and Ws[1] (up), both d0 x d1, and H = SiLU(X Wg) * (X Wu).
+    Returns uint16 arrays (len(rows) or M) x d_S, and (..) x d_1 for H.
     """
     lib = _load()
     X = _u16(X)
     Ws = [_u16(w) for w in Ws]
     M = X.shape[0]
-    dims = [X.shape[1]] + [w.shape[1] for w in Ws]
-    for s, w in enumerate(Ws):
+    if gated and (len(Ws) < 3 or Ws[0].shape != Ws[1].shape):
+        raise ValueError("a gated chain needs gate and up matrices of one shape, then the rest")
+    stage_ws = Ws[1:] if gated else Ws
+    dims = [X.shape[1]] + [w.shape[1] for w in stage_ws]
+    for s, w in enumerate(stage_ws):
         if w.shape[0] != dims[s]:
             raise ValueError(f"W{s + 1} has {w.shape[0]} rows, expected {dims[s]}")
     dims_a = np.array(dims, dtype=np.int64)
@@ -100,8 +106,8 @@ def chain(X, Ws: Sequence, gelu: bool = False, residual: bool = False,
         n = M
     Y = np.empty((n, dims[-1]), dtype=np.uint16)
     H = np.empty((n, dims[1]), dtype=np.uint16) if return_h else None
-    rc = lib.oracle_chain(M, len(Ws), dims_a.ctypes.data, X.ctypes.data, wptrs, int(gelu),
-                          int(residual), rows.ctypes.data if rows is not None else None, n,
+    rc = lib.oracle_chain(M, len(stage_ws), dims_a.ctypes.data, X.ctypes.data, wptrs, int(gelu),
+                          int(residual), int(gated), rows.ctypes.data if rows is not None else None, n,
                           Y.ctypes.data, H.ctypes.data if H is not None else None,
                           threads or default_threads())
     if rc != 0:
@@ -142,3 +148,8 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
 def bf16_to_f32(b: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> fp32 (exact: shift into the upper half)."""
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def silu(x: float) -> float:
+    """The oracle's SiLU, x / (1 + e^-x) in double."""
+    return float(_load().oracle_silu(float(x)))

@@ -26,6 +26,12 @@
  *   - Chains with the GeLU option apply GeLU (tanh form) to the fp32 accumulator of every GEMM
  *     before rounding; with the residual option the last stage adds the chain input X (as fp32)
  *     to that value and rounds once.
+ *   - Gated chains (the SwiGLU MLP block the paper's critique names as the test of its claim:
+ *     an activation between the two matrix multiplies) compute the first stage from two weight
+ *     matrices, H = SiLU(X Wg) * (X Wu), the gated linear unit with the Swish-1 gate of Shazeer,
+ *     "GLU Variants Improve Transformer" (2020, eq. 6): both accumulators in fp32, SiLU and the
+ *     product in double, one rounding to bf16.  Later stages are unchanged (GeLU, if asked for,
+ *     applies to them only).
  *   - Dependency granularity is the whole tile: a consumer tile needs every producer tile that
  *     owns any element of the rows it reads (it reads all columns, since the next GEMM's
  *     reduction dimension is the producer's column dimension).
@@ -85,6 +91,14 @@ double oracle_gelu_tanh(double x)
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* SiLU (Swish-1): x * sigmoid(x) = x / (1 + e^-x), evaluated in double.                       */
+/* ------------------------------------------------------------------------------------------ */
+double oracle_silu(double x)
+{
+    return x / (1.0 + exp(-x));
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* The chain, one row at a time.  Row i of every intermediate depends only on row i of X.      */
 /* ------------------------------------------------------------------------------------------ */
 
@@ -93,8 +107,9 @@ typedef struct {
     int32_t num_gemms;
     const int64_t *dims;      /* num_gemms + 1 entries: dims[0] = K of the first GEMM        */
     const uint16_t *X;        /* M x dims[0], row-major bf16 bits                            */
-    const uint16_t *const *W; /* W[s]: dims[s] x dims[s+1], row-major bf16 bits              */
-    int32_t gelu;             /* apply GeLU(tanh) to every GEMM's accumulator                */
+    const uint16_t *const *W; /* W[s + gated]: dims[s] x dims[s+1], row-major bf16 bits      */
+    int32_t gelu;             /* apply GeLU(tanh) to every (ungated) GEMM's accumulator      */
+    int32_t gated;            /* first stage: H = SiLU(X W[0]) * (X W[1])                    */
     int32_t residual;         /* add X to the last stage (requires dims[last] == dims[0])    */
     const int64_t *rows;      /* rows to compute (NULL: 0..M-1)                              */
     int64_t nrows;
@@ -124,9 +139,10 @@ static void *chain_worker(void *arg)
     uint16_t *cur = (uint16_t *)malloc((size_t)job->maxdim * sizeof(uint16_t));
     uint16_t *nxt = (uint16_t *)malloc((size_t)job->maxdim * sizeof(uint16_t));
     float *acc = (float *)malloc((size_t)job->maxdim * sizeof(float));
-    if (!cur || !nxt || !acc) {
+    float *up = (float *)malloc((size_t)job->maxdim * sizeof(float));
+    if (!cur || !nxt || !acc || !up) {
         job->status = -2;
-        free(cur); free(nxt); free(acc);
+        free(cur); free(nxt); free(acc); free(up);
         return NULL;
     }
     const int32_t S = job->num_gemms;
@@ -138,11 +154,16 @@ static void *chain_worker(void *arg)
         memcpy(cur, xrow, (size_t)d_in * sizeof(uint16_t));
         for (int32_t s = 0; s < S; ++s) {
             const int64_t K = job->dims[s], N = job->dims[s + 1];
-            row_times_matrix(cur, K, job->W[s], N, acc);
+            const int gated = job->gated && s == 0;
+            row_times_matrix(cur, K, job->W[s == 0 ? 0 : s + job->gated], N, acc);
+            if (gated)
+                row_times_matrix(cur, K, job->W[1], N, up);
             const int last = (s == S - 1);
             for (int64_t n = 0; n < N; ++n) {
                 float v = acc[n];
-                if (job->gelu)
+                if (gated)
+                    v = (float)(oracle_silu((double)v) * (double)up[n]);
+                else if (job->gelu)
                     v = (float)oracle_gelu_tanh((double)v);
                 if (last && job->residual)
                     v = v + bf16_bits_to_float(xrow[n]);
@@ -154,14 +175,14 @@ static void *chain_worker(void *arg)
         }
         memcpy(job->Y + r * d_out, cur, (size_t)d_out * sizeof(uint16_t));
     }
-    free(cur); free(nxt); free(acc);
+    free(cur); free(nxt); free(acc); free(up);
     return NULL;
 }
 
 /* Returns 0 on success, -1 on bad arguments, -2 on host allocation failure. */
 int oracle_chain(int64_t M, int32_t num_gemms, const int64_t *dims, const uint16_t *X,
-                 const uint16_t *const *W, int32_t gelu, int32_t residual, const int64_t *rows,
-                 int64_t nrows, uint16_t *Y, uint16_t *H, int32_t threads)
+                 const uint16_t *const *W, int32_t gelu, int32_t residual, int32_t gated,
+                 const int64_t *rows, int64_t nrows, uint16_t *Y, uint16_t *H, int32_t threads)
 {
     if (M < 0 || num_gemms < 1 || !dims || !X || !W || !Y)
         return -1;
@@ -190,7 +211,7 @@ int oracle_chain(int64_t M, int32_t num_gemms, const int64_t *dims, const uint16
     pthread_t tid[256];
     int started[256];
     for (int32_t t = 0; t < threads; ++t) {
-        chain_job j = {M, num_gemms, dims, X, W, gelu, residual, rows, nrows, Y, H,
+        chain_job j = {M, num_gemms, dims, X, W, gelu, gated != 0, residual, rows, nrows, Y, H,
                        nrows * t / threads, nrows * (t + 1) / threads, maxdim, 0};
         jobs[t] = j;
         started[t] = (threads > 1) && pthread_create(&tid[t], NULL, chain_worker, &jobs[t]) == 0;

@@ -6,6 +6,7 @@ Fig. 3-5; no dataset is involved).
 
 Recipe: one ``torch.Generator('cpu')`` seeded with ``seed`` draws, in the order X, W1, W2, ...,
 each tensor as ``randn(float32) * std`` and then casts it to bfloat16 (round to nearest even).
+A gated chain draws X, W_gate, W_up, W2, ... (gate and up share the first stage's std).
 ``N(0, 1/d)`` in a workload description means variance 1/d, i.e. ``std = 1/sqrt(d)``.
 """
 from __future__ import annotations
@@ -32,6 +33,7 @@ class Workload:
     tile_m: int = 0                # 0: library default
     tile_n: int = 0
     description: str = ""
+    gated: bool = False            # first stage from two weights: SiLU(X Wg) * (X Wu)
 
     @property
     def num_gemms(self) -> int:
@@ -39,13 +41,16 @@ class Workload:
 
     @property
     def flops(self) -> int:
-        return sum(2 * self.M * self.dims[i] * self.dims[i + 1] for i in range(self.num_gemms))
+        f = sum(2 * self.M * self.dims[i] * self.dims[i + 1] for i in range(self.num_gemms))
+        return f + (2 * self.M * self.dims[0] * self.dims[1] if self.gated else 0)
 
     @property
     def algorithmic_bytes(self) -> int:
         """X + every W + Y, plus each intermediate written once and read once (bf16)."""
         b = self.M * self.dims[0] * 2
         b += sum(self.dims[i] * self.dims[i + 1] * 2 for i in range(self.num_gemms))
+        if self.gated:
+            b += self.dims[0] * self.dims[1] * 2
         b += self.M * self.dims[-1] * 2
         b += sum(2 * self.M * d * 2 for d in self.dims[1:-1])
         if self.residual:
@@ -72,6 +77,11 @@ WORKLOADS = {
     "llama_m256_4096_14336": Workload(
         "llama_m256_4096_14336", 256, (4096, 14336, 4096), 1.0, (_sq(4096), _sq(14336)),
         description="X[256x4096] W1[4096x14336] W2[14336x4096], W1~N(0,1/4096), W2~N(0,1/14336)"),
+    "llama_swiglu_m256_4096_14336": Workload(
+        "llama_swiglu_m256_4096_14336", 256, (4096, 14336, 4096), 1.0, (_sq(4096), _sq(14336)),
+        gated=True,
+        description="Llama-style gated MLP: X[256x4096], Wg,Wu[4096x14336]~N(0,1/4096), "
+                    "H = SiLU(X Wg) * (X Wu), W2[14336x4096]~N(0,1/14336)"),
     "gelu4_m512_d8192": Workload(
         "gelu4_m512_d8192", 512, (8192,) * 5, 1.0, (_sq(8192),) * 4, gelu=True, residual=True,
         description="4 GEMMs d=8192, GeLU(tanh) after each, residual X at the end, M=512"),
@@ -80,11 +90,12 @@ WORKLOADS = {
 
 def make_workload(name: str, M: int, dims: Sequence[int], x_std: float = 1.0,
                   w_std: Optional[Sequence[float]] = None, gelu: bool = False,
-                  residual: bool = False, tile_m: int = 0, tile_n: int = 0) -> Workload:
+                  residual: bool = False, tile_m: int = 0, tile_n: int = 0, gated: bool = False) -> Workload:
     dims = tuple(int(d) for d in dims)
     if w_std is None:
         w_std = tuple(_sq(d) for d in dims[:-1])
-    return Workload(name, int(M), dims, float(x_std), tuple(w_std), gelu, residual, tile_m, tile_n)
+    return Workload(name, int(M), dims, float(x_std), tuple(w_std), gelu, residual, tile_m, tile_n,
+                    gated=gated)
 
 
 def draw(w: Workload, seed: int = 0) -> Tuple[torch.Tensor, List[torch.Tensor]]:
@@ -93,13 +104,13 @@ def draw(w: Workload, seed: int = 0) -> Tuple[torch.Tensor, List[torch.Tensor]]:
     g.manual_seed(seed)
     x = (torch.randn(w.M, w.dims[0], generator=g, dtype=torch.float32) * w.x_std).to(torch.bfloat16)
     ws = []
-    for i in range(w.num_gemms):
+    for i in ([0] if w.gated else []) + list(range(w.num_gemms)):
         t = torch.randn(w.dims[i], w.dims[i + 1], generator=g, dtype=torch.float32) * w.w_std[i]
         ws.append(t.to(torch.bfloat16))
     return x, ws
 
 
-def draw_integer(M: int, dims: Sequence[int], seed: int = 0, values=(-1, 0, 1)):
+def draw_integer(M: int, dims: Sequence[int], seed: int = 0, values=(-1, 0, 1), gated: bool = False):
     """Integer-valued bf16 inputs: every entry drawn uniformly from ``values``.
 
     With small integers every partial sum is an integer; while the sums stay below 2**24 in
@@ -110,7 +121,7 @@ def draw_integer(M: int, dims: Sequence[int], seed: int = 0, values=(-1, 0, 1)):
     vals = torch.tensor(values, dtype=torch.float32)
     x = vals[torch.randint(0, len(values), (M, dims[0]), generator=g)].to(torch.bfloat16)
     ws = [vals[torch.randint(0, len(values), (dims[i], dims[i + 1]), generator=g)].to(torch.bfloat16)
-          for i in range(len(dims) - 1)]
+          for i in ([0] if gated else []) + list(range(len(dims) - 1))]
     return x, ws
 
 

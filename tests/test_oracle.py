@@ -69,6 +69,79 @@ def test_gelu_matches_torch_float64(oracle_mod):
     assert torch.max(torch.abs(ours - ref)).item() < 1e-13
 
 
+def test_silu_identities(oracle_mod):
+    # x*sigmoid(x): odd part x/2 (so silu(x) - silu(-x) = x), limits x and 0, and the textbook
+    # minimum of about -0.27846 at x = -1.27846 (the root of 1 + x(1 - sigmoid(x)) = 0)
+    assert oracle_mod.silu(0.0) == 0.0
+    for x in np.linspace(-8, 8, 129):
+        assert abs((oracle_mod.silu(x) - oracle_mod.silu(-x)) - x) <= 1e-14 * max(1.0, abs(x))
+    assert abs(oracle_mod.silu(40.0) - 40.0) < 1e-12
+    assert abs(oracle_mod.silu(-40.0)) < 1e-12
+    xs = np.linspace(-1.35, -1.2, 3001)
+    vals = np.array([oracle_mod.silu(v) for v in xs])
+    assert abs(xs[np.argmin(vals)] + 1.27846) < 1e-4 and abs(vals.min() + 0.27846) < 1e-5
+
+
+def test_silu_matches_torch_float64(oracle_mod):
+    xs = torch.linspace(-20, 20, 2001, dtype=torch.float64)
+    ref = torch.nn.functional.silu(xs)
+    ours = torch.tensor([oracle_mod.silu(float(v)) for v in xs], dtype=torch.float64)
+    assert torch.max(torch.abs(ours - ref) / (1.0 + torch.abs(ref))).item() < 1e-15
+
+
+def gated_bound_ok(got_bits, x, wg, wu):
+    """H = SiLU(x wg) * (x wu) against the exact products (math.fsum) and an independent sigmoid
+    (1 + tanh(z/2)) / 2.  Each fp32 accumulator is within g A of its exact value (any order of K
+    additions); SiLU has slope below 1.1, so the product is within the linearised bound below,
+    plus half a bf16 ulp of rounding."""
+    K = x.shape[1]
+    u = 2.0 ** -24
+    g = K * u / (1 - K * u)
+    ge, ue = exact_matmul(x, wg), exact_matmul(x, wu)
+    dg = g * (np.abs(x.astype(np.float64)) @ np.abs(wg.astype(np.float64)))
+    du = g * (np.abs(x.astype(np.float64)) @ np.abs(wu.astype(np.float64)))
+    silu = ge * 0.5 * (1.0 + np.tanh(ge / 2.0))
+    exact = silu * ue
+    lin = 1.1 * dg * (np.abs(ue) + du) + np.abs(silu) * du + 1e-300
+    bound = 2.0 ** -8 * (np.abs(exact) + lin) + lin * (1 + 1e-6)
+    got = f32(got_bits).astype(np.float64)
+    return bool(np.all(np.abs(got - exact) <= bound)), float(np.max(np.abs(got - exact) - bound))
+
+
+@pytest.mark.parametrize("M,K,N1,N2", [(12, 32, 24, 40), (9, 64, 48, 16)])
+def test_gated_chain_vs_exact_triple_loop(oracle_mod, M, K, N1, N2):
+    w = si.make_workload("t", M, (K, N1, N2), gated=True)
+    X, (Wg, Wu, W2) = si.draw(w, seed=5)
+    Y, H = oracle_mod.chain(si.bits(X), [si.bits(Wg), si.bits(Wu), si.bits(W2)], gated=True,
+                            return_h=True, threads=2)
+    x, wg, wu, w2 = (f32(si.bits(t)) for t in (X, Wg, Wu, W2))
+    ok, excess = gated_bound_ok(H, x, wg, wu)
+    assert ok, excess
+    ok, excess = stage_bound_ok(Y, f32(H), w2)     # the second stage is a plain GEMM of H
+    assert ok, excess
+
+
+def test_gated_chain_planted_mistakes_fail_the_pin(oracle_mod):
+    M, K, N = 16, 48, 40
+    w = si.make_workload("t", M, (K, N, N), gated=True)
+    X, (Wg, Wu, W2) = si.draw(w, seed=6)
+    x, wg, wu = (f32(si.bits(t)) for t in (X, Wg, Wu))
+    # gate and up swapped, or the gate's SiLU dropped: both must fall outside the bound
+    _, Hs = oracle_mod.chain(si.bits(X), [si.bits(Wu), si.bits(Wg), si.bits(W2)], gated=True,
+                             return_h=True)
+    assert not gated_bound_ok(Hs, x, wg, wu)[0]
+    prod = (exact_matmul(x, wg) * exact_matmul(x, wu)).astype(np.float32)
+    assert not gated_bound_ok(oracle_mod.round_bf16(prod), x, wg, wu)[0]
+
+
+def test_gated_chain_zero_gate_is_exactly_zero(oracle_mod):
+    # SiLU(0) = 0: a zero gate matrix zeroes H, and with it Y, bit for bit
+    X, (Wg, Wu, W2) = si.draw_integer(8, (64, 32, 16), seed=7, gated=True)
+    Y, H = oracle_mod.chain(si.bits(X), [np.zeros_like(si.bits(Wg)), si.bits(Wu), si.bits(W2)], gated=True,
+                            return_h=True)
+    assert not np.any(f32(H)) and not np.any(f32(Y))
+
+
 # ------------------------------------------------------------------------------ the chain ----
 def exact_matmul(a, b):
     """float64 matrix of exactly-summed (math.fsum) products; inputs are bf16 values as floats."""
