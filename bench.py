@@ -213,7 +213,7 @@ def cpu_oracle_baseline(w, X, Ws, budget_s: float, Y_gpu=None):
     # pick a row count that takes about budget_s / 3 per call, then repeat within the budget
     rows = si.sample_rows(w.M, min(w.M, 8), seed=3)
     t0 = time.perf_counter()
-    oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+    oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, gated=w.gated, rows=rows, threads=threads)
     per_row = (time.perf_counter() - t0) / len(rows)
     n = int(max(1, min(w.M, (budget_s / 3) / max(per_row, 1e-9))))
     rows = np.arange(w.M, dtype=np.int64) if n >= w.M else si.sample_rows(w.M, n, seed=4)
@@ -221,7 +221,7 @@ def cpu_oracle_baseline(w, X, Ws, budget_s: float, Y_gpu=None):
     parity = None
     while total_t < budget_s or calls == 0:
         t0 = time.perf_counter()
-        Yo = oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+        Yo = oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, gated=w.gated, rows=rows, threads=threads)
         total_t += time.perf_counter() - t0
         total_rows += len(rows)
         calls += 1
@@ -265,16 +265,16 @@ def run_reference(args, w):
     threads = oracle.default_threads()
     rows = si.sample_rows(w.M, min(w.M, 4), seed=3)
     t0 = time.perf_counter()
-    oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+    oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, gated=w.gated, rows=rows, threads=threads)
     per_row = (time.perf_counter() - t0) / len(rows)
     n = int(max(1, min(w.M, budget / max(per_row, 1e-9))))
     rows = np.arange(w.M, dtype=np.int64) if n >= w.M else si.sample_rows(w.M, n, seed=4)
     for _ in range(args.warmup):
-        oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+        oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, gated=w.gated, rows=rows, threads=threads)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, rows=rows, threads=threads)
+        oracle.chain(xb, wb, gelu=w.gelu, residual=w.residual, gated=w.gated, rows=rows, threads=threads)
         times.append(time.perf_counter() - t0)
     step_s = statistics.mean(times)
     flops = w.flops / w.M * len(rows)
@@ -432,7 +432,7 @@ def main():
         return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
                         microbatch_rows=rows, device=local, raster_group=args.raster_group,
                         pipe_stages=args.pipe_stages, acc_split=args.acc_split,
-                        weight_layout=args.weight_layout, k_split=ksplit)
+                        weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()
@@ -524,7 +524,11 @@ def main():
 
                 def torch_chain():
                     h = Xd
-                    for t in Wd_kn:
+                    rest = Wd_kn
+                    if w.gated:   # SwiGLU block in torch: silu(X Wg) * (X Wu), then the rest
+                        h = torch.nn.functional.silu(torch.matmul(h, Wd_kn[0])) * torch.matmul(h, Wd_kn[1])
+                        rest = Wd_kn[2:]
+                    for t in rest:
                         h = torch.matmul(h, t)
                     Y.copy_(h)
                 g = capture(torch_chain)
@@ -578,7 +582,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
-                       "residual": w.residual, "mode": args.mode, "tile_m": 128, "tile_n": info["tile_n"],
+                       "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": 128, "tile_n": info["tile_n"],
                        "k_split": info["k_split"], "cluster_size": info["cluster_size"],
                        "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",

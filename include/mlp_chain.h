@@ -122,6 +122,14 @@ typedef struct {
                                            alternate between two accumulators that the epilogue
                                            adds (even + odd), so consecutive MMAs do not depend on
                                            each other; needs 4 * tile_n <= 512                    */
+    int32_t gated;                      /* nonzero: the first GEMM is a gated linear unit with a
+                                           SiLU gate (the SwiGLU MLP block): run() takes
+                                           S + 1 weights, W[0] = gate and W[1] = up (both
+                                           dims[0] x dims[1]), and A_1 = SiLU(X W[0]) * (X W[1])
+                                           from two fp32 accumulators, rounded once; W[s + 1] is
+                                           the weight of GEMM s >= 1.  The gated GEMM runs
+                                           unsplit with tile_n <= 128 and acc_split 1; epilogue
+                                           (GeLU) applies to the later GEMMs only                 */
 } mlp_chain_desc;
 
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG).  t_* are %globaltimer ns;
@@ -161,7 +169,8 @@ mlp_status mlp_chain_create(const mlp_chain_desc *desc, mlp_chain_t *out);
 mlp_status mlp_chain_workspace_size(mlp_chain_t h, size_t *bytes);
 
 /* Enqueue the whole chain on `stream` (asynchronous).  X: M x dims[0]; W[s]: dims[s] x
- * dims[s+1]; Y: M x dims[S]; workspace: >= mlp_chain_workspace_size bytes, 256-byte aligned.
+ * dims[s+1] (S + 1 weights when gated: see mlp_chain_desc.gated); Y: M x dims[S]; workspace:
+ * >= mlp_chain_workspace_size bytes, 256-byte aligned.
  * All device pointers.  Returns INVALID_ARG for null or misaligned pointers, CUDA if a launch
  * fails, DEVICE_STATE if a previous device error has not been collected by mlp_chain_check. */
 mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *const *W, void *Y,

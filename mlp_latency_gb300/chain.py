@@ -49,7 +49,8 @@ class Chain:
     """One handle of the library: a fixed chain shape, tile shape and launch mode.
 
     Shapes follow the header: X[M x dims[0]], W[s][dims[s] x dims[s+1]] (weight_layout "kn") or
-    W[s][dims[s+1] x dims[s]] ("nk", nn.Linear's layout), Y[M x dims[-1]].
+    W[s][dims[s+1] x dims[s]] ("nk", nn.Linear's layout), Y[M x dims[-1]].  With ``gated`` the
+    first GEMM is SwiGLU and run() takes one more weight: [W_gate, W_up, W_2, ...].
     """
 
     def __init__(self, M: int, dims: Sequence[int], *, tile_n: Optional[Sequence[int]] = None,
@@ -57,7 +58,7 @@ class Chain:
                  microbatch_rows: int = 0, device: int = 0, event_log: bool = False,
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
-                 weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None):
+                 weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -87,7 +88,9 @@ class Chain:
         d.weight_layout = {"kn": 0, "nk": 1}[weight_layout]
         for i, v in enumerate(k_split or []):
             d.k_split[i] = int(v)
+        d.gated = int(bool(gated))
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
+        self.n_weights = len(self.dims) - 1 + int(bool(gated))
         self._lib = lib
         h = ctypes.c_void_p()
         _check(lib.mlp_chain_create(ctypes.byref(d), ctypes.byref(h)), "mlp_chain_create")
@@ -119,6 +122,8 @@ class Chain:
         return n.value
 
     def _wptrs(self, Ws):
+        if len(Ws) != self.n_weights:
+            raise ValueError(f"expected {self.n_weights} weight tensors, got {len(Ws)}")
         for i, w in enumerate(Ws):
             self._wbuf[i] = w.data_ptr() if hasattr(w, "data_ptr") else int(w)
         return self._wbuf

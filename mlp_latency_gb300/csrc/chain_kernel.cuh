@@ -64,6 +64,8 @@ struct StageParams {
     int32_t items;          // cluster items of this stage
     float *partials;        // split-K through global memory: one 128 x BN fp32 buffer per CTA
     int32_t dsmem_reduce;   // split-K through the owners' shared memory (BN * 512 <= recv_bytes)
+    int32_t gated;          // SwiGLU: B tiles of gate (mapB) and up (mapU) weights, accumulators
+                            // side by side in TMEM, output SiLU(gate) * up; unsplit
 };
 
 // Stage boundary s -> s+1.  The scoreboard holds one counter per group of consumer tiles with
@@ -93,6 +95,7 @@ struct EventRec {
 struct ChainParams {
     CUtensorMap mapA[kMaxStages];
     CUtensorMap mapB[kMaxStages];
+    CUtensorMap mapU;                    // up-projection weights of a gated first stage
     StageParams st[kMaxStages];
     BoundaryParams bd[kMaxStages - 1];
     int32_t num_stages;
@@ -481,7 +484,9 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t box_cols = b_swz / 2;
         const uint32_t box_bytes = kBK * b_swz;
         const int32_t nbox = BN / box_cols;
-        const uint32_t bytes = kABytes + static_cast<uint32_t>(kBK * BN * 2);
+        const bool gated = spr.gated != 0;
+        const uint32_t b_tile_bytes = static_cast<uint32_t>(kBK * BN * 2);
+        const uint32_t bytes = kABytes + (gated ? 2u : 1u) * b_tile_bytes;
         int32_t kb0, kb1;
         slice_range(k_blocks, kbps, item.split, kb0, kb1);
         const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
@@ -506,11 +511,15 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             mbar_arrive_expect_tx(&c->full[ps], bytes);
             // Weights first: they depend on nothing, so in the K-granular mode they are in
             // flight while this k block's producers finish.
-            if (b_kmajor) {
-                tma_load_2d(b, mapB, &c->full[ps], kb * kBK, n0, pol_w);
-            } else {
-                for (int32_t j = 0; j < nbox; ++j)
-                    tma_load_2d(b + j * box_bytes, mapB, &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
+            for (int32_t u = 0; u < (gated ? 2 : 1); ++u) {   // gate (or plain) weights, then up
+                const CUtensorMap *mb = u ? &p.mapU : mapB;
+                uint8_t *bt = b + u * b_tile_bytes;
+                if (b_kmajor) {
+                    tma_load_2d(bt, mb, &c->full[ps], kb * kBK, n0, pol_w);
+                } else {
+                    for (int32_t j = 0; j < nbox; ++j)
+                        tma_load_2d(bt + j * box_bytes, mb, &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
+                }
             }
             if (kwait_s) {
                 const int32_t hi = min((kb * kBK + kBK - 1) / pBN, ptn - 1);
@@ -571,6 +580,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             continue;
         const StageParams &spr = p.st[item.stage];
         const uint32_t BN = static_cast<uint32_t>(spr.BN);
+        const bool gated = spr.gated != 0;
         const bool b_kmajor = spr.b_kmajor != 0;
         const uint32_t b_swz = static_cast<uint32_t>(spr.b_swz);
         int32_t kb0, kb1;
@@ -606,7 +616,14 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                 // overwrites.
                 const uint32_t j = static_cast<uint32_t>(kb - kb0) * (kBK / 16) + kk;
                 const uint32_t sub = split2 ? (j & 1u) : 0u;
-                mma_bf16_ss(d_tmem + sub * sub_stride, ad, bd, idesc, j >= (split2 ? 2u : 1u) ? 1u : 0u);
+                const uint32_t accum = j >= (split2 ? 2u : 1u) ? 1u : 0u;
+                mma_bf16_ss(d_tmem + sub * sub_stride, ad, bd, idesc, accum);
+                if (gated) {   // up weights (the next B tile of the slot), same A, accumulator BN columns on
+                    const uint32_t u_addr = b_addr + BN * kBK * 2u;
+                    const uint64_t ud = b_kmajor ? smem_desc(u_addr + kk * 32u, 16u, 1024u, 2u)
+                                                 : smem_desc(u_addr + kk * 16u * b_swz, kBK * b_swz, 8u * b_swz, b_code);
+                    mma_bf16_ss(d_tmem + BN, ad, ud, idesc, accum);
+                }
             }
             issued = true;
             mma_commit(&c->empty[ps]);  // frees the ring slot once these MMAs have read it
@@ -939,6 +956,16 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             for (int32_t c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t r[32];
                 load_acc(split2, sub_stride, taddr + c0, r);
+                if (spr.gated) {   // SwiGLU: SiLU(gate) * up, both fp32, rounded once below
+                    uint32_t u[32];
+                    tmem_ld_32x32b_x32(taddr + BN + c0, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float g = __uint_as_float(r[e]);
+                        r[e] = __float_as_uint(g / (1.0f + expf(-g)) * __uint_as_float(u[e]));
+                    }
+                }
                 store_chunk_warp(od, row0, n0 + c0, r, stage, lane);
             }
             tc_fence_before();
@@ -1135,6 +1162,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             prefetch_tensormap(&p.mapA[i]);
             prefetch_tensormap(&p.mapB[i]);
         }
+        if (p.st[0].gated)
+            prefetch_tensormap(&p.mapU);
     }
     if (warp == 1) {
         tmem_alloc(&c->tmem_base, p.tmem_cols);

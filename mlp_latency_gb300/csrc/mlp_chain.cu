@@ -92,7 +92,9 @@ struct mlp_chain {
     int32_t stage_base[MLP_MAX_GEMMS + 1] = {};
     // cached launch parameters (tensor maps are re-encoded only when a pointer changes)
     ChainParams params;
-    const void *c_X = nullptr, *c_W[MLP_MAX_GEMMS] = {}, *c_Y = nullptr, *c_ws = nullptr;
+    const void *c_X = nullptr, *c_W[MLP_MAX_GEMMS + 1] = {}, *c_Y = nullptr, *c_ws = nullptr;
+    int n_w = 0;             // weight pointers per run: S, plus the up matrix of a gated chain
+    int acc_cols = 0;        // TMEM columns of one accumulator buffer
     bool params_valid = false;
     bool fault_armed = false;   // MLP_DEBUG_DROP_DECREMENT fires on the first run only
     // micro-batch streams and events
@@ -225,6 +227,9 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_INVALID_ARG;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < mlpc::kBM || d->microbatch_rows % mlpc::kBM))
         return MLP_ERR_INVALID_ARG;
+    if (d->gated && (d->acc_split == 2 || (d->tile_n[0] != 0 && d->tile_n[0] > 128) ||
+                     (d->k_split[0] != 0 && d->k_split[0] != 1)))
+        return MLP_ERR_UNSUPPORTED;   // the gated GEMM keeps gate and up side by side in TMEM, unsplit
     if (d->grid_ctas < 0 || d->raster_group < 0 || d->pipe_stages < 0 || d->pipe_stages == 1 ||
         d->pipe_stages > mlpc::kMaxPipe || d->acc_split < 0 || d->acc_split > 2 || d->weight_layout < 0 ||
         d->weight_layout > 1)
@@ -285,7 +290,11 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
                                                                              : MLP_ERR_INVALID_ARG;
         }
         int bn = 0, split = 0;
-        if (choose_tiles(h->tiles_m, d->dims[s], d->dims[s + 1], clusters, tn, ks, &bn, &split) >= 1e29) {
+        // a gated GEMM issues two MMAs per k step into two accumulators: unsplit, at most 128 wide
+        const bool gate_s = d->gated && s == 0;
+        const int tn_s = gate_s && tn == 0 ? 128 : tn;
+        const int ks_s = gate_s ? 1 : ks;
+        if (choose_tiles(h->tiles_m, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn, &split) >= 1e29) {
             release(h);
             return MLP_ERR_UNSUPPORTED;   // no valid tile / split for this request
         }
@@ -304,6 +313,9 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->items[s] = (tiles + tpi - 1) / tpi;
     }
     h->stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
+    if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles
+        h->stage_bytes = std::max(h->stage_bytes, mlpc::kABytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
+    h->n_w = S + (d->gated ? 1 : 0);
     // split tiles up to 128 wide reduce through shared memory (distributed, within the cluster)
     for (int s = 0; s < S; ++s)
         if (h->split[s] > 1 && h->BN[s] * 512u <= mlpc::kRecvBytes)
@@ -313,7 +325,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     if (d->pipe_stages)
         h->num_pipe = std::min(h->num_pipe, d->pipe_stages);
     h->acc_split = d->acc_split == 2 ? 2 : 1;
-    if (h->acc_split * 2 * h->max_bn > 512) {
+    h->acc_cols = std::max(h->acc_split * h->max_bn, d->gated ? 2 * h->BN[0] : 0);
+    if (2 * h->acc_cols > 512) {
         release(h);
         return MLP_ERR_UNSUPPORTED;
     }
@@ -323,7 +336,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     }
     h->smem = mlpc::chain_smem_bytes(h->num_pipe, h->stage_bytes, h->recv_bytes);
     h->tmem_cols = 32;
-    while (h->tmem_cols < static_cast<uint32_t>(2 * h->acc_split * h->max_bn))
+    while (h->tmem_cols < static_cast<uint32_t>(2 * h->acc_cols))
         h->tmem_cols *= 2;
     h->stage_base[0] = 0;
     h->tile_base[0] = 0;
@@ -489,7 +502,7 @@ extern "C" mlp_status mlp_chain_workspace_size(mlp_chain_t h, size_t *bytes)
 static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const *W, void *Y, void *ws)
 {
     bool same = h->params_valid && X == h->c_X && Y == h->c_Y && ws == h->c_ws;
-    for (int s = 0; s < h->S && same; ++s)
+    for (int s = 0; s < h->n_w && same; ++s)
         same = W[s] == h->c_W[s];
     if (same)
         return MLP_OK;
@@ -509,12 +522,14 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         }
         if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
             return MLP_ERR_CUDA;
-        const bool w_ok = d.weight_layout == 1
-                              ? encode_2d(&P.mapB[s], W[s], d.dims[s + 1], d.dims[s], h->BN[s], mlpc::kBK,
-                                          CU_TENSOR_MAP_SWIZZLE_128B)
-                              : encode_2d(&P.mapB[s], W[s], d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
-                                          h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-        if (!w_ok)
+        auto encode_w = [&](CUtensorMap *m, const void *w) {
+            return d.weight_layout == 1
+                       ? encode_2d(m, w, d.dims[s + 1], d.dims[s], h->BN[s], mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : encode_2d(m, w, d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
+                                   h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        };
+        const bool gate_s = d.gated && s == 0;
+        if (!encode_w(&P.mapB[s], W[s == 0 ? 0 : s + (d.gated ? 1 : 0)]) || (gate_s && !encode_w(&P.mapU, W[1])))
             return MLP_ERR_CUDA;
         mlpc::StageParams &sp = P.st[s];
         sp.M = static_cast<int32_t>(d.M);
@@ -533,7 +548,8 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.partials = h->partials[s];
         sp.dsmem_reduce = h->split[s] > 1 && h->recv_bytes && h->BN[s] * 512u <= h->recv_bytes;
         sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
-        sp.gelu = d.epilogue == MLP_EPI_GELU_TANH;
+        sp.gelu = d.epilogue == MLP_EPI_GELU_TANH && !gate_s;
+        sp.gated = gate_s;
         sp.residual = (d.residual && s + 1 == h->S) ? static_cast<const __nv_bfloat16 *>(X) : nullptr;
         a_ptr = out_ptr;
     }
@@ -563,7 +579,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     P.num_pipe = h->num_pipe;
     P.stage_bytes = h->stage_bytes;
     P.tmem_cols = h->tmem_cols;
-    P.acc_stride = h->acc_split * h->max_bn;
+    P.acc_stride = h->acc_cols;
     P.acc_split = h->acc_split;
     P.sub_stride = h->max_bn;
     P.drop_tile = -1;
@@ -579,7 +595,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     h->c_X = X;
     h->c_Y = Y;
     h->c_ws = ws;
-    for (int s = 0; s < h->S; ++s)
+    for (int s = 0; s < h->n_w; ++s)
         h->c_W[s] = W[s];
     h->params_valid = true;
     return MLP_OK;
@@ -624,7 +640,7 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
     auto misaligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) != 0; };
     if (misaligned(X) || misaligned(Y) || (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)))
         return MLP_ERR_INVALID_ARG;
-    for (int s = 0; s < h->S; ++s)
+    for (int s = 0; s < h->n_w; ++s)
         if (!W[s] || misaligned(W[s]))
             return MLP_ERR_INVALID_ARG;
     if (cudaSetDevice(h->device) != cudaSuccess)

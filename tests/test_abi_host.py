@@ -113,9 +113,9 @@ def _desc(**kw):
         d.dims[i] = v
     d.in_dtype, d.acc_dtype, d.h_dtype, d.out_dtype = 1, 2, 1, 1
     for k, v in kw.items():
-        if k == "dims":
+        if k in ("dims", "tile_n", "k_split"):
             for i, x in enumerate(v):
-                d.dims[i] = x
+                getattr(d, k)[i] = x
         else:
             setattr(d, k, v)
     return d
@@ -131,6 +131,10 @@ def _desc(**kw):
     ({"residual": 1, "dims": (256, 256, 512)}, mc.ERR_INVALID_ARG),
     ({"mode": 2, "microbatch_rows": 100}, mc.ERR_INVALID_ARG),
     ({"mode": 7}, mc.ERR_INVALID_ARG),
+    # a gated (SwiGLU) first GEMM keeps gate and up side by side in TMEM: unsplit, <= 128 wide
+    ({"gated": 1, "acc_split": 2}, mc.ERR_UNSUPPORTED),
+    ({"gated": 1, "k_split": (2, 0)}, mc.ERR_UNSUPPORTED),
+    ({"gated": 1, "tile_n": (256, 0)}, mc.ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_descriptors_before_touching_cuda(lib, kw, expect):
     h = ctypes.c_void_p()
