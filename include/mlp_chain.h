@@ -17,7 +17,9 @@
  * tile stores its output, fences, and decrements the counter of every consumer tile that reads
  * it; the decrement that reaches zero pushes that consumer's tile id onto the queue.  Consumer
  * CTAs poll the queue in a short prologue, adopt the dequeued tile id in place of their own
- * and run the unchanged GEMM body.  Here all stages run in ONE persistent, warp-specialised
+ * and run the unchanged GEMM body.  (Here the counters count releases up to an epoch-scaled
+ * target instead of down to zero, one counter per group of consumer tiles with the same
+ * producers, and a consumer acquires its group counter before it reads the producers' output.)  Here all stages run in ONE persistent, warp-specialised
  * kernel on one GPU (one CTA per SM): the pages put one layer per GPU instead.
  * MLP_MODE_SEQUENTIAL launches the same tile engine once per GEMM, back to back on one stream
  * (the pages' "two consecutive GEMMs" baseline, section III-C).  MLP_MODE_MICROBATCH splits

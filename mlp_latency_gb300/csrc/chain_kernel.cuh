@@ -19,7 +19,7 @@
 //               section III-C, Fig. 2b).
 //   warp 3      pulls the protocol's counters, queues and dependency tables into L2 at launch.
 //   warps 4-7   epilogue: TMEM -> registers -> (split-K reduction) -> (GeLU / residual) ->
-//               bf16 -> global, then the injected epilogue: fence, scoreboard decrements and
+//               bf16 -> global, then the injected epilogue: fence, scoreboard releases and
 //               queue pushes (section III-A; fence placement per the memory-consistency
 //               discussion of section V).
 // The scheduler and epilogue warps would otherwise wait at pipeline barriers, so the protocol
@@ -75,8 +75,9 @@ struct BoundaryParams {
     const int32_t *pg_tgt;
     const int32_t *grp_off;    // group -> member consumer tiles (CSR)
     const int32_t *grp_mem;
-    const int32_t *grp_init;   // releases each group waits for: producer tiles x split x kEpiWarps
-    uint32_t *count;           // one counter per group
+    const int32_t *grp_init;   // releases each group waits for per run: producer tiles x split x kEpiWarps
+    const int32_t *cgrp;       // consumer tile -> its group
+    uint32_t *count;           // one counter per group: releases so far, over all runs of the handle
     unsigned long long *queue; // one slot per consumer tile
     uint32_t *tail;
     // K-granular mode: per producer tile, the releases seen so far (ready_quota per run,
@@ -231,51 +232,63 @@ __device__ __forceinline__ void arrive_rank(uint64_t *bar, uint32_t rank, uint32
 }
 
 // ------------------------------------------------------------------------------ scheduler --
-// Rank 0 of each cluster: obtain the next cluster item and broadcast it.
+// The tiles of one cluster item: pipelined ticket t, or the `item`-th static item of a
+// non-pipelined launch.  Returns the stage (-1: no work left) and fills tiles[0 .. ntiles).
+__device__ __forceinline__ int32_t item_tiles(const ChainParams &p, int32_t t, int32_t &ntiles,
+                                              int32_t (&tiles)[kMaxCluster])
+{
+    ntiles = 0;
+    if (p.pipelined) {
+        if (t >= p.stage_base[p.num_stages])
+            return -1;
+        const int32_t s = stage_of_ticket(p.stage_base, t);
+        const StageParams &sp = p.st[s];
+        const int32_t ntile_stage = sp.tiles_m * sp.tiles_n;
+        const int32_t first = (t - p.stage_base[s]) * sp.tiles_per_item;
+        ntiles = min(sp.tiles_per_item, ntile_stage - first);
+        // Stage 0 tiles (and every stage's in the K-granular mode) follow the raster order; a
+        // consumer item of the queue protocol carries work-queue slots (first + j), which the
+        // CTAs that run it poll themselves (resolve_queue_slot), so the broadcast is off the
+        // path from a queue push to the first load.
+        for (int32_t j = 0; j < ntiles; ++j)
+            tiles[j] = (s == 0 || p.kwait) ? raster_tile(first + j, sp.tiles_m, sp.tiles_n, p.raster_group) : first + j;
+        return s;
+    }
+    const StageParams &sp = p.st[p.first_stage];
+    const int32_t n_local = (p.m_tile_end - p.m_tile_begin) * sp.tiles_n;
+    const int32_t first = t * sp.tiles_per_item;
+    if (first >= n_local)
+        return -1;
+    ntiles = min(sp.tiles_per_item, n_local - first);
+    for (int32_t j = 0; j < ntiles; ++j)
+        tiles[j] = p.m_tile_begin * sp.tiles_n + first + j;
+    return p.first_stage;
+}
+
+// Rank 0 of each cluster: obtain the cluster's next items and broadcast them.  Item 0 is
+// ticket (or static item) = the cluster's id, which every CTA writes into its own ring slot 0 at
+// launch; from item 1 on, pipelined tickets come from a device-wide counter offset by the
+// number of clusters.
 __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
 {
-    const int32_t total = p.pipelined ? p.stage_base[p.num_stages] : 0;
     const int32_t cs = p.cs;
-    for (int32_t it = 0;; ++it) {
+    const int32_t nclusters = static_cast<int32_t>(num_clusters_x());
+    if (c->item_stage[0] < 0)
+        return;   // not even a first item for this cluster
+    for (int32_t it = 1;; ++it) {
         const int32_t slot = it % kSchedDepth;
         const uint32_t ph = (it / kSchedDepth) & 1;
         if (!wait_bar(&c->sempty[slot], ph ^ 1, c, p, true, true))
             return;
         // Take tickets just in time: a ticket taken early would sit in this cluster while
         // others idle, so wait until the TMA warp is about to finish its current slice.
-        if (it > 0 && !wait_bar(&c->want_next, (it - 1) & 1, c, p))
+        if (!wait_bar(&c->want_next, (it - 1) & 1, c, p))
             return;
-        int32_t stage = -1, ntiles = 0;
+        const int32_t t = p.pipelined ? nclusters + static_cast<int32_t>(atom_add_relaxed_gpu(p.ticket, 1u))
+                                      : static_cast<int32_t>(cluster_id_x()) + it * nclusters;
+        int32_t ntiles = 0;
         int32_t tiles[kMaxCluster];
-        if (p.pipelined) {
-            const int32_t t = static_cast<int32_t>(atom_add_relaxed_gpu(p.ticket, 1u));
-            if (t < total) {
-                const int32_t s = stage_of_ticket(p.stage_base, t);
-                const StageParams &sp = p.st[s];
-                const int32_t ntile_stage = sp.tiles_m * sp.tiles_n;
-                const int32_t first = (t - p.stage_base[s]) * sp.tiles_per_item;
-                ntiles = min(sp.tiles_per_item, ntile_stage - first);
-                // Stage 0 tiles (and every stage's in the K-granular mode) follow the raster order;
-                // a consumer item of the queue protocol carries work-queue slots
-                // (first + j), which the CTAs that run it poll themselves (resolve_queue_slot), so
-                // the broadcast below is off the path from a queue push to the first load.
-                for (int32_t j = 0; j < ntiles; ++j)
-                    tiles[j] = (s == 0 || p.kwait) ? raster_tile(first + j, sp.tiles_m, sp.tiles_n, p.raster_group)
-                                                   : first + j;
-                stage = s;
-            }
-        } else {
-            const StageParams &sp = p.st[p.first_stage];
-            const int32_t n_local = (p.m_tile_end - p.m_tile_begin) * sp.tiles_n;
-            const int32_t item = static_cast<int32_t>(cluster_id_x()) + it * static_cast<int32_t>(num_clusters_x());
-            const int32_t first = item * sp.tiles_per_item;
-            if (first < n_local) {
-                stage = p.first_stage;
-                ntiles = min(sp.tiles_per_item, n_local - first);
-                for (int32_t j = 0; j < ntiles; ++j)
-                    tiles[j] = p.m_tile_begin * sp.tiles_n + first + j;
-            }
-        }
+        const int32_t stage = item_tiles(p, t, ntiles, tiles);
         // Broadcast: rank r gets tile r / S of the item (or none) and k-slice r % S.  All items
         // are written first and released by one fence: a release arrive per rank would cost a
         // round trip each and start the last rank's slice that much later than the first's.
@@ -305,10 +318,10 @@ struct Item {
 // `qslot` of the boundary before stage s until this run's entry lands, with back-off and a
 // deadline.  Returns the consumer tile it names, or -1 after an error (status recorded, this
 // CTA's abort flag raised).  The caller orders its later TMA reads with a proxy fence.
-__device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl *c, int32_t s, int32_t qslot)
+__device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl *c, int32_t s, int32_t qslot,
+                                                      bool acquire)
 {
-    // Relaxed polls (an acquire load costs a fence per iteration); the fence after the loop
-    // turns the load that saw the entry into the acquire.
+    // Relaxed polls: the entry only names the tile (the acquire is on the group counter below).
     const unsigned long long *q = p.bd[s - 1].queue + qslot;
     uint64_t v = ld_relaxed_gpu_u64(q);
     if (!queue_entry_ready(v, c->epoch)) {
@@ -333,12 +346,30 @@ __device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl
             }
         }
     }
-    fence_acq_rel_gpu();
     const int32_t tile = queue_entry_tile(v);
     if (tile < 0 || tile >= p.st[s].tiles_m * p.st[s].tiles_n) {
         atomicCAS(p.status, 0u, kStatusBadTile);
         c->abort_flag = 1;
         return -1;
+    }
+    if (acquire) {
+        // The queue entry names the tile; the synchronisation with the producers is an acquire
+        // of the tile's group counter, which every producer warp incremented with a release
+        // (fence + relaxed add): reading the run's final count makes all of their stores
+        // visible.  The pusher therefore stores the entries without a fence of its own.
+        const BoundaryParams &bd = p.bd[s - 1];
+        const int32_t g = bd.cgrp[tile];
+        const uint32_t want = static_cast<uint32_t>(bd.grp_init[g]) * (c->epoch + 1u);
+        const uint64_t t0 = globaltimer_ns();
+        while (static_cast<int32_t>(ld_acquire_gpu_u32(bd.count + g) - want) < 0) {
+            if (c->abort_flag)
+                return -1;
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                atomicCAS(p.status, 0u, kStatusTimeout);
+                c->abort_flag = 1;
+                return -1;
+            }
+        }
     }
     return tile;
 }
@@ -457,7 +488,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         int32_t tile = item.tile;
         const bool kwait_s = kwait && s > 0;
         if (pipelined && s > 0 && !kwait) {
-            tile = resolve_queue_slot(p, c, s, item.tile);
+            tile = resolve_queue_slot(p, c, s, item.tile, true);
             if (tile < 0) {
                 free_item_slot(c, slot);
                 break;
@@ -756,7 +787,7 @@ __device__ __forceinline__ void load_acc(bool split2, uint32_t sub_stride, uint3
 }
 
 // What the release of one producer tile reads from the dependency tables, loaded while the
-// tile's mainloop still runs so that the release itself is a decrement, one queue reservation
+// tile's mainloop still runs so that the release itself is one atomic add, one queue reservation
 // and the stores.  Filled in full when the tile feeds exactly one group (a GEMM chain's row
 // panel); `ne` is the number of groups it feeds.  Lane i holds members i and 32 + i.
 struct ReleasePlan {
@@ -783,21 +814,23 @@ __device__ __forceinline__ ReleasePlan plan_release(const ChainParams &p, int32_
 }
 
 // Producer side of the protocol for the rows one epilogue warp stored of a finished tile (or of
-// one split-K slice of it): decrement every group counter the tile feeds (a group waits for
-// kEpiWarps x S decrements per producer tile); the decrement that reaches zero re-arms the
-// counter and publishes the group's members on the work-queue.  Called by the whole warp right
-// after a fence.acq_rel.gpu that follows its stores.
+// one split-K slice of it): count one release on every group counter the tile feeds.  A group
+// waits for grp_init = producer tiles x S x kEpiWarps releases per run; counters accumulate over
+// the handle's runs, so run e is complete at grp_init x (e + 1) and nothing is re-armed.  The
+// add that completes the count publishes the group's members on the work-queue.  Called by the
+// whole warp right after a fence.acq_rel.gpu that follows its stores.
 __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, int32_t lane,
                                              const ReleasePlan &pl)
 {
     const BoundaryParams &bd = p.bd[s];
     if (pl.ne == 1) {
-        // One group: lane 0 decrements (the caller's fence and this relaxed decrement are the
-        // release); the last decrement re-arms the counter and reserves the group's queue slots.
+        // One group: lane 0 counts this release (the caller's fence and this relaxed add are the
+        // release); the add that completes the run's count reserves the group's queue slots.
         uint32_t q0 = 0, fire = 0;
         if (lane == 0) {
-            const uint32_t old = atom_add_relaxed_gpu(bd.count + pl.g, 0xffffffffu);
-            if (old == 1u) {
+            const uint32_t want = static_cast<uint32_t>(pl.init) * (c->epoch + 1u);
+            const uint32_t old = atom_add_relaxed_gpu(bd.count + pl.g, 1u);
+            if (old + 1u == want) {
                 fire = 1;
                 q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(pl.n));
             }
@@ -805,20 +838,14 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
         if (!__shfl_sync(0xffffffffu, fire, 0))
             return;
         q0 = __shfl_sync(0xffffffffu, q0, 0);
-        // Lane 0's decrement saw every other producer's release; the syncwarp and each lane's
-        // fence turn that into an acquire for the whole warp and release the pushes below.
-        __syncwarp();
-        fence_acq_rel_gpu();
+        // No fence: a consumer that finds its entry acquires the group counter before it reads
+        // a byte of the producers' output (resolve_queue_slot).
         if (lane < pl.n)
             st_relaxed_gpu_u64(bd.queue + q0 + lane, queue_entry(c->epoch, pl.mem0));
         if (lane + 32 < pl.n)
             st_relaxed_gpu_u64(bd.queue + q0 + 32 + lane, queue_entry(c->epoch, pl.mem1));
         for (int32_t i = lane + 64; i < pl.n; i += 32)
             st_relaxed_gpu_u64(bd.queue + q0 + i, queue_entry(c->epoch, bd.grp_mem[pl.m0 + i]));
-        // Re-arm for the next run (no producer of this run touches the counter again); after
-        // the pushes, so the fence above does not wait for it.
-        if (lane == 0)
-            bd.count[pl.g] = static_cast<uint32_t>(pl.init);
         return;
     }
     const int32_t e0 = bd.pg_off[tile], e1 = bd.pg_off[tile + 1];
@@ -828,18 +855,13 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
         bool fire = false;
         if (e < e1) {
             g = bd.pg_tgt[e];
-            // The caller's fence.acq_rel.gpu and this relaxed decrement form the release of every
-            // store the epilogue's meeting ordered before it (each writer fenced before it
-            // arrived); the last decrement's acquire is the fence below, before the pushes.
-            const uint32_t old = atom_add_relaxed_gpu(bd.count + g, 0xffffffffu);
-            fire = (old == 1u);
-            if (fire)   // re-arm for the next run; no producer touches it again
-                bd.count[g] = static_cast<uint32_t>(bd.grp_init[g]);
+            // The caller's fence.acq_rel.gpu and this relaxed add form the release of the warp's
+            // stores; consumers acquire them through the counter.
+            const uint32_t old = atom_add_relaxed_gpu(bd.count + g, 1u);
+            fire = (old + 1u == static_cast<uint32_t>(bd.grp_init[g]) * (c->epoch + 1u));
         }
-        // Every group this warp completed is published by the whole warp: the lane whose
-        // decrement reached zero saw every earlier producer's release; __syncwarp
-        // orders that before each lane's release fence, which makes its relaxed queue stores
-        // carry the release.
+        // Every group this warp completed is published by the whole warp with relaxed stores (the
+        // consumers' acquire is on the group counter, see resolve_queue_slot).
         uint32_t todo = __ballot_sync(0xffffffffu, fire);
         while (todo) {
             const int32_t src = __ffs(todo) - 1;
@@ -850,8 +872,6 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
             if (lane == src)
                 q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(n));
             q0 = __shfl_sync(0xffffffffu, q0, src);
-            __syncwarp();
-            fence_acq_rel_gpu();
             for (int32_t i = lane; i < n; i += 32)
                 st_relaxed_gpu_u64(bd.queue + q0 + i, queue_entry(c->epoch, bd.grp_mem[m0 + i]));
         }
@@ -867,9 +887,9 @@ __device__ __forceinline__ void log_end(const ChainParams &p, int32_t s, int32_t
 
 // Injected epilogue of a finished tile or split-K slice, run by each epilogue warp for the 32
 // rows it stored.  The caller has fenced the warp's stores at gpu scope (after the warp's last
-// __syncwarp, so the fence is cumulative over all its lanes); that fence and the relaxed
-// decrement in release_tile form the release.  Each of the four warps of each of the S slices
-// decrements once (counters start at producer tiles x S x 4), so no warp waits for another.
+// __syncwarp, so the fence is cumulative over all its lanes); that fence and the relaxed add in
+// release_tile form the release.  Each of the four warps of each of the S slices releases once
+// (a group counts producer tiles x S x 4 releases per run), so no warp waits for another.
 __device__ __forceinline__ void publish(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile, bool log_it,
                                         bool producer, int32_t warp, int32_t lane, const ReleasePlan &pl)
 {
@@ -927,7 +947,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         if (pipelined && s > 0 && !kwait) {   // the TMA warp of this CTA polled the same slot first
             int32_t t = 0;
             if (lane == 0)
-                t = resolve_queue_slot(p, c, s, item.tile);
+                t = resolve_queue_slot(p, c, s, item.tile, false);   // reads no producer data
             tile = __shfl_sync(0xffffffffu, t, 0);
             if (tile < 0)
                 break;
@@ -1148,6 +1168,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             mbar_init(&c->sfull[i], 1);
             mbar_init(&c->sempty[i], 6 * p.cs);   // TMA + MMA + 4 epilogue warps of every rank
         }
+        {   // the cluster's first item needs no ticket and no broadcast: write it into slot 0 here
+            int32_t ntiles = 0;
+            int32_t tiles[kMaxCluster];
+            const int32_t stage = item_tiles(p, static_cast<int32_t>(cluster_id_x()), ntiles, tiles);
+            const int32_t S = stage >= 0 ? p.st[stage].split : 1;
+            const int32_t j = static_cast<int32_t>(rank) / S;
+            c->item_stage[0] = stage;
+            c->item_tile[0] = (stage >= 0 && j < ntiles) ? tiles[j] : -1;
+            c->item_split[0] = static_cast<int32_t>(rank) % S;
+        }
         mbar_init(&c->drain, 1);
         mbar_init(&c->want_next, 1);
         mbar_init(&c->red_bar, 4 * p.cs);          // 4 warps x S siblings, each arriving cs/S times
@@ -1156,6 +1186,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         c->skip = ld_relaxed_gpu_u32(p.status) != 0;   // sticky error: do nothing
         c->epoch = p.pipelined ? ld_relaxed_gpu_u32(p.epoch) : 0u;
         fence_barrier_init();
+        mbar_arrive(&c->sfull[0]);   // item 0 is in place (a local arrival, before any remote one)
     }
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < p.num_stages; ++i) {

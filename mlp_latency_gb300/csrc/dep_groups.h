@@ -18,6 +18,7 @@ struct DepGroups {
     std::vector<int32_t> pg_off, pg_tgt;    // producer -> groups it feeds (ascending)
     std::vector<int32_t> grp_off, grp_mem;  // group -> member consumer tiles (ascending)
     std::vector<int32_t> grp_init;          // producers each group waits for
+    std::vector<int32_t> cons_grp;          // consumer tile -> its group
 };
 
 // prod_off[P+1] / prod_tgt: producer -> consumers CSR (consumer ids ascending per producer).

@@ -84,6 +84,7 @@ mlpc::DepGroups mlpc::build_groups(const int32_t *prod_off, const int32_t *prod_
         group_of[c] = gid;
         members[gid].push_back(c);
     }
+    g.cons_grp = group_of;
     g.grp_off.push_back(0);
     for (auto &m : members) {
         g.grp_mem.insert(g.grp_mem.end(), m.begin(), m.end());

@@ -56,6 +56,7 @@ bool encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, in
 
 struct DeviceBoundary {
     int32_t *pg_off = nullptr, *pg_tgt = nullptr, *grp_off = nullptr, *grp_mem = nullptr, *grp_init = nullptr;
+    int32_t *cgrp = nullptr;
     uint32_t *count = nullptr, *tail = nullptr, *ready = nullptr;
     unsigned long long *queue = nullptr;
     size_t groups = 0, consumers = 0, producers = 0;
@@ -176,7 +177,7 @@ static mlp_status full_reset(mlp_chain *h)
         return MLP_ERR_CUDA;
     for (int b = 0; b + 1 < h->S; ++b) {
         const DeviceBoundary &db = h->db[b];
-        if (cudaMemcpy(db.count, db.grp_init, db.groups * sizeof(int32_t), cudaMemcpyDeviceToDevice) != cudaSuccess ||
+        if (cudaMemset(db.count, 0, db.groups * sizeof(uint32_t)) != cudaSuccess ||
             cudaMemset(db.queue, 0, db.consumers * sizeof(unsigned long long)) != cudaSuccess ||
             cudaMemset(h->db[b].tail, 0, sizeof(uint32_t)) != cudaSuccess ||
             cudaMemset(db.ready, 0, db.producers * sizeof(uint32_t)) != cudaSuccess)
@@ -389,6 +390,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         bytes = align_up(bytes, 256) + G.grp_mem.size() * 4;
         bytes = align_up(bytes, 256) + G.grp_init.size() * 4;      // init
         bytes = align_up(bytes, 256) + G.grp_init.size() * 4;      // count
+        bytes = align_up(bytes, 256) + G.cons_grp.size() * 4;      // consumer -> group
         bytes = align_up(bytes, 256) + h->init[b].size() * 8;      // queue
         bytes = align_up(bytes, 256) + 4;                          // tail
         bytes = align_up(bytes, 256) + (h->off[b].size() - 1) * 4; // ready (K-granular mode)
@@ -431,6 +433,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         db.grp_mem = static_cast<int32_t *>(take(G.grp_mem.size() * 4));
         db.grp_init = static_cast<int32_t *>(take(G.grp_init.size() * 4));
         db.count = static_cast<uint32_t *>(take(G.grp_init.size() * 4));
+        db.cgrp = static_cast<int32_t *>(take(G.cons_grp.size() * 4));
         db.queue = static_cast<unsigned long long *>(take(db.consumers * 8));
         db.tail = static_cast<uint32_t *>(take(4));
         db.producers = h->off[b].size() - 1;
@@ -443,6 +446,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         up(db.pg_tgt, G.pg_tgt);
         up(db.grp_off, G.grp_off);
         up(db.grp_mem, G.grp_mem);
+        up(db.cgrp, G.cons_grp);
         // A producer tile is released by each epilogue warp of each of its S split-K slices.
         std::vector<int32_t> releases(G.grp_init);
         for (int32_t &v : releases)
@@ -560,6 +564,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.bd[b].grp_mem = h->db[b].grp_mem;
         P.bd[b].grp_init = h->db[b].grp_init;
         P.bd[b].count = h->db[b].count;
+        P.bd[b].cgrp = h->db[b].cgrp;
         P.bd[b].queue = h->db[b].queue;
         P.bd[b].tail = h->db[b].tail;
         P.bd[b].ready = h->db[b].ready;
@@ -835,7 +840,7 @@ NoallocDevice g_noalloc_dev[64];
 std::mutex g_noalloc_mutex;
 
 struct NoallocLayout {
-    size_t ctrl, pg_off, pg_tgt, grp_off, grp_mem, grp_init, count, queue, tail, h, total;
+    size_t ctrl, pg_off, pg_tgt, grp_off, grp_mem, grp_init, count, cgrp, queue, tail, h, total;
 };
 
 // Groups are the row panels (tiles_m of them); every producer feeds exactly its own panel.
@@ -850,6 +855,7 @@ NoallocLayout noalloc_layout(int64_t M, int64_t N1, int P, int C, int G)
     o = align_up(o, 256); L.grp_mem = o;  o += static_cast<size_t>(C) * 4;
     o = align_up(o, 256); L.grp_init = o; o += static_cast<size_t>(G) * 4;
     o = align_up(o, 256); L.count = o; o += static_cast<size_t>(G) * 4;
+    o = align_up(o, 256); L.cgrp = o;  o += static_cast<size_t>(C) * 4;
     o = align_up(o, 256); L.queue = o; o += static_cast<size_t>(C) * 8;
     o = align_up(o, 256); L.tail = o;  o += 4;
     o = align_up(o, 256); L.h = o;     o += static_cast<size_t>(M) * N1 * 2;
@@ -860,7 +866,7 @@ NoallocLayout noalloc_layout(int64_t M, int64_t N1, int P, int C, int G)
 // Writes the whole protocol state of one run into the scratch: control words cleared, the
 // grouped dependency array of equal-height row tiles (producer tile (m, n) feeds row panel m;
 // panel m holds consumer tiles m*Cn .. m*Cn+Cn-1 and waits for its Pn producer tiles),
-// counters armed, queue slots emptied.  Nothing of a previous call survives.
+// counters and the epoch cleared, queue slots emptied.  Nothing of a previous call survives.
 __global__ void noalloc_setup_kernel(uint8_t *base, NoallocLayout L, int Pn, int Cn, int tiles_m)
 {
     const int P = tiles_m * Pn, C = tiles_m * Cn, G = tiles_m;
@@ -871,6 +877,7 @@ __global__ void noalloc_setup_kernel(uint8_t *base, NoallocLayout L, int Pn, int
     int32_t *grp_mem = reinterpret_cast<int32_t *>(base + L.grp_mem);
     int32_t *grp_init = reinterpret_cast<int32_t *>(base + L.grp_init);
     uint32_t *count = reinterpret_cast<uint32_t *>(base + L.count);
+    int32_t *cgrp = reinterpret_cast<int32_t *>(base + L.cgrp);
     unsigned long long *queue = reinterpret_cast<unsigned long long *>(base + L.queue);
     const int stride = gridDim.x * blockDim.x;
     const int i0 = blockIdx.x * blockDim.x + threadIdx.x;
@@ -887,11 +894,12 @@ __global__ void noalloc_setup_kernel(uint8_t *base, NoallocLayout L, int Pn, int
         grp_off[g] = g * Cn;
         if (g < G) {
             grp_init[g] = Pn * mlpc::kEpiWarps;   // each epilogue warp of a tile releases its rows
-            count[g] = static_cast<uint32_t>(Pn * mlpc::kEpiWarps);
+            count[g] = 0u;                        // the epoch word is cleared too: run 0's target
         }
     }
     for (int c = i0; c < C; c += stride) {
         grp_mem[c] = c;
+        cgrp[c] = c / Cn;
         queue[c] = 0;
     }
 }
@@ -999,6 +1007,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     P_.bd[0].grp_mem = reinterpret_cast<const int32_t *>(base + L.grp_mem);
     P_.bd[0].grp_init = reinterpret_cast<const int32_t *>(base + L.grp_init);
     P_.bd[0].count = reinterpret_cast<uint32_t *>(base + L.count);
+    P_.bd[0].cgrp = reinterpret_cast<const int32_t *>(base + L.cgrp);
     P_.bd[0].queue = reinterpret_cast<unsigned long long *>(base + L.queue);
     P_.bd[0].tail = reinterpret_cast<uint32_t *>(base + L.tail);
     P_.num_stages = 2;

@@ -291,6 +291,13 @@ __device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const unsigned long long 
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ld_relaxed_gpu_u32(const uint32_t *p)
 {
     uint32_t v;
