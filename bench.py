@@ -377,7 +377,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tile-n", default=None, help="comma-separated tile widths per GEMM (0 = library choice)")
     ap.add_argument("--k-split", default=None, help="comma-separated split-K factors per GEMM (0 = library choice)")
-    ap.add_argument("--mode", default="pipelined", choices=["pipelined", "pipelined_kwait", "sequential", "microbatch"])
+    ap.add_argument("--mode", default="pipelined", choices=["pipelined", "pipelined_kwait", "pipelined_lamport", "sequential", "microbatch"])
     ap.add_argument("--microbatch-rows", type=int, default=0)
     ap.add_argument("--raster-group", type=int, default=0)
     ap.add_argument("--pipe-stages", type=int, default=0)
@@ -495,7 +495,7 @@ def main():
         baselines = {}
         k_base = min(args.steps, 300)
         if not args.no_baselines:
-            for mode in ("sequential", "pipelined", "pipelined_kwait"):
+            for mode in ("sequential", "pipelined", "pipelined_kwait", "pipelined_lamport"):
                 if mode == args.mode:
                     continue
                 ch = make(mode)

@@ -32,6 +32,15 @@
  * weight tiles are requested before the wait).  Every mode uses the same tiles in the same
  * order of k, so Y is bit-identical across modes.
  *
+ * MLP_MODE_PIPELINED_LAMPORT is the paper's Lamport-synchronisation alternative (section V):
+ * the same queue protocol with no fence on either side.  run() first fills the intermediates
+ * with bf16 -0.0 (one extra launch); producers store +0.0 for an exact -0.0 and publish without
+ * a release; a consumer scans each 64-deep A tile it loads from an intermediate in shared
+ * memory and re-loads it until no -0.0 is left, before the tensor cores read it.  Y is
+ * bit-identical to the other modes except where an intermediate is an exact -0.0, which this
+ * mode stores as +0.0.  The plain data race it relies on (a load that sees either the sentinel
+ * or the final value, never an older one) is outside the PTX memory model, as on the pages.
+ *
  * Conventions for every entry point.
  *   - Matrices are dense, row-major, bf16, with 16-byte aligned base pointers; every
  *     dimension except M must be a multiple of 8 (one 16-byte TMA unit).
@@ -76,7 +85,9 @@ typedef enum {
     MLP_MODE_PIPELINED = 0,   /* one persistent grid, scoreboard + work-queue (CTA-pipelining) */
     MLP_MODE_SEQUENTIAL = 1,  /* one launch per GEMM, back to back                              */
     MLP_MODE_MICROBATCH = 2,  /* row chunks, GEMM s+1 of chunk i overlaps GEMM s of chunk i+1   */
-    MLP_MODE_PIPELINED_KWAIT = 3  /* one persistent grid, per-k-block producer waits, no queue  */
+    MLP_MODE_PIPELINED_KWAIT = 3, /* one persistent grid, per-k-block producer waits, no queue  */
+    MLP_MODE_PIPELINED_LAMPORT = 4 /* the queue protocol without fences: sentinel-filled
+                                      intermediates, consumers validate what they load         */
 } mlp_mode;
 
 typedef enum { MLP_EPI_NONE = 0, MLP_EPI_GELU_TANH = 1 } mlp_epilogue;
@@ -88,6 +99,9 @@ typedef enum { MLP_EPI_NONE = 0, MLP_EPI_GELU_TANH = 1 } mlp_epilogue;
                                            scoreboard decrements, so its consumers never become
                                            ready and their bounded wait must end the run with
                                            MLP_ERR_TIMEOUT                                       */
+#define MLP_DEBUG_FORCE_RELOAD 4u       /* MLP_MODE_PIPELINED_LAMPORT test hook: treat every
+                                           consumer A tile as unfinished once, so each is loaded
+                                           twice (exercises the re-load path; same results)       */
 
 typedef struct {
     int64_t M;                          /* rows of X (any value >= 1)                           */

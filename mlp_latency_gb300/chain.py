@@ -16,8 +16,8 @@ from ._lib import ChainDesc, ChainInfo, Event
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_DEVICE_STATE, ERR_BAD_TILE = range(8)
 DT_BF16, DT_F32 = 1, 2
-MODES = {"pipelined": 0, "sequential": 1, "microbatch": 2, "pipelined_kwait": 3}
-DEBUG_EVENT_LOG, DEBUG_DROP_DECREMENT = 1, 2
+MODES = {"pipelined": 0, "sequential": 1, "microbatch": 2, "pipelined_kwait": 3, "pipelined_lamport": 4}
+DEBUG_EVENT_LOG, DEBUG_DROP_DECREMENT, DEBUG_FORCE_RELOAD = 1, 2, 4
 
 EVENT_DTYPE = np.dtype([("stage", np.int32), ("tile", np.int32), ("smid", np.int32), ("cta", np.int32),
                         ("t_start", np.uint64), ("t_end", np.uint64), ("seq_start", np.uint32),
@@ -58,7 +58,8 @@ class Chain:
                  microbatch_rows: int = 0, device: int = 0, event_log: bool = False,
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
-                 weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False):
+                 weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False,
+                 force_reload: bool = False):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -75,7 +76,7 @@ class Chain:
         d.mode = MODES[mode]
         d.microbatch_rows = int(microbatch_rows)
         d.device = int(device)
-        flags = DEBUG_EVENT_LOG if event_log else 0
+        flags = (DEBUG_EVENT_LOG if event_log else 0) | (DEBUG_FORCE_RELOAD if force_reload else 0)
         if drop_tile is not None:
             flags |= DEBUG_DROP_DECREMENT
             d.drop_tile = int(drop_tile)

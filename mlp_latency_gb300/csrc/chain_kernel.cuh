@@ -17,7 +17,9 @@
 //               broadcasts it (stage, tile or queue slot, k-slice) to every CTA of the cluster
 //               through distributed shared memory (the scheduler warp's CGA broadcast of
 //               section III-C, Fig. 2b).
-//   warp 3      pulls the protocol's counters, queues and dependency tables into L2 at launch.
+//   warp 3      pulls the protocol's counters, queues and dependency tables into L2 at launch;
+//               in a Lamport run it then validates every consumer A tile before the MMAs
+//               (role_validate).
 //   warps 4-7   epilogue: TMEM -> registers -> (split-K reduction) -> (GeLU / residual) ->
 //               bf16 -> global, then the injected epilogue: fence, scoreboard releases and
 //               queue pushes (section III-A; fence placement per the memory-consistency
@@ -102,6 +104,8 @@ struct ChainParams {
     int32_t num_stages;
     int32_t pipelined;
     int32_t kwait;                       // pipelined with per-k-block producer waits, no work-queue
+    int32_t lamport;                     // pipelined, fence-free: consumers validate what they load
+    int32_t force_reload;                // Lamport test hook: reload every consumer A tile once
     int32_t first_stage;                 // non-pipelined launches run this single stage
     int32_t m_tile_begin, m_tile_end;    // ... over these row tiles
     int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
@@ -134,6 +138,8 @@ struct __align__(8) Ctrl {
     uint64_t sfull[kSchedDepth], sempty[kSchedDepth];
     uint64_t drain;
     uint64_t want_next;   // TMA -> scheduler: take the next ticket now
+    uint64_t valid[kMaxPipe];   // Lamport: the slot's A tile holds no sentinel (warp 3 -> MMA)
+    uint64_t reload[kMaxPipe];  // Lamport: completion of a reloaded A tile
     uint64_t red_bar;     // split-K: every sibling's partial is written
     uint64_t done_bar;    // split-K: every sibling has read its parts of my partial
     int32_t item_stage[kSchedDepth], item_tile[kSchedDepth], item_split[kSchedDepth];
@@ -488,7 +494,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         int32_t tile = item.tile;
         const bool kwait_s = kwait && s > 0;
         if (pipelined && s > 0 && !kwait) {
-            tile = resolve_queue_slot(p, c, s, item.tile, true);
+            tile = resolve_queue_slot(p, c, s, item.tile, !p.lamport);   // Lamport: validated instead
             if (tile < 0) {
                 free_item_slot(c, slot);
                 break;
@@ -596,6 +602,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint32_t acc_stride = static_cast<uint32_t>(p.acc_stride);
     const uint32_t sub_stride = static_cast<uint32_t>(p.sub_stride);
     const bool split2 = p.acc_split == 2;
+    const bool lamport = p.pipelined && p.lamport;
     int32_t ps = 0;
     uint32_t pph = 0;
     uint32_t local_tiles = 0;
@@ -628,10 +635,12 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         for (int32_t kb = kb0; kb < kb1; ++kb) {
             // TMA fills and tcgen05.mma reads are both async-proxy operations ordered by the
             // mbarrier's transaction count: no tcgen05 fence is needed per k block.
-            if (!wait_bar(&c->full[ps], pph, c, p)) {
+            if (!wait_bar(lamport ? &c->valid[ps] : &c->full[ps], pph, c, p)) {
                 ok = false;
                 break;
             }
+            if (lamport)   // the slot reached this thread through warp 3, not through its copies
+                tc_fence_after();
             const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(ps) * stage_bytes);
             const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
@@ -674,6 +683,140 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
     }
 }
 
+// ------------------------------------------------------------------ Lamport validation --
+// The sentinel a Lamport run pre-fills every intermediate with: bf16 -0.0.  Producers of such a
+// run write +0.0 for an exact negative zero, so no output value equals it.
+constexpr uint32_t kSentinel = 0x8000u;
+
+// True on every lane if any of the 8192 bf16 values of the 16 KB tile at `a` is the sentinel.
+// Volatile shared loads (the tile is rewritten by TMA between two scans), issued eight at a
+// time before any of them is tested, so the scan costs a few load latencies, not 32.
+__device__ __forceinline__ bool tile_has_sentinel(const uint8_t *a, int32_t lane)
+{
+    const uint32_t base = smem_u32(a) + static_cast<uint32_t>(lane) * 16u;
+    uint32_t hit = 0;
+#pragma unroll 1
+    for (int b = 0; b < static_cast<int>(kABytes / 512); b += 8) {
+        uint32_t w[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[i][0]), "=r"(w[i][1]), "=r"(w[i][2]), "=r"(w[i][3])
+                         : "r"(base + static_cast<uint32_t>(b + i) * 512u));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                hit |= static_cast<uint32_t>((w[i][e] & 0xffffu) == kSentinel) |
+                       static_cast<uint32_t>((w[i][e] >> 16) == kSentinel);
+    }
+    return __any_sync(0xffffffffu, hit != 0u);
+}
+
+// Lamport mode only (warp 3, all lanes): the fence-free variant of the protocol (section V,
+// Lamport synchronisation).  Producers publish without fences, so a consumer's A tile (the
+// previous stage's output) may be read before all of it has landed.  For every k block the MMA
+// warp will consume, this warp waits for the slot's copies, scans a consumer stage's A tile for
+// the sentinel, re-loads the tile until it holds none (with a deadline), and only then hands the
+// slot to the MMA warp through valid[slot].  First-stage tiles read the chain input and pass.
+__device__ __forceinline__ void role_validate(const ChainParams &p, Ctrl *c, uint8_t *ring)
+{
+    const int32_t lane = threadIdx.x & 31;
+    const int32_t num_pipe = p.num_pipe;
+    const uint32_t stage_bytes = p.stage_bytes;
+    const uint64_t pol_act = policy_evict_last();
+    int32_t ps = 0;
+    uint32_t pph = 0;
+    uint32_t rl_phase = 0;     // bit i: parity of reload[i]'s next phase
+    uint32_t rl_pending = 0;   // bit i: a reload into slot i is in flight
+    bool ok = true;
+    for (int32_t it = 0; ok; ++it) {
+        const int32_t slot = it % kSchedDepth;
+        if (!warp_wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true))
+            break;
+        Item item{0, 0, 0};
+        if (lane == 0)
+            item = take_item(c, slot);
+        item.stage = __shfl_sync(0xffffffffu, item.stage, 0);
+        item.tile = __shfl_sync(0xffffffffu, item.tile, 0);
+        item.split = __shfl_sync(0xffffffffu, item.split, 0);
+        if (item.stage < 0)
+            break;
+        if (item.tile < 0)
+            continue;
+        const int32_t s = item.stage;
+        const bool check = s > 0;
+        int32_t tile = item.tile;
+        if (check) {   // the queue slot names the tile (the TMA warp of this CTA polled it first)
+            int32_t t = 0;
+            if (lane == 0)
+                t = resolve_queue_slot(p, c, s, item.tile, false);
+            tile = __shfl_sync(0xffffffffu, t, 0);
+            if (tile < 0)
+                break;
+        }
+        const StageParams &spr = p.st[s];
+        int32_t kb0, kb1;
+        slice_range(spr.k_blocks, spr.kb_per_split, item.split, kb0, kb1);
+        const int32_t m0 = (tile / spr.tiles_n) * kBM;
+        for (int32_t kb = kb0; kb < kb1 && ok; ++kb) {
+            if (!warp_wait_bar(&c->full[ps], pph, c, p)) {
+                ok = false;
+                break;
+            }
+            mbar_try_wait(&c->full[ps], pph);   // every lane acquires the completed phase
+            if (check) {
+                uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
+                bool force = p.force_reload != 0;
+                uint64_t t0 = 0;
+                while (force || tile_has_sentinel(a, lane)) {
+                    force = false;
+                    const uint64_t now = globaltimer_ns();
+                    if (t0 == 0) {
+                        t0 = now;
+                    } else if (now - t0 > p.timeout_ns) {
+                        if (lane == 0) {
+                            atomicCAS(p.status, 0u, kStatusTimeout);
+                            c->abort_flag = 1;
+                        }
+                        ok = false;
+                        break;
+                    }
+                    // this warp's reads of the tile come before the copy that overwrites it
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&c->reload[ps], kABytes);
+                        tma_load_2d(a, &p.mapA[s], &c->reload[ps], kb * kBK, m0, pol_act);
+                    }
+                    rl_pending |= 1u << ps;
+                    if (!warp_wait_bar(&c->reload[ps], (rl_phase >> ps) & 1u, c, p)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_try_wait(&c->reload[ps], (rl_phase >> ps) & 1u);
+                    rl_pending &= ~(1u << ps);
+                    rl_phase ^= 1u << ps;
+                }
+                if (!ok)
+                    break;
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&c->valid[ps]);
+            if (++ps == num_pipe) {
+                ps = 0;
+                pph ^= 1;
+            }
+        }
+    }
+    // after an abort, a reload still in flight lands before the CTA's shared memory goes away
+    if (lane == 0)
+        for (int32_t i = 0; i < kMaxPipe; ++i)
+            if (rl_pending & (1u << i))
+                wait_bar(&c->reload[i], (rl_phase >> i) & 1u, c, p, false);
+}
+
 // -------------------------------------------------------------------------------- epilogue --
 // Two fp32 values to packed bf16 (lo in the low half), round to nearest even on the bit
 // pattern: add half an ulp of the kept part plus its lowest kept bit, keep the upper 16 bits;
@@ -701,7 +844,18 @@ struct OutDesc {
     __nv_bfloat16 *out;
     const __nv_bfloat16 *residual;
     int32_t M, N, gelu;
+    int32_t canon;   // Lamport producer: store +0.0 for -0.0, so no output equals the sentinel
 };
+
+// Both bf16 halves of w with -0.0 replaced by +0.0.
+__device__ __forceinline__ uint32_t canon_neg_zero(uint32_t w)
+{
+    if ((w & 0xffffu) == 0x8000u)
+        w &= 0xffff0000u;
+    if ((w >> 16) == 0x8000u)
+        w &= 0x0000ffffu;
+    return w;
+}
 
 template <bool kGelu>
 __device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row0, int32_t n, const uint32_t (&r)[32],
@@ -742,9 +896,14 @@ __device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row
     }
 #pragma unroll
     for (int sg = 0; sg < 4; ++sg) {
-        const uint4 o = make_uint4(pack_bf16x2_rne(v[sg * 8], v[sg * 8 + 1]), pack_bf16x2_rne(v[sg * 8 + 2], v[sg * 8 + 3]),
-                                   pack_bf16x2_rne(v[sg * 8 + 4], v[sg * 8 + 5]),
-                                   pack_bf16x2_rne(v[sg * 8 + 6], v[sg * 8 + 7]));
+        uint4 o = make_uint4(pack_bf16x2_rne(v[sg * 8], v[sg * 8 + 1]), pack_bf16x2_rne(v[sg * 8 + 2], v[sg * 8 + 3]),
+                             pack_bf16x2_rne(v[sg * 8 + 4], v[sg * 8 + 5]), pack_bf16x2_rne(v[sg * 8 + 6], v[sg * 8 + 7]));
+        if (sp.canon) {
+            o.x = canon_neg_zero(o.x);
+            o.y = canon_neg_zero(o.y);
+            o.z = canon_neg_zero(o.z);
+            o.w = canon_neg_zero(o.w);
+        }
         *reinterpret_cast<uint4 *>(stage + stage_off(lane, sg)) = o;
     }
     __syncwarp();
@@ -923,6 +1082,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
     const size_t partial_floats = static_cast<size_t>(p.partial_floats);
     const bool pipelined = p.pipelined != 0;
     const bool kwait = pipelined && p.kwait != 0;
+    const bool lamport = pipelined && p.lamport != 0;
     const int32_t num_stages = p.num_stages;
     const bool logging = p.events != nullptr;
     const size_t cbase = static_cast<size_t>(cluster_id_x()) * cs;
@@ -956,10 +1116,10 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = spr.split;
         const bool dsmem = spr.dsmem_reduce != 0;
         float *const partials = spr.partials;
-        const OutDesc od{spr.out, spr.residual, spr.M, spr.N, spr.gelu};
+        const bool producer = pipelined && s + 1 < num_stages;
+        const OutDesc od{spr.out, spr.residual, spr.M, spr.N, spr.gelu, lamport && producer};
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
-        const bool producer = pipelined && s + 1 < num_stages;
         ReleasePlan pl{0, -1, 0, 0, 0, -1, -1};
         if (producer && !kwait)
             pl = plan_release(p, s, tile, lane);
@@ -994,7 +1154,8 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 mbar_arrive(&c->tempty[acc]);   // the MMA warp may reuse this accumulator
             ++local_tiles;
             if (producer || (pipelined && logging)) {
-                fence_acq_rel_gpu();   // this warp's stores, released at gpu scope for the consumers
+                if (!lamport)   // this warp's stores, released at gpu scope for the consumers
+                    fence_acq_rel_gpu();
                 publish(p, c, s, tile, logging, producer, warp, lane, pl);
             }
             continue;
@@ -1056,7 +1217,10 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                     r[e] = __float_as_uint(acc_v[e]);
                 store_chunk_warp(od, row0, n0 + (item.split * cpo + oc) * 32, r, stage, lane);
             }
-            fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
+            if (lamport)           // (a Lamport run publishes the slice without a release)
+                fence_acq_rel_cluster();
+            else                   // the slice stores, released at gpu scope for the consumers
+                fence_acq_rel_gpu();
             __syncwarp();
             if (lane == 0)         // my receive buffer is read: siblings may send the next tile
                 for (int32_t q = 0; q < S; ++q)
@@ -1133,7 +1297,10 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 r[e] = __float_as_uint(acc_v[e]);
             store_chunk_warp(od, row0, n0 + c0, r, stage, lane);
         }
-        fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
+        if (lamport)
+            fence_acq_rel_cluster();
+        else                   // the slice stores, released at gpu scope for the consumers
+            fence_acq_rel_gpu();
         __syncwarp();
         if (lane == 0)         // the siblings' partials are read: they may overwrite them
             for (int32_t q = 0; q < S; ++q)
@@ -1159,6 +1326,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         for (int i = 0; i < p.num_pipe; ++i) {
             mbar_init(&c->full[i], 1);
             mbar_init(&c->empty[i], 1);
+            mbar_init(&c->valid[i], 1);
+            mbar_init(&c->reload[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&c->tfull[i], 1);
@@ -1166,7 +1335,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
         for (int i = 0; i < kSchedDepth; ++i) {
             mbar_init(&c->sfull[i], 1);
-            mbar_init(&c->sempty[i], 6 * p.cs);   // TMA + MMA + 4 epilogue warps of every rank
+            // TMA + MMA + 4 epilogue warps of every rank (+ the Lamport validator)
+            mbar_init(&c->sempty[i], (p.pipelined && p.lamport ? 7 : 6) * p.cs);
         }
         {   // the cluster's first item needs no ticket and no broadcast: write it into slot 0 here
             int32_t ntiles = 0;
@@ -1223,6 +1393,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             const uint32_t step = gridDim.x * 32u * 128u;
             for (uint32_t off = (blockIdx.x * 32u + static_cast<uint32_t>(lane)) * 128u; off < p.meta_bytes; off += step)
                 prefetch_l2_keep(p.meta + off);
+            if (p.pipelined && p.lamport)
+                role_validate(p, c, ring);
         } else if (warp >= 4) {
             role_epilogue(p, c, tmem_base, rank, ring + staging_offset(p.num_pipe, p.stage_bytes),
                           ring + recv_offset(p.num_pipe, p.stage_bytes));

@@ -65,7 +65,19 @@ struct DeviceBoundary {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Both pipelined modes run one persistent, co-resident grid over all stages.
-bool is_pipelined(int mode) { return mode == MLP_MODE_PIPELINED || mode == MLP_MODE_PIPELINED_KWAIT; }
+bool is_pipelined(int mode)
+{
+    return mode == MLP_MODE_PIPELINED || mode == MLP_MODE_PIPELINED_KWAIT || mode == MLP_MODE_PIPELINED_LAMPORT;
+}
+
+// Lamport runs: every intermediate starts as the sentinel, bf16 -0.0 (two per 32-bit word).
+__global__ void fill_sentinel_kernel(uint4 *p, size_t n16)
+{
+    const uint4 v = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
 
 }  // namespace
 
@@ -658,6 +670,17 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
     if (is_pipelined(h->desc.mode)) {
         P.pipelined = 1;
         P.kwait = h->desc.mode == MLP_MODE_PIPELINED_KWAIT;
+        P.lamport = h->desc.mode == MLP_MODE_PIPELINED_LAMPORT;
+        P.force_reload = P.lamport && (h->desc.debug_flags & MLP_DEBUG_FORCE_RELOAD) != 0;
+        if (P.lamport && h->S > 1) {
+            size_t bytes = 0;
+            mlp_chain_workspace_size(h, &bytes);
+            const size_t n16 = bytes / 16;   // every intermediate is a multiple of 16 bytes
+            const int blocks = static_cast<int>(std::min<size_t>(4 * h->num_sms, (n16 + 255) / 256));
+            fill_sentinel_kernel<<<std::max(blocks, 1), 256, 0, st>>>(static_cast<uint4 *>(workspace), n16);
+            if (cudaGetLastError() != cudaSuccess)
+                return MLP_ERR_CUDA;
+        }
         if (h->fault_armed) {
             P.drop_tile = h->desc.drop_tile;
             h->fault_armed = false;
@@ -795,7 +818,7 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->pipe_stages = h->num_pipe;
     info->smem_bytes = static_cast<int32_t>(h->smem);
     info->tmem_cols = static_cast<int32_t>(h->tmem_cols);
-    info->launches_per_run = is_pipelined(h->desc.mode) ? 1
+    info->launches_per_run = is_pipelined(h->desc.mode) ? (h->desc.mode == MLP_MODE_PIPELINED_LAMPORT && h->S > 1 ? 2 : 1)
                              : h->desc.mode == MLP_MODE_SEQUENTIAL ? h->S
                                                                    : h->S * h->n_chunks;
     info->cluster_size = h->cs;
