@@ -689,12 +689,15 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
 constexpr uint32_t kSentinel = 0x8000u;
 
 // True on every lane if any of the 8192 bf16 values of the 16 KB tile at `a` is the sentinel.
-// Volatile shared loads (the tile is rewritten by TMA between two scans), issued eight at a
-// time before any of them is tested, so the scan costs a few load latencies, not 32.
+// A half equals the sentinel exactly when it is zero after an XOR with the sentinel, so the
+// scan keeps a running per-half unsigned minimum of w ^ sentinel (two operations per word) and
+// tests it once.  Volatile shared loads (the tile is rewritten by TMA between two scans),
+// eight in flight before any is used.
 __device__ __forceinline__ bool tile_has_sentinel(const uint8_t *a, int32_t lane)
 {
     const uint32_t base = smem_u32(a) + static_cast<uint32_t>(lane) * 16u;
-    uint32_t hit = 0;
+    const uint32_t flip = kSentinel | (kSentinel << 16);
+    uint32_t m = 0xffffffffu;
 #pragma unroll 1
     for (int b = 0; b < static_cast<int>(kABytes / 512); b += 8) {
         uint32_t w[8][4];
@@ -707,10 +710,9 @@ __device__ __forceinline__ bool tile_has_sentinel(const uint8_t *a, int32_t lane
         for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                hit |= static_cast<uint32_t>((w[i][e] & 0xffffu) == kSentinel) |
-                       static_cast<uint32_t>((w[i][e] >> 16) == kSentinel);
+                m = __vminu2(m, w[i][e] ^ flip);
     }
-    return __any_sync(0xffffffffu, hit != 0u);
+    return __any_sync(0xffffffffu, (m & 0xffffu) == 0u || (m >> 16) == 0u);
 }
 
 // Lamport mode only (warp 3, all lanes): the fence-free variant of the protocol (section V,
