@@ -629,7 +629,10 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * acc_stride;
-        const uint32_t idesc = idesc_bf16_f32(kBM, BN, b_kmajor ? 0u : 1u);
+        // A gated tile's gate and up weight tiles lie back to back in the slot, laid out exactly
+        // like one B tile twice as wide, so one MMA of N = 2 BN fills both accumulators (gate in
+        // columns [0, BN), up in [BN, 2 BN)): an MMA costs the same for any N <= 256.
+        const uint32_t idesc = idesc_bf16_f32(kBM, gated ? 2u * BN : BN, b_kmajor ? 0u : 1u);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
         bool ok = true;
         for (int32_t kb = kb0; kb < kb1; ++kb) {
@@ -658,12 +661,6 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                 const uint32_t sub = split2 ? (j & 1u) : 0u;
                 const uint32_t accum = j >= (split2 ? 2u : 1u) ? 1u : 0u;
                 mma_bf16_ss(d_tmem + sub * sub_stride, ad, bd, idesc, accum);
-                if (gated) {   // up weights (the next B tile of the slot), same A, accumulator BN columns on
-                    const uint32_t u_addr = b_addr + BN * kBK * 2u;
-                    const uint64_t ud = b_kmajor ? smem_desc(u_addr + kk * 32u, 16u, 1024u, 2u)
-                                                 : smem_desc(u_addr + kk * 16u * b_swz, kBK * b_swz, 8u * b_swz, b_code);
-                    mma_bf16_ss(d_tmem + BN, ad, ud, idesc, accum);
-                }
             }
             issued = true;
             mma_commit(&c->empty[ps]);  // frees the ring slot once these MMAs have read it
