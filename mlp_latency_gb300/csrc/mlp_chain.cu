@@ -166,8 +166,10 @@ static double choose_tiles(int64_t tiles_m, int64_t K, int64_t N, const int clus
             // a persistent grid quantises into whole waves only while units are few
             const double waves = units <= 2 * slots ? std::ceil(units / slots) : units / slots;
             const double rows = 128.0 + (bn >= 64 ? bn : 64);
-            const double t_mma = kbps * 4 * 140.0 / 1900.0;          // us
-            const double t_tma = kbps * rows * 1.2e-3;               // us
+            // measured on GB300: a 128 x N x 16 MMA takes about max(48, N / 2) cycles; the
+            // streaming rate with the MMAs running is about 1.2 ns per 128-byte operand row
+            const double t_mma = kbps * 4 * std::max(48.0, bn / 2.0) / 2000.0;   // us
+            const double t_tma = kbps * rows * 1.2e-3;                           // us
             const double t_unit = std::max(t_mma, t_tma) + 1.0 + (S > 1 ? 4.0 : 0.0);
             const double t_hbm = static_cast<double>(K) * N * 2 / 6.5e6;
             const double t = std::max(waves * t_unit, t_hbm);
