@@ -24,4 +24,13 @@ struct DepGroups {
 // prod_off[P+1] / prod_tgt: producer -> consumers CSR (consumer ids ascending per producer).
 DepGroups build_groups(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C);
 
+// One group per run of `g` consecutive consumer row panels (consumer tile c lies in row panel
+// c / tiles_n).  A merged group waits for the union of its members' producers, so it is never
+// ready before any of its members would have been; when the producers finish those panels
+// together (the first stage's raster walks g panels column by column) it costs nothing.  Its
+// members are listed column by column -- all of its panels at n = 0, then n = 1, ... -- so that
+// consecutive queue slots read the same weight column slab and share it in L2.
+DepGroups merge_groups_by_panel(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C,
+                                int32_t tiles_n, int32_t g);
+
 }  // namespace mlpc

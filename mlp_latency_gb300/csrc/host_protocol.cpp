@@ -103,6 +103,48 @@ mlpc::DepGroups mlpc::build_groups(const int32_t *prod_off, const int32_t *prod_
     return g;
 }
 
+mlpc::DepGroups mlpc::merge_groups_by_panel(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C,
+                                            int32_t tiles_n, int32_t g)
+{
+    const int32_t panels = (C + tiles_n - 1) / tiles_n;
+    const int32_t supers = (panels + g - 1) / g;
+    std::vector<std::vector<int32_t>> in(static_cast<size_t>(C));
+    for (int32_t p = 0; p < P; ++p)
+        for (int32_t e = prod_off[p]; e < prod_off[p + 1]; ++e)
+            in[static_cast<size_t>(prod_tgt[e])].push_back(p);
+    DepGroups r;
+    r.cons_grp.assign(static_cast<size_t>(C), 0);
+    r.grp_off.push_back(0);
+    for (int32_t sg = 0; sg < supers; ++sg) {
+        const int32_t m0 = sg * g, m1 = std::min(panels, m0 + g);
+        std::vector<int32_t> producers;
+        for (int32_t n = 0; n < tiles_n; ++n)
+            for (int32_t m = m0; m < m1; ++m) {
+                const int32_t c = m * tiles_n + n;
+                if (c >= C)
+                    continue;
+                r.grp_mem.push_back(c);
+                r.cons_grp[static_cast<size_t>(c)] = sg;
+                producers.insert(producers.end(), in[static_cast<size_t>(c)].begin(), in[static_cast<size_t>(c)].end());
+            }
+        std::sort(producers.begin(), producers.end());
+        producers.erase(std::unique(producers.begin(), producers.end()), producers.end());
+        r.grp_init.push_back(static_cast<int32_t>(producers.size()));
+        r.grp_off.push_back(static_cast<int32_t>(r.grp_mem.size()));
+    }
+    r.pg_off.push_back(0);
+    for (int32_t p = 0; p < P; ++p) {
+        std::vector<int32_t> gs;
+        for (int32_t e = prod_off[p]; e < prod_off[p + 1]; ++e)
+            gs.push_back(r.cons_grp[static_cast<size_t>(prod_tgt[e])]);
+        std::sort(gs.begin(), gs.end());
+        gs.erase(std::unique(gs.begin(), gs.end()), gs.end());
+        r.pg_tgt.insert(r.pg_tgt.end(), gs.begin(), gs.end());
+        r.pg_off.push_back(static_cast<int32_t>(r.pg_tgt.size()));
+    }
+    return r;
+}
+
 // ------------------------------------------------------------------------------------------
 // Host model of the protocol: `threads` host threads play the persistent CTAs.  Each takes
 // tickets in stage order; first-stage tickets map to tiles through raster_tile(); later-stage

@@ -395,8 +395,16 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], mlpc::kBM, h->BN[b], mlpc::kBM, h->BN[b + 1],
                        h->off[b].data(), h->tgt[b].data(), nnz, h->init[b].data());
         h->tgt[b].resize(static_cast<size_t>(nnz));
-        h->grp[b] = mlpc::build_groups(h->off[b].data(), h->tgt[b].data(), static_cast<int32_t>(h->off[b].size() - 1),
-                                       static_cast<int32_t>(h->init[b].size()));
+        // The first stage's raster walks groups of rg row panels column by column, so those
+        // panels' consumers become ready together: one scoreboard group per rg panels, pushed
+        // column by column so that neighbouring queue slots share a weight slab in L2.
+        const int rg = d->raster_group ? d->raster_group : (h->tiles_m >= 8 ? 4 : 1);
+        h->grp[b] = rg > 1 ? mlpc::merge_groups_by_panel(h->off[b].data(), h->tgt[b].data(),
+                                                         static_cast<int32_t>(h->off[b].size() - 1),
+                                                         static_cast<int32_t>(h->init[b].size()), h->tiles_n[b + 1], rg)
+                           : mlpc::build_groups(h->off[b].data(), h->tgt[b].data(),
+                                                static_cast<int32_t>(h->off[b].size() - 1),
+                                                static_cast<int32_t>(h->init[b].size()));
         const mlpc::DepGroups &G = h->grp[b];
         bytes = align_up(bytes, 256) + G.pg_off.size() * 4;
         bytes = align_up(bytes, 256) + std::max<size_t>(G.pg_tgt.size(), 1) * 4;

@@ -149,11 +149,14 @@ def test_grouped_raster_matches(mc):
 
 
 # ------------------------------------------------------------------------ the protocol log --
-def test_event_log_respects_every_dependency(mc):
-    M, dims, tn = 640, (256, 512, 384), [64, 128]
+# 640 rows: one scoreboard group per row panel; 1152 rows (9 panels): groups merged per raster
+# group of 4 (4, 4, 1 panels) or 3, consumers pushed column by column
+@pytest.mark.parametrize("M,rg", [(640, 0), (1152, 0), (1152, 3)])
+def test_event_log_respects_every_dependency(mc, oracle_mod, M, rg):
+    dims, tn = (256, 512, 384), [64, 128]
     X, Ws = si.draw(si.make_workload("t", M, dims), seed=10)
     Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
-    with mc.Chain(M, dims, tile_n=tn, event_log=True) as ch:
+    with mc.Chain(M, dims, tile_n=tn, event_log=True, raster_group=rg) as ch:
         ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
         Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
         for _ in range(2):   # the second run checks the re-armed scoreboard
@@ -175,6 +178,10 @@ def test_event_log_respects_every_dependency(mc):
                     assert prod["seq_end"][p] < cons["seq_start"][c]
                     assert prod["t_end"][p] <= cons["t_start"][c]
             assert np.all(init == info["tiles_n"][0])
+        Yo = oracle_mod.chain(bits(X), [bits(t) for t in Ws])
+        assert_close_to_oracle(Y.cpu(), Yo)
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=tn)
+    assert torch.equal(Y.cpu().view(torch.int16), Ys.view(torch.int16))
 
 
 def test_dropped_decrement_times_out_then_recovers(mc):
