@@ -41,8 +41,11 @@ TUNED_TILES = {
     "gelu4_m512_d8192": [0, 0, 0, 0],
 }
 TUNED_SPLIT = {}
+# every source that shapes the measured launch: the kernel and the host code that picks its tiles,
+# raster and scoreboard groups
 KERNEL_SOURCES = ["mlp_latency_gb300/csrc/chain_kernel.cuh", "mlp_latency_gb300/csrc/ptx.cuh",
-                  "mlp_latency_gb300/csrc/protocol.h", "mlp_latency_gb300/csrc/dep_groups.h"]
+                  "mlp_latency_gb300/csrc/protocol.h", "mlp_latency_gb300/csrc/dep_groups.h",
+                  "mlp_latency_gb300/csrc/mlp_chain.cu", "mlp_latency_gb300/csrc/host_protocol.cpp"]
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 

@@ -124,7 +124,8 @@ typedef struct {
     int32_t grid_ctas;                  /* 0 = one CTA per SM                                    */
     int32_t raster_group;               /* first-stage raster: 1 = row panels in order; g > 1 =
                                            groups of g row panels, column-major inside a group;
-                                           0 = library choice (4 when there are >= 8 panels)     */
+                                           0 = library choice (8 from 16 panels, 4 from 8);
+                                           pipelined consumers are grouped the same way         */
     int32_t pipe_stages;                /* shared-memory ring depth: 0 = as deep as fits         */
     int32_t weight_layout;              /* 0: W_s stored dims[s] x dims[s+1] row-major (K x N);
                                            1: stored transposed, dims[s+1] x dims[s] row-major

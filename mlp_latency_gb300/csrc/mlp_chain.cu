@@ -64,6 +64,11 @@ struct DeviceBoundary {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// First-stage raster (and consumer grouping) when the caller leaves it to the library: groups of
+// 8 row panels from 16 panels up, of 4 from 8 (measured best on GB300 for 16 and 64 panels; a
+// group of all panels serialises the stages), none below.
+int default_raster_group(int tiles_m) { return tiles_m >= 16 ? 8 : (tiles_m >= 8 ? 4 : 1); }
+
 // Both pipelined modes run one persistent, co-resident grid over all stages.
 bool is_pipelined(int mode)
 {
@@ -398,7 +403,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         // The first stage's raster walks groups of rg row panels column by column, so those
         // panels' consumers become ready together: one scoreboard group per rg panels, pushed
         // column by column so that neighbouring queue slots share a weight slab in L2.
-        const int rg = d->raster_group ? d->raster_group : (h->tiles_m >= 8 ? 4 : 1);
+        const int rg = d->raster_group ? d->raster_group : default_raster_group(h->tiles_m);
         h->grp[b] = rg > 1 ? mlpc::merge_groups_by_panel(h->off[b].data(), h->tgt[b].data(),
                                                          static_cast<int32_t>(h->off[b].size() - 1),
                                                          static_cast<int32_t>(h->init[b].size()), h->tiles_n[b + 1], rg)
@@ -600,9 +605,9 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     P.cs = h->cs;
     P.partial_floats = mlpc::kBM * h->max_bn;
     P.recv_bytes = h->recv_bytes;
-    // Default first-stage raster: groups of 4 row panels once there are enough panels, so a
-    // weight column slab is reused from L2 by 4 panels instead of being streamed again per panel.
-    P.raster_group = d.raster_group ? d.raster_group : (h->tiles_m >= 8 ? 4 : 1);
+    // Grouped first-stage raster: a weight column slab is reused from L2 by the panels of a group
+    // instead of being streamed again per panel.
+    P.raster_group = d.raster_group ? d.raster_group : default_raster_group(h->tiles_m);
     P.num_pipe = h->num_pipe;
     P.stage_bytes = h->stage_bytes;
     P.tmem_cols = h->tmem_cols;
