@@ -60,6 +60,8 @@ struct StageParams {
     const __nv_bfloat16 *residual;  // M x N (the chain input) or null
     int32_t gelu;
     int32_t b_kmajor;       // 1: weights stored N x K, B tile is K-major (one box of BN rows)
+    int32_t b_3d;           // weights K x N with N a multiple of the box width: the map is a 3-D
+                            // view (box column, k, box) and one copy loads every box of a B tile
     int32_t split;          // S: CTAs sharing one tile along k (divides the cluster size)
     int32_t kb_per_split;   // k blocks of each slice (the last one may get fewer)
     int32_t tiles_per_item; // cluster size / S
@@ -480,9 +482,10 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint16_t mc_mask = static_cast<uint16_t>((1u << p.cs) - 1u);
     int32_t ps = 0;
     uint32_t pph = 0;
-    uint32_t fills[kMaxPipe];
-    for (int i = 0; i < kMaxPipe; ++i)
-        fills[i] = 0;
+    // Ring slots are filled in order 0, 1, ..., num_pipe - 1, 0, ...: the count of copies issued
+    // says how often each slot was filled (a per-slot array would live in local memory, and its
+    // read-modify-write sits on the per-k-block issue path).
+    uint32_t issued = 0;
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
         if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true, true))
@@ -519,6 +522,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         }
         const StageParams &spr = p.st[s];
         const int32_t tiles_n = spr.tiles_n, BN = spr.BN, b_swz = spr.b_swz, b_kmajor = spr.b_kmajor;
+        const bool b_3d = spr.b_3d != 0;
         const int32_t k_blocks = spr.k_blocks, kbps = spr.kb_per_split;
         const CUtensorMap *mapA = &p.mapA[s];
         const CUtensorMap *mapB = &p.mapB[s];
@@ -559,6 +563,8 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                 uint8_t *bt = b + u * b_tile_bytes;
                 if (b_kmajor) {
                     tma_load_2d(bt, mb, &c->full[ps], kb * kBK, n0, pol_w);
+                } else if (b_3d) {   // every box of the tile in one copy: (box column, k, box)
+                    tma_load_3d(bt, mb, &c->full[ps], 0, kb * kBK, n0 / box_cols, pol_w);
                 } else {
                     for (int32_t j = 0; j < nbox; ++j)
                         tma_load_2d(bt + j * box_bytes, mb, &c->full[ps], n0 + j * box_cols, kb * kBK, pol_w);
@@ -584,7 +590,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                                       m0 + static_cast<int32_t>(mc_rank * mc_rows), mc_mask);
             else
                 tma_load_2d(a, mapA, &c->full[ps], kb * kBK, m0, pol_act);
-            ++fills[ps];
+            ++issued;
             if (++ps == num_pipe) {
                 ps = 0;
                 pph ^= 1;
@@ -598,9 +604,12 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     }
     if (c->abort_flag) {
         // Let every copy this thread issued land before the CTA's shared memory goes away.
-        for (int32_t i = 0; i < num_pipe; ++i)
-            if (fills[i] > 0)
-                wait_bar(&c->full[i], (fills[i] - 1) & 1, c, p, false);
+        const uint32_t np = static_cast<uint32_t>(num_pipe);
+        for (uint32_t i = 0; i < np; ++i) {
+            const uint32_t fills = issued / np + (i < issued % np ? 1u : 0u);
+            if (fills > 0)
+                wait_bar(&c->full[i], (fills - 1) & 1, c, p, false);
+        }
     }
 }
 

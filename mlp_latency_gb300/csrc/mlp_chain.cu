@@ -54,6 +54,36 @@ bool encode_2d(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// B operand map over K x N row-major weights, in boxes of k_rows x (b_swz / 2) columns.  When N
+// is a multiple of the box width the map is a 3-D view (column in box, k, box) with the box
+// stride one box row (b_swz bytes): one copy then loads all BN / box columns of a tile in the
+// same shared-memory layout as one 2-D copy per box, with a single instruction to issue.  A
+// ragged N keeps the 2-D map, whose bounds zero-fill the columns past N.
+bool encode_w_kn(CUtensorMap *map, const void *ptr, int64_t K, int64_t N, int k_rows, int b_swz, int bn,
+                 int32_t *is_3d)
+{
+    const int box_cols = b_swz / 2;
+    const CUtensorMapSwizzle swz = b_swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    *is_3d = 0;
+    if (bn <= box_cols || N % box_cols != 0)
+        return encode_2d(map, ptr, K, N, k_rows, box_cols, swz);
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(box_cols), static_cast<cuuint64_t>(K),
+                          static_cast<cuuint64_t>(N / box_cols)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(b_swz)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(k_rows),
+                         static_cast<cuuint32_t>(bn / box_cols)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return encode_2d(map, ptr, K, N, k_rows, box_cols, swz);   // the driver refused the view
+    *is_3d = 1;
+    return true;
+}
+
 struct DeviceBoundary {
     int32_t *pg_off = nullptr, *pg_tgt = nullptr, *grp_off = nullptr, *grp_mem = nullptr, *grp_init = nullptr;
     int32_t *cgrp = nullptr;
@@ -571,16 +601,25 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         if (d.a_multicast &&
             !encode_2d(&P.mapAp[s], a_ptr, d.M, d.dims[s], mlpc::kBM / h->cs, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
             return MLP_ERR_CUDA;
-        auto encode_w = [&](CUtensorMap *m, const void *w) {
+        int32_t b_3d = 0, u_3d = 0;
+        auto encode_w = [&](CUtensorMap *m, const void *w, int32_t *is_3d) {
+            *is_3d = 0;
             return d.weight_layout == 1
                        ? encode_2d(m, w, d.dims[s + 1], d.dims[s], h->BN[s], mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B)
-                       : encode_2d(m, w, d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
-                                   h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                       : encode_w_kn(m, w, d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s], h->BN[s], is_3d);
         };
         const bool gate_s = d.gated && s == 0;
-        if (!encode_w(&P.mapB[s], W[s == 0 ? 0 : s + (d.gated ? 1 : 0)]) || (gate_s && !encode_w(&P.mapU, W[1])))
+        if (!encode_w(&P.mapB[s], W[s == 0 ? 0 : s + (d.gated ? 1 : 0)], &b_3d) ||
+            (gate_s && !encode_w(&P.mapU, W[1], &u_3d)))
             return MLP_ERR_CUDA;
         mlpc::StageParams &sp = P.st[s];
+        sp.b_3d = b_3d && (!gate_s || u_3d);   // gate and up maps share the stage's copy shape
+        if (gate_s && b_3d != u_3d &&
+            !(encode_2d(&P.mapB[s], W[0], d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
+                        h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
+              encode_2d(&P.mapU, W[1], d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s] / 2,
+                        h->b_swz[s] == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)))
+            return MLP_ERR_CUDA;
         sp.M = static_cast<int32_t>(d.M);
         sp.K = static_cast<int32_t>(d.dims[s]);
         sp.N = static_cast<int32_t>(d.dims[s + 1]);
@@ -1039,11 +1078,12 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     void *o_ptr[2] = {H, Y};
     for (int s = 0; s < 2; ++s) {
         const int b_swz = bn[s] >= 64 ? 128 : 64;
+        int32_t b_3d = 0;
         if (!encode_2d(&P_.mapA[s], a_ptr[s], M, dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&P_.mapB[s], w_ptr[s], dims[s], dims[s + 1], mlpc::kBK, b_swz / 2,
-                       b_swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+            !encode_w_kn(&P_.mapB[s], w_ptr[s], dims[s], dims[s + 1], mlpc::kBK, b_swz, bn[s], &b_3d))
             return MLP_ERR_CUDA;
         mlpc::StageParams &sp = P_.st[s];
+        sp.b_3d = b_3d;
         sp.M = static_cast<int32_t>(M);
         sp.K = static_cast<int32_t>(dims[s]);
         sp.N = static_cast<int32_t>(dims[s + 1]);
