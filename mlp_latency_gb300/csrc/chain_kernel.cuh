@@ -546,6 +546,36 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         int32_t ready_hi = -1;
         const int32_t slice_last = kwait_s ? min(((kb1 - 1) * kBK + kBK - 1) / pBN, ptn - 1) : 0;
         bool ok = true;
+        if (!kwait_s && !a_mcast && !gated && (b_kmajor || b_3d || nbox == 1)) {
+            // The common case: two copies per k block (the B tile in one copy whatever its
+            // layout), no per-k-block mode branches; see role_mma for why that matters.
+            const int32_t bx = b_kmajor ? 0 : (b_3d ? 0 : n0);   // B coordinates, k excluded
+            const int32_t by = b_kmajor ? n0 : (b_3d ? n0 / box_cols : 0);
+            const int32_t b_form = b_kmajor ? 0 : (b_3d ? 1 : 2);
+            for (int32_t kb = kb0; kb < kb1; ++kb) {
+                if (leader && kb == lead_kb)
+                    mbar_arrive(&c->want_next);
+                if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
+                mbar_arrive_expect_tx(&c->full[ps], bytes);
+                const int32_t k = kb * kBK;
+                if (b_form == 0)
+                    tma_load_2d(a + kABytes, mapB, &c->full[ps], k, by, pol_w);
+                else if (b_form == 1)
+                    tma_load_3d(a + kABytes, mapB, &c->full[ps], 0, k, by, pol_w);
+                else
+                    tma_load_2d(a + kABytes, mapB, &c->full[ps], bx, k, pol_w);
+                tma_load_2d(a, mapA, &c->full[ps], k, m0, pol_act);
+                ++issued;
+                if (++ps == num_pipe) {
+                    ps = 0;
+                    pph ^= 1;
+                }
+            }
+        } else
         for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (leader && kb == lead_kb)
                 mbar_arrive(&c->want_next);
@@ -656,6 +686,38 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         const uint32_t idesc = idesc_bf16_f32(kBM, gated ? 2u * BN : BN, b_kmajor ? 0u : 1u);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
         bool ok = true;
+        if (!lamport && !split2 && !a_mcast) {
+            // The common case, kept free of per-k-block branches and address arithmetic: one
+            // thread issues this loop back to back, so every instruction in it is on the path.
+            // Descriptors are built once for ring slot 0; a slot's (and a 16-deep k step's)
+            // offset adds to the 14-bit start-address field in 16-byte units, which cannot
+            // carry out of it (shared memory is below 2^18 bytes).
+            const uint32_t ring_base = smem_u32(ring);
+            const uint64_t ad0 = smem_desc(ring_base, 16u, 1024u, 2u);
+            const uint64_t bd0 = b_kmajor ? smem_desc(ring_base + kABytes, 16u, 1024u, 2u)
+                                          : smem_desc(ring_base + kABytes, kBK * b_swz, 8u * b_swz, b_code);
+            const uint64_t bstep = b_kmajor ? 2u : b_swz;   // 16-byte units per 16-deep k step
+            const uint64_t slot16 = stage_bytes >> 4;
+            uint32_t accum = 0;
+            for (int32_t kb = kb0; kb < kb1; ++kb) {
+                if (!wait_bar(&c->full[ps], pph, c, p)) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t off = static_cast<uint64_t>(ps) * slot16;
+#pragma unroll
+                for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
+                    mma_bf16_ss(d_tmem, ad0 + off + 2u * kk, bd0 + off + bstep * kk, idesc, accum);
+                    accum = 1u;   // the slice's first k step overwrites the accumulator
+                }
+                issued = true;
+                mma_commit(&c->empty[ps]);
+                if (++ps == num_pipe) {
+                    ps = 0;
+                    pph ^= 1;
+                }
+            }
+        } else
         for (int32_t kb = kb0; kb < kb1; ++kb) {
             // TMA fills and tcgen05.mma reads are both async-proxy operations ordered by the
             // mbarrier's transaction count: no tcgen05 fence is needed per k block.
