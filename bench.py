@@ -354,7 +354,7 @@ def run_sweep(args):
                     raise RuntimeError(f"{mode} (rows {rows}) differs from the first mode at M={M}")
                 return med
 
-        for mode in ("sequential", "pipelined", "pipelined_kwait"):
+        for mode in ("sequential", "sequential_pdl", "pipelined", "pipelined_kwait"):
             line[f"{mode}_us"] = timed(mode)
         best = None
         rows = 128
@@ -380,7 +380,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--tile-n", default=None, help="comma-separated tile widths per GEMM (0 = library choice)")
     ap.add_argument("--k-split", default=None, help="comma-separated split-K factors per GEMM (0 = library choice)")
-    ap.add_argument("--mode", default="pipelined", choices=["pipelined", "pipelined_kwait", "pipelined_lamport", "sequential", "microbatch"])
+    ap.add_argument("--mode", default="pipelined", choices=["pipelined", "pipelined_kwait", "pipelined_lamport", "sequential", "sequential_pdl", "microbatch"])
     ap.add_argument("--microbatch-rows", type=int, default=0)
     ap.add_argument("--raster-group", type=int, default=0)
     ap.add_argument("--pipe-stages", type=int, default=0)
@@ -501,7 +501,7 @@ def main():
         baselines = {}
         k_base = min(args.steps, 300)
         if not args.no_baselines:
-            for mode in ("sequential", "pipelined", "pipelined_kwait", "pipelined_lamport"):
+            for mode in ("sequential", "sequential_pdl", "pipelined", "pipelined_kwait", "pipelined_lamport"):
                 if mode == args.mode:
                     continue
                 ch = make(mode)

@@ -32,6 +32,15 @@
  * weight tiles are requested before the wait).  Every mode uses the same tiles in the same
  * order of k, so Y is bit-identical across modes.
  *
+ * MLP_MODE_SEQUENTIAL_PDL is the pages' two-kernel form (one kernel per layer, the consumer
+ * launched while the producer still runs) without its flag polling across kernels, which
+ * nothing makes safe on one GPU (co-residency of two grids is not guaranteed): GEMM s+1 is a
+ * programmatic dependent launch of GEMM s.  Every CTA of GEMM s allows its dependents at start;
+ * GEMM s+1's CTAs then take SMs as GEMM s's CTAs retire, run their set-up (barriers, TMEM,
+ * descriptor prefetch) and wait in the TMA warp, before the first load of GEMM s's output, for
+ * GEMM s to complete (griddepcontrol.wait, a hardware dependency).  Same tiles and k order as
+ * MLP_MODE_SEQUENTIAL, so Y is bit-identical to it.
+ *
  * MLP_MODE_PIPELINED_LAMPORT is the paper's Lamport-synchronisation alternative (section V):
  * the same queue protocol with no fence on either side.  run() first fills the intermediates
  * with bf16 -0.0 (one extra launch); producers store +0.0 for an exact -0.0 and publish without
@@ -86,8 +95,10 @@ typedef enum {
     MLP_MODE_SEQUENTIAL = 1,  /* one launch per GEMM, back to back                              */
     MLP_MODE_MICROBATCH = 2,  /* row chunks, GEMM s+1 of chunk i overlaps GEMM s of chunk i+1   */
     MLP_MODE_PIPELINED_KWAIT = 3, /* one persistent grid, per-k-block producer waits, no queue  */
-    MLP_MODE_PIPELINED_LAMPORT = 4 /* the queue protocol without fences: sentinel-filled
+    MLP_MODE_PIPELINED_LAMPORT = 4, /* the queue protocol without fences: sentinel-filled
                                       intermediates, consumers validate what they load         */
+    MLP_MODE_SEQUENTIAL_PDL = 5 /* one launch per GEMM, each later one a programmatic dependent
+                                   launch of the one before (no spin on another kernel's flags) */
 } mlp_mode;
 
 typedef enum { MLP_EPI_NONE = 0, MLP_EPI_GELU_TANH = 1 } mlp_epilogue;

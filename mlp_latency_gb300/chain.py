@@ -16,7 +16,8 @@ from ._lib import ChainDesc, ChainInfo, Event
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_DEVICE_STATE, ERR_BAD_TILE = range(8)
 DT_BF16, DT_F32 = 1, 2
-MODES = {"pipelined": 0, "sequential": 1, "microbatch": 2, "pipelined_kwait": 3, "pipelined_lamport": 4}
+MODES = {"pipelined": 0, "sequential": 1, "microbatch": 2, "pipelined_kwait": 3, "pipelined_lamport": 4,
+         "sequential_pdl": 5}
 DEBUG_EVENT_LOG, DEBUG_DROP_DECREMENT, DEBUG_FORCE_RELOAD = 1, 2, 4
 
 EVENT_DTYPE = np.dtype([("stage", np.int32), ("tile", np.int32), ("smid", np.int32), ("cta", np.int32),

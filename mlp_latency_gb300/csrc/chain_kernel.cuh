@@ -109,6 +109,9 @@ struct ChainParams {
     int32_t kwait;                       // pipelined with per-k-block producer waits, no work-queue
     int32_t lamport;                     // pipelined, fence-free: consumers validate what they load
     int32_t force_reload;                // Lamport test hook: reload every consumer A tile once
+    int32_t pdl_wait;                    // programmatic dependent of the previous stage's launch:
+                                         // the TMA warp waits for it before its first load
+    int32_t pdl_trigger;                 // a later stage is launched as this launch's dependent
     int32_t first_stage;                 // non-pipelined launches run this single stage
     int32_t m_tile_begin, m_tile_end;    // ... over these row tiles
     int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
@@ -482,6 +485,8 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint16_t mc_mask = static_cast<uint16_t>((1u << p.cs) - 1u);
     int32_t ps = 0;
     uint32_t pph = 0;
+    if (p.pdl_wait)   // the previous GEMM's output (this launch's A) is complete and visible
+        griddep_wait();
     // Ring slots are filled in order 0, 1, ..., num_pipe - 1, 0, ...: the count of copies issued
     // says how often each slot was filled (a per-slot array would live in local memory, and its
     // read-modify-write sits on the per-k-block issue path).
@@ -1465,6 +1470,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     cluster_sync_all();   // every barrier of the cluster is initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = c->tmem_base;
+    if (p.pdl_trigger && threadIdx.x == 0)
+        griddep_launch_dependents();   // the next GEMM's CTAs may take SMs as this grid's retire
 
     if (!c->skip) {
         if (warp == 0) {

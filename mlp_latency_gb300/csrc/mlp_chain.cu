@@ -273,7 +273,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_INVALID_ARG;
     if (d->residual && d->dims[S] != d->dims[0])
         return MLP_ERR_INVALID_ARG;
-    if (!is_pipelined(d->mode) && d->mode != MLP_MODE_SEQUENTIAL && d->mode != MLP_MODE_MICROBATCH)
+    if (!is_pipelined(d->mode) && d->mode != MLP_MODE_SEQUENTIAL && d->mode != MLP_MODE_MICROBATCH &&
+        d->mode != MLP_MODE_SEQUENTIAL_PDL)
         return MLP_ERR_INVALID_ARG;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < mlpc::kBM || d->microbatch_rows % mlpc::kBM))
         return MLP_ERR_INVALID_ARG;
@@ -693,22 +694,31 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
 
 static bool launch(const ChainParams &P, int grid, size_t smem, cudaStream_t st)
 {
-    if (P.cs == 1) {
+    if (P.cs == 1 && !P.pdl_wait) {
         mlpc::chain_kernel<<<grid, mlpc::kThreads, smem, st>>>(P);
         return cudaGetLastError() == cudaSuccess;
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(P.cs);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (P.cs > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(P.cs);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (P.pdl_wait) {   // a programmatic dependent of the previous launch on this stream
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(mlpc::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, mlpc::chain_kernel, P) == cudaSuccess && cudaGetLastError() == cudaSuccess;
 }
 
@@ -740,6 +750,8 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
         return ps;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ChainParams P = h->params;
+    P.pdl_wait = 0;
+    P.pdl_trigger = 0;
     if (is_pipelined(h->desc.mode)) {
         P.pipelined = 1;
         P.kwait = h->desc.mode == MLP_MODE_PIPELINED_KWAIT;
@@ -764,11 +776,14 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
         return launch(P, h->grid, h->smem, st) ? MLP_OK : MLP_ERR_CUDA;
     }
     P.pipelined = 0;
-    if (h->desc.mode == MLP_MODE_SEQUENTIAL) {
+    if (h->desc.mode == MLP_MODE_SEQUENTIAL || h->desc.mode == MLP_MODE_SEQUENTIAL_PDL) {
+        const bool pdl = h->desc.mode == MLP_MODE_SEQUENTIAL_PDL;
         for (int s = 0; s < h->S; ++s) {
             P.first_stage = s;
             P.m_tile_begin = 0;
             P.m_tile_end = h->tiles_m;
+            P.pdl_wait = pdl && s > 0;
+            P.pdl_trigger = pdl && s + 1 < h->S;
             if (!launch(P, static_grid(h, h->items[s]), h->smem, st))
                 return MLP_ERR_CUDA;
         }
@@ -892,7 +907,7 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->smem_bytes = static_cast<int32_t>(h->smem);
     info->tmem_cols = static_cast<int32_t>(h->tmem_cols);
     info->launches_per_run = is_pipelined(h->desc.mode) ? (h->desc.mode == MLP_MODE_PIPELINED_LAMPORT && h->S > 1 ? 2 : 1)
-                             : h->desc.mode == MLP_MODE_SEQUENTIAL ? h->S
+                             : (h->desc.mode == MLP_MODE_SEQUENTIAL || h->desc.mode == MLP_MODE_SEQUENTIAL_PDL) ? h->S
                                                                    : h->S * h->n_chunks;
     info->cluster_size = h->cs;
     for (int s = 0; s < h->S; ++s)

@@ -207,6 +207,18 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t 
                  : "memory");
 }
 
+// ------------------------------------------------------------ programmatic dependent launch --
+// Wait until every grid this one depends on (a programmatic dependent launch) has completed and
+// its memory operations are visible; a no-op when the launch has no such dependency.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow this grid's programmatic dependents to be scheduled (once every CTA has said so or
+// exited).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- tcgen05/TMEM --
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
 {

@@ -130,6 +130,7 @@ def _desc(**kw):
     ({"tile_m": 96}, mc.ERR_UNSUPPORTED),
     ({"residual": 1, "dims": (256, 256, 512)}, mc.ERR_INVALID_ARG),
     ({"mode": 2, "microbatch_rows": 100}, mc.ERR_INVALID_ARG),
+    ({"mode": 6}, mc.ERR_INVALID_ARG),                             # modes 0 .. 5
     ({"mode": 7}, mc.ERR_INVALID_ARG),
     # a gated (SwiGLU) first GEMM keeps gate and up side by side in TMEM: unsplit, <= 128 wide
     ({"gated": 1, "acc_split": 2}, mc.ERR_UNSUPPORTED),
