@@ -27,6 +27,7 @@
 // The scheduler and epilogue warps would otherwise wait at pipeline barriers, so the protocol
 // work overlaps the next tile's mainloop: the hiding of section III-C, Fig. 2b.
 #pragma once
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -485,7 +486,10 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint16_t mc_mask = static_cast<uint16_t>((1u << p.cs) - 1u);
     int32_t ps = 0;
     uint32_t pph = 0;
-    if (p.pdl_wait)   // the previous GEMM's output (this launch's A) is complete and visible
+    // Programmatic dependent launch: the previous GEMM's output (this launch's A) is complete and
+    // visible after this.  (Sending the first ring-full of weight copies before the wait measured
+    // slower: they compete with the previous GEMM's last loads.)
+    if (p.pdl_wait)
         griddep_wait();
     // Ring slots are filled in order 0, 1, ..., num_pipe - 1, 0, ...: the count of copies issued
     // says how often each slot was filled (a per-slot array would live in local memory, and its
@@ -551,35 +555,50 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         int32_t ready_hi = -1;
         const int32_t slice_last = kwait_s ? min(((kb1 - 1) * kBK + kBK - 1) / pBN, ptn - 1) : 0;
         bool ok = true;
-        if (!kwait_s && !a_mcast && !gated && (b_kmajor || b_3d || nbox == 1)) {
-            // The common case: two copies per k block (the B tile in one copy whatever its
-            // layout), no per-k-block mode branches; see role_mma for why that matters.
+        if (!kwait_s && !a_mcast && (b_kmajor || b_3d || nbox == 1)) {
+            // The common case: two copies per k block (three for a gated stage: gate and up
+            // weights), the B tile in one copy whatever its layout, no per-k-block mode
+            // branches; see role_mma for why that matters.
             const int32_t bx = b_kmajor ? 0 : (b_3d ? 0 : n0);   // B coordinates, k excluded
             const int32_t by = b_kmajor ? n0 : (b_3d ? n0 / box_cols : 0);
             const int32_t b_form = b_kmajor ? 0 : (b_3d ? 1 : 2);
-            for (int32_t kb = kb0; kb < kb1; ++kb) {
-                if (leader && kb == lead_kb)
-                    mbar_arrive(&c->want_next);
-                if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
-                    ok = false;
-                    break;
+            const CUtensorMap *mapU = &p.mapU;
+            // One loop per stage kind, so the plain loop carries no test for the gated copy.
+            auto k_loop = [&](auto gated_kind) {
+                constexpr bool kGated = decltype(gated_kind)::value;
+                for (int32_t kb = kb0; kb < kb1; ++kb) {
+                    if (leader && kb == lead_kb)
+                        mbar_arrive(&c->want_next);
+                    if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
+                    mbar_arrive_expect_tx(&c->full[ps], bytes);
+                    const int32_t k = kb * kBK;
+#pragma unroll
+                    for (int32_t u = 0; u < (kGated ? 2 : 1); ++u) {   // gate (or plain) weights, then up
+                        const CUtensorMap *mb = u ? mapU : mapB;
+                        uint8_t *bt = a + kABytes + u * b_tile_bytes;
+                        if (b_form == 0)
+                            tma_load_2d(bt, mb, &c->full[ps], k, by, pol_w);
+                        else if (b_form == 1)
+                            tma_load_3d(bt, mb, &c->full[ps], 0, k, by, pol_w);
+                        else
+                            tma_load_2d(bt, mb, &c->full[ps], bx, k, pol_w);
+                    }
+                    tma_load_2d(a, mapA, &c->full[ps], k, m0, pol_act);
+                    ++issued;
+                    if (++ps == num_pipe) {
+                        ps = 0;
+                        pph ^= 1;
+                    }
                 }
-                uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
-                mbar_arrive_expect_tx(&c->full[ps], bytes);
-                const int32_t k = kb * kBK;
-                if (b_form == 0)
-                    tma_load_2d(a + kABytes, mapB, &c->full[ps], k, by, pol_w);
-                else if (b_form == 1)
-                    tma_load_3d(a + kABytes, mapB, &c->full[ps], 0, k, by, pol_w);
-                else
-                    tma_load_2d(a + kABytes, mapB, &c->full[ps], bx, k, pol_w);
-                tma_load_2d(a, mapA, &c->full[ps], k, m0, pol_act);
-                ++issued;
-                if (++ps == num_pipe) {
-                    ps = 0;
-                    pph ^= 1;
-                }
-            }
+            };
+            if (gated)
+                k_loop(std::true_type{});
+            else
+                k_loop(std::false_type{});
         } else
         for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (leader && kb == lead_kb)
