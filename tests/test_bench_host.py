@@ -1,0 +1,55 @@
+"""Host-side logic of bench.py that needs no GPU: the DRAM-traffic figure is taken from a committed
+ncu summary only while that summary was captured on the current kernel and host sources, and the
+peak denominators come from the measured-peaks file when present, else the stated fallback."""
+import json
+import os
+
+import pytest
+
+import bench
+
+
+def _write_profile(dirpath, workload, sha, traffic):
+    p = dirpath / f"chain_kernel_{workload}.md"
+    p.write_text(f"# summary\n\n- kernel_source_sha256: `{sha}`\n- traffic_bytes_per_launch: {traffic}\n\n| a | b |\n")
+    return p
+
+
+def test_every_hashed_source_exists():
+    for f in bench.KERNEL_SOURCES:
+        assert os.path.exists(os.path.join(bench.ROOT, f)), f
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+
+
+def test_traffic_only_from_a_summary_of_this_kernel(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILE_DIR", str(tmp_path))
+    assert bench.recorded_traffic("decode_m128_d4096") is None            # no summary
+    _write_profile(tmp_path, "decode_m128_d4096", bench.kernel_source_hash(), 69006848)
+    assert bench.recorded_traffic("decode_m128_d4096") == 69006848.0
+    _write_profile(tmp_path, "decode_m128_d4096", "0" * 16, 69006848)     # taken on another kernel
+    assert bench.recorded_traffic("decode_m128_d4096") is None
+    _write_profile(tmp_path, "decode_m128_d4096", bench.kernel_source_hash(), "n/a")
+    assert bench.recorded_traffic("decode_m128_d4096") is None
+
+
+def test_committed_summaries_parse():
+    # each committed summary names its workload, its kernel source and a positive traffic figure
+    d = bench.PROFILE_DIR
+    names = [f for f in os.listdir(d) if f.startswith("chain_kernel_") and f.endswith(".md")]
+    assert names
+    for n in names:
+        text = open(os.path.join(d, n)).read()
+        assert "kernel_source_sha256: `" in text and "--clock-control none" in text
+        line = next(l for l in text.splitlines() if l.startswith("- traffic_bytes_per_launch:"))
+        assert float(line.split(":", 1)[1]) > 0
+
+
+def test_peaks_from_the_measured_file_else_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    fb = bench.load_peaks()
+    assert fb["source"] == "fallback" and fb["hbm_gbs"] == 6800.0 and fb["bf16_tflops"] == 1900.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6698.5, "bf16_tflops": 1927.1,
+                                                              "bf16_tflops_sustained": 1727.7}))
+    p = bench.load_peaks()
+    assert p["source"] == "measured" and p["hbm_gbs"] == 6698.5 and p["bf16_tflops_sustained"] == 1727.7
