@@ -52,6 +52,17 @@ class Chain:
     Shapes follow the header: X[M x dims[0]], W[s][dims[s] x dims[s+1]] (weight_layout "kn") or
     W[s][dims[s+1] x dims[s]] ("nk", nn.Linear's layout), Y[M x dims[-1]].  With ``gated`` the
     first GEMM is SwiGLU and run() takes one more weight: [W_gate, W_up, W_2, ...].
+
+    ``mode`` (every mode gives bit-identical Y for the same tiles):
+      "pipelined"          one persistent grid, scoreboard counters and work-queue (CTA-pipelining);
+      "pipelined_kwait"    one persistent grid, consumers wait per 64-deep k block of their input;
+      "pipelined_lamport"  the queue protocol without fences, consumers validate a sentinel;
+      "sequential"         one launch per GEMM;
+      "sequential_pdl"     one launch per GEMM, each a programmatic dependent launch of the one before;
+      "microbatch"         row chunks of ``microbatch_rows``, GEMMs of different chunks overlapped.
+    ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice); ``a_multicast`` 2/4/8 shares each
+    activation tile across a cluster by TMA multicast (one row panel, unsplit GEMMs).  Errors raise
+    MlpChainError with the library's status.
     """
 
     def __init__(self, M: int, dims: Sequence[int], *, tile_n: Optional[Sequence[int]] = None,
