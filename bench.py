@@ -385,8 +385,6 @@ def main():
     ap.add_argument("--raster-group", type=int, default=0)
     ap.add_argument("--pipe-stages", type=int, default=0)
     ap.add_argument("--acc-split", type=int, default=0)
-    ap.add_argument("--a-multicast", type=int, default=0,
-                    help="clusters of 2/4/8 CTAs sharing each activation tile by TMA multicast (one row panel)")
     ap.add_argument("--weight-layout", default="kn", choices=["kn", "nk"],
                     help="nk: weights stored transposed (nn.Linear layout)")
     ap.add_argument("--no-baselines", action="store_true", help="skip sequential/micro-batch/cuBLAS lines")
@@ -437,8 +435,7 @@ def main():
         return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
                         microbatch_rows=rows, device=local, raster_group=args.raster_group,
                         pipe_stages=args.pipe_stages, acc_split=args.acc_split,
-                        weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated,
-                        a_multicast=args.a_multicast if mode != "pipelined_lamport" else 0)
+                        weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()

@@ -158,14 +158,6 @@ typedef struct {
                                            the weight of GEMM s >= 1.  The gated GEMM runs
                                            unsplit with tile_n <= 128 and acc_split 1; epilogue
                                            (GeLU) applies to the later GEMMs only                 */
-    int32_t a_multicast;                /* 0: off; 2, 4 or 8: thread-block clusters of that many
-                                           CTAs run adjacent column tiles of one row panel, and
-                                           each CTA loads 1/n of the shared activation tile and
-                                           multicasts it to the cluster (TMA multicast), so the
-                                           tile is read from L2 once per cluster instead of once
-                                           per CTA.  Needs M <= 128 (one row panel), every GEMM
-                                           unsplit with a multiple of n column tiles, no gating
-                                           and not MLP_MODE_PIPELINED_LAMPORT; else UNSUPPORTED   */
 } mlp_chain_desc;
 
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG).  t_* are %globaltimer ns;

@@ -60,9 +60,8 @@ class Chain:
       "sequential"         one launch per GEMM;
       "sequential_pdl"     one launch per GEMM, each a programmatic dependent launch of the one before;
       "microbatch"         row chunks of ``microbatch_rows``, GEMMs of different chunks overlapped.
-    ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice); ``a_multicast`` 2/4/8 shares each
-    activation tile across a cluster by TMA multicast (one row panel, unsplit GEMMs).  Errors raise
-    MlpChainError with the library's status.
+    ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice).  Errors raise MlpChainError with
+    the library's status.
     """
 
     def __init__(self, M: int, dims: Sequence[int], *, tile_n: Optional[Sequence[int]] = None,
@@ -71,7 +70,7 @@ class Chain:
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
                  weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False,
-                 force_reload: bool = False, a_multicast: int = 0):
+                 force_reload: bool = False):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -102,7 +101,6 @@ class Chain:
         for i, v in enumerate(k_split or []):
             d.k_split[i] = int(v)
         d.gated = int(bool(gated))
-        d.a_multicast = int(a_multicast)
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
         self.n_weights = len(self.dims) - 1 + int(bool(gated))
         self._lib = lib

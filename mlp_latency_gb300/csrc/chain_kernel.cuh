@@ -102,7 +102,6 @@ struct ChainParams {
     CUtensorMap mapA[kMaxStages];
     CUtensorMap mapB[kMaxStages];
     CUtensorMap mapU;                    // up-projection weights of a gated first stage
-    CUtensorMap mapAp[kMaxStages];       // activation pieces of 128 / cs rows (A multicast)
     StageParams st[kMaxStages];
     BoundaryParams bd[kMaxStages - 1];
     int32_t num_stages;
@@ -118,7 +117,6 @@ struct ChainParams {
     int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
     int32_t tile_base[kMaxStages + 1];   // first event-log record of each stage
     int32_t cs;                          // cluster size
-    int32_t a_mcast;                     // clusters share each activation tile via TMA multicast
     int32_t raster_group;
     int32_t num_pipe;                    // shared-memory ring depth
     uint32_t stage_bytes;                // bytes of one ring slot (A + B)
@@ -480,10 +478,6 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     const bool pipelined = p.pipelined != 0;
     const bool kwait = pipelined && p.kwait != 0;
     EventRec *const events = pipelined ? p.events : nullptr;
-    const bool a_mcast = p.a_mcast != 0;
-    const uint32_t mc_rank = cluster_ctarank();
-    const uint32_t mc_rows = static_cast<uint32_t>(kBM / p.cs);
-    const uint16_t mc_mask = static_cast<uint16_t>((1u << p.cs) - 1u);
     int32_t ps = 0;
     uint32_t pph = 0;
     // Programmatic dependent launch: the previous GEMM's output (this launch's A) is complete and
@@ -555,7 +549,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         int32_t ready_hi = -1;
         const int32_t slice_last = kwait_s ? min(((kb1 - 1) * kBK + kBK - 1) / pBN, ptn - 1) : 0;
         bool ok = true;
-        if (!kwait_s && !a_mcast && (b_kmajor || b_3d || nbox == 1)) {
+        if (!kwait_s && (b_kmajor || b_3d || nbox == 1)) {
             // The common case: two copies per k block (three for a gated stage: gate and up
             // weights), the B tile in one copy whatever its layout, no per-k-block mode
             // branches; see role_mma for why that matters.
@@ -639,11 +633,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             }
             // (after a failed wait the load still goes out, so that the slot's transaction
             // count completes and the drain below accounts for every copy in flight)
-            if (a_mcast)   // my 128 / cs rows of the activation tile, into every CTA of the cluster
-                tma_load_2d_multicast(a + mc_rank * mc_rows * (kBK * 2), &p.mapAp[s], &c->full[ps], kb * kBK,
-                                      m0 + static_cast<int32_t>(mc_rank * mc_rows), mc_mask);
-            else
-                tma_load_2d(a, mapA, &c->full[ps], kb * kBK, m0, pol_act);
+            tma_load_2d(a, mapA, &c->full[ps], kb * kBK, m0, pol_act);
             ++issued;
             if (++ps == num_pipe) {
                 ps = 0;
@@ -676,8 +666,6 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint32_t sub_stride = static_cast<uint32_t>(p.sub_stride);
     const bool split2 = p.acc_split == 2;
     const bool lamport = p.pipelined && p.lamport;
-    const bool a_mcast = p.a_mcast != 0;
-    const uint16_t mc_mask = static_cast<uint16_t>((1u << p.cs) - 1u);
     int32_t ps = 0;
     uint32_t pph = 0;
     uint32_t local_tiles = 0;
@@ -710,7 +698,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         const uint32_t idesc = idesc_bf16_f32(kBM, gated ? 2u * BN : BN, b_kmajor ? 0u : 1u);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
         bool ok = true;
-        if (!lamport && !split2 && !a_mcast) {
+        if (!lamport && !split2) {
             // The common case, kept free of per-k-block branches and address arithmetic: one
             // thread issues this loop back to back, so every instruction in it is on the path.
             // Descriptors are built once for ring slot 0; a slot's (and a 16-deep k step's)
@@ -770,12 +758,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                 mma_bf16_ss(d_tmem + sub * sub_stride, ad, bd, idesc, accum);
             }
             issued = true;
-            // frees the ring slot once these MMAs have read it (in every CTA of the cluster when
-            // its CTAs fill each other's slots)
-            if (a_mcast)
-                mma_commit_multicast(&c->empty[ps], mc_mask);
-            else
-                mma_commit(&c->empty[ps]);
+            mma_commit(&c->empty[ps]);   // frees the ring slot once these MMAs have read it
             if (++ps == num_pipe) {
                 ps = 0;
                 pph ^= 1;
@@ -1436,8 +1419,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.num_pipe; ++i) {
             mbar_init(&c->full[i], 1);
-            // with A multicast a slot is refilled only once every CTA of the cluster consumed it
-            mbar_init(&c->empty[i], p.a_mcast ? p.cs : 1);
+            mbar_init(&c->empty[i], 1);
             mbar_init(&c->valid[i], 1);
             mbar_init(&c->reload[i], 1);
         }
@@ -1477,9 +1459,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
         if (p.st[0].gated)
             prefetch_tensormap(&p.mapU);
-        if (p.a_mcast)
-            for (int i = 0; i < p.num_stages; ++i)
-                prefetch_tensormap(&p.mapAp[i]);
     }
     if (warp == 1) {
         tmem_alloc(&c->tmem_base, p.tmem_cols);

@@ -278,8 +278,6 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_INVALID_ARG;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < mlpc::kBM || d->microbatch_rows % mlpc::kBM))
         return MLP_ERR_INVALID_ARG;
-    if (d->a_multicast != 0 && d->a_multicast != 2 && d->a_multicast != 4 && d->a_multicast != 8)
-        return MLP_ERR_INVALID_ARG;
     if (d->gated && (d->acc_split == 2 || (d->tile_n[0] != 0 && d->tile_n[0] > 128) ||
                      (d->k_split[0] != 0 && d->k_split[0] != 1)))
         return MLP_ERR_UNSUPPORTED;   // the gated GEMM keeps gate and up side by side in TMEM, unsplit
@@ -359,18 +357,6 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->split[s] = split;
         h->kb_per_split[s] = (h->k_blocks[s] + split - 1) / split;
         h->cs = std::max(h->cs, split);
-    }
-    if (d->a_multicast) {
-        // every CTA of a cluster must stream the same activation k-blocks in the same order: one
-        // row panel, unsplit stages, whole clusters of column tiles
-        bool ok = h->tiles_m == 1 && !d->gated && d->mode != MLP_MODE_PIPELINED_LAMPORT;
-        for (int s = 0; s < S && ok; ++s)
-            ok = h->split[s] == 1 && h->tiles_n[s] % d->a_multicast == 0;
-        if (!ok) {
-            release(h);
-            return MLP_ERR_UNSUPPORTED;
-        }
-        h->cs = d->a_multicast;
     }
     for (int s = 0; s < S; ++s) {
         const int tpi = h->cs / h->split[s];
@@ -598,10 +584,6 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         }
         if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
             return MLP_ERR_CUDA;
-        // multicast: each CTA of the cluster loads 128 / cs rows of the activation tile
-        if (d.a_multicast &&
-            !encode_2d(&P.mapAp[s], a_ptr, d.M, d.dims[s], mlpc::kBM / h->cs, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
-            return MLP_ERR_CUDA;
         int32_t b_3d = 0, u_3d = 0;
         auto encode_w = [&](CUtensorMap *m, const void *w, int32_t *is_3d) {
             *is_3d = 0;
@@ -661,7 +643,6 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.tile_base[s] = h->tile_base[s];
     }
     P.cs = h->cs;
-    P.a_mcast = d.a_multicast ? 1 : 0;
     P.partial_floats = mlpc::kBM * h->max_bn;
     P.recv_bytes = h->recv_bytes;
     // Grouped first-stage raster: a weight column slab is reused from L2 by the panels of a group

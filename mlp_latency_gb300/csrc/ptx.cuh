@@ -186,18 +186,6 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
-// 2-D tiled load delivered to the same shared-memory offset in every CTA of the cluster named in
-// cta_mask; each destination's mbarrier at `bar`'s offset counts the bytes it received.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
-                                                      int32_t c1, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 // Prefetch a 2-D box into L2 only (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t c0, int32_t c1)
 {
@@ -257,16 +245,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
-                 : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same shared-memory offset in every CTA of the
-// cluster named in cta_mask.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     smem_u32(bar)),
-                 "h"(cta_mask)
                  : "memory");
 }
 

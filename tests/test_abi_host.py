@@ -136,7 +136,6 @@ def _desc(**kw):
     ({"gated": 1, "acc_split": 2}, mc.ERR_UNSUPPORTED),
     ({"gated": 1, "k_split": (2, 0)}, mc.ERR_UNSUPPORTED),
     ({"gated": 1, "tile_n": (256, 0)}, mc.ERR_UNSUPPORTED),
-    ({"a_multicast": 3}, mc.ERR_INVALID_ARG),                       # clusters of 2, 4 or 8
 ])
 def test_create_rejects_bad_descriptors_before_touching_cuda(lib, kw, expect):
     h = ctypes.c_void_p()
