@@ -31,7 +31,7 @@ import numpy as np  # noqa: E402
 import seeded_inputs as si  # noqa: E402
 
 METRIC = "single-batch 2-layer GEMM latency (µs) and TFLOP/s vs roofline on 1 GB300"
-DEFAULT_WORKLOAD = "decode_m128_d4096"
+DEFAULT_WORKLOAD = "prefill_m2048_d8192"
 # tile widths per GEMM measured best on GB300 (0: the library cost model chooses)
 TUNED_TILES = {
     "tiny_m64_d256": [64, 64],
@@ -93,7 +93,7 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, uuid: str, period_s: float = 0.005):
+    def __init__(self, uuid: str, period_s: float = 0.0005):
         self.period = period_s
         self.samples = []
         self.max_mhz = None
@@ -184,6 +184,44 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+# ------------------------------------------------------------------------ phase breakdown --
+def phase_breakdown(events: np.ndarray, deps) -> dict:
+    """Per-stage phase times (µs, medians over tiles) of one pipelined run, from its event log:
+    the single-GPU analogues of the pages' per-phase overheads (CTA-Pipelining, section III-C,
+    Fig. 2b).
+      mainloop          tile start (its item taken and, for a consumer, its queue entry and group
+                        counter acquired) -> accumulator complete;
+      epilogue (T1)     accumulator complete -> release: split-K exchange, bf16 stores, the fence
+                        and the scoreboard release, i.e. the producer epilogue with its fence;
+      handoff (T3)      for consumer tiles: the last release of its producers -> its start, i.e.
+                        the queue push, the consumer's poll and acquire, and the TMA warp's pickup;
+      span              first start -> last release of the stage.
+    The scheduler's broadcast (T4) happens before a tile's start and is not timed separately.
+    `deps[b]` is the dependency CSR (prod_off, prod_tgt) of boundary b."""
+    out = {}
+    t0 = int(events["t_start"].min())
+    for s in sorted(set(int(v) for v in events["stage"])):
+        e = events[events["stage"] == s]
+        st = {"tiles": int(len(e)),
+              "first_start_us": (int(e["t_start"].min()) - t0) / 1e3,
+              "span_us": (int(e["t_end"].max()) - int(e["t_start"].min())) / 1e3,
+              "mainloop_us": float(np.median((e["t_acc"].astype(np.int64) - e["t_start"].astype(np.int64)))) / 1e3,
+              "epilogue_T1_us": float(np.median((e["t_end"].astype(np.int64) - e["t_acc"].astype(np.int64)))) / 1e3}
+        if s > 0:
+            prev = events[events["stage"] == s - 1]
+            t_end_p = dict(zip(prev["tile"].tolist(), prev["t_end"].astype(np.int64).tolist()))
+            off, tgt = deps[s - 1]
+            last = {}
+            for p in range(len(off) - 1):
+                for c in tgt[off[p]:off[p + 1]]:
+                    last[int(c)] = max(last.get(int(c), 0), t_end_p[p])
+            h = [int(r["t_start"]) - last[int(r["tile"])] for r in e]
+            st["handoff_T3_us"] = float(np.median(h)) / 1e3
+            st["handoff_T3_min_us"] = float(np.min(h)) / 1e3
+        out[f"stage{s}"] = st
+    return out
 
 
 # ----------------------------------------------------------------------------- timing --
@@ -431,11 +469,11 @@ def main():
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def make(mode, rows=0):
+    def make(mode, rows=0, **kw):
         return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
                         microbatch_rows=rows, device=local, raster_group=args.raster_group,
                         pipe_stages=args.pipe_stages, acc_split=args.acc_split,
-                        weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated)
+                        weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated, **kw)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()
@@ -539,6 +577,17 @@ def main():
                     flush(); g.replay()
                 baselines["torch_matmul_us"] = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
 
+        # ---- per-phase times of one pipelined run, from the event log (untimed build) ---------
+        phases = None
+        if args.mode == "pipelined" and w.num_gemms > 1:
+            with make("pipelined", event_log=True) as ch:
+                for _ in range(3):
+                    flush()
+                    ch.run(Xd, Wd, Y, ws, stream=stream)
+                if ch.check(stream) != 0:
+                    raise RuntimeError("device status set in the event-log run")
+                phases = phase_breakdown(ch.event_log(), [ch.deps(b)[:2] for b in range(w.num_gemms - 1)])
+
         # ---- end to end through the host-buffer C-ABI call ------------------------------------
         Xh = X.pin_memory()
         Yh = torch.empty(w.M, w.dims[-1], dtype=torch.bfloat16).pin_memory()
@@ -594,6 +643,7 @@ def main():
             "latency_us": {"median": lat_us, "mean": mean_ms * 1e3, "p10": pct(ms, 0.1) * 1e3,
                            "p90": pct(ms, 0.9) * 1e3},
             "baselines": baselines,
+            "phases": phases,
             "roofline": roof,
             "cpu_baseline": cpu,
             "parity_vs_oracle_sample": parity,

@@ -213,18 +213,59 @@ mlp_status mlp_chain_run_host(mlp_chain_t h, const void *X_host, const void *con
 
 /* Synchronise `stream`, read the device status word and clear it.  Returns OK, TIMEOUT or
  * BAD_TILE; after a device error the handle's scoreboard, queues and tickets are re-initialised
- * so the next run starts clean. */
+ * so the next run starts clean.  The pages' consumer prologue polls the work-queue without a
+ * limit (section III-A, Fig. 1; the polling CTA of section III-C, Fig. 2); here every such wait
+ * has a deadline, because on one GPU nothing guarantees that the producer runs, and this call is
+ * where a wait that ran out is reported (TIMEOUT) instead of hanging the device. */
 mlp_status mlp_chain_check(mlp_chain_t h, void *stream);
 
 /* The dependency array of stage boundary b (GEMM b produces, GEMM b+1 consumes), as host
  * arrays owned by the handle: prod_off[P+1], prod_tgt[prod_off[P]] (consumer ids ascending for
- * each producer), init_count[C].  Tile ids are row-major over each GEMM's tile grid. */
+ * each producer), init_count[C].  Tile ids are row-major over each GEMM's tile grid.  This is the
+ * host-built dependency array of section III-A (derived from the static dataflow of tiles: a
+ * consumer tile reads one or more producer tiles); the pages leave its format open, and CSR by
+ * producer plus an in-degree per consumer is this library's reading.  Valid until destroy. */
 mlp_status mlp_chain_get_deps(mlp_chain_t h, int32_t boundary, const int32_t **prod_off,
                               const int32_t **prod_tgt, const int32_t **init_count,
                               int32_t *P, int32_t *C);
 
+/* The scoreboard of one stage boundary: the counters the consumer prologue waits on (section
+ * III-A, the scoreboard initialised from the dependency array).  Consumer tiles are partitioned
+ * into groups that share one counter:
+ *   - raster_group <= 1: a group is a class of consumer tiles with identical producer sets,
+ *     numbered by its smallest member, members ascending (for a GEMM chain with equal row tiles:
+ *     one row panel);
+ *   - raster_group = g > 1: a group is the consumer tiles of g consecutive row panels (the last
+ *     group may hold fewer), listed column by column, so its queue slots follow weight columns.
+ * A group waits for grp_target = |union of its members' producer sets| x releases_per_producer
+ * releases per run (each epilogue warp of each split-K slice of a producer tile releases once).
+ * Every array is caller-owned and filled only when all six pointers are non-NULL; with any
+ * pointer NULL only the five sizes are written (query them first).  Layout: int32, plain CSR:
+ *   pg_off[producers + 1], pg_tgt[edges]   producer tile -> groups it feeds, ascending;
+ *   grp_off[groups + 1],  grp_mem[consumers]  group -> member consumer tiles (push order);
+ *   grp_target[groups];   cons_grp[consumers]  consumer tile -> its group. */
+typedef struct {
+    int32_t producers, consumers, groups, edges; /* sizes (written by the call)                 */
+    int32_t releases_per_producer;               /* split-K slices x epilogue warps              */
+    int32_t *pg_off, *pg_tgt, *grp_off, *grp_mem, *grp_target, *cons_grp;   /* caller buffers     */
+} mlp_scoreboard;
+
+/* Host-only scoreboard builder (no GPU needed), the routine mlp_chain_create uses: the groups of
+ * the dependency array that mlp_deps_build gives for M x n_out producer tiles of bm x bn_p and
+ * M x n_next consumer tiles of bm x bn_c.  Returns OK, or INVALID_ARG for a bad size or NULL sb. */
+mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm, int32_t bn_p, int32_t bn_c,
+                                int32_t raster_group, int32_t releases_per_producer, mlp_scoreboard *sb);
+
+/* The scoreboard tables the kernel of handle `h` waits on at stage boundary b, copied back from
+ * the device (synchronous: waits for the device first) into sb's buffers; sizes as in
+ * mlp_scoreboard_build.  INVALID_ARG for a bad boundary, CUDA if a copy fails. */
+mlp_status mlp_chain_get_scoreboard(mlp_chain_t h, int32_t boundary, mlp_scoreboard *sb);
+
 /* Copy the event log of the last pipelined run (synchronises the device) into host_buf, up to
- * cap records; *n = records written.  INVALID_ARG without MLP_DEBUG_EVENT_LOG. */
+ * cap records; *n = records written.  INVALID_ARG without MLP_DEBUG_EVENT_LOG.  The records are
+ * this library's form of the pages' per-phase timestamps (section III-C, Fig. 2: epilogue,
+ * visibility, queue fetch and broadcast timed inside the kernels): globaltimer stamps at tile
+ * start, accumulator complete and release, plus a device-wide sequence number for ordering. */
 mlp_status mlp_chain_get_event_log(mlp_chain_t h, mlp_event *host_buf, size_t cap, size_t *n);
 
 mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info);
@@ -240,15 +281,22 @@ int64_t mlp_deps_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm_p, i
                        int32_t bm_c, int32_t bn_c, int32_t *prod_off, int32_t *prod_tgt,
                        int64_t tgt_cap, int32_t *init_count);
 
-/* Host model of the scoreboard / work-queue protocol (no GPU needed): `threads` host threads
- * run the same ticket, decrement, push and poll steps as the kernel on std::atomic state, with
- * seeded random delays, over a chain of `num_gemms` stages of tiles_m x tiles_n[s] tiles
- * (consumers read whole row panels).  order_out (optional, one entry per tile of all stages)
- * receives tiles in completion order as stage << 24 | tile.  With drop_tile >= 0 that
- * first-stage tile withholds its decrements and the run must end in MLP_ERR_TIMEOUT after
- * timeout_ms.  Returns OK when every tile ran exactly once after all of its producers. */
-mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
-                              int32_t threads, uint64_t seed, int32_t drop_tile,
+/* Host model of the scoreboard / work-queue protocol (no GPU needed): `threads` host threads play
+ * the persistent CTAs over a chain of `num_gemms` stages of tiles_m x tiles_n[s] tiles (consumers
+ * read whole row panels) and run the kernel's protocol with its tables and its arithmetic
+ * (protocol.h): first-stage raster and scoreboard groups of `raster_group` row panels (0 or 1:
+ * none), releases_per_tile releases per finished tile (the kernel's split-K slices x epilogue
+ * warps), counters that count up and accumulate over three back-to-back runs against the run's
+ * epoch-scaled target, the completing release pushing the group's members column by column,
+ * relaxed queue polls followed by an acquire of the group counter before a consumer reads its
+ * producers' output (plain reads: a missing happens-before edge is a data race for
+ * ThreadSanitizer, a stale value fails the run), and seeded random delays.  order_out (optional,
+ * one entry per tile of all stages) receives the first run's tiles in completion order as
+ * stage << 24 | tile.  With drop_tile >= 0 that first-stage tile withholds its releases and the
+ * run must end in MLP_ERR_TIMEOUT after timeout_ms.  Returns OK when every tile ran exactly once
+ * per run after all of its producers and every counter ends each run exactly at its target. */
+mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n, int32_t raster_group,
+                              int32_t releases_per_tile, int32_t threads, uint64_t seed, int32_t drop_tile,
                               uint32_t timeout_ms, int32_t *order_out);
 
 /* Allocation-free run of the two-GEMM chain (the paper has no counterpart to this entry point).
@@ -264,14 +312,20 @@ mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t 
  * the process exits.  It calls no cudaMalloc/cudaFree or other allocating routine.
  *   - Limit: shapes whose scratch (mainly M*N1*2 bytes of H) exceeds the array are rejected
  *     with MLP_ERR_INVALID_ARG before anything is enqueued.
- *   - The first call on a device (the current device) looks up the array's device address and
- *     sets the kernel's shared-memory limit; make that first call before any stream capture.
+ *   - The array and the kernel image are committed when the library's device code is loaded
+ *     into a context: at the library's first CUDA call there, or, with lazy module loading (CUDA's
+ *     default), possibly inside the first call of this entry point on that device.  So make one
+ *     call (or create one handle) at start-up, outside any context that must not allocate, and
+ *     before any stream capture; after that a call allocates nothing.
+ *   - Each call looks up the array's device address and sets the kernel's shared-memory limit on
+ *     the current device (both are per context, so a cudaDeviceReset needs nothing else).
  *   - Every call shares the one array: each call first re-initialises all of its state on
  *     `stream` (a small set-up kernel, then the chain kernel), so nothing of the previous call
  *     leaks in, but calls whose execution overlaps on the GPU (different streams, threads or
  *     processes sharing the device context) race and give wrong results.
  *   - With sync_check != 0 the call synchronises `stream` and returns MLP_ERR_TIMEOUT or
- *     MLP_ERR_BAD_TILE if the device reported one; with 0 it returns after enqueueing. */
+ *     MLP_ERR_BAD_TILE if the device reported one; with 0 it returns after enqueueing.  Pass 0
+ *     while `stream` is being captured (a synchronisation would invalidate the capture). */
 #define MLP_NOALLOC_SCRATCH_BYTES (16u << 20)
 mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, int64_t N2, const void *X,
                                  const void *W1, const void *W2, void *Y, int32_t sync_check,

@@ -79,6 +79,12 @@ class ChainInfo(ctypes.Structure):
     ]
 
 
+class Scoreboard(ctypes.Structure):
+    _fields_ = [("producers", i32), ("consumers", i32), ("groups", i32), ("edges", i32),
+                ("releases_per_producer", i32), ("pg_off", vp), ("pg_tgt", vp), ("grp_off", vp),
+                ("grp_mem", vp), ("grp_target", vp), ("cons_grp", vp)]
+
+
 # every symbol include/mlp_chain.h declares: name -> (restype, argtypes)
 SIGNATURES = {
     "mlp_chain_create": (ctypes.c_int, [ctypes.POINTER(ChainDesc), ctypes.POINTER(vp)]),
@@ -88,11 +94,13 @@ SIGNATURES = {
     "mlp_chain_check": (ctypes.c_int, [vp, vp]),
     "mlp_chain_get_deps": (ctypes.c_int, [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                           ctypes.POINTER(vp), ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+    "mlp_scoreboard_build": (ctypes.c_int, [i64, i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(Scoreboard)]),
+    "mlp_chain_get_scoreboard": (ctypes.c_int, [vp, i32, ctypes.POINTER(Scoreboard)]),
     "mlp_chain_get_event_log": (ctypes.c_int, [vp, vp, szt, ctypes.POINTER(szt)]),
     "mlp_chain_get_info": (ctypes.c_int, [vp, ctypes.POINTER(ChainInfo)]),
     "mlp_chain_destroy": (ctypes.c_int, [vp]),
     "mlp_deps_build": (i64, [i64, i64, i64, i32, i32, i32, i32, vp, vp, i64, vp]),
-    "mlp_protocol_model": (ctypes.c_int, [i32, i32, vp, i32, u64, i32, u32, vp]),
+    "mlp_protocol_model": (ctypes.c_int, [i32, i32, vp, i32, i32, i32, u64, i32, u32, vp]),
     "mlp_chain_run_noalloc": (ctypes.c_int, [i64, i64, i64, i64, vp, vp, vp, vp, i32, vp]),
     "mlp_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }

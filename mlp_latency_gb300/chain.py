@@ -12,7 +12,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 from . import _lib
-from ._lib import ChainDesc, ChainInfo, Event
+from ._lib import ChainDesc, ChainInfo, Event, Scoreboard
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_DEVICE_STATE, ERR_BAD_TILE = range(8)
 DT_BF16, DT_F32 = 1, 2
@@ -169,6 +169,12 @@ class Chain:
         inita = np.ctypeslib.as_array(ctypes.cast(init, ctypes.POINTER(ctypes.c_int32)), (C.value,)).copy()
         return offa, tgta, inita
 
+    def scoreboard(self, boundary: int = 0) -> dict:
+        """The scoreboard tables the kernel waits on at this stage boundary, read back from the
+        device (mlp_chain_get_scoreboard): see _scoreboard_arrays for the keys."""
+        return _scoreboard_arrays(lambda sb: self._lib.mlp_chain_get_scoreboard(self._h, boundary, ctypes.byref(sb)),
+                                  "get_scoreboard")
+
     def event_log(self) -> np.ndarray:
         info = self.info()
         cap = sum(info["tiles_m"][s] * info["tiles_n"][s] for s in range(info["num_gemms"]))
@@ -206,15 +212,43 @@ def deps_build(M: int, n_out: int, n_next: int, bm_p: int, bn_p: int, bm_c: int,
     return off, tgt[:nnz], init
 
 
+def _scoreboard_arrays(call, what: str) -> dict:
+    """Two calls of an mlp_scoreboard filler: sizes, then the arrays.  Keys: producers, consumers,
+    groups, releases_per_producer, pg_off, pg_tgt, grp_off, grp_mem, grp_target, cons_grp."""
+    sb = Scoreboard()
+    _check(call(sb), what)
+    arr = {"pg_off": np.zeros(sb.producers + 1, np.int32), "pg_tgt": np.zeros(max(sb.edges, 1), np.int32),
+           "grp_off": np.zeros(sb.groups + 1, np.int32), "grp_mem": np.zeros(max(sb.consumers, 1), np.int32),
+           "grp_target": np.zeros(max(sb.groups, 1), np.int32), "cons_grp": np.zeros(max(sb.consumers, 1), np.int32)}
+    for k, a in arr.items():
+        setattr(sb, k, a.ctypes.data)
+    _check(call(sb), what)
+    sizes = {"pg_tgt": sb.edges, "grp_mem": sb.consumers, "grp_target": sb.groups, "cons_grp": sb.consumers}
+    out = {k: (a[: sizes[k]] if k in sizes else a) for k, a in arr.items()}
+    out.update(producers=sb.producers, consumers=sb.consumers, groups=sb.groups,
+               releases_per_producer=sb.releases_per_producer)
+    return out
+
+
+def scoreboard_build(M: int, n_out: int, n_next: int, bm: int, bn_p: int, bn_c: int, raster_group: int = 1,
+                     releases_per_producer: int = 4) -> dict:
+    """Host-only scoreboard builder (mlp_scoreboard_build), the routine mlp_chain_create uses."""
+    lib = _lib.load()
+    return _scoreboard_arrays(lambda sb: lib.mlp_scoreboard_build(M, n_out, n_next, bm, bn_p, bn_c, raster_group,
+                                                                  releases_per_producer, ctypes.byref(sb)),
+                              "mlp_scoreboard_build")
+
+
 def protocol_model(tiles_m: int, tiles_n: Sequence[int], threads: int = 8, seed: int = 0,
-                   drop_tile: int = -1, timeout_ms: int = 2000, return_order: bool = False):
+                   drop_tile: int = -1, timeout_ms: int = 2000, return_order: bool = False,
+                   raster_group: int = 1, releases_per_tile: int = 4):
     """Run the host-thread protocol model (mlp_protocol_model); returns (status, order)."""
     lib = _lib.load()
     tn = np.ascontiguousarray(tiles_n, dtype=np.int32)
     total = int(tiles_m * tn.sum())
     order = np.full(total, -1, dtype=np.int32) if return_order else None
-    st = lib.mlp_protocol_model(len(tn), tiles_m, tn.ctypes.data, threads, seed, drop_tile, timeout_ms,
-                                order.ctypes.data if order is not None else None)
+    st = lib.mlp_protocol_model(len(tn), tiles_m, tn.ctypes.data, raster_group, releases_per_tile, threads, seed,
+                                drop_tile, timeout_ms, order.ctypes.data if order is not None else None)
     return int(st), order
 
 

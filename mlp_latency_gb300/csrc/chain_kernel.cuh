@@ -371,9 +371,9 @@ __device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl
         // visible.  The pusher therefore stores the entries without a fence of its own.
         const BoundaryParams &bd = p.bd[s - 1];
         const int32_t g = bd.cgrp[tile];
-        const uint32_t want = static_cast<uint32_t>(bd.grp_init[g]) * (c->epoch + 1u);
+        const uint32_t want = run_target(bd.grp_init[g], c->epoch);
         const uint64_t t0 = globaltimer_ns();
-        while (static_cast<int32_t>(ld_acquire_gpu_u32(bd.count + g) - want) < 0) {
+        while (!count_reached(ld_acquire_gpu_u32(bd.count + g), want)) {
             if (c->abort_flag)
                 return -1;
             if (globaltimer_ns() - t0 > p.timeout_ns) {
@@ -411,16 +411,16 @@ __device__ __forceinline__ Item take_item(Ctrl *c, int32_t slot)
 __device__ __forceinline__ bool wait_producer(const ChainParams &p, Ctrl *c, int32_t s, int32_t ptile)
 {
     const BoundaryParams &bd = p.bd[s - 1];
-    const uint32_t want = bd.ready_quota * (c->epoch + 1u);
+    const uint32_t want = run_target(static_cast<int32_t>(bd.ready_quota), c->epoch);
     const uint32_t *r = bd.ready + ptile;
-    if (static_cast<int32_t>(ld_relaxed_gpu_u32(r) - want) >= 0)
+    if (count_reached(ld_relaxed_gpu_u32(r), want))
         return true;
     const uint64_t t0 = globaltimer_ns();
     uint32_t backoff = 32;
     while (true) {
         __nanosleep(backoff);
         backoff = backoff < 64 ? backoff * 2 : 64;
-        if (static_cast<int32_t>(ld_relaxed_gpu_u32(r) - want) >= 0)
+        if (count_reached(ld_relaxed_gpu_u32(r), want))
             return true;
         if (c->abort_flag)
             return false;
@@ -443,7 +443,7 @@ __device__ __forceinline__ int32_t scan_ready(const ChainParams &p, const Ctrl *
                                               int32_t hi, int32_t last)
 {
     const BoundaryParams &bd = p.bd[s - 1];
-    const uint32_t want = bd.ready_quota * (c->epoch + 1u);
+    const uint32_t want = run_target(static_cast<int32_t>(bd.ready_quota), c->epoch);
     while (hi < last) {
         uint32_t v[8];
 #pragma unroll
@@ -451,7 +451,7 @@ __device__ __forceinline__ int32_t scan_ready(const ChainParams &p, const Ctrl *
             v[j] = hi + 1 + j <= last ? ld_relaxed_gpu_u32(bd.ready + pbase + hi + 1 + j) : 0u;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            if (hi + 1 + j > last || static_cast<int32_t>(v[j] - want) < 0)
+            if (hi + 1 + j > last || !count_reached(v[j], want))
                 return hi + j;
         }
         hi += 8;
@@ -1081,9 +1081,8 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
         // release); the add that completes the run's count reserves the group's queue slots.
         uint32_t q0 = 0, fire = 0;
         if (lane == 0) {
-            const uint32_t want = static_cast<uint32_t>(pl.init) * (c->epoch + 1u);
             const uint32_t old = atom_add_relaxed_gpu(bd.count + pl.g, 1u);
-            if (old + 1u == want) {
+            if (release_completes(old, run_target(pl.init, c->epoch))) {
                 fire = 1;
                 q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(pl.n));
             }
@@ -1111,7 +1110,7 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
             // The caller's fence.acq_rel.gpu and this relaxed add form the release of the warp's
             // stores; consumers acquire them through the counter.
             const uint32_t old = atom_add_relaxed_gpu(bd.count + g, 1u);
-            fire = (old + 1u == static_cast<uint32_t>(bd.grp_init[g]) * (c->epoch + 1u));
+            fire = release_completes(old, run_target(bd.grp_init[g], c->epoch));
         }
         // Every group this warp completed is published by the whole warp with relaxed stores (the
         // consumers' acquire is on the group counter, see resolve_queue_slot).

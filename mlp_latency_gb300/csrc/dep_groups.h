@@ -33,4 +33,9 @@ DepGroups build_groups(const int32_t *prod_off, const int32_t *prod_tgt, int32_t
 DepGroups merge_groups_by_panel(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C,
                                 int32_t tiles_n, int32_t g);
 
+// The scoreboard groups of one stage boundary, as mlp_chain_create uploads them: row-panel
+// groups merged per raster group of g > 1 panels, else classes of identical producer sets.
+DepGroups scoreboard_groups(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C,
+                            int32_t tiles_n, int32_t g);
+
 }  // namespace mlpc

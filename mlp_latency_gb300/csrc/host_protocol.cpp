@@ -145,36 +145,92 @@ mlpc::DepGroups mlpc::merge_groups_by_panel(const int32_t *prod_off, const int32
     return r;
 }
 
+mlpc::DepGroups mlpc::scoreboard_groups(const int32_t *prod_off, const int32_t *prod_tgt, int32_t P, int32_t C,
+                                        int32_t tiles_n, int32_t g)
+{
+    return g > 1 ? merge_groups_by_panel(prod_off, prod_tgt, P, C, tiles_n, g) : build_groups(prod_off, prod_tgt, P, C);
+}
+
+extern "C" mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm, int32_t bn_p,
+                                           int32_t bn_c, int32_t raster_group, int32_t releases_per_producer,
+                                           mlp_scoreboard *sb)
+{
+    if (!sb || releases_per_producer < 1)
+        return MLP_ERR_INVALID_ARG;
+    const int64_t nnz = mlp_deps_build(M, n_out, n_next, bm, bn_p, bm, bn_c, nullptr, nullptr, 0, nullptr);
+    if (nnz < 0)
+        return MLP_ERR_INVALID_ARG;
+    const int64_t P = ((M + bm - 1) / bm) * ((n_out + bn_p - 1) / bn_p);
+    const int64_t C = ((M + bm - 1) / bm) * ((n_next + bn_c - 1) / bn_c);
+    std::vector<int32_t> off(static_cast<size_t>(P + 1)), tgt(static_cast<size_t>(std::max<int64_t>(nnz, 1))),
+        init(static_cast<size_t>(C));
+    mlp_deps_build(M, n_out, n_next, bm, bn_p, bm, bn_c, off.data(), tgt.data(), nnz, init.data());
+    const int32_t tiles_n = static_cast<int32_t>((n_next + bn_c - 1) / bn_c);
+    const mlpc::DepGroups G = mlpc::scoreboard_groups(off.data(), tgt.data(), static_cast<int32_t>(P),
+                                                static_cast<int32_t>(C), tiles_n, raster_group);
+    sb->producers = static_cast<int32_t>(P);
+    sb->consumers = static_cast<int32_t>(C);
+    sb->groups = static_cast<int32_t>(G.grp_init.size());
+    sb->edges = static_cast<int32_t>(G.pg_tgt.size());
+    sb->releases_per_producer = releases_per_producer;
+    if (!sb->pg_off || !sb->pg_tgt || !sb->grp_off || !sb->grp_mem || !sb->grp_target || !sb->cons_grp)
+        return MLP_OK;
+    std::copy(G.pg_off.begin(), G.pg_off.end(), sb->pg_off);
+    std::copy(G.pg_tgt.begin(), G.pg_tgt.end(), sb->pg_tgt);
+    std::copy(G.grp_off.begin(), G.grp_off.end(), sb->grp_off);
+    std::copy(G.grp_mem.begin(), G.grp_mem.end(), sb->grp_mem);
+    std::copy(G.cons_grp.begin(), G.cons_grp.end(), sb->cons_grp);
+    for (size_t g = 0; g < G.grp_init.size(); ++g)
+        sb->grp_target[g] = G.grp_init[g] * releases_per_producer;
+    return MLP_OK;
+}
+
 // ------------------------------------------------------------------------------------------
-// Host model of the protocol: `threads` host threads play the persistent CTAs.  Each takes
-// tickets in stage order; first-stage tickets map to tiles through raster_tile(); later-stage
-// tickets poll the matching work-queue slot (acquire) until this run's entry lands; a tile's
-// "work" is a seeded random sleep; its epilogue decrements (acq_rel) the counters of its
-// consumers and the decrement that reaches zero re-arms the counter and pushes (release).
-// Two runs are played back to back (epochs 0 and 1) to exercise the re-arm and epoch tags.
+// Host model of the protocol: `threads` host threads play the persistent CTAs and run the
+// kernel's protocol steps on std::atomic state, with the kernel's tables and arithmetic:
+//   - tickets in stage order; first-stage tickets map to tiles through raster_tile(rg);
+//   - scoreboard groups from scoreboard_groups() (merged per rg row panels, members column by
+//     column), each waiting for grp_init x R releases per run, R = releases one producer tile
+//     makes (split-K slices x epilogue warps on the device);
+//   - a finished tile makes R releases, each after writing its own part of the tile's output:
+//     one acq_rel add of +1 on every group it feeds (on the device: fence.acq_rel.gpu + a
+//     relaxed add, the PTX form of a release RMW); the add that completes the run's target,
+//     run_target(init, epoch), reserves the group's queue slots on the tail and stores the
+//     members there with relaxed stores, tagged with the epoch;
+//   - a consumer ticket polls its queue slot with relaxed loads until this run's entry lands,
+//     then acquires the named tile's group counter until it reaches the run's target, and only
+//     then reads the producers' output (plain, non-atomic reads: a missing happens-before edge is
+//     a data race that ThreadSanitizer reports, and a stale value fails the run);
+//   - counters accumulate over three back-to-back runs (epochs 0, 1, 2) and are never reset;
+//     between runs only the ticket and the tails are cleared, as the last CTA out does.
 // ------------------------------------------------------------------------------------------
 namespace {
 
 struct ModelBoundary {
     std::vector<int32_t> off, tgt, init;
     mlpc::DepGroups grp;
-    std::vector<std::atomic<uint32_t>> count;   // one per group
+    std::vector<int32_t> target;                 // releases per run, per group
+    std::vector<std::vector<int32_t>> in;        // consumer -> its producers
+    std::vector<std::atomic<uint32_t>> count;    // one per group, accumulating over runs
     std::vector<std::atomic<uint64_t>> queue;
     std::atomic<uint32_t> tail{0};
+    std::vector<uint32_t> data;                  // producer output: R parts per producer tile
 };
 
 }  // namespace
 
 extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
-                                         int32_t threads, uint64_t seed, int32_t drop_tile,
-                                         uint32_t timeout_ms, int32_t *order_out)
+                                         int32_t raster_group, int32_t releases_per_tile, int32_t threads,
+                                         uint64_t seed, int32_t drop_tile, uint32_t timeout_ms, int32_t *order_out)
 {
-    if (num_gemms < 1 || num_gemms > MLP_MAX_GEMMS || tiles_m < 1 || !tiles_n || threads < 1 || threads > 512)
+    if (num_gemms < 1 || num_gemms > MLP_MAX_GEMMS || tiles_m < 1 || !tiles_n || threads < 1 || threads > 512 ||
+        raster_group < 0 || releases_per_tile < 1 || releases_per_tile > 64)
         return MLP_ERR_INVALID_ARG;
     for (int s = 0; s < num_gemms; ++s)
         if (tiles_n[s] < 1)
             return MLP_ERR_INVALID_ARG;
     const int S = num_gemms;
+    const int32_t R = releases_per_tile;
     int32_t base[MLP_MAX_GEMMS + 1];
     base[0] = 0;
     for (int s = 0; s < S; ++s)
@@ -184,29 +240,39 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
     std::vector<ModelBoundary> bd(S > 1 ? S - 1 : 0);
     for (int b = 0; b + 1 < S; ++b) {
         // tiles as unit cells: a tiles_m x tiles_n[b] producer grid, tiles_m x tiles_n[b+1] consumers
+        ModelBoundary &B = bd[b];
         const int64_t nnz = mlp_deps_build(tiles_m, tiles_n[b], tiles_n[b + 1], 1, 1, 1, 1, nullptr, nullptr, 0, nullptr);
-        bd[b].off.resize(static_cast<size_t>(tiles_m) * tiles_n[b] + 1);
-        bd[b].tgt.resize(static_cast<size_t>(nnz));
-        bd[b].init.resize(static_cast<size_t>(tiles_m) * tiles_n[b + 1]);
-        mlp_deps_build(tiles_m, tiles_n[b], tiles_n[b + 1], 1, 1, 1, 1, bd[b].off.data(), bd[b].tgt.data(), nnz,
-                       bd[b].init.data());
-        bd[b].grp = mlpc::build_groups(bd[b].off.data(), bd[b].tgt.data(),
-                                       static_cast<int32_t>(bd[b].off.size() - 1),
-                                       static_cast<int32_t>(bd[b].init.size()));
-        bd[b].count = std::vector<std::atomic<uint32_t>>(bd[b].grp.grp_init.size());
-        bd[b].queue = std::vector<std::atomic<uint64_t>>(bd[b].init.size());
-        for (size_t i = 0; i < bd[b].grp.grp_init.size(); ++i)
-            bd[b].count[i].store(static_cast<uint32_t>(bd[b].grp.grp_init[i]));
-        for (size_t i = 0; i < bd[b].init.size(); ++i)
-            bd[b].queue[i].store(0);
+        B.off.resize(static_cast<size_t>(tiles_m) * tiles_n[b] + 1);
+        B.tgt.resize(static_cast<size_t>(nnz));
+        B.init.resize(static_cast<size_t>(tiles_m) * tiles_n[b + 1]);
+        mlp_deps_build(tiles_m, tiles_n[b], tiles_n[b + 1], 1, 1, 1, 1, B.off.data(), B.tgt.data(), nnz, B.init.data());
+        const int32_t P = static_cast<int32_t>(B.off.size() - 1), C = static_cast<int32_t>(B.init.size());
+        B.grp = mlpc::scoreboard_groups(B.off.data(), B.tgt.data(), P, C, tiles_n[b + 1], raster_group);
+        for (int32_t v : B.grp.grp_init)
+            B.target.push_back(v * R);
+        B.in.assign(static_cast<size_t>(C), {});
+        for (int32_t p = 0; p < P; ++p)
+            for (int32_t e = B.off[p]; e < B.off[p + 1]; ++e)
+                B.in[static_cast<size_t>(B.tgt[e])].push_back(p);
+        B.count = std::vector<std::atomic<uint32_t>>(B.grp.grp_init.size());
+        B.queue = std::vector<std::atomic<uint64_t>>(static_cast<size_t>(C));
+        for (auto &c : B.count)
+            c.store(0);
+        for (auto &q : B.queue)
+            q.store(0);
+        B.data.assign(static_cast<size_t>(P) * R, 0u);
     }
 
     std::atomic<uint32_t> ticket{0}, seq{0}, status{0};
     std::vector<std::atomic<uint32_t>> start_seq(total), end_seq(total), runs(total);
     std::atomic<int32_t> order_pos{0};
     const auto timeout = std::chrono::milliseconds(timeout_ms ? timeout_ms : 2000);
+    auto fail = [&](uint32_t code) {
+        uint32_t z = 0;
+        status.compare_exchange_strong(z, code);
+    };
 
-    for (uint32_t epoch = 0; epoch < 2; ++epoch) {
+    for (uint32_t epoch = 0; epoch < 3; ++epoch) {
         for (int32_t i = 0; i < total; ++i) {
             start_seq[i].store(0);
             end_seq[i].store(0);
@@ -223,29 +289,42 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                 const int32_t local = t - base[s];
                 int32_t tile;
                 if (s == 0) {
-                    tile = mlpc::raster_tile(local, tiles_m, tiles_n[0], 1);
+                    tile = mlpc::raster_tile(local, tiles_m, tiles_n[0], raster_group);
                 } else {
+                    ModelBoundary &B = bd[s - 1];
                     const auto t0 = std::chrono::steady_clock::now();
-                    uint64_t v;
-                    while (true) {
-                        v = bd[s - 1].queue[local].load(std::memory_order_acquire);
-                        if (mlpc::queue_entry_ready(v, epoch))
-                            break;
+                    auto expired = [&]() {
                         if (status.load(std::memory_order_relaxed) != 0)
-                            return;
+                            return true;
                         if (std::chrono::steady_clock::now() - t0 > timeout) {
-                            uint32_t z = 0;
-                            status.compare_exchange_strong(z, MLP_ERR_TIMEOUT);
-                            return;
+                            fail(MLP_ERR_TIMEOUT);
+                            return true;
                         }
                         std::this_thread::yield();
-                    }
+                        return false;
+                    };
+                    // relaxed polls of the queue slot: the entry only names the tile
+                    uint64_t v;
+                    while (!mlpc::queue_entry_ready(v = B.queue[local].load(std::memory_order_relaxed), epoch))
+                        if (expired())
+                            return;
                     tile = mlpc::queue_entry_tile(v);
                     if (tile < 0 || tile >= tiles_m * tiles_n[s]) {
-                        uint32_t z = 0;
-                        status.compare_exchange_strong(z, MLP_ERR_BAD_TILE);
+                        fail(MLP_ERR_BAD_TILE);
                         return;
                     }
+                    // the acquire that makes every producer's output visible
+                    const int32_t g = B.grp.cons_grp[static_cast<size_t>(tile)];
+                    const uint32_t want = mlpc::run_target(B.target[static_cast<size_t>(g)], epoch);
+                    while (!mlpc::count_reached(B.count[static_cast<size_t>(g)].load(std::memory_order_acquire), want))
+                        if (expired())
+                            return;
+                    for (int32_t p : B.in[static_cast<size_t>(tile)])
+                        for (int32_t r = 0; r < R; ++r)
+                            if (B.data[static_cast<size_t>(p) * R + r] != epoch + 1u) {
+                                fail(MLP_ERR_DEVICE_STATE);
+                                return;
+                            }
                 }
                 const int32_t id = base[s] + tile;
                 start_seq[id].store(seq.fetch_add(1) + 1);
@@ -254,20 +333,25 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                 end_seq[id].store(seq.fetch_add(1) + 1);
                 if (order_out && epoch == 0)
                     order_out[order_pos.fetch_add(1)] = (s << 24) | tile;
-                if (s + 1 < S && !(s == 0 && tile == drop_tile)) {
-                    ModelBoundary &b = bd[s];
-                    const mlpc::DepGroups &G = b.grp;
+                if (s + 1 >= S)
+                    continue;
+                ModelBoundary &B = bd[s];
+                const mlpc::DepGroups &G = B.grp;
+                for (int32_t r = 0; r < R; ++r) {   // the epilogue warps of the split-K slices
+                    B.data[static_cast<size_t>(tile) * R + r] = epoch + 1u;   // this release's rows
+                    if (s == 0 && tile == drop_tile)
+                        continue;   // fault injection: the stores land, the releases never come
+                    if (delay(rng) < 8)
+                        std::this_thread::yield();
                     for (int32_t e = G.pg_off[tile]; e < G.pg_off[tile + 1]; ++e) {
                         const int32_t g = G.pg_tgt[e];
-                        const uint32_t old = b.count[g].fetch_sub(1, std::memory_order_acq_rel);
-                        if (old == 1u) {
-                            b.count[g].store(static_cast<uint32_t>(G.grp_init[g]), std::memory_order_relaxed);
-                            const int32_t n = G.grp_off[g + 1] - G.grp_off[g];
-                            const uint32_t slot0 = b.tail.fetch_add(static_cast<uint32_t>(n), std::memory_order_relaxed);
-                            for (int32_t i = 0; i < n; ++i)
-                                b.queue[slot0 + i].store(mlpc::queue_entry(epoch, G.grp_mem[G.grp_off[g] + i]),
-                                                         std::memory_order_release);
-                        }
+                        const uint32_t old = B.count[static_cast<size_t>(g)].fetch_add(1, std::memory_order_acq_rel);
+                        if (!mlpc::release_completes(old, mlpc::run_target(B.target[static_cast<size_t>(g)], epoch)))
+                            continue;
+                        const int32_t m0 = G.grp_off[g], n = G.grp_off[g + 1] - m0;
+                        const uint32_t q0 = B.tail.fetch_add(static_cast<uint32_t>(n), std::memory_order_relaxed);
+                        for (int32_t i = 0; i < n; ++i)
+                            B.queue[q0 + i].store(mlpc::queue_entry(epoch, G.grp_mem[m0 + i]), std::memory_order_relaxed);
                     }
                 }
             }
@@ -283,11 +367,16 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
         for (int32_t i = 0; i < total; ++i)
             if (runs[i].load() != 1)
                 return MLP_ERR_DEVICE_STATE;
-        for (int b = 0; b + 1 < S; ++b)
+        for (int b = 0; b + 1 < S; ++b) {
             for (int32_t p = 0; p + 1 < static_cast<int32_t>(bd[b].off.size()); ++p)
                 for (int32_t e = bd[b].off[p]; e < bd[b].off[p + 1]; ++e)
                     if (!(end_seq[base[b] + p].load() < start_seq[base[b + 1] + bd[b].tgt[e]].load()))
                         return MLP_ERR_DEVICE_STATE;
+            // every counter sits exactly at this run's target: nothing lost, nothing counted twice
+            for (size_t g = 0; g < bd[b].count.size(); ++g)
+                if (bd[b].count[g].load() != mlpc::run_target(bd[b].target[g], epoch))
+                    return MLP_ERR_DEVICE_STATE;
+        }
         // what the last CTA out does on the device
         ticket.store(0);
         for (auto &b : bd)

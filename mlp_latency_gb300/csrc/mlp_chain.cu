@@ -435,12 +435,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         // panels' consumers become ready together: one scoreboard group per rg panels, pushed
         // column by column so that neighbouring queue slots share a weight slab in L2.
         const int rg = d->raster_group ? d->raster_group : default_raster_group(h->tiles_m);
-        h->grp[b] = rg > 1 ? mlpc::merge_groups_by_panel(h->off[b].data(), h->tgt[b].data(),
-                                                         static_cast<int32_t>(h->off[b].size() - 1),
-                                                         static_cast<int32_t>(h->init[b].size()), h->tiles_n[b + 1], rg)
-                           : mlpc::build_groups(h->off[b].data(), h->tgt[b].data(),
-                                                static_cast<int32_t>(h->off[b].size() - 1),
-                                                static_cast<int32_t>(h->init[b].size()));
+        h->grp[b] = mlpc::scoreboard_groups(h->off[b].data(), h->tgt[b].data(), static_cast<int32_t>(h->off[b].size() - 1),
+                                            static_cast<int32_t>(h->init[b].size()), h->tiles_n[b + 1], rg);
         const mlpc::DepGroups &G = h->grp[b];
         bytes = align_up(bytes, 256) + G.pg_off.size() * 4;
         bytes = align_up(bytes, 256) + std::max<size_t>(G.pg_tgt.size(), 1) * 4;
@@ -855,6 +851,31 @@ extern "C" mlp_status mlp_chain_get_deps(mlp_chain_t h, int32_t b, const int32_t
     return MLP_OK;
 }
 
+extern "C" mlp_status mlp_chain_get_scoreboard(mlp_chain_t h, int32_t b, mlp_scoreboard *sb)
+{
+    if (!h || !sb || b < 0 || b + 1 >= h->S)
+        return MLP_ERR_INVALID_ARG;
+    const DeviceBoundary &db = h->db[b];
+    const mlpc::DepGroups &G = h->grp[b];
+    sb->producers = static_cast<int32_t>(db.producers);
+    sb->consumers = static_cast<int32_t>(db.consumers);
+    sb->groups = static_cast<int32_t>(db.groups);
+    sb->edges = static_cast<int32_t>(G.pg_tgt.size());
+    sb->releases_per_producer = h->split[b] * mlpc::kEpiWarps;
+    if (!sb->pg_off || !sb->pg_tgt || !sb->grp_off || !sb->grp_mem || !sb->grp_target || !sb->cons_grp)
+        return MLP_OK;
+    // the tables as the kernel reads them: copied back from the device block
+    auto down = [](int32_t *dst, const int32_t *src, size_t n) {
+        return n == 0 || cudaMemcpy(dst, src, n * 4, cudaMemcpyDeviceToHost) == cudaSuccess;
+    };
+    if (cudaSetDevice(h->device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        !down(sb->pg_off, db.pg_off, db.producers + 1) || !down(sb->pg_tgt, db.pg_tgt, G.pg_tgt.size()) ||
+        !down(sb->grp_off, db.grp_off, db.groups + 1) || !down(sb->grp_mem, db.grp_mem, db.consumers) ||
+        !down(sb->grp_target, db.grp_init, db.groups) || !down(sb->cons_grp, db.cgrp, db.consumers))
+        return MLP_ERR_CUDA;
+    return MLP_OK;
+}
+
 extern "C" mlp_status mlp_chain_get_event_log(mlp_chain_t h, mlp_event *buf, size_t cap, size_t *n)
 {
     if (!h || !buf || !n || !h->d_events)
@@ -923,12 +944,8 @@ namespace {
 
 __device__ __align__(256) static uint8_t g_noalloc_scratch[MLP_NOALLOC_SCRATCH_BYTES];
 
-struct NoallocDevice {
-    bool ready = false;
-    uint8_t *scratch = nullptr;  // device address of g_noalloc_scratch on this device
-    int num_sms = 0;
-};
-NoallocDevice g_noalloc_dev[64];
+// SM count per device ordinal (a property of the device, not of a context: safe to keep).
+int g_noalloc_sms[64] = {};
 std::mutex g_noalloc_mutex;
 
 struct NoallocLayout {
@@ -1015,35 +1032,33 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return MLP_ERR_CUDA;
 
-    NoallocDevice nd;
+    // Set-up on the current device, every call: the scratch array's device address and the
+    // kernel's shared-memory limit belong to the current context (a cudaDeviceReset makes a new
+    // one), so neither is cached; only the SM count is.  Once the module is loaded these calls
+    // allocate nothing.
+    int num_sms = 0, smem_optin = 0;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-        NoallocDevice &slot = g_noalloc_dev[dev];
-        if (!slot.ready) {
-            // One-time set-up on this device (the current one): the scratch array's device
-            // address, the SM count and the kernel's shared-memory limit.
-            int major = 0, minor = 0, smem_optin = 0;
+        if (g_noalloc_sms[dev] == 0) {
+            int major = 0, minor = 0;
             cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
             if (major != 10 || minor != 3)
                 return MLP_ERR_UNSUPPORTED;
-            void *ptr = nullptr;
-            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr)
+            if (cudaDeviceGetAttribute(&g_noalloc_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return MLP_ERR_CUDA;
-            if (cudaDeviceGetAttribute(&slot.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-                cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
-                    cudaSuccess)
-                return MLP_ERR_CUDA;
-            slot.scratch = static_cast<uint8_t *>(ptr);
-            slot.ready = true;
         }
-        nd = slot;
+        num_sms = g_noalloc_sms[dev];
     }
+    void *scratch_ptr = nullptr;
+    if (cudaGetSymbolAddress(&scratch_ptr, g_noalloc_scratch) != cudaSuccess || !scratch_ptr ||
+        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
+        return MLP_ERR_CUDA;
 
     // Tiling: the same choices mlp_chain_create makes for this shape.
     const int tiles_m = static_cast<int>((M + mlpc::kBM - 1) / mlpc::kBM);
-    const int no_clusters[4] = {nd.num_sms, 0, 0, 0};   // this entry point runs without clusters
+    const int no_clusters[4] = {num_sms, 0, 0, 0};   // this entry point runs without clusters
     int bn[2] = {256, 256}, unused = 1;
     choose_tiles(tiles_m, K, N1, no_clusters, 0, 1, &bn[0], &unused);
     choose_tiles(tiles_m, N1, N2, no_clusters, 0, 1, &bn[1], &unused);
@@ -1055,8 +1070,6 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
 
     const int max_bn = std::max(bn[0], bn[1]);
     const uint32_t stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * max_bn * 2);
-    int smem_optin = 0;
-    cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     const int num_pipe = static_cast<int>(std::min<size_t>(
         mlpc::kMaxPipe, (smem_optin - 1024 - 4 * mlpc::kEpiStageBytes - sizeof(mlpc::Ctrl)) / stage_bytes));   // no split: no receive buffer
     if (num_pipe < 2)
@@ -1065,7 +1078,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     while (tmem_cols < static_cast<uint32_t>(2 * max_bn))
         tmem_cols *= 2;
 
-    uint8_t *base = nd.scratch;
+    uint8_t *base = static_cast<uint8_t *>(scratch_ptr);
     void *H = base + L.h;
     ChainParams P_;
     std::memset(&P_, 0, sizeof(P_));
@@ -1135,7 +1148,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     noalloc_setup_kernel<<<setup_blocks, 256, 0, st>>>(base, L, tn[0], tn[1], tiles_m);
     if (cudaGetLastError() != cudaSuccess)
         return MLP_ERR_CUDA;
-    const int grid = std::min(nd.num_sms, P + C);
+    const int grid = std::min(num_sms, P + C);
     if (!launch(P_, grid, mlpc::chain_smem_bytes(num_pipe, stage_bytes, 0), st))
         return MLP_ERR_CUDA;
     if (!sync_check)

@@ -1,5 +1,6 @@
 // protocol.h -- the pure (host + device) arithmetic of the CTA-pipelining protocol: ticket to
-// stage, first-stage raster order, and the epoch-tagged work-queue entry.  The CUDA kernel and
+// stage, first-stage raster order, the epoch-tagged work-queue entry and the run targets of the
+// accumulating scoreboard counters.  The CUDA kernel and
 // the host-thread protocol model both use these, so the model exercises the kernel's logic.
 //
 // Work-queue entry (one 64-bit word per slot): high 32 bits = run epoch + 1, low 32 bits = the
@@ -29,6 +30,21 @@ MLPC_HD bool queue_entry_ready(uint64_t v, uint32_t epoch)
 }
 
 MLPC_HD int32_t queue_entry_tile(uint64_t v) { return static_cast<int32_t>(v & 0xffffffffu); }
+
+// Scoreboard counters count releases and are never re-armed: a counter accumulates over all
+// runs of a handle, so a group that waits for `per_run` releases in every run has completed run
+// `epoch` (0, 1, ...) once its count reaches per_run x (epoch + 1).
+MLPC_HD uint32_t run_target(int32_t per_run, uint32_t epoch)
+{
+    return static_cast<uint32_t>(per_run) * (epoch + 1u);
+}
+
+// The release that took the count from `old` to old + 1 completed the run (and so publishes the
+// group's members on the work-queue).
+MLPC_HD bool release_completes(uint32_t old, uint32_t target) { return old + 1u == target; }
+
+// A count read by a waiter has reached the run's target (wrap-safe comparison).
+MLPC_HD bool count_reached(uint32_t v, uint32_t target) { return static_cast<int32_t>(v - target) >= 0; }
 
 // Tickets are issued stage by stage: [base[0], base[1]) are first-stage tiles, ...
 MLPC_HD int32_t stage_of_ticket(const int32_t *base, int32_t t)

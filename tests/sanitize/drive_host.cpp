@@ -25,13 +25,28 @@ int main()
                                            static_cast<int32_t>(d[5]), static_cast<int32_t>(d[6]), off.data(), tgt.data(),
                                            nnz, init.data()) != nnz;
     }
-    const int32_t tn2[2] = {4, 4}, tn4[4] = {3, 5, 2, 4};
+    const int32_t tn2[2] = {4, 4}, tn4[4] = {3, 5, 2, 4}, tn3[3] = {3, 2, 3};
     for (uint64_t seed = 1; seed <= 3; ++seed) {
         std::vector<int32_t> order(64 * 16);
-        fails += mlp_protocol_model(2, 4, tn2, 8, seed, -1, 2000, order.data()) != MLP_OK;
-        fails += mlp_protocol_model(4, 3, tn4, 6, seed, -1, 2000, order.data()) != MLP_OK;
+        fails += mlp_protocol_model(2, 4, tn2, 1, 4, 8, seed, -1, 2000, order.data()) != MLP_OK;
+        fails += mlp_protocol_model(4, 3, tn4, 1, 16, 6, seed, -1, 2000, order.data()) != MLP_OK;
+        fails += mlp_protocol_model(3, 17, tn3, 8, 8, 12, seed, -1, 2000, order.data()) != MLP_OK;   // merged groups
     }
-    fails += mlp_protocol_model(2, 2, tn2, 4, 5, 1, 200, nullptr) != MLP_ERR_TIMEOUT;   // withheld release
+    fails += mlp_protocol_model(2, 2, tn2, 1, 4, 4, 5, 1, 200, nullptr) != MLP_ERR_TIMEOUT;   // withheld release
+    for (int32_t rg : {1, 3, 8}) {   // the grouped scoreboard tables, sizes first
+        mlp_scoreboard sb{};
+        fails += mlp_scoreboard_build(1000, 512, 384, 128, 128, 64, rg, 4, &sb) != MLP_OK;
+        std::vector<int32_t> pg_off(sb.producers + 1), pg_tgt(sb.edges), grp_off(sb.groups + 1), grp_mem(sb.consumers),
+            grp_target(sb.groups), cons_grp(sb.consumers);
+        sb.pg_off = pg_off.data();
+        sb.pg_tgt = pg_tgt.data();
+        sb.grp_off = grp_off.data();
+        sb.grp_mem = grp_mem.data();
+        sb.grp_target = grp_target.data();
+        sb.cons_grp = cons_grp.data();
+        fails += mlp_scoreboard_build(1000, 512, 384, 128, 128, 64, rg, 4, &sb) != MLP_OK;
+        fails += grp_off[sb.groups] != sb.consumers;
+    }
     std::printf("host driver: %d failures\n", fails);
     return fails != 0;
 }

@@ -90,19 +90,24 @@ def test_tiny_config_has_four_producers_per_consumer(lib):
     assert off.tolist() == [0, 4, 8, 12, 16]
 
 
-@pytest.mark.parametrize("tiles_m,tiles_n,threads,seed", [
-    (1, [4, 4], 4, 0), (4, [8, 3], 8, 1), (3, [5, 7, 2, 4], 6, 2), (6, [2, 9], 16, 3), (2, [1, 1], 3, 4),
+@pytest.mark.parametrize("tiles_m,tiles_n,threads,seed,rg,rel", [
+    (1, [4, 4], 4, 0, 1, 4), (4, [8, 3], 8, 1, 1, 16), (3, [5, 7, 2, 4], 6, 2, 1, 4), (6, [2, 9], 16, 3, 1, 8),
+    (2, [1, 1], 3, 4, 1, 4), (9, [4, 5], 8, 5, 4, 8), (17, [3, 2, 3], 12, 6, 8, 4), (7, [2, 6], 6, 7, 3, 32),
 ])
-def test_protocol_model_orders_every_tile(lib, tiles_m, tiles_n, threads, seed):
-    st, order = mc.protocol_model(tiles_m, tiles_n, threads=threads, seed=seed, return_order=True)
+def test_protocol_model_orders_every_tile(lib, tiles_m, tiles_n, threads, seed, rg, rel):
+    """Merged raster groups, several releases per tile, counters accumulating over three runs."""
+    st, order = mc.protocol_model(tiles_m, tiles_n, threads=threads, seed=seed, return_order=True,
+                                  raster_group=rg, releases_per_tile=rel)
     assert st == mc.OK
     total = tiles_m * sum(tiles_n)
     assert sorted(order.tolist()) == sorted((s << 24) | t for s in range(len(tiles_n))
                                             for t in range(tiles_m * tiles_n[s]))
 
 
-def test_protocol_model_dropped_decrement_times_out(lib):
-    st, _ = mc.protocol_model(2, [4, 4], threads=4, seed=5, drop_tile=1, timeout_ms=200)
+@pytest.mark.parametrize("rg", [1, 4])
+def test_protocol_model_dropped_decrement_times_out(lib, rg):
+    st, _ = mc.protocol_model(8 if rg > 1 else 2, [4, 4], threads=4, seed=5, drop_tile=1, timeout_ms=200,
+                              raster_group=rg)
     assert st == mc.ERR_TIMEOUT
 
 
@@ -148,3 +153,33 @@ def test_null_arguments(lib):
     assert lib.mlp_chain_run(None, None, None, None, None, None) == mc.ERR_INVALID_ARG
     assert lib.mlp_chain_check(None, None) == mc.ERR_INVALID_ARG
     assert lib.mlp_chain_destroy(None) == mc.ERR_INVALID_ARG
+
+
+# (M, n_out, n_next, bm, bn_p, bn_c): one row panel, several, ragged M and N, unequal widths
+SB_SHAPES = [
+    (64, 256, 256, 128, 64, 64),
+    (128, 4096, 4096, 128, 128, 128),
+    (300, 192, 160, 128, 64, 32),
+    (1000, 512, 384, 128, 128, 64),
+    (2048, 1024, 512, 128, 256, 128),
+    (2100, 640, 256, 128, 256, 256),
+    (1, 64, 64, 128, 64, 64),
+]
+
+
+@pytest.mark.parametrize("shape", SB_SHAPES)
+@pytest.mark.parametrize("rg", [1, 3, 4, 8])
+@pytest.mark.parametrize("releases", [4, 16])
+def test_scoreboard_matches_oracle_enumeration(lib, oracle_mod, shape, rg, releases):
+    """The grouped counters and their targets (what the consumer prologue waits on) equal the ones
+    rebuilt from the oracle's brute-force tile-overlap enumeration, element by element."""
+    import expected_scoreboard as es
+    got = mc.scoreboard_build(*shape, raster_group=rg, releases_per_producer=releases)
+    es.assert_equal(got, es.expected(oracle_mod, *shape, rg, releases))
+
+
+def test_scoreboard_decode_is_one_group_waiting_for_every_release(lib):
+    # M = 128: one row panel, every consumer depends on all 32 producers, each releasing S x 4 times
+    sb = mc.scoreboard_build(128, 4096, 4096, 128, 128, 128, raster_group=1, releases_per_producer=16)
+    assert sb["groups"] == 1 and sb["grp_target"].tolist() == [32 * 16]
+    assert sb["grp_mem"].tolist() == list(range(32))

@@ -53,3 +53,22 @@ def test_peaks_from_the_measured_file_else_fallback(tmp_path, monkeypatch):
                                                               "bf16_tflops_sustained": 1727.7}))
     p = bench.load_peaks()
     assert p["source"] == "measured" and p["hbm_gbs"] == 6698.5 and p["bf16_tflops_sustained"] == 1727.7
+
+
+def test_phase_breakdown_from_a_hand_made_event_log():
+    """Two producers feeding two consumers (every consumer needs both): the phases come out as
+    the differences of the stamps, the hand-off from the later producer's release."""
+    import numpy as np
+    import bench
+    from mlp_latency_gb300.chain import EVENT_DTYPE
+    ev = np.zeros(4, dtype=EVENT_DTYPE)
+    #            stage tile  t_start t_acc  t_end
+    rows = [(0, 0, 1000, 5000, 6000), (0, 1, 1000, 6000, 8000),
+            (1, 0, 9000, 12000, 13000), (1, 1, 10000, 12000, 14000)]
+    for i, (s, t, a, b, c) in enumerate(rows):
+        ev[i]["stage"], ev[i]["tile"], ev[i]["t_start"], ev[i]["t_acc"], ev[i]["t_end"] = s, t, a, b, c
+    deps = [(np.array([0, 2, 4]), np.array([0, 1, 0, 1]))]
+    ph = bench.phase_breakdown(ev, deps)
+    assert ph["stage0"]["mainloop_us"] == 4.5 and ph["stage0"]["epilogue_T1_us"] == 1.5
+    assert ph["stage1"]["handoff_T3_us"] == 1.5 and ph["stage1"]["handoff_T3_min_us"] == 1.0
+    assert ph["stage1"]["first_start_us"] == 8.0 and ph["stage1"]["span_us"] == 5.0

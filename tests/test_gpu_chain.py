@@ -344,3 +344,25 @@ def test_split_k_dropped_decrement_times_out_then_recovers(mc):
         Y2 = Y.cpu()
     Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=[128, 128], k_split=[4, 2])
     assert torch.equal(Y2.view(torch.int16), Ys.view(torch.int16))
+
+
+# ------------------------------------------------------------------------- the scoreboard --
+@pytest.mark.parametrize("M,dims,tn,ks,rg", [
+    (128, (4096, 4096, 4096), [128, 128], [4, 4], 0),        # decode: one group, split releases
+    (2048, (1024, 1024, 512), [256, 128], [1, 1], 0),        # 16 panels: merged groups of 8
+    (1152, (512, 768, 256), [128, 64], [1, 2], 3),           # 9 panels, groups of 3, split consumer
+    (300, (256, 384, 512), [64, 128], [1, 1], 1),            # ragged, unmerged
+    (512, (512, 512, 512, 512, 512), [128, 128, 128, 128], [1, 1, 1, 1], 0),   # 3 boundaries
+])
+def test_device_scoreboard_matches_oracle_enumeration(mc, oracle_mod, M, dims, tn, ks, rg):
+    """The counters' tables as the kernel reads them (copied back from the device) equal the ones
+    rebuilt from the oracle's brute-force enumeration, bit for bit, for every stage boundary."""
+    import expected_scoreboard as es
+    with mc.Chain(M, dims, tile_n=tn, k_split=ks, raster_group=rg) as ch:
+        info = ch.info()
+        tiles_m = info["tiles_m"][0]
+        g = rg if rg else (8 if tiles_m >= 16 else (4 if tiles_m >= 8 else 1))
+        for b in range(len(dims) - 2):
+            want = es.expected(oracle_mod, M, dims[b + 1], dims[b + 2], info["tile_m"], info["tile_n"][b],
+                               info["tile_n"][b + 1], g, info["k_split"][b] * 4)
+            es.assert_equal(ch.scoreboard(b), want)
