@@ -119,15 +119,15 @@ typedef struct {
     int32_t num_gemms;                  /* S, 1..MLP_MAX_GEMMS                                   */
     int64_t dims[MLP_MAX_GEMMS + 1];    /* K, N1, N2, ...: W_s is dims[s] x dims[s+1]            */
     mlp_dtype in_dtype, acc_dtype, h_dtype, out_dtype; /* must be BF16, F32, BF16, BF16         */
-    int32_t tile_m;                     /* 0 or 128 (rows per tile; 64 is accepted and run as a
-                                           128-row tile, which gives the same dependency array
-                                           whenever M <= 64)                                    */
+    int32_t tile_m;                     /* rows per tile: 0 (= 128), 128, or 64 (tcgen05 MMAs of
+                                           M = 64: half the activation bytes per tile, twice the
+                                           row panels; micro-batch chunks of 64 rows)           */
     int32_t tile_n[MLP_MAX_GEMMS];      /* per GEMM: 0 (library choice), 32, 64, 128 or 256     */
     int32_t tile_k;                     /* 0 or 64                                               */
     mlp_epilogue epilogue;              /* applied after every GEMM                              */
     int32_t residual;                   /* nonzero: last stage adds X (needs dims[S] == dims[0]) */
     mlp_mode mode;
-    int32_t microbatch_rows;            /* MICROBATCH: rows per chunk, a multiple of 128        */
+    int32_t microbatch_rows;            /* MICROBATCH: rows per chunk, a multiple of tile_m     */
     int32_t device;                     /* CUDA device ordinal                                  */
     uint32_t debug_flags;               /* MLP_DEBUG_* bits                                     */
     int32_t drop_tile;                  /* with MLP_DEBUG_DROP_DECREMENT                         */

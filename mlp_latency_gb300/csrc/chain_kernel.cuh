@@ -38,14 +38,14 @@ namespace mlpc {
 
 constexpr int kMaxStages = 4;
 constexpr int kMaxCluster = 8;
-constexpr int kBM = 128;          // rows per tile = TMEM lanes
+constexpr int kBM = 128;          // rows of the largest tile (= TMEM lanes); a launch uses bm = 64 or 128
 constexpr int kBK = 64;           // 64 bf16 = 128 bytes = one 128B-swizzle row
 constexpr int kThreads = 256;
 constexpr int kEpiWarps = 4;      // epilogue warps; each releases its own rows of a tile
 constexpr int kSchedDepth = 4;
 constexpr int kMaxPipe = 16;
 constexpr int kTicketLead = 4;    // k-blocks before the end of a slice at which the next ticket is taken
-constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KB: the A tile of a 128-row tile
 
 // Device status codes (match mlp_status).
 constexpr uint32_t kStatusTimeout = 5;
@@ -117,6 +117,8 @@ struct ChainParams {
     int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
     int32_t tile_base[kMaxStages + 1];   // first event-log record of each stage
     int32_t cs;                          // cluster size
+    int32_t bm;                          // rows per tile: 128, or 64 (tcgen05 M = 64)
+    uint32_t a_bytes;                    // bytes of one A tile in a ring slot: bm x 64 bf16
     int32_t raster_group;
     int32_t num_pipe;                    // shared-memory ring depth
     uint32_t stage_bytes;                // bytes of one ring slot (A + B)
@@ -478,11 +480,14 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     const bool pipelined = p.pipelined != 0;
     const bool kwait = pipelined && p.kwait != 0;
     EventRec *const events = pipelined ? p.events : nullptr;
+    const int32_t bm = p.bm;
+    const uint32_t a_bytes = p.a_bytes;
     int32_t ps = 0;
     uint32_t pph = 0;
     // Programmatic dependent launch: the previous GEMM's output (this launch's A) is complete and
     // visible after this.  (Sending the first ring-full of weight copies before the wait measured
-    // slower: they compete with the previous GEMM's last loads.)
+    // slower: they compete with the previous GEMM's last loads; so did prefetching its weights
+    // into L2 with bulk tensor prefetches, which occupy the TMA engine like copies.)
     if (p.pdl_wait)
         griddep_wait();
     // Ring slots are filled in order 0, 1, ..., num_pipe - 1, 0, ...: the count of copies issued
@@ -529,14 +534,14 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t k_blocks = spr.k_blocks, kbps = spr.kb_per_split;
         const CUtensorMap *mapA = &p.mapA[s];
         const CUtensorMap *mapB = &p.mapB[s];
-        const int32_t m0 = (tile / tiles_n) * kBM;
+        const int32_t m0 = (tile / tiles_n) * bm;
         const int32_t n0 = (tile % tiles_n) * BN;
         const int32_t box_cols = b_swz / 2;
         const uint32_t box_bytes = kBK * b_swz;
         const int32_t nbox = BN / box_cols;
         const bool gated = spr.gated != 0;
         const uint32_t b_tile_bytes = static_cast<uint32_t>(kBK * BN * 2);
-        const uint32_t bytes = kABytes + (gated ? 2u : 1u) * b_tile_bytes;
+        const uint32_t bytes = a_bytes + (gated ? 2u : 1u) * b_tile_bytes;
         int32_t kb0, kb1;
         slice_range(k_blocks, kbps, item.split, kb0, kb1);
         const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
@@ -573,7 +578,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
 #pragma unroll
                     for (int32_t u = 0; u < (kGated ? 2 : 1); ++u) {   // gate (or plain) weights, then up
                         const CUtensorMap *mb = u ? mapU : mapB;
-                        uint8_t *bt = a + kABytes + u * b_tile_bytes;
+                        uint8_t *bt = a + a_bytes + u * b_tile_bytes;
                         if (b_form == 0)
                             tma_load_2d(bt, mb, &c->full[ps], k, by, pol_w);
                         else if (b_form == 1)
@@ -602,7 +607,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                 break;
             }
             uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
-            uint8_t *b = a + kABytes;
+            uint8_t *b = a + a_bytes;
             mbar_arrive_expect_tx(&c->full[ps], bytes);
             // Weights first: they depend on nothing, so in the K-granular mode they are in
             // flight while this k block's producers finish.
@@ -666,6 +671,8 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
     const uint32_t sub_stride = static_cast<uint32_t>(p.sub_stride);
     const bool split2 = p.acc_split == 2;
     const bool lamport = p.pipelined && p.lamport;
+    const int32_t bm = p.bm;
+    const uint32_t a_bytes = p.a_bytes;
     int32_t ps = 0;
     uint32_t pph = 0;
     uint32_t local_tiles = 0;
@@ -695,7 +702,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         // A gated tile's gate and up weight tiles lie back to back in the slot, laid out exactly
         // like one B tile twice as wide, so one MMA of N = 2 BN fills both accumulators (gate in
         // columns [0, BN), up in [BN, 2 BN)): an MMA costs the same for any N <= 256.
-        const uint32_t idesc = idesc_bf16_f32(kBM, gated ? 2u * BN : BN, b_kmajor ? 0u : 1u);
+        const uint32_t idesc = idesc_bf16_f32(static_cast<uint32_t>(bm), gated ? 2u * BN : BN, b_kmajor ? 0u : 1u);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
         bool ok = true;
         if (!lamport && !split2) {
@@ -706,8 +713,8 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             // carry out of it (shared memory is below 2^18 bytes).
             const uint32_t ring_base = smem_u32(ring);
             const uint64_t ad0 = smem_desc(ring_base, 16u, 1024u, 2u);
-            const uint64_t bd0 = b_kmajor ? smem_desc(ring_base + kABytes, 16u, 1024u, 2u)
-                                          : smem_desc(ring_base + kABytes, kBK * b_swz, 8u * b_swz, b_code);
+            const uint64_t bd0 = b_kmajor ? smem_desc(ring_base + a_bytes, 16u, 1024u, 2u)
+                                          : smem_desc(ring_base + a_bytes, kBK * b_swz, 8u * b_swz, b_code);
             const uint64_t bstep = b_kmajor ? 2u : b_swz;   // 16-byte units per 16-deep k step
             const uint64_t slot16 = stage_bytes >> 4;
             uint32_t accum = 0;
@@ -740,7 +747,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             if (lamport)   // the slot reached this thread through warp 3, not through its copies
                 tc_fence_after();
             const uint32_t a_addr = smem_u32(ring + static_cast<size_t>(ps) * stage_bytes);
-            const uint32_t b_addr = a_addr + kABytes;
+            const uint32_t b_addr = a_addr + a_bytes;
 #pragma unroll
             for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
                 // A: K-major, 128B swizzle; a 16-wide k step is 32 bytes along the row.
@@ -780,18 +787,19 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
 // run write +0.0 for an exact negative zero, so no output value equals it.
 constexpr uint32_t kSentinel = 0x8000u;
 
-// True on every lane if any of the 8192 bf16 values of the 16 KB tile at `a` is the sentinel.
+// True on every lane if any of the bf16 values of the A tile at `a` (a_bytes: 8 or 16 KB) is the
+// sentinel.
 // A half equals the sentinel exactly when it is zero after an XOR with the sentinel, so the
 // scan keeps a running per-half unsigned minimum of w ^ sentinel (two operations per word) and
 // tests it once.  Volatile shared loads (the tile is rewritten by TMA between two scans),
 // eight in flight before any is used.
-__device__ __forceinline__ bool tile_has_sentinel(const uint8_t *a, int32_t lane)
+__device__ __forceinline__ bool tile_has_sentinel(const uint8_t *a, uint32_t a_bytes, int32_t lane)
 {
     const uint32_t base = smem_u32(a) + static_cast<uint32_t>(lane) * 16u;
     const uint32_t flip = kSentinel | (kSentinel << 16);
     uint32_t m = 0xffffffffu;
 #pragma unroll 1
-    for (int b = 0; b < static_cast<int>(kABytes / 512); b += 8) {
+    for (int b = 0; b < static_cast<int>(a_bytes / 512); b += 8) {
         uint32_t w[8][4];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -852,7 +860,7 @@ __device__ __forceinline__ void role_validate(const ChainParams &p, Ctrl *c, uin
         const StageParams &spr = p.st[s];
         int32_t kb0, kb1;
         slice_range(spr.k_blocks, spr.kb_per_split, item.split, kb0, kb1);
-        const int32_t m0 = (tile / spr.tiles_n) * kBM;
+        const int32_t m0 = (tile / spr.tiles_n) * p.bm;
         for (int32_t kb = kb0; kb < kb1 && ok; ++kb) {
             if (!warp_wait_bar(&c->full[ps], pph, c, p)) {
                 ok = false;
@@ -863,7 +871,7 @@ __device__ __forceinline__ void role_validate(const ChainParams &p, Ctrl *c, uin
                 uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
                 bool force = p.force_reload != 0;
                 uint64_t t0 = 0;
-                while (force || tile_has_sentinel(a, lane)) {
+                while (force || tile_has_sentinel(a, p.a_bytes, lane)) {
                     force = false;
                     const uint64_t now = globaltimer_ns();
                     if (t0 == 0) {
@@ -880,7 +888,7 @@ __device__ __forceinline__ void role_validate(const ChainParams &p, Ctrl *c, uin
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&c->reload[ps], kABytes);
+                        mbar_arrive_expect_tx(&c->reload[ps], p.a_bytes);
                         tma_load_2d(a, &p.mapA[s], &c->reload[ps], kb * kBK, m0, pol_act);
                     }
                     rl_pending |= 1u << ps;
@@ -951,9 +959,10 @@ __device__ __forceinline__ uint32_t canon_neg_zero(uint32_t w)
     return w;
 }
 
+// Rows row0 .. row_lim - 1 are stored (row_lim <= M; a warp of a 64-row tile holds 16 rows).
 template <bool kGelu>
-__device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row0, int32_t n, const uint32_t (&r)[32],
-                                                   uint8_t *stage, int32_t lane)
+__device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row0, int32_t row_lim, int32_t n,
+                                                   const uint32_t (&r)[32], uint8_t *stage, int32_t lane)
 {
     float v[32];
 #pragma unroll
@@ -970,7 +979,7 @@ __device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row
             const int rr = it * 8 + (lane >> 2), sg = lane & 3;
             const int32_t gm = row0 + rr, gn = n + sg * 8;
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (gm < sp.M && gn < sp.N)
+            if (gm < row_lim && gn < sp.N)
                 x = *reinterpret_cast<const uint4 *>(sp.residual + static_cast<size_t>(gm) * sp.N + gn);
             *reinterpret_cast<uint4 *>(stage + stage_off(rr, sg)) = x;
         }
@@ -1005,7 +1014,7 @@ __device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row
     for (int it = 0; it < 4; ++it) {
         const int rr = it * 8 + (lane >> 2), sg = lane & 3;
         const int32_t gm = row0 + rr, gn = n + sg * 8;
-        if (gm < sp.M && gn < sp.N)   // N is a multiple of 8: a segment is all in or all out
+        if (gm < row_lim && gn < sp.N)   // N is a multiple of 8: a segment is all in or all out
             *reinterpret_cast<uint4 *>(sp.out + static_cast<size_t>(gm) * sp.N + gn) =
                 *reinterpret_cast<const uint4 *>(stage + stage_off(rr, sg));
     }
@@ -1014,13 +1023,13 @@ __device__ __forceinline__ void store_chunk_warp_t(const OutDesc sp, int32_t row
 
 // GeLU is chosen once per call by a uniform branch, so the plain path carries no tanh code
 // (a per-element test inside the unrolled loop could be if-converted into evaluating it always).
-__device__ __forceinline__ void store_chunk_warp(const OutDesc sp, int32_t row0, int32_t n, const uint32_t (&r)[32],
-                                                 uint8_t *stage, int32_t lane)
+__device__ __forceinline__ void store_chunk_warp(const OutDesc sp, int32_t row0, int32_t row_lim, int32_t n,
+                                                 const uint32_t (&r)[32], uint8_t *stage, int32_t lane)
 {
     if (sp.gelu)
-        store_chunk_warp_t<true>(sp, row0, n, r, stage, lane);
+        store_chunk_warp_t<true>(sp, row0, row_lim, n, r, stage, lane);
     else
-        store_chunk_warp_t<false>(sp, row0, n, r, stage, lane);
+        store_chunk_warp_t<false>(sp, row0, row_lim, n, r, stage, lane);
 }
 
 // 32 accumulator columns of this thread's TMEM lane (sub-accumulators summed, even + odd).
@@ -1165,7 +1174,13 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
     const int32_t warp = threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     const int32_t quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31
-    const int32_t row = quad * 32 + lane;
+    // Accumulator rows of this warp's TMEM sub-partition: with M = 128 lane l of sub-partition q
+    // holds row 32q + l; with M = 64 its first 16 lanes hold rows 16q .. 16q+15 (the tcgen05
+    // data-path layout of a 64-row MMA) and lanes 16 .. 31 hold nothing.
+    const int32_t bm = p.bm;
+    const int32_t rpw = bm / 4;                 // rows per warp
+    const int32_t row = quad * rpw + lane;      // this lane's row of the tile (valid if lane < rpw)
+    const bool row_ok = lane < rpw;
     uint8_t *stage = staging + quad * kEpiStageBytes;
     // kernel-uniform parameters in registers (see role_tma)
     const uint32_t acc_stride = static_cast<uint32_t>(p.acc_stride);
@@ -1221,7 +1236,8 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         tc_fence_after();
         if (logging && warp == 4 && lane == 0 && item.split == 0)
             p.events[p.tile_base[s] + tile].t_acc = globaltimer_ns();
-        const int32_t row0 = (tile / tiles_n) * kBM + quad * 32;   // this warp's first row
+        const int32_t row0 = (tile / tiles_n) * bm + quad * rpw;   // this warp's first row
+        const int32_t row_lim = min(spr.M, row0 + rpw);
         const int32_t n0 = (tile % tiles_n) * BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * acc_stride;
 
@@ -1239,7 +1255,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                         r[e] = __float_as_uint(g / (1.0f + expf(-g)) * __uint_as_float(u[e]));
                     }
                 }
-                store_chunk_warp(od, row0, n0 + c0, r, stage, lane);
+                store_chunk_warp(od, row0, row_lim, n0 + c0, r, stage, lane);
             }
             tc_fence_before();
             __syncwarp();
@@ -1270,11 +1286,12 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 load_acc(split2, sub_stride, taddr + ch * 32, r);
                 const int32_t owner = ch / cpo, oc = ch % cpo;
                 const uint32_t dst = map_to_rank(recv, g0 + owner) +
-                                     static_cast<uint32_t>((((item.split * cpo + oc) * 8) * kBM + row) * 16);
+                                     static_cast<uint32_t>((((item.split * cpo + oc) * 8) * bm + row) * 16);
+                if (row_ok)
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    st_cluster_v4_f32(dst + v * kBM * 16, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                    for (int v = 0; v < 8; ++v)
+                        st_cluster_v4_f32(dst + v * bm * 16, __uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
             }
             tc_fence_before();
             __syncwarp();
@@ -1293,11 +1310,11 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     acc_v[e] = 0.0f;
-                for (int32_t q = 0; q < S; ++q) {
-                    const uint32_t src = recv_u32 + static_cast<uint32_t>((((q * cpo + oc) * 8) * kBM + row) * 16);
+                for (int32_t q = 0; q < S && row_ok; ++q) {
+                    const uint32_t src = recv_u32 + static_cast<uint32_t>((((q * cpo + oc) * 8) * bm + row) * 16);
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
-                        const float4 x = ld_shared_v4_f32(src + v * kBM * 16);
+                        const float4 x = ld_shared_v4_f32(src + v * bm * 16);
                         acc_v[4 * v] += x.x;
                         acc_v[4 * v + 1] += x.y;
                         acc_v[4 * v + 2] += x.z;
@@ -1308,7 +1325,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
                     r[e] = __float_as_uint(acc_v[e]);
-                store_chunk_warp(od, row0, n0 + (item.split * cpo + oc) * 32, r, stage, lane);
+                store_chunk_warp(od, row0, row_lim, n0 + (item.split * cpo + oc) * 32, r, stage, lane);
             }
             if (lamport)           // (a Lamport run publishes the slice without a release)
                 fence_acq_rel_cluster();
@@ -1333,11 +1350,12 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         for (int32_t c0 = 0; c0 < BN; c0 += 32) {
             uint32_t r[32];
             load_acc(split2, sub_stride, taddr + c0, r);
-            float4 *dst = reinterpret_cast<float4 *>(mine) + (c0 / 32) * 8 * kBM + row;
+            float4 *dst = reinterpret_cast<float4 *>(mine) + (c0 / 32) * 8 * bm + row;
+            if (row_ok)
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-                dst[v * kBM] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                           __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                for (int v = 0; v < 8; ++v)
+                    dst[v * bm] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                              __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
         }
         tc_fence_before();
         __syncwarp();
@@ -1360,8 +1378,8 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 acc_v[e] = 0.0f;
-            const size_t off = static_cast<size_t>((c0 / 32) * 8 * kBM + row);   // in float4
-            for (int32_t qb = 0; qb < S; qb += 2) {
+            const size_t off = static_cast<size_t>((c0 / 32) * 8 * bm + row);   // in float4
+            for (int32_t qb = 0; qb < S && row_ok; qb += 2) {
                 float4 v[2][8];
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq)
@@ -1370,7 +1388,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                             reinterpret_cast<const float4 *>(partials + (cbase + g0 + qb + qq) * partial_floats) + off;
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            v[qq][i] = __ldcg(src + i * kBM);
+                            v[qq][i] = __ldcg(src + i * bm);
                     }
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq)
@@ -1388,7 +1406,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 #pragma unroll
             for (int e = 0; e < 32; ++e)
                 r[e] = __float_as_uint(acc_v[e]);
-            store_chunk_warp(od, row0, n0 + c0, r, stage, lane);
+            store_chunk_warp(od, row0, row_lim, n0 + c0, r, stage, lane);
         }
         if (lamport)
             fence_acq_rel_cluster();

@@ -119,6 +119,7 @@ __global__ void fill_sentinel_kernel(uint4 *p, size_t n16)
 struct mlp_chain {
     mlp_chain_desc desc{};
     int device = 0, num_sms = 0, S = 0;
+    int bm = mlpc::kBM;      // rows per tile: 128, or 64 (tcgen05 M = 64)
     int BN[MLP_MAX_GEMMS] = {}, tiles_m = 0, tiles_n[MLP_MAX_GEMMS] = {}, k_blocks[MLP_MAX_GEMMS] = {};
     int b_swz[MLP_MAX_GEMMS] = {};
     int num_pipe = 0, max_bn = 0, grid = 0, acc_split = 1;
@@ -173,7 +174,7 @@ extern "C" const char *mlp_status_str(mlp_status s)
 // and a stage cannot beat the HBM time of its weights.  clusters[i] = co-resident clusters of
 // 2^i CTAs.  Candidates with idle k slices or reduction slices narrower than 32 columns are
 // skipped.  Returns the estimated microseconds.
-static double choose_tiles(int64_t tiles_m, int64_t K, int64_t N, const int clusters[4], int fixed_bn,
+static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const int clusters[4], int fixed_bn,
                            int fixed_split, int *bn_out, int *split_out)
 {
     const int k_blocks = static_cast<int>((K + 63) / 64);
@@ -200,7 +201,7 @@ static double choose_tiles(int64_t tiles_m, int64_t K, int64_t N, const int clus
             const double units = tiles * S;
             // a persistent grid quantises into whole waves only while units are few
             const double waves = units <= 2 * slots ? std::ceil(units / slots) : units / slots;
-            const double rows = 128.0 + (bn >= 64 ? bn : 64);
+            const double rows = bm + (bn >= 64 ? bn : 64);
             // measured on GB300: a 128 x N x 16 MMA takes about max(48, N / 2) cycles; the
             // streaming rate with the MMAs running is about 1.2 ns per 128-byte operand row
             const double t_mma = kbps * 4 * std::max(48.0, bn / 2.0) / 2000.0;   // us
@@ -276,7 +277,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     if (!is_pipelined(d->mode) && d->mode != MLP_MODE_SEQUENTIAL && d->mode != MLP_MODE_MICROBATCH &&
         d->mode != MLP_MODE_SEQUENTIAL_PDL)
         return MLP_ERR_INVALID_ARG;
-    if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < mlpc::kBM || d->microbatch_rows % mlpc::kBM))
+    const int bm = d->tile_m == 64 ? 64 : mlpc::kBM;
+    if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < bm || d->microbatch_rows % bm))
         return MLP_ERR_INVALID_ARG;
     if (d->gated && (d->acc_split == 2 || (d->tile_n[0] != 0 && d->tile_n[0] > 128) ||
                      (d->k_split[0] != 0 && d->k_split[0] != 1)))
@@ -307,7 +309,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_UNSUPPORTED;
     }
 
-    h->tiles_m = static_cast<int>((d->M + mlpc::kBM - 1) / mlpc::kBM);
+    h->bm = bm;
+    h->tiles_m = static_cast<int>((d->M + bm - 1) / bm);
     // The device maximum, so that handles with different ring depths can share the kernel.
     if (cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
         cudaSuccess) {
@@ -345,7 +348,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         const bool gate_s = d->gated && s == 0;
         const int tn_s = gate_s && tn == 0 ? 128 : tn;
         const int ks_s = gate_s ? 1 : ks;
-        if (choose_tiles(h->tiles_m, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn, &split) >= 1e29) {
+        if (choose_tiles(h->tiles_m, bm, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn, &split) >= 1e29) {
             release(h);
             return MLP_ERR_UNSUPPORTED;   // no valid tile / split for this request
         }
@@ -363,13 +366,14 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         const int tiles = h->tiles_m * h->tiles_n[s];
         h->items[s] = (tiles + tpi - 1) / tpi;
     }
-    h->stage_bytes = mlpc::kABytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
+    const uint32_t a_bytes = static_cast<uint32_t>(bm * mlpc::kBK * 2);
+    h->stage_bytes = a_bytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
     if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles
-        h->stage_bytes = std::max(h->stage_bytes, mlpc::kABytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
+        h->stage_bytes = std::max(h->stage_bytes, a_bytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
     h->n_w = S + (d->gated ? 1 : 0);
     // split tiles up to 128 wide reduce through shared memory (distributed, within the cluster)
     for (int s = 0; s < S; ++s)
-        if (h->split[s] > 1 && h->BN[s] * 512u <= mlpc::kRecvBytes)
+        if (h->split[s] > 1 && static_cast<uint32_t>(h->BN[s] * bm * 4) <= mlpc::kRecvBytes)
             h->recv_bytes = mlpc::kRecvBytes;
     const size_t fixed = 1024 + 4 * mlpc::kEpiStageBytes + h->recv_bytes + sizeof(mlpc::Ctrl);
     h->num_pipe = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - fixed) / h->stage_bytes));
@@ -386,6 +390,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_UNSUPPORTED;
     }
     h->smem = mlpc::chain_smem_bytes(h->num_pipe, h->stage_bytes, h->recv_bytes);
+
     h->tmem_cols = 32;
     while (h->tmem_cols < static_cast<uint32_t>(2 * h->acc_cols))
         h->tmem_cols *= 2;
@@ -419,7 +424,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     // dependency arrays (host), then one device block for all library-owned state
     size_t bytes = 8 * sizeof(uint32_t);
     for (int b = 0; b + 1 < S; ++b) {
-        const int64_t nnz = mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], mlpc::kBM, h->BN[b], mlpc::kBM,
+        const int64_t nnz = mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], bm, h->BN[b], bm,
                                            h->BN[b + 1], nullptr, nullptr, 0, nullptr);
         if (nnz < 0) {
             release(h);
@@ -428,7 +433,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->off[b].resize(static_cast<size_t>(h->tiles_m) * h->tiles_n[b] + 1);
         h->tgt[b].resize(static_cast<size_t>(std::max<int64_t>(nnz, 1)));
         h->init[b].resize(static_cast<size_t>(h->tiles_m) * h->tiles_n[b + 1]);
-        mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], mlpc::kBM, h->BN[b], mlpc::kBM, h->BN[b + 1],
+        mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], bm, h->BN[b], bm, h->BN[b + 1],
                        h->off[b].data(), h->tgt[b].data(), nnz, h->init[b].data());
         h->tgt[b].resize(static_cast<size_t>(nnz));
         // The first stage's raster walks groups of rg row panels column by column, so those
@@ -455,8 +460,10 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     }
     // split-K partial sums: per stage that splits, one 128 x max_bn fp32 buffer per CTA slot
     const int cta_slots = std::max(h->grid, h->max_clusters * h->cs);
-    const size_t partial_bytes = static_cast<size_t>(cta_slots) * mlpc::kBM * h->max_bn * sizeof(float);
-    auto global_partials = [&](int s) { return h->split[s] > 1 && !(h->recv_bytes && h->BN[s] * 512u <= h->recv_bytes); };
+    const size_t partial_bytes = static_cast<size_t>(cta_slots) * bm * h->max_bn * sizeof(float);
+    auto global_partials = [&](int s) {
+        return h->split[s] > 1 && !(h->recv_bytes && static_cast<uint32_t>(h->BN[s] * bm * 4) <= h->recv_bytes);
+    };
     for (int s = 0; s < S; ++s)
         if (global_partials(s))
             bytes = align_up(bytes, 256) + partial_bytes;
@@ -525,7 +532,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_CUDA;
     }
     if (d->mode == MLP_MODE_MICROBATCH) {
-        const int rows_tiles = d->microbatch_rows / mlpc::kBM;
+        const int rows_tiles = d->microbatch_rows / bm;
         h->chunk_tiles = rows_tiles;
         h->n_chunks = (h->tiles_m + rows_tiles - 1) / rows_tiles;
         h->events.assign(static_cast<size_t>(h->n_chunks) * S, nullptr);
@@ -578,7 +585,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         } else {
             out_ptr = Y;
         }
-        if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], mlpc::kBM, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], h->bm, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
             return MLP_ERR_CUDA;
         int32_t b_3d = 0, u_3d = 0;
         auto encode_w = [&](CUtensorMap *m, const void *w, int32_t *is_3d) {
@@ -613,7 +620,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.tiles_per_item = h->cs / h->split[s];
         sp.items = h->items[s];
         sp.partials = h->partials[s];
-        sp.dsmem_reduce = h->split[s] > 1 && h->recv_bytes && h->BN[s] * 512u <= h->recv_bytes;
+        sp.dsmem_reduce = h->split[s] > 1 && h->recv_bytes && static_cast<uint32_t>(h->BN[s] * h->bm * 4) <= h->recv_bytes;
         sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
         sp.gelu = d.epilogue == MLP_EPI_GELU_TANH && !gate_s;
         sp.gated = gate_s;
@@ -639,7 +646,9 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.tile_base[s] = h->tile_base[s];
     }
     P.cs = h->cs;
-    P.partial_floats = mlpc::kBM * h->max_bn;
+    P.partial_floats = h->bm * h->max_bn;
+    P.bm = h->bm;
+    P.a_bytes = static_cast<uint32_t>(h->bm * mlpc::kBK * 2);
     P.recv_bytes = h->recv_bytes;
     // Grouped first-stage raster: a weight column slab is reused from L2 by the panels of a group
     // instead of being streamed again per panel.
@@ -896,7 +905,7 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
         return MLP_ERR_INVALID_ARG;
     std::memset(info, 0, sizeof(*info));
     info->num_gemms = h->S;
-    info->tile_m = mlpc::kBM;
+    info->tile_m = h->bm;
     info->tile_k = mlpc::kBK;
     for (int s = 0; s < h->S; ++s) {
         info->tile_n[s] = h->BN[s];
@@ -1060,8 +1069,8 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     const int tiles_m = static_cast<int>((M + mlpc::kBM - 1) / mlpc::kBM);
     const int no_clusters[4] = {num_sms, 0, 0, 0};   // this entry point runs without clusters
     int bn[2] = {256, 256}, unused = 1;
-    choose_tiles(tiles_m, K, N1, no_clusters, 0, 1, &bn[0], &unused);
-    choose_tiles(tiles_m, N1, N2, no_clusters, 0, 1, &bn[1], &unused);
+    choose_tiles(tiles_m, mlpc::kBM, K, N1, no_clusters, 0, 1, &bn[0], &unused);
+    choose_tiles(tiles_m, mlpc::kBM, N1, N2, no_clusters, 0, 1, &bn[1], &unused);
     const int tn[2] = {static_cast<int>((N1 + bn[0] - 1) / bn[0]), static_cast<int>((N2 + bn[1] - 1) / bn[1])};
     const int P = tiles_m * tn[0], C = tiles_m * tn[1];
     const NoallocLayout L = noalloc_layout(M, N1, P, C, tiles_m);
@@ -1127,6 +1136,8 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     P_.tile_base[2] = P + C;
     P_.cs = 1;
     P_.partial_floats = mlpc::kBM * max_bn;
+    P_.bm = mlpc::kBM;
+    P_.a_bytes = mlpc::kABytes;
     P_.num_pipe = num_pipe;
     P_.stage_bytes = stage_bytes;
     P_.tmem_cols = tmem_cols;

@@ -186,15 +186,6 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
-// Prefetch a 2-D box into L2 only (no shared memory, no completion tracking).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t c0, int32_t c1)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
 // ------------------------------------------------------------ programmatic dependent launch --
 // Wait until every grid this one depends on (a programmatic dependent launch) has completed and
 // its memory operations are visible; a no-op when the launch has no such dependency.
