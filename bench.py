@@ -361,12 +361,16 @@ def run_sweep(args):
         Xd, Wd = X.to(dev), [t.to(dev) for t in Ws]
         Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
         ref = None
+        tiles = None     # the first handle's tile widths and splits, kept by the 64-row handles
         line = {"sweep": "sequence length", "M": M, "dims": [d, d, d], "flops": w.flops,
                 "l2": "flushed between steps", "graph": "one CUDA graph replay per step"}
 
         def timed(mode, rows=0):
-            nonlocal ref
-            with mc.Chain(M, w.dims, mode=mode, microbatch_rows=rows, device=local) as ch:
+            nonlocal ref, tiles
+            kw = dict(tile_m=64, tile_n=tiles[0], k_split=tiles[1]) if rows % 128 else {}
+            with mc.Chain(M, w.dims, mode=mode, microbatch_rows=rows, device=local, **kw) as ch:
+                if tiles is None:
+                    tiles = (ch.info()["tile_n"], ch.info()["k_split"])
                 ws = torch.empty(max(ch.workspace_size(), 256), dtype=torch.uint8, device=dev)
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.stream(stream):
@@ -395,7 +399,7 @@ def run_sweep(args):
         for mode in ("sequential", "sequential_pdl", "pipelined", "pipelined_kwait"):
             line[f"{mode}_us"] = timed(mode)
         best = None
-        rows = 128
+        rows = 64
         while rows <= M // 2:
             t = timed("microbatch", rows)
             line[f"microbatch_{rows}_us"] = t
@@ -546,9 +550,9 @@ def main():
                 baselines[f"{mode}_us"] = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
                 ch.close()
             best = None
-            rows = 128
+            rows = 64   # chunks of 64 rows run 64-row tiles (tcgen05 M = 64)
             while rows <= w.M // 2:
-                ch = make("microbatch", rows)
+                ch = make("microbatch", rows, tile_m=64 if rows % 128 else 0)
                 g = capture(lambda ch=ch: ch.run(Xd, Wd, Y, ws, stream=stream))
                 for _ in range(args.warmup):
                     flush(); g.replay()
@@ -634,7 +638,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": mean_ms_all, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
-                       "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": 128, "tile_n": info["tile_n"],
+                       "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": info["tile_m"], "tile_n": info["tile_n"],
                        "k_split": info["k_split"], "cluster_size": info["cluster_size"],
                        "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",
