@@ -187,7 +187,7 @@ def barrier(world: int):
 
 
 # ------------------------------------------------------------------------ phase breakdown --
-def phase_breakdown(events: np.ndarray, deps) -> dict:
+def phase_breakdown(events: np.ndarray, deps, ctas: np.ndarray = None) -> dict:
     """Per-stage phase times (µs, medians over tiles) of one pipelined run, from its event log:
     the single-GPU analogues of the pages' per-phase overheads (CTA-Pipelining, section III-C,
     Fig. 2b).
@@ -199,9 +199,19 @@ def phase_breakdown(events: np.ndarray, deps) -> dict:
                         the queue push, the consumer's poll and acquire, and the TMA warp's pickup;
       span              first start -> last release of the stage.
     The scheduler's broadcast (T4) happens before a tile's start and is not timed separately.
-    `deps[b]` is the dependency CSR (prod_off, prod_tgt) of boundary b."""
+    `deps[b]` is the dependency CSR (prod_off, prod_tgt) of boundary b.  With the per-CTA records
+    (`ctas`: entry, set-up done, exit) it adds the kernel's own span, the CTAs' entry spread, their
+    set-up (barriers, TMEM, cluster sync) and the teardown after the last tile's release."""
     out = {}
     t0 = int(events["t_start"].min())
+    if ctas is not None and len(ctas):
+        entry, setup, exit_ = (ctas[k].astype(np.int64) for k in ("t_start", "t_acc", "t_end"))
+        out["kernel"] = {"ctas": int(len(ctas)),
+                         "span_us": float(exit_.max() - entry.min()) / 1e3,
+                         "entry_spread_us": float(entry.max() - entry.min()) / 1e3,
+                         "setup_us": float(np.median(setup - entry)) / 1e3,
+                         "first_tile_after_entry_us": float(t0 - entry.min()) / 1e3,
+                         "teardown_us": float(exit_.max() - int(events["t_end"].max())) / 1e3}
     for s in sorted(set(int(v) for v in events["stage"])):
         e = events[events["stage"] == s]
         st = {"tiles": int(len(e)),
@@ -590,7 +600,8 @@ def main():
                     ch.run(Xd, Wd, Y, ws, stream=stream)
                 if ch.check(stream) != 0:
                     raise RuntimeError("device status set in the event-log run")
-                phases = phase_breakdown(ch.event_log(), [ch.deps(b)[:2] for b in range(w.num_gemms - 1)])
+                phases = phase_breakdown(ch.event_log(), [ch.deps(b)[:2] for b in range(w.num_gemms - 1)],
+                                         ch.cta_log())
 
         # ---- end to end through the host-buffer C-ABI call ------------------------------------
         Xh = X.pin_memory()

@@ -160,7 +160,9 @@ typedef struct {
                                            (GeLU) applies to the later GEMMs only                 */
 } mlp_chain_desc;
 
-/* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG).  t_* are %globaltimer ns;
+/* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG), stage by stage, followed by one
+ * record per CTA of the launch with stage = -1, tile = cta = the CTA index, t_start = kernel
+ * entry, t_acc = set-up done (barriers, TMEM, cluster sync), t_end = exit.  t_* are %globaltimer ns;
  * seq_* come from one device-wide counter, taken after the consumer's acquire (start) and
  * before the producer's scoreboard release (end), so seq_end(p) < seq_start(c) for every
  * dependency p -> c.  In MLP_MODE_PIPELINED_KWAIT a consumer starts before its producers end
@@ -262,7 +264,7 @@ mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_next, int32_
 mlp_status mlp_chain_get_scoreboard(mlp_chain_t h, int32_t boundary, mlp_scoreboard *sb);
 
 /* Copy the event log of the last pipelined run (synchronises the device) into host_buf, up to
- * cap records; *n = records written.  INVALID_ARG without MLP_DEBUG_EVENT_LOG.  The records are
+ * cap records (tiles of all stages + CTAs of the launch); *n = records written.  INVALID_ARG without MLP_DEBUG_EVENT_LOG.  The records are
  * this library's form of the pages' per-phase timestamps (section III-C, Fig. 2: epilogue,
  * visibility, queue fetch and broadcast timed inside the kernels): globaltimer stamps at tile
  * start, accumulator complete and release, plus a device-wide sequence number for ordering. */

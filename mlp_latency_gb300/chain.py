@@ -175,13 +175,25 @@ class Chain:
         return _scoreboard_arrays(lambda sb: self._lib.mlp_chain_get_scoreboard(self._h, boundary, ctypes.byref(sb)),
                                   "get_scoreboard")
 
-    def event_log(self) -> np.ndarray:
+    def _full_log(self):
         info = self.info()
-        cap = sum(info["tiles_m"][s] * info["tiles_n"][s] for s in range(info["num_gemms"]))
+        tiles = sum(info["tiles_m"][s] * info["tiles_n"][s] for s in range(info["num_gemms"]))
+        cap = tiles + info["grid_ctas"]
         buf = np.zeros(cap, dtype=EVENT_DTYPE)
         n = ctypes.c_size_t()
         _check(self._lib.mlp_chain_get_event_log(self._h, buf.ctypes.data, cap, ctypes.byref(n)), "event_log")
-        return buf[: n.value]
+        return buf[: n.value], tiles
+
+    def event_log(self) -> np.ndarray:
+        """One record per tile of the last pipelined run (event_log=True)."""
+        buf, tiles = self._full_log()
+        return buf[:tiles]
+
+    def cta_log(self) -> np.ndarray:
+        """One record per CTA of the last pipelined run: t_start = entry, t_acc = set-up done,
+        t_end = exit (stage = -1)."""
+        buf, tiles = self._full_log()
+        return buf[tiles:]
 
     def info(self) -> dict:
         i = ChainInfo()

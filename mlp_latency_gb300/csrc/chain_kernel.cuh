@@ -135,7 +135,8 @@ struct ChainParams {
     uint32_t *epoch;
     uint32_t *status;
     uint32_t *seq;
-    EventRec *events;                    // null: no event log
+    EventRec *events;                    // null: no event log; else one record per tile of every
+                                         // stage (tile_base), then one per CTA of the launch
     const uint8_t *meta;                 // protocol state (counters, queues, dependency tables) ...
     uint32_t meta_bytes;                 // ... prefetched into L2 at launch (0: none)
 };
@@ -1432,6 +1433,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int32_t warp = threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
+    // a pipelined run's event log also records each CTA's lifetime: entry, set-up done, exit
+    EventRec *const cta_rec = (p.pipelined && p.events) ? p.events + p.tile_base[p.num_stages] + blockIdx.x : nullptr;
+    if (cta_rec && threadIdx.x == 0)
+        cta_rec->t_start = globaltimer_ns();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.num_pipe; ++i) {
@@ -1485,6 +1490,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     cluster_sync_all();   // every barrier of the cluster is initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = c->tmem_base;
+    if (cta_rec && threadIdx.x == 0)
+        cta_rec->t_acc = globaltimer_ns();
     if (p.pdl_trigger && threadIdx.x == 0)
         griddep_launch_dependents();   // the next GEMM's CTAs may take SMs as this grid's retire
 
@@ -1535,6 +1542,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
     }
     cluster_sync_all();   // no CTA leaves while a peer may still write to its shared memory
+    if (cta_rec && threadIdx.x == 0) {
+        cta_rec->stage = -1;
+        cta_rec->tile = static_cast<int32_t>(blockIdx.x);
+        cta_rec->smid = static_cast<int32_t>(smid());
+        cta_rec->cta = static_cast<int32_t>(blockIdx.x);
+        cta_rec->t_end = globaltimer_ns();
+    }
 }
 
 }  // namespace mlpc

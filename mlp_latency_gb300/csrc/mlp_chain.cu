@@ -455,7 +455,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         bytes = align_up(bytes, 256) + (h->off[b].size() - 1) * 4; // ready (K-granular mode)
     }
     if (d->debug_flags & MLP_DEBUG_EVENT_LOG) {
-        h->n_events = static_cast<size_t>(total);
+        h->n_events = static_cast<size_t>(total) + static_cast<size_t>(h->grid);   // tiles, then CTAs
         bytes = align_up(bytes, 256) + h->n_events * sizeof(mlpc::EventRec);
     }
     // split-K partial sums: per stage that splits, one 128 x max_bn fp32 buffer per CTA slot

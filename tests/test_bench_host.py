@@ -72,3 +72,9 @@ def test_phase_breakdown_from_a_hand_made_event_log():
     assert ph["stage0"]["mainloop_us"] == 4.5 and ph["stage0"]["epilogue_T1_us"] == 1.5
     assert ph["stage1"]["handoff_T3_us"] == 1.5 and ph["stage1"]["handoff_T3_min_us"] == 1.0
     assert ph["stage1"]["first_start_us"] == 8.0 and ph["stage1"]["span_us"] == 5.0
+    ctas = np.zeros(2, dtype=EVENT_DTYPE)
+    ctas["stage"] = -1
+    ctas["t_start"], ctas["t_acc"], ctas["t_end"] = [200, 400], [700, 1000], [14500, 15000]
+    k = bench.phase_breakdown(ev, deps, ctas)["kernel"]
+    assert k["span_us"] == 14.8 and k["entry_spread_us"] == 0.2 and k["setup_us"] == 0.55
+    assert k["first_tile_after_entry_us"] == 0.8 and k["teardown_us"] == 1.0

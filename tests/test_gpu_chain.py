@@ -366,3 +366,21 @@ def test_device_scoreboard_matches_oracle_enumeration(mc, oracle_mod, M, dims, t
             want = es.expected(oracle_mod, M, dims[b + 1], dims[b + 2], info["tile_m"], info["tile_n"][b],
                                info["tile_n"][b + 1], g, info["k_split"][b] * 4)
             es.assert_equal(ch.scoreboard(b), want)
+
+
+def test_cta_lifetime_records_bracket_every_tile(mc):
+    """The per-CTA records of the event log (entry, set-up done, exit) are ordered and enclose the
+    start and release of every tile."""
+    M, dims = 512, (256, 512, 256)
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=12)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=[64, 64], event_log=True) as ch:
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        ch.run(Xd, Wd, Y, ws)
+        assert ch.check() == 0
+        ctas, tiles, grid = ch.cta_log(), ch.event_log(), ch.info()["grid_ctas"]
+    assert len(ctas) == grid and sorted(ctas["cta"].tolist()) == list(range(grid))
+    assert (ctas["stage"] == -1).all()
+    assert (ctas["t_start"] <= ctas["t_acc"]).all() and (ctas["t_acc"] <= ctas["t_end"]).all()
+    assert tiles["t_start"].min() >= ctas["t_acc"].min() and tiles["t_end"].max() <= ctas["t_end"].max()
