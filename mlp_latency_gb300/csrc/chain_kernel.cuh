@@ -84,7 +84,8 @@ struct BoundaryParams {
     const int32_t *cgrp;       // consumer tile -> its group
     uint32_t *count;           // one counter per group: releases so far, over all runs of the handle
     unsigned long long *queue; // one slot per consumer tile
-    uint32_t *tail;
+    uint32_t *tail;            // queue slots reserved so far, over all runs of the handle
+    uint32_t slots_per_run;    // consumer tiles: the tail's increments in one run
     // K-granular mode: per producer tile, the releases seen so far (ready_quota per run,
     // accumulated over the handle's runs and compared against the run's epoch).
     uint32_t *ready;
@@ -130,9 +131,9 @@ struct ChainParams {
     uint32_t recv_bytes;                 // split-K receive buffer in shared memory (0: none)
     int32_t drop_tile;                   // fault injection (-1: off)
     uint64_t timeout_ns;
-    uint32_t *ticket;
-    uint32_t *done;
-    uint32_t *epoch;
+    uint32_t *ticket;                    // tickets taken so far, over all runs of the handle
+    uint32_t tickets_per_run;            // cluster items of all stages: the ticket's increments in one run
+    unsigned long long *launches;        // CTAs started so far: run e's CTAs read e x ctas ..
     uint32_t *status;
     uint32_t *seq;
     EventRec *events;                    // null: no event log; else one record per tile of every
@@ -299,7 +300,8 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
         // others idle, so wait until the TMA warp is about to finish its current slice.
         if (!wait_bar(&c->want_next, (it - 1) & 1, c, p))
             return;
-        const int32_t t = p.pipelined ? nclusters + static_cast<int32_t>(atom_add_relaxed_gpu(p.ticket, 1u))
+        const int32_t t = p.pipelined ? nclusters + static_cast<int32_t>(run_relative(
+                                                        atom_add_relaxed_gpu(p.ticket, 1u), c->epoch, p.tickets_per_run))
                                       : static_cast<int32_t>(cluster_id_x()) + it * nclusters;
         int32_t ntiles = 0;
         int32_t tiles[kMaxCluster];
@@ -1094,7 +1096,8 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
             const uint32_t old = atom_add_relaxed_gpu(bd.count + pl.g, 1u);
             if (release_completes(old, run_target(pl.init, c->epoch))) {
                 fire = 1;
-                q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(pl.n));
+                q0 = run_relative(atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(pl.n)), c->epoch,
+                                  bd.slots_per_run);
             }
         }
         if (!__shfl_sync(0xffffffffu, fire, 0))
@@ -1132,7 +1135,7 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
             const int32_t m0 = bd.grp_off[gg], n = bd.grp_off[gg + 1] - m0;
             uint32_t q0 = 0;
             if (lane == src)
-                q0 = atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(n));
+                q0 = run_relative(atom_add_relaxed_gpu(bd.tail, static_cast<uint32_t>(n)), c->epoch, bd.slots_per_run);
             q0 = __shfl_sync(0xffffffffu, q0, src);
             for (int32_t i = lane; i < n; i += 32)
                 st_relaxed_gpu_u64(bd.queue + q0 + i, queue_entry(c->epoch, bd.grp_mem[m0 + i]));
@@ -1439,6 +1442,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         cta_rec->t_start = globaltimer_ns();
 
     if (threadIdx.x == 0) {
+        // Both reads go out first, so their latency overlaps the barrier set-up below.
+        const uint64_t launch_no = p.pipelined ? atom_add_relaxed_gpu_u64(p.launches, 1ull) : 0ull;
+        const uint32_t status0 = ld_relaxed_gpu_u32(p.status);
         for (int i = 0; i < p.num_pipe; ++i) {
             mbar_init(&c->full[i], 1);
             mbar_init(&c->empty[i], 1);
@@ -1469,8 +1475,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         mbar_init(&c->red_bar, 4 * p.cs);          // 4 warps x S siblings, each arriving cs/S times
         mbar_init(&c->done_bar, 4 * p.cs);
         c->abort_flag = 0;
-        c->skip = ld_relaxed_gpu_u32(p.status) != 0;   // sticky error: do nothing
-        c->epoch = p.pipelined ? ld_relaxed_gpu_u32(p.epoch) : 0u;
+        c->skip = status0 != 0;   // sticky error: do nothing
+        c->epoch = p.pipelined ? epoch_of_launch(launch_no, gridDim.x) : 0u;
         fence_barrier_init();
         mbar_arrive(&c->sfull[0]);   // item 0 is in place (a local arrival, before any remote one)
     }
@@ -1526,21 +1532,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
-    if (threadIdx.x == 0 && p.pipelined && !c->skip) {
-        // The last CTA out re-arms the run-wide counters for the next run.  Scoreboard counters
-        // were re-armed by their last producer; queue slots carry the run's epoch instead of
-        // being cleared.
-        fence_acq_rel_gpu();
-        const uint32_t old = atom_add_acq_rel_gpu(p.done, 1u);
-        if (old == gridDim.x - 1) {
-            *p.ticket = 0;
-            for (int b = 0; b + 1 < p.num_stages; ++b)
-                *p.bd[b].tail = 0;
-            *p.done = 0;
-            *p.epoch = c->epoch + 1;
-            fence_acq_rel_gpu();
-        }
-    }
+    // Nothing is reset for the next run: scoreboard counters, the ticket, the queue tails and the
+    // launch counter all accumulate over runs (protocol.h), and queue slots carry the run's epoch.
     cluster_sync_all();   // no CTA leaves while a peer may still write to its shared memory
     if (cta_rec && threadIdx.x == 0) {
         cta_rec->stage = -1;

@@ -188,7 +188,9 @@ extern "C" mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_n
 // ------------------------------------------------------------------------------------------
 // Host model of the protocol: `threads` host threads play the persistent CTAs and run the
 // kernel's protocol steps on std::atomic state, with the kernel's tables and arithmetic:
-//   - tickets in stage order; first-stage tickets map to tiles through raster_tile(rg);
+//   - every thread takes its run's epoch from a launch counter it adds 1 to at its start, has a
+//     static first ticket (its own index) and takes the rest from a ticket counter, in stage
+//     order; first-stage tickets map to tiles through raster_tile(rg);
 //   - scoreboard groups from scoreboard_groups() (merged per rg row panels, members column by
 //     column), each waiting for grp_init x R releases per run, R = releases one producer tile
 //     makes (split-K slices x epilogue warps on the device);
@@ -201,8 +203,9 @@ extern "C" mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_n
 //     then acquires the named tile's group counter until it reaches the run's target, and only
 //     then reads the producers' output (plain, non-atomic reads: a missing happens-before edge is
 //     a data race that ThreadSanitizer reports, and a stale value fails the run);
-//   - counters accumulate over three back-to-back runs (epochs 0, 1, 2) and are never reset;
-//     between runs only the ticket and the tails are cleared, as the last CTA out does.
+//   - nothing is reset between three back-to-back runs (epochs 0, 1, 2): scoreboard counters,
+//     the ticket, the queue tails and the launch counter accumulate, and each run reads its own
+//     share of them relative to its epoch (protocol.h).
 // ------------------------------------------------------------------------------------------
 namespace {
 
@@ -264,6 +267,7 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
     }
 
     std::atomic<uint32_t> ticket{0}, seq{0}, status{0};
+    std::atomic<uint64_t> launches{0};
     std::vector<std::atomic<uint32_t>> start_seq(total), end_seq(total), runs(total);
     std::atomic<int32_t> order_pos{0};
     const auto timeout = std::chrono::milliseconds(timeout_ms ? timeout_ms : 2000);
@@ -281,10 +285,15 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
         auto worker = [&](int tid) {
             std::mt19937_64 rng(seed * 7919u + static_cast<uint64_t>(tid) * 104729u + epoch);
             std::uniform_int_distribution<int> delay(0, 40);
-            while (true) {
-                const int32_t t = static_cast<int32_t>(ticket.fetch_add(1, std::memory_order_relaxed));
-                if (t >= total)
-                    return;
+            const uint32_t run = mlpc::epoch_of_launch(launches.fetch_add(1, std::memory_order_relaxed),
+                                                       static_cast<uint32_t>(threads));
+            if (run != epoch) {
+                fail(MLP_ERR_DEVICE_STATE);
+                return;
+            }
+            for (int32_t t = tid; t < total;
+                 t = threads + static_cast<int32_t>(mlpc::run_relative(ticket.fetch_add(1, std::memory_order_relaxed),
+                                                                       run, static_cast<uint32_t>(total)))) {
                 const int32_t s = mlpc::stage_of_ticket(base, t);
                 const int32_t local = t - base[s];
                 int32_t tile;
@@ -349,7 +358,8 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                         if (!mlpc::release_completes(old, mlpc::run_target(B.target[static_cast<size_t>(g)], epoch)))
                             continue;
                         const int32_t m0 = G.grp_off[g], n = G.grp_off[g + 1] - m0;
-                        const uint32_t q0 = B.tail.fetch_add(static_cast<uint32_t>(n), std::memory_order_relaxed);
+                        const uint32_t q0 = mlpc::run_relative(B.tail.fetch_add(static_cast<uint32_t>(n), std::memory_order_relaxed),
+                                                               run, static_cast<uint32_t>(B.queue.size()));
                         for (int32_t i = 0; i < n; ++i)
                             B.queue[q0 + i].store(mlpc::queue_entry(epoch, G.grp_mem[m0 + i]), std::memory_order_relaxed);
                     }
@@ -377,10 +387,6 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                 if (bd[b].count[g].load() != mlpc::run_target(bd[b].target[g], epoch))
                     return MLP_ERR_DEVICE_STATE;
         }
-        // what the last CTA out does on the device
-        ticket.store(0);
-        for (auto &b : bd)
-            b.tail.store(0);
     }
     return MLP_OK;
 }

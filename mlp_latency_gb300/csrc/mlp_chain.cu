@@ -135,7 +135,7 @@ struct mlp_chain {
     mlpc::DepGroups grp[MLP_MAX_GEMMS - 1];
     void *dev_block = nullptr;
     DeviceBoundary db[MLP_MAX_GEMMS - 1];
-    uint32_t *d_ctrl = nullptr;  // ticket, done, epoch, status, seq
+    uint32_t *d_ctrl = nullptr;  // words: 0 ticket, 1 status, 2 seq, 4-5 launch counter (u64)
     mlpc::EventRec *d_events = nullptr;
     size_t n_events = 0;
     int32_t stage_base[MLP_MAX_GEMMS + 1] = {};
@@ -637,6 +637,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.bd[b].cgrp = h->db[b].cgrp;
         P.bd[b].queue = h->db[b].queue;
         P.bd[b].tail = h->db[b].tail;
+        P.bd[b].slots_per_run = static_cast<uint32_t>(h->db[b].consumers);
         P.bd[b].ready = h->db[b].ready;
         P.bd[b].ready_quota = static_cast<uint32_t>(h->split[b] * mlpc::kEpiWarps);
     }
@@ -662,10 +663,10 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     P.drop_tile = -1;
     P.timeout_ns = static_cast<uint64_t>(d.timeout_us ? d.timeout_us : 2000000u) * 1000ull;
     P.ticket = h->d_ctrl + 0;
-    P.done = h->d_ctrl + 1;
-    P.epoch = h->d_ctrl + 2;
-    P.status = h->d_ctrl + 3;
-    P.seq = h->d_ctrl + 4;
+    P.status = h->d_ctrl + 1;
+    P.seq = h->d_ctrl + 2;
+    P.launches = reinterpret_cast<unsigned long long *>(h->d_ctrl + 4);
+    P.tickets_per_run = static_cast<uint32_t>(h->stage_base[h->S]);
     P.events = h->d_events;
     P.meta = reinterpret_cast<const uint8_t *>(h->d_ctrl);
     P.meta_bytes = static_cast<uint32_t>(h->meta_bytes);
@@ -832,7 +833,7 @@ extern "C" mlp_status mlp_chain_check(mlp_chain_t h, void *stream)
         if (s && cudaStreamSynchronize(s) != cudaSuccess)
             return MLP_ERR_CUDA;
     uint32_t status = 0;
-    if (cudaMemcpy(&status, h->d_ctrl + 3, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (cudaMemcpy(&status, h->d_ctrl + 1, sizeof(status), cudaMemcpyDeviceToHost) != cudaSuccess)
         return MLP_ERR_CUDA;
     if (status == 0)
         return MLP_OK;
@@ -1148,10 +1149,11 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     P_.timeout_ns = 2000000000ull;
     uint32_t *ctrl = reinterpret_cast<uint32_t *>(base + L.ctrl);
     P_.ticket = ctrl + 0;
-    P_.done = ctrl + 1;
-    P_.epoch = ctrl + 2;
-    P_.status = ctrl + 3;
-    P_.seq = ctrl + 4;
+    P_.status = ctrl + 1;
+    P_.seq = ctrl + 2;
+    P_.launches = reinterpret_cast<unsigned long long *>(ctrl + 4);
+    P_.tickets_per_run = static_cast<uint32_t>(P + C);
+    P_.bd[0].slots_per_run = static_cast<uint32_t>(C);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const long long work = std::max(C, P + 1);
@@ -1165,7 +1167,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     if (!sync_check)
         return MLP_OK;
     uint32_t status = 0;
-    if (cudaMemcpyAsync(&status, ctrl + 3, sizeof(status), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+    if (cudaMemcpyAsync(&status, ctrl + 1, sizeof(status), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return MLP_ERR_CUDA;
     if (status == 0)

@@ -46,6 +46,17 @@ MLPC_HD bool release_completes(uint32_t old, uint32_t target) { return old + 1u 
 // A count read by a waiter has reached the run's target (wrap-safe comparison).
 MLPC_HD bool count_reached(uint32_t v, uint32_t target) { return static_cast<int32_t>(v - target) >= 0; }
 
+// Run-wide counters are never reset either.  Every CTA of a pipelined launch adds 1 to a 64-bit
+// launch counter once, at its start, so run e's CTAs read e x ctas .. e x ctas + ctas - 1: the
+// run's epoch is that value divided by the CTA count.
+MLPC_HD uint32_t epoch_of_launch(uint64_t old, uint32_t ctas) { return static_cast<uint32_t>(old / ctas); }
+
+// A run takes exactly `per_run` increments of the ticket counter (one per cluster item: every
+// valid ticket once, plus one past the end per cluster that had a first item) and of each stage
+// boundary's queue tail (one per consumer tile), so run e's own count is the raw value minus
+// per_run x e (mod 2^32, so the counters may wrap).
+MLPC_HD uint32_t run_relative(uint32_t raw, uint32_t epoch, uint32_t per_run) { return raw - per_run * epoch; }
+
 // Tickets are issued stage by stage: [base[0], base[1]) are first-stage tiles, ...
 MLPC_HD int32_t stage_of_ticket(const int32_t *base, int32_t t)
 {

@@ -348,6 +348,13 @@ __device__ __forceinline__ uint32_t atom_add_relaxed_gpu(uint32_t *p, uint32_t v
     return old;
 }
 
+__device__ __forceinline__ uint64_t atom_add_relaxed_gpu_u64(unsigned long long *p, uint64_t v)
+{
+    uint64_t old;
+    asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;

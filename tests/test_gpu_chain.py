@@ -384,3 +384,15 @@ def test_cta_lifetime_records_bracket_every_tile(mc):
     assert (ctas["stage"] == -1).all()
     assert (ctas["t_start"] <= ctas["t_acc"]).all() and (ctas["t_acc"] <= ctas["t_end"]).all()
     assert tiles["t_start"].min() >= ctas["t_acc"].min() and tiles["t_end"].max() <= ctas["t_end"].max()
+
+
+@pytest.mark.parametrize("mode", ["pipelined", "pipelined_kwait", "pipelined_lamport"])
+def test_many_runs_of_one_handle_without_any_reset(mc, mode):
+    """Tickets, queue tails, scoreboard counters and the launch counter accumulate over runs and
+    are read relative to each run's epoch: forty back-to-back runs (split-K releases, merged
+    scoreboard groups, a partial last row panel) all give the same bits."""
+    M, dims = 1100, (256, 512, 384)
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=13)
+    outs, _, _ = run_chain(mc, X, Ws, mode=mode, reps=40, tile_n=[64, 128], k_split=[2, 2], raster_group=3)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
