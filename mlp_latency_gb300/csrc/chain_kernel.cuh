@@ -150,6 +150,7 @@ struct __align__(8) Ctrl {
     uint64_t want_next;   // TMA -> scheduler: take the next ticket now
     uint64_t valid[kMaxPipe];   // Lamport: the slot's A tile holds no sentinel (warp 3 -> MMA)
     uint64_t reload[kMaxPipe];  // Lamport: completion of a reloaded A tile
+    uint64_t epoch_bar;   // the run's epoch is in `epoch` (warp 3, once per launch)
     uint64_t red_bar;     // split-K: every sibling's partial is written
     uint64_t done_bar;    // split-K: every sibling has read its parts of my partial
     int32_t item_stage[kSchedDepth], item_tile[kSchedDepth], item_split[kSchedDepth];
@@ -222,6 +223,16 @@ __device__ __forceinline__ bool warp_wait_bar(uint64_t *bar, uint32_t parity, Ct
     return ok != 0;
 }
 
+// As warp_wait_bar, and then every lane acquires the completed phase itself (a try_wait that
+// succeeds at once), so every lane may read what the arriving thread published.
+__device__ __forceinline__ bool warp_wait_bar_all(uint64_t *bar, uint32_t parity, Ctrl *c, const ChainParams &p)
+{
+    if (!warp_wait_bar(bar, parity, c, p))
+        return false;
+    mbar_try_wait(bar, parity);
+    return true;
+}
+
 __device__ __forceinline__ float gelu_tanh_f32(float x)
 {
     const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
@@ -291,6 +302,8 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
     const int32_t nclusters = static_cast<int32_t>(num_clusters_x());
     if (c->item_stage[0] < 0)
         return;   // not even a first item for this cluster
+    if (p.pipelined && !wait_bar(&c->epoch_bar, 0, c, p))   // tickets are read relative to the epoch
+        return;
     for (int32_t it = 1;; ++it) {
         const int32_t slot = it % kSchedDepth;
         const uint32_t ph = (it / kSchedDepth) & 1;
@@ -497,6 +510,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     // says how often each slot was filled (a per-slot array would live in local memory, and its
     // read-modify-write sits on the per-k-block issue path).
     uint32_t issued = 0;
+    bool have_epoch = false;   // the run's epoch is needed from the first consumer item on
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
         if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true, true))
@@ -513,6 +527,13 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t s = item.stage;
         int32_t tile = item.tile;
         const bool kwait_s = kwait && s > 0;
+        if (pipelined && s > 0 && !have_epoch) {   // queue entries and ready counts carry the epoch
+            if (!wait_bar(&c->epoch_bar, 0, c, p)) {
+                free_item_slot(c, slot);
+                break;
+            }
+            have_epoch = true;
+        }
         if (pipelined && s > 0 && !kwait) {
             tile = resolve_queue_slot(p, c, s, item.tile, !p.lamport);   // Lamport: validated instead
             if (tile < 0) {
@@ -1200,6 +1221,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
     const size_t cbase = static_cast<size_t>(cluster_id_x()) * cs;
     uint32_t local_tiles = 0;
     uint32_t nsplit = 0;                        // split-K tiles this CTA took part in
+    bool have_epoch = false;
     for (int32_t it = 0;; ++it) {
         const int32_t slot = it % kSchedDepth;
         if (!warp_wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true))
@@ -1216,6 +1238,11 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             continue;
         const int32_t s = item.stage;
         int32_t tile = item.tile;
+        if (pipelined && !have_epoch) {   // queue slots, releases and pushes carry the run's epoch
+            if (!warp_wait_bar_all(&c->epoch_bar, 0, c, p))
+                break;
+            have_epoch = true;
+        }
         if (pipelined && s > 0 && !kwait) {   // the TMA warp of this CTA polled the same slot first
             int32_t t = 0;
             if (lane == 0)
@@ -1442,8 +1469,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         cta_rec->t_start = globaltimer_ns();
 
     if (threadIdx.x == 0) {
-        // Both reads go out first, so their latency overlaps the barrier set-up below.
-        const uint64_t launch_no = p.pipelined ? atom_add_relaxed_gpu_u64(p.launches, 1ull) : 0ull;
+        // The status read goes out first, so its latency overlaps the barrier set-up below.
         const uint32_t status0 = ld_relaxed_gpu_u32(p.status);
         for (int i = 0; i < p.num_pipe; ++i) {
             mbar_init(&c->full[i], 1);
@@ -1475,8 +1501,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         mbar_init(&c->red_bar, 4 * p.cs);          // 4 warps x S siblings, each arriving cs/S times
         mbar_init(&c->done_bar, 4 * p.cs);
         c->abort_flag = 0;
+        mbar_init(&c->epoch_bar, 1);
         c->skip = status0 != 0;   // sticky error: do nothing
-        c->epoch = p.pipelined ? epoch_of_launch(launch_no, gridDim.x) : 0u;
+        c->epoch = 0;
         fence_barrier_init();
         mbar_arrive(&c->sfull[0]);   // item 0 is in place (a local arrival, before any remote one)
     }
@@ -1513,6 +1540,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             if (lane == 0 && rank == 0)
                 role_scheduler(p, c);
         } else if (warp == 3) {
+            // The run's epoch, from the launch counter every CTA adds 1 to (protocol.h): taken
+            // here, after the set-up, so its round trip delays no first load; every role that
+            // needs it waits for epoch_bar first.
+            if (lane == 0) {
+                if (p.pipelined)
+                    c->epoch = epoch_of_launch(atom_add_relaxed_gpu_u64(p.launches, 1ull), gridDim.x);
+                mbar_arrive(&c->epoch_bar);
+            }
             // The protocol's few kilobytes of state are cold after whatever ran before (the
             // release and the consumer prologue would each pay HBM misses in sequence), so the
             // otherwise idle warp pulls them into L2 now, spread over the grid.
