@@ -237,7 +237,8 @@ __device__ __forceinline__ float gelu_tanh_f32(float x)
 {
     const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
     const float k1 = 0.044715f;
-    return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+    // the epilogue's critical path on one-wave stages: one MUFU tanh instead of a tanhf call
+    return 0.5f * x * (1.0f + tanh_approx(k0 * (x + k1 * x * x * x)));
 }
 
 // Arrive on the same mbarrier in CTA `rank` of this cluster, `count` times, without release
@@ -1283,7 +1284,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const float g = __uint_as_float(r[e]);
-                        r[e] = __float_as_uint(g / (1.0f + expf(-g)) * __uint_as_float(u[e]));
+                        r[e] = __float_as_uint(__fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(u[e]));
                     }
                 }
                 store_chunk_warp(od, row0, row_lim, n0 + c0, r, stage, lane);

@@ -355,6 +355,15 @@ __device__ __forceinline__ uint64_t atom_add_relaxed_gpu_u64(unsigned long long 
     return old;
 }
 
+// The hardware tanh approximation (one MUFU operation; the PTX ISA bounds its relative error by
+// about 2^-11, below the 2^-9 of the bf16 rounding that follows it in the epilogue).
+__device__ __forceinline__ float tanh_approx(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;
