@@ -183,3 +183,12 @@ def test_scoreboard_decode_is_one_group_waiting_for_every_release(lib):
     sb = mc.scoreboard_build(128, 4096, 4096, 128, 128, 128, raster_group=1, releases_per_producer=16)
     assert sb["groups"] == 1 and sb["grp_target"].tolist() == [32 * 16]
     assert sb["grp_mem"].tolist() == list(range(32))
+
+
+def test_scoreboard_build_rejects_bad_arguments(lib):
+    sb = _lib.Scoreboard()
+    assert lib.mlp_scoreboard_build(128, 256, 256, 128, 64, 64, 1, 4, None) == mc.ERR_INVALID_ARG
+    assert lib.mlp_scoreboard_build(0, 256, 256, 128, 64, 64, 1, 4, ctypes.byref(sb)) == mc.ERR_INVALID_ARG
+    assert lib.mlp_scoreboard_build(128, 256, 256, 128, 0, 64, 1, 4, ctypes.byref(sb)) == mc.ERR_INVALID_ARG
+    assert lib.mlp_scoreboard_build(128, 256, 256, 128, 64, 64, 1, 0, ctypes.byref(sb)) == mc.ERR_INVALID_ARG
+    assert lib.mlp_chain_get_scoreboard(None, 0, ctypes.byref(sb)) == mc.ERR_INVALID_ARG

@@ -44,6 +44,7 @@ def test_oracle_under_asan_ubsan(tmp_path):
 def test_host_protocol_under_sanitizers(tmp_path, sanitize):
     extra = ["-fno-sanitize-recover=undefined"] if "undefined" in sanitize else []
     cmd = ["g++", "-std=c++17", "-O1", "-g", "-fno-omit-frame-pointer", f"-fsanitize={sanitize}", *extra, "-pthread",
+           "-Wall", "-Wextra", "-Wshadow", "-Werror",
            "-I", os.path.join(ROOT, "include"), os.path.join(HERE, "drive_host.cpp"),
            os.path.join(ROOT, "mlp_latency_gb300", "csrc", "host_protocol.cpp"), "-o", "drive_host"]
     assert "0 failures" in _build_and_run(cmd, "drive_host", tmp_path)
