@@ -19,8 +19,9 @@
  * CTAs poll the queue in a short prologue, adopt the dequeued tile id in place of their own
  * and run the unchanged GEMM body.  (Here the counters count releases up to an epoch-scaled
  * target instead of down to zero, one counter per group of consumer tiles with the same
- * producers, and a consumer acquires its group counter before it reads the producers' output.)  Here all stages run in ONE persistent, warp-specialised
- * kernel on one GPU (one CTA per SM): the pages put one layer per GPU instead.
+ * producers, and a consumer acquires its group counter before it reads the producers' output;
+ * mlp_chain_get_scoreboard returns those counters' tables.)  All stages run in ONE persistent,
+ * warp-specialised kernel on one GPU (one CTA per SM): the pages put one layer per GPU instead.
  * MLP_MODE_SEQUENTIAL launches the same tile engine once per GEMM, back to back on one stream
  * (the pages' "two consecutive GEMMs" baseline, section III-C).  MLP_MODE_MICROBATCH splits
  * X into row chunks and overlaps GEMM s of chunk i with GEMM s+1 of chunk i-1 on separate
@@ -255,8 +256,9 @@ typedef struct {
 /* Host-only scoreboard builder (no GPU needed), the routine mlp_chain_create uses: the groups of
  * the dependency array that mlp_deps_build gives for M x n_out producer tiles of bm x bn_p and
  * M x n_next consumer tiles of bm x bn_c.  Returns OK, or INVALID_ARG for a bad size or NULL sb. */
-mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm, int32_t bn_p, int32_t bn_c,
-                                int32_t raster_group, int32_t releases_per_producer, mlp_scoreboard *sb);
+mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm, int32_t bn_p,
+                                int32_t bn_c, int32_t raster_group, int32_t releases_per_producer,
+                                mlp_scoreboard *sb);
 
 /* The scoreboard tables the kernel of handle `h` waits on at stage boundary b, copied back from
  * the device (synchronous: waits for the device first) into sb's buffers; sizes as in
@@ -297,9 +299,9 @@ int64_t mlp_deps_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm_p, i
  * stage << 24 | tile.  With drop_tile >= 0 that first-stage tile withholds its releases and the
  * run must end in MLP_ERR_TIMEOUT after timeout_ms.  Returns OK when every tile ran exactly once
  * per run after all of its producers and every counter ends each run exactly at its target. */
-mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n, int32_t raster_group,
-                              int32_t releases_per_tile, int32_t threads, uint64_t seed, int32_t drop_tile,
-                              uint32_t timeout_ms, int32_t *order_out);
+mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
+                              int32_t raster_group, int32_t releases_per_tile, int32_t threads,
+                              uint64_t seed, int32_t drop_tile, uint32_t timeout_ms, int32_t *order_out);
 
 /* Allocation-free run of the two-GEMM chain (the paper has no counterpart to this entry point).
  *
