@@ -159,10 +159,6 @@ typedef struct {
                                            the weight of GEMM s >= 1.  The gated GEMM runs
                                            unsplit with tile_n <= 128 and acc_split 1; epilogue
                                            (GeLU) applies to the later GEMMs only                 */
-    int32_t commit_every;               /* ring slots freed by the MMA thread's commit: 0 = library
-                                           choice, 1 = after every k block, 2 = in pairs (one
-                                           commit per two k blocks; used only where every item of a
-                                           launch takes the branch-free loops and the ring is even) */
 } mlp_chain_desc;
 
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG), stage by stage, followed by one

@@ -61,7 +61,7 @@ class ChainDesc(ctypes.Structure):
         ("epilogue", ctypes.c_int), ("residual", i32), ("mode", ctypes.c_int),
         ("microbatch_rows", i32), ("device", i32), ("debug_flags", u32), ("drop_tile", i32),
         ("timeout_us", u32), ("grid_ctas", i32), ("raster_group", i32), ("pipe_stages", i32),
-        ("weight_layout", i32), ("k_split", i32 * MAX_GEMMS), ("acc_split", i32), ("gated", i32), ("commit_every", i32),
+        ("weight_layout", i32), ("k_split", i32 * MAX_GEMMS), ("acc_split", i32), ("gated", i32),
     ]
 
 

@@ -70,7 +70,7 @@ class Chain:
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
                  weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False,
-                 force_reload: bool = False, commit_every: int = 0):
+                 force_reload: bool = False):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -101,7 +101,6 @@ class Chain:
         for i, v in enumerate(k_split or []):
             d.k_split[i] = int(v)
         d.gated = int(bool(gated))
-        d.commit_every = int(commit_every)
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
         self.n_weights = len(self.dims) - 1 + int(bool(gated))
         self._lib = lib

@@ -113,9 +113,6 @@ struct ChainParams {
     int32_t pdl_wait;                    // programmatic dependent of the previous stage's launch:
                                          // the TMA warp waits for it before its first load
     int32_t pdl_trigger;                 // a later stage is launched as this launch's dependent
-    int32_t commit_pairs;                // ring slots are freed in pairs: the MMA thread commits only
-                                         // after odd slots, the TMA thread waits once per pair (only
-                                         // when every item of the launch takes the common-case loops)
     int32_t first_stage;                 // non-pipelined launches run this single stage
     int32_t m_tile_begin, m_tile_end;    // ... over these row tiles
     int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
@@ -502,7 +499,6 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     EventRec *const events = pipelined ? p.events : nullptr;
     const int32_t bm = p.bm;
     const uint32_t a_bytes = p.a_bytes;
-    const int32_t pair_mask = p.commit_pairs ? 1 : 0;
     int32_t ps = 0;
     uint32_t pph = 0;
     // Programmatic dependent launch: the previous GEMM's output (this launch's A) is complete and
@@ -591,15 +587,13 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             const int32_t by = b_kmajor ? n0 : (b_3d ? n0 / box_cols : 0);
             const int32_t b_form = b_kmajor ? 0 : (b_3d ? 1 : 2);
             const CUtensorMap *mapU = &p.mapU;
-            // One loop per stage kind, so the plain loop carries no test for the gated copy.  With
-            // paired slots the even slot of a pair waits for the pair's (odd slot's) barrier, which
-            // the MMA thread's commit completes once both slots are read; the odd slot is free then.
+            // One loop per stage kind, so the plain loop carries no test for the gated copy.
             auto k_loop = [&](auto gated_kind) {
                 constexpr bool kGated = decltype(gated_kind)::value;
                 for (int32_t kb = kb0; kb < kb1; ++kb) {
                     if (leader && kb == lead_kb)
                         mbar_arrive(&c->want_next);
-                    if ((ps & pair_mask) == 0 && !wait_bar(&c->empty[ps + pair_mask], pph ^ 1, c, p)) {
+                    if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
                         ok = false;
                         break;
                     }
@@ -704,7 +698,6 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
     const bool lamport = p.pipelined && p.lamport;
     const int32_t bm = p.bm;
     const uint32_t a_bytes = p.a_bytes;
-    const int32_t pair_mask = p.commit_pairs ? 1 : 0;
     int32_t ps = 0;
     uint32_t pph = 0;
     uint32_t local_tiles = 0;
@@ -762,8 +755,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                     accum = 1u;   // the slice's first k step overwrites the accumulator
                 }
                 issued = true;
-                if ((ps & pair_mask) == pair_mask)   // every slot, or the second slot of a pair
-                    mma_commit(&c->empty[ps]);
+                mma_commit(&c->empty[ps]);
                 if (++ps == num_pipe) {
                     ps = 0;
                     pph ^= 1;

@@ -151,7 +151,6 @@ struct mlp_chain {
     std::vector<cudaEvent_t> events;
     cudaEvent_t fork = nullptr;
     int n_chunks = 0, chunk_tiles = 0;
-    bool pairs_ok = false;   // ring slots may be released in pairs (commit_every)
 };
 
 extern "C" const char *mlp_status_str(mlp_status s)
@@ -284,8 +283,6 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     if (d->gated && (d->acc_split == 2 || (d->tile_n[0] != 0 && d->tile_n[0] > 128) ||
                      (d->k_split[0] != 0 && d->k_split[0] != 1)))
         return MLP_ERR_UNSUPPORTED;   // the gated GEMM keeps gate and up side by side in TMEM, unsplit
-    if (d->commit_every < 0 || d->commit_every > 2)
-        return MLP_ERR_INVALID_ARG;
     if (d->grid_ctas < 0 || d->raster_group < 0 || d->pipe_stages < 0 || d->pipe_stages == 1 ||
         d->pipe_stages > mlpc::kMaxPipe || d->acc_split < 0 || d->acc_split > 2 || d->weight_layout < 0 ||
         d->weight_layout > 1)
@@ -657,12 +654,6 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     // Grouped first-stage raster: a weight column slab is reused from L2 by the panels of a group
     // instead of being streamed again per panel.
     P.raster_group = d.raster_group ? d.raster_group : default_raster_group(h->tiles_m);
-    // Paired slot releases need every item to take the branch-free loops of both roles (checked
-    // per run for the K-granular and Lamport modes) and an even ring.
-    bool common = h->acc_split == 1 && h->num_pipe % 2 == 0 && d.commit_every != 1;
-    for (int s = 0; s < h->S; ++s)
-        common = common && (P.st[s].b_kmajor || P.st[s].b_3d || P.st[s].BN <= P.st[s].b_swz / 2);
-    h->pairs_ok = common && d.commit_every == 2;
     P.num_pipe = h->num_pipe;
     P.stage_bytes = h->stage_bytes;
     P.tmem_cols = h->tmem_cols;
@@ -753,7 +744,6 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
         P.kwait = h->desc.mode == MLP_MODE_PIPELINED_KWAIT;
         P.lamport = h->desc.mode == MLP_MODE_PIPELINED_LAMPORT;
         P.force_reload = P.lamport && (h->desc.debug_flags & MLP_DEBUG_FORCE_RELOAD) != 0;
-        P.commit_pairs = h->pairs_ok && !P.kwait && !P.lamport;
         if (P.lamport && h->S > 1) {
             size_t bytes = 0;
             mlp_chain_workspace_size(h, &bytes);
@@ -773,7 +763,6 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
         return launch(P, h->grid, h->smem, st) ? MLP_OK : MLP_ERR_CUDA;
     }
     P.pipelined = 0;
-    P.commit_pairs = h->pairs_ok;
     if (h->desc.mode == MLP_MODE_SEQUENTIAL || h->desc.mode == MLP_MODE_SEQUENTIAL_PDL) {
         const bool pdl = h->desc.mode == MLP_MODE_SEQUENTIAL_PDL;
         for (int s = 0; s < h->S; ++s) {

@@ -396,20 +396,3 @@ def test_many_runs_of_one_handle_without_any_reset(mc, mode):
     outs, _, _ = run_chain(mc, X, Ws, mode=mode, reps=40, tile_n=[64, 128], k_split=[2, 2], raster_group=3)
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
-
-
-@pytest.mark.parametrize("mode", ["pipelined", "sequential", "sequential_pdl", "microbatch"])
-@pytest.mark.parametrize("M,dims,tn,ks", [(640, (320, 576, 448), [64, 128], [1, 1]),     # 5 and 9 k blocks per tile
-                                          (256, (1088, 512, 320), [128, 64], [2, 1]),    # split slices of 9 and 8
-                                          (300, (256, 384, 264), [256, 32], [1, 1])])
-def test_paired_slot_release_changes_no_bits(mc, oracle_mod, mode, M, dims, tn, ks):
-    """Freeing ring slots in pairs (one commit per two k blocks) only changes when the TMA thread
-    may refill them: Y is bit-identical to one commit per k block, including slices with an odd
-    number of k blocks (a tile then ends on the first slot of a pair), over repeated runs."""
-    X, Ws = si.draw(si.make_workload("t", M, dims), seed=14)
-    kw = dict(mode=mode, tile_n=tn, k_split=ks, microbatch_rows=128 if mode == "microbatch" else 0)
-    ref, _, _ = run_chain(mc, X, Ws, commit_every=1, **kw)
-    outs, _, _ = run_chain(mc, X, Ws, commit_every=2, reps=3, **kw)
-    for y in outs:
-        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
-    assert_close_to_oracle(outs[-1], oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
