@@ -437,6 +437,8 @@ def main():
     ap.add_argument("--raster-group", type=int, default=0)
     ap.add_argument("--pipe-stages", type=int, default=0)
     ap.add_argument("--acc-split", type=int, default=0)
+    ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
+                    help="0: library choice, 1: one CTA per tile, 2: CTA pairs (256-row tiles, tcgen05 cta_group::2)")
     ap.add_argument("--weight-layout", default="kn", choices=["kn", "nk"],
                     help="nk: weights stored transposed (nn.Linear layout)")
     ap.add_argument("--no-baselines", action="store_true", help="skip sequential/micro-batch/cuBLAS lines")
@@ -487,7 +489,8 @@ def main():
         return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
                         microbatch_rows=rows, device=local, raster_group=args.raster_group,
                         pipe_stages=args.pipe_stages, acc_split=args.acc_split,
-                        weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated, **kw)
+                        weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated,
+                        cta_pair=kw.pop("cta_pair", args.cta_pair), **kw)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()
@@ -562,7 +565,8 @@ def main():
             best = None
             rows = 64   # chunks of 64 rows run 64-row tiles (tcgen05 M = 64)
             while rows <= w.M // 2:
-                ch = make("microbatch", rows, tile_m=64 if rows % 128 else 0)
+                ch = make("microbatch", rows, tile_m=64 if rows % 128 else 0,
+                          cta_pair=args.cta_pair if rows % 256 == 0 else 0)   # pairs need 256-row chunks
                 g = capture(lambda ch=ch: ch.run(Xd, Wd, Y, ws, stream=stream))
                 for _ in range(args.warmup):
                     flush(); g.replay()
@@ -650,7 +654,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
                        "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": info["tile_m"], "tile_n": info["tile_n"],
-                       "k_split": info["k_split"], "cluster_size": info["cluster_size"],
+                       "k_split": info["k_split"], "cluster_size": info["cluster_size"], "cta_pair": info["cta_pair"],
                        "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",
                        "l2": f"flushed between steps (write of {2 * l2 >> 20} MiB, outside the timed events)",

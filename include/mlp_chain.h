@@ -159,6 +159,15 @@ typedef struct {
                                            the weight of GEMM s >= 1.  The gated GEMM runs
                                            unsplit with tile_n <= 128 and acc_split 1; epilogue
                                            (GeLU) applies to the later GEMMs only                 */
+    int32_t cta_pair;                   /* 0 or 1: one CTA per tile; 2: CTA pairs (tcgen05
+                                           cta_group::2), each pair computing a 256-row tile, each
+                                           CTA loading its 128 rows of the activations and half of
+                                           the weight tile's columns (tiles 128 or 256 wide), so a
+                                           k block's fill per SM shrinks by a third and the ring
+                                           gets deeper.  Plain stages only: no gating, split-K or
+                                           split accumulators, not the K-granular or Lamport
+                                           modes (else UNSUPPORTED); micro-batch chunks are
+                                           multiples of 256 rows                                 */
 } mlp_chain_desc;
 
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG), stage by stage, followed by one
@@ -188,6 +197,7 @@ typedef struct {
     int32_t launches_per_run;           /* kernels one mlp_chain_run enqueues                     */
     int32_t cluster_size;               /* CTAs per thread-block cluster                          */
     int32_t k_split[MLP_MAX_GEMMS];
+    int32_t cta_pair;                   /* 2: CTA pairs (tile_m is then the pair's 256 rows)      */
 } mlp_chain_info;
 
 typedef struct mlp_chain *mlp_chain_t;

@@ -61,7 +61,7 @@ class ChainDesc(ctypes.Structure):
         ("epilogue", ctypes.c_int), ("residual", i32), ("mode", ctypes.c_int),
         ("microbatch_rows", i32), ("device", i32), ("debug_flags", u32), ("drop_tile", i32),
         ("timeout_us", u32), ("grid_ctas", i32), ("raster_group", i32), ("pipe_stages", i32),
-        ("weight_layout", i32), ("k_split", i32 * MAX_GEMMS), ("acc_split", i32), ("gated", i32),
+        ("weight_layout", i32), ("k_split", i32 * MAX_GEMMS), ("acc_split", i32), ("gated", i32), ("cta_pair", i32),
     ]
 
 
@@ -75,7 +75,7 @@ class ChainInfo(ctypes.Structure):
         ("num_gemms", i32), ("tile_m", i32), ("tile_k", i32), ("tile_n", i32 * MAX_GEMMS),
         ("tiles_m", i32 * MAX_GEMMS), ("tiles_n", i32 * MAX_GEMMS), ("grid_ctas", i32),
         ("num_sms", i32), ("pipe_stages", i32), ("smem_bytes", i32), ("tmem_cols", i32),
-        ("launches_per_run", i32), ("cluster_size", i32), ("k_split", i32 * MAX_GEMMS),
+        ("launches_per_run", i32), ("cluster_size", i32), ("k_split", i32 * MAX_GEMMS), ("cta_pair", i32),
     ]
 
 

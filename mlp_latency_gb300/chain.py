@@ -60,7 +60,8 @@ class Chain:
       "sequential"         one launch per GEMM;
       "sequential_pdl"     one launch per GEMM, each a programmatic dependent launch of the one before;
       "microbatch"         row chunks of ``microbatch_rows``, GEMMs of different chunks overlapped.
-    ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice).  Errors raise MlpChainError with
+    ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice).  ``cta_pair=2`` runs 256-row
+    tiles on CTA pairs (tcgen05 cta_group::2).  Errors raise MlpChainError with
     the library's status.
     """
 
@@ -70,7 +71,7 @@ class Chain:
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
                  weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False,
-                 force_reload: bool = False):
+                 force_reload: bool = False, cta_pair: int = 0):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -101,6 +102,7 @@ class Chain:
         for i, v in enumerate(k_split or []):
             d.k_split[i] = int(v)
         d.gated = int(bool(gated))
+        d.cta_pair = int(cta_pair)
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
         self.n_weights = len(self.dims) - 1 + int(bool(gated))
         self._lib = lib
@@ -203,7 +205,7 @@ class Chain:
                 "tiles_m": list(i.tiles_m[:S]), "tiles_n": list(i.tiles_n[:S]), "grid_ctas": i.grid_ctas,
                 "num_sms": i.num_sms, "pipe_stages": i.pipe_stages, "smem_bytes": i.smem_bytes,
                 "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run,
-                "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S])}
+                "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S]), "cta_pair": i.cta_pair}
 
 
 def deps_build(M: int, n_out: int, n_next: int, bm_p: int, bn_p: int, bm_c: int, bn_c: int):

@@ -113,6 +113,7 @@ struct ChainParams {
     int32_t pdl_wait;                    // programmatic dependent of the previous stage's launch:
                                          // the TMA warp waits for it before its first load
     int32_t pdl_trigger;                 // a later stage is launched as this launch's dependent
+    int32_t pair;                        // 2: CTA pairs (chain_kernel<2>), each tile 2 bm rows
     int32_t first_stage;                 // non-pipelined launches run this single stage
     int32_t m_tile_begin, m_tile_end;    // ... over these row tiles
     int32_t stage_base[kMaxStages + 1];  // pipelined: first ticket (cluster item) of each stage
@@ -486,8 +487,15 @@ __device__ __forceinline__ void slice_range(int32_t k_blocks, int32_t kb_per_spl
 }
 
 // ---------------------------------------------------------------------------- TMA producer --
+// With a CTA pair (kPair = 2) each CTA loads its own 128 rows of the 256-row A tile and its half
+// of the B tile's columns into its own ring, and both CTAs' copies complete on the leader's full
+// barrier.  The leader arms each fill (expect_tx of both CTAs' bytes) before it lets the peer fill
+// the same slot (a relaxed arrive on the peer's empty barrier), so the peer only ever copies into
+// phases the leader waits for; the leader's own empty barrier is released by its MMA commit.
+template <int kPair>
 __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t *ring, bool leader)
 {
+    constexpr bool kPairMode = kPair == 2;
     // Kernel parameters live in constant memory behind a generic pointer; every asm statement
     // with a memory clobber would force them to be re-read, so the loop works from registers.
     const int32_t num_pipe = p.num_pipe;
@@ -499,6 +507,11 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
     EventRec *const events = pipelined ? p.events : nullptr;
     const int32_t bm = p.bm;
     const uint32_t a_bytes = p.a_bytes;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t half = kPairMode ? (rank & 1u) : 0u;   // 0: the pair's leader
+    // shared::cluster addresses of the leader's full barriers and of the peer's empty barriers
+    const uint32_t full_lead0 = kPairMode ? map_to_rank(&c->full[0], rank & ~1u) : 0u;
+    const uint32_t empty_peer0 = kPairMode ? map_to_rank(&c->empty[0], rank | 1u) : 0u;
     int32_t ps = 0;
     uint32_t pph = 0;
     // Programmatic dependent launch: the previous GEMM's output (this launch's A) is complete and
@@ -559,16 +572,18 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t k_blocks = spr.k_blocks, kbps = spr.kb_per_split;
         const CUtensorMap *mapA = &p.mapA[s];
         const CUtensorMap *mapB = &p.mapB[s];
-        const int32_t m0 = (tile / tiles_n) * bm;
-        const int32_t n0 = (tile % tiles_n) * BN;
+        // a pair's tile is 2 bm rows: this CTA's rows and its half of the tile's columns
+        const int32_t bn_cta = BN / kPair;
+        const int32_t m0 = (tile / tiles_n) * (kPair * bm) + static_cast<int32_t>(half) * bm;
+        const int32_t n0 = (tile % tiles_n) * BN + static_cast<int32_t>(half) * bn_cta;
         const int32_t box_cols = b_swz / 2;
         const uint32_t box_bytes = kBK * b_swz;
-        const int32_t nbox = BN / box_cols;
+        const int32_t nbox = bn_cta / box_cols;
         const bool gated = spr.gated != 0;
-        const uint32_t b_tile_bytes = static_cast<uint32_t>(kBK * BN * 2);
+        const uint32_t b_tile_bytes = static_cast<uint32_t>(kBK * bn_cta * 2);
         const uint32_t bytes = a_bytes + (gated ? 2u : 1u) * b_tile_bytes;
         int32_t kb0, kb1;
-        slice_range(k_blocks, kbps, item.split, kb0, kb1);
+        slice_range(k_blocks, kbps, kPairMode ? 0 : item.split, kb0, kb1);   // a pair's halves run the whole k range
         const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
         // K-granular mode: the A tile of k block kb reads columns [kb*64, kb*64+64) of the
         // previous stage's output, written by producer tiles kb*64/pBN .. (kb*64+63)/pBN of the
@@ -579,7 +594,44 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         int32_t ready_hi = -1;
         const int32_t slice_last = kwait_s ? min(((kb1 - 1) * kBK + kBK - 1) / pBN, ptn - 1) : 0;
         bool ok = true;
-        if (!kwait_s && (b_kmajor || b_3d || nbox == 1)) {
+        if constexpr (kPairMode) {
+            // Pair stages are plain (no K-granular waits, gating or Lamport): the B tile's half is
+            // one copy (N x K weights, or a 3-D view of K x N ones), or one per box (ragged N).
+            const int32_t bx = b_kmajor ? 0 : (b_3d ? 0 : n0);
+            const int32_t by = b_kmajor ? n0 : (b_3d ? n0 / box_cols : 0);
+            const int32_t b_form = b_kmajor ? 0 : (b_3d ? 1 : 2);
+            const uint32_t pair_bytes = 2u * bytes;
+            for (int32_t kb = kb0; kb < kb1; ++kb) {
+                if (leader && kb == lead_kb)
+                    mbar_arrive(&c->want_next);
+                // the leader waits for its MMA's release of the slot's previous fill; the peer for
+                // the leader's go-ahead for this fill
+                if (!wait_bar(&c->empty[ps], half ? pph : pph ^ 1, c, p, true, half != 0)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
+                const uint32_t fb = full_lead0 + static_cast<uint32_t>(ps) * 8u;
+                if (!half) {
+                    mbar_arrive_expect_tx(&c->full[ps], pair_bytes);
+                    mbar_arrive_relaxed_cluster(empty_peer0 + static_cast<uint32_t>(ps) * 8u, 1u);
+                }
+                const int32_t k = kb * kBK;
+                if (b_form == 0)
+                    tma_load_2d_pair(a + a_bytes, mapB, fb, k, by, pol_w);
+                else if (b_form == 1)
+                    tma_load_3d_pair(a + a_bytes, mapB, fb, 0, k, by, pol_w);
+                else   // a ragged N keeps the 2-D map: one copy per 64-column box of the half
+                    for (int32_t j = 0; j < nbox; ++j)
+                        tma_load_2d_pair(a + a_bytes + j * box_bytes, mapB, fb, bx + j * box_cols, k, pol_w);
+                tma_load_2d_pair(a, mapA, fb, k, m0, pol_act);
+                ++issued;
+                if (++ps == num_pipe) {
+                    ps = 0;
+                    pph ^= 1;
+                }
+            }
+        } else if (!kwait_s && (b_kmajor || b_3d || nbox == 1)) {
             // The common case: two copies per k block (three for a gated stage: gate and up
             // weights), the B tile in one copy whatever its layout, no per-k-block mode
             // branches; see role_mma for why that matters.
@@ -676,8 +728,10 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         if (!ok)
             break;
     }
-    if (c->abort_flag) {
-        // Let every copy this thread issued land before the CTA's shared memory goes away.
+    if (c->abort_flag && !half) {
+        // Let every copy this thread issued land before the CTA's shared memory goes away.  A
+        // pair's leader waits for both CTAs' copies: the peer fills only phases the leader armed,
+        // and keeps its shared memory until the kernel's final cluster barrier.
         const uint32_t np = static_cast<uint32_t>(num_pipe);
         for (uint32_t i = 0; i < np; ++i) {
             const uint32_t fills = issued / np + (i < issued % np ? 1u : 0u);
@@ -688,8 +742,25 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
 }
 
 // ------------------------------------------------------------------------------ MMA issuer --
+// With a CTA pair the leader issues every MMA (M = 2 bm rows, its TMEM holding the first bm rows
+// and the peer's the rest), releases its own ring slots (the TMA role forwards them to the peer)
+// and signals both CTAs' accumulator barriers; the peer's MMA thread only walks the item ring.
+template <int kPair>
 __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t *ring, uint32_t tmem_base)
 {
+    constexpr bool kPairMode = kPair == 2;
+    const uint32_t rank = cluster_ctarank();
+    if (kPairMode && (rank & 1u)) {
+        for (int32_t it = 0;; ++it) {
+            const int32_t slot = it % kSchedDepth;
+            if (!wait_bar(&c->sfull[slot], (it / kSchedDepth) & 1, c, p, true, true))
+                return;
+            if (take_item(c, slot).stage < 0)
+                return;
+        }
+    }
+    // the peer's accumulator barriers (shared::cluster), for the leader's second commit
+    const uint32_t tfull_peer0 = kPairMode ? map_to_rank(&c->tfull[0], rank | 1u) : 0u;
     const int32_t num_pipe = p.num_pipe;
     const uint32_t stage_bytes = p.stage_bytes;
     const uint32_t acc_stride = static_cast<uint32_t>(p.acc_stride);
@@ -720,14 +791,15 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         slice_range(spr.k_blocks, spr.kb_per_split, item.split, kb0, kb1);
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
-        if (!wait_bar(&c->tempty[acc], acc_ph ^ 1, c, p))
+        // (a pair's accumulator is released by both CTAs' epilogue warps: remote arrivals)
+        if (!wait_bar(&c->tempty[acc], acc_ph ^ 1, c, p, true, kPairMode))
             break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * acc_stride;
         // A gated tile's gate and up weight tiles lie back to back in the slot, laid out exactly
         // like one B tile twice as wide, so one MMA of N = 2 BN fills both accumulators (gate in
         // columns [0, BN), up in [BN, 2 BN)): an MMA costs the same for any N <= 256.
-        const uint32_t idesc = idesc_bf16_f32(static_cast<uint32_t>(bm), gated ? 2u * BN : BN, b_kmajor ? 0u : 1u);
+        const uint32_t idesc = idesc_bf16_f32(static_cast<uint32_t>(kPair * bm), gated ? 2u * BN : BN, b_kmajor ? 0u : 1u);
         const uint32_t b_code = b_swz == 128 ? 2u : (b_swz == 64 ? 4u : 6u);
         bool ok = true;
         if (!lamport && !split2) {
@@ -744,18 +816,19 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             const uint64_t slot16 = stage_bytes >> 4;
             uint32_t accum = 0;
             for (int32_t kb = kb0; kb < kb1; ++kb) {
-                if (!wait_bar(&c->full[ps], pph, c, p)) {
+                // (a pair's fill also completes through the peer's copies: acquire at cluster scope)
+                if (!wait_bar(&c->full[ps], pph, c, p, true, kPairMode)) {
                     ok = false;
                     break;
                 }
                 const uint64_t off = static_cast<uint64_t>(ps) * slot16;
 #pragma unroll
                 for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
-                    mma_bf16_ss(d_tmem, ad0 + off + 2u * kk, bd0 + off + bstep * kk, idesc, accum);
+                    mma_bf16_ss_g<kPair>(d_tmem, ad0 + off + 2u * kk, bd0 + off + bstep * kk, idesc, accum);
                     accum = 1u;   // the slice's first k step overwrites the accumulator
                 }
                 issued = true;
-                mma_commit(&c->empty[ps]);
+                mma_commit_g<kPair>(smem_u32(&c->empty[ps]));
                 if (++ps == num_pipe) {
                     ps = 0;
                     pph ^= 1;
@@ -787,10 +860,10 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
                 const uint32_t j = static_cast<uint32_t>(kb - kb0) * (kBK / 16) + kk;
                 const uint32_t sub = split2 ? (j & 1u) : 0u;
                 const uint32_t accum = j >= (split2 ? 2u : 1u) ? 1u : 0u;
-                mma_bf16_ss(d_tmem + sub * sub_stride, ad, bd, idesc, accum);
+                mma_bf16_ss_g<kPair>(d_tmem + sub * sub_stride, ad, bd, idesc, accum);
             }
             issued = true;
-            mma_commit(&c->empty[ps]);   // frees the ring slot once these MMAs have read it
+            mma_commit_g<kPair>(smem_u32(&c->empty[ps]));   // frees the ring slot once these MMAs have read it
             if (++ps == num_pipe) {
                 ps = 0;
                 pph ^= 1;
@@ -798,11 +871,13 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         }
         if (!ok)
             break;
-        mma_commit(&c->tfull[acc]);     // accumulator ready for the epilogue
+        mma_commit_g<kPair>(smem_u32(&c->tfull[acc]));     // accumulator ready for the epilogue
+        if (kPairMode)                                       // ... of both CTAs of the pair
+            mma_commit_g<kPair>(tfull_peer0 + acc * 8u);
         ++local_tiles;
     }
     if (c->abort_flag && issued) {
-        mma_commit(&c->drain);
+        mma_commit_g<kPair>(smem_u32(&c->drain));
         wait_bar(&c->drain, 0, c, p, false);
     }
 }
@@ -1193,9 +1268,16 @@ __device__ __forceinline__ void publish(const ChainParams &p, Ctrl *c, int32_t s
     release_tile(p, c, s, tile, lane, pl);
 }
 
+// With a CTA pair each CTA stores the rows its TMEM holds (the leader the tile's first bm rows, the
+// peer the rest) and releases them; the accumulator goes back to the leader's MMA thread through
+// the leader's tempty barrier, which counts both CTAs' epilogue warps.
+template <int kPair>
 __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uint32_t tmem_base, uint32_t rank,
                                               uint8_t *staging, uint8_t *recv)
 {
+    constexpr bool kPairMode = kPair == 2;
+    const int32_t half = kPairMode ? static_cast<int32_t>(rank & 1u) : 0;
+    const uint32_t tempty_lead0 = kPairMode ? map_to_rank(&c->tempty[0], rank & ~1u) : 0u;
     const uint32_t recv_u32 = smem_u32(recv);
     const int32_t warp = threadIdx.x / 32;
     const int32_t lane = threadIdx.x & 31;
@@ -1253,7 +1335,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 break;
         }
         const StageParams &spr = p.st[s];
-        const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = spr.split;
+        const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = kPairMode ? 1 : spr.split;
         const bool dsmem = spr.dsmem_reduce != 0;
         float *const partials = spr.partials;
         const bool producer = pipelined && s + 1 < num_stages;
@@ -1263,12 +1345,12 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         ReleasePlan pl{0, -1, 0, 0, 0, -1, -1};
         if (producer && !kwait)
             pl = plan_release(p, s, tile, lane);
-        if (!warp_wait_bar(&c->tfull[acc], acc_ph, c, p))
+        if (!warp_wait_bar(&c->tfull[acc], acc_ph, c, p, kPairMode))   // (a pair's: the leader's commit)
             break;
         tc_fence_after();
         if (logging && warp == 4 && lane == 0 && item.split == 0)
             p.events[p.tile_base[s] + tile].t_acc = globaltimer_ns();
-        const int32_t row0 = (tile / tiles_n) * bm + quad * rpw;   // this warp's first row
+        const int32_t row0 = (tile / tiles_n) * (kPair * bm) + half * bm + quad * rpw;   // this warp's first row
         const int32_t row_lim = min(spr.M, row0 + rpw);
         const int32_t n0 = (tile % tiles_n) * BN;
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * acc_stride;
@@ -1291,13 +1373,17 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&c->tempty[acc]);   // the MMA warp may reuse this accumulator
+            if (lane == 0) {   // the MMA warp may reuse this accumulator
+                if (kPairMode)
+                    mbar_arrive_cluster(tempty_lead0 + acc * 8u);
+                else
+                    mbar_arrive(&c->tempty[acc]);
+            }
             ++local_tiles;
             if (producer || (pipelined && logging)) {
                 if (!lamport)   // this warp's stores, released at gpu scope for the consumers
                     fence_acq_rel_gpu();
-                publish(p, c, s, tile, logging, producer, warp, lane, pl);
+                publish(p, c, s, tile, logging && half == 0, producer, warp, lane, pl);
             }
             continue;
         }
@@ -1455,6 +1541,10 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
 }
 
 // ------------------------------------------------------------------------------ the kernel --
+// kPair = 1: one CTA per tile (tcgen05 cta_group::1).  kPair = 2: clusters of CTA pairs, each pair
+// computing 2 bm-row tiles with cta_group::2 MMAs (every tcgen05 allocation, MMA and commit of a
+// kernel uses one CTA group, hence two instantiations).
+template <int kPair>
 __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ ChainParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1480,7 +1570,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&c->tfull[i], 1);
-            mbar_init(&c->tempty[i], 4);
+            mbar_init(&c->tempty[i], 4 * kPair);   // a pair's: both CTAs' epilogue warps
         }
         for (int i = 0; i < kSchedDepth; ++i) {
             mbar_init(&c->sfull[i], 1);
@@ -1517,8 +1607,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             prefetch_tensormap(&p.mapU);
     }
     if (warp == 1) {
-        tmem_alloc(&c->tmem_base, p.tmem_cols);
-        tmem_relinquish();
+        tmem_alloc_g<kPair>(&c->tmem_base, p.tmem_cols);   // with a pair: one warp in each CTA, together
+        tmem_relinquish_g<kPair>();
     }
     tc_fence_before();
     cluster_sync_all();   // every barrier of the cluster is initialised before any remote arrive
@@ -1532,10 +1622,10 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     if (!c->skip) {
         if (warp == 0) {
             if (lane == 0)
-                role_tma(p, c, ring, rank == 0);
+                role_tma<kPair>(p, c, ring, rank == 0);
         } else if (warp == 1) {
             if (lane == 0)
-                role_mma(p, c, ring, tmem_base);
+                role_mma<kPair>(p, c, ring, tmem_base);
             __syncwarp();
         } else if (warp == 2) {
             if (lane == 0 && rank == 0)
@@ -1558,15 +1648,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             if (p.pipelined && p.lamport)
                 role_validate(p, c, ring);
         } else if (warp >= 4) {
-            role_epilogue(p, c, tmem_base, rank, ring + staging_offset(p.num_pipe, p.stage_bytes),
+            role_epilogue<kPair>(p, c, tmem_base, rank, ring + staging_offset(p.num_pipe, p.stage_bytes),
                           ring + recv_offset(p.num_pipe, p.stage_bytes));
         }
     }
     tc_fence_before();
-    __syncthreads();
+    // A pair frees its TMEM together, and only once the leader's MMAs (which write the peer's
+    // TMEM) and both CTAs' epilogues are done.
+    if constexpr (kPair == 2)
+        cluster_sync_all();
+    else
+        __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, p.tmem_cols);
+        tmem_dealloc_g<kPair>(tmem_base, p.tmem_cols);
     }
     // Nothing is reset for the next run: scoreboard counters, the ticket, the queue tails and the
     // launch counter all accumulate over runs (protocol.h), and queue slots carry the run's epoch.

@@ -119,7 +119,8 @@ __global__ void fill_sentinel_kernel(uint4 *p, size_t n16)
 struct mlp_chain {
     mlp_chain_desc desc{};
     int device = 0, num_sms = 0, S = 0;
-    int bm = mlpc::kBM;      // rows per tile: 128, or 64 (tcgen05 M = 64)
+    int bm = mlpc::kBM;      // rows per CTA's tile: 128, or 64 (tcgen05 M = 64)
+    int pair = 1;            // 2: CTA pairs, each tile pair x bm rows (chain_kernel<2>)
     int BN[MLP_MAX_GEMMS] = {}, tiles_m = 0, tiles_n[MLP_MAX_GEMMS] = {}, k_blocks[MLP_MAX_GEMMS] = {};
     int b_swz[MLP_MAX_GEMMS] = {};
     int num_pipe = 0, max_bn = 0, grid = 0, acc_split = 1;
@@ -219,6 +220,13 @@ static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const 
     return best;
 }
 
+// Scoreboard releases one producer tile of stage b makes per run: one per epilogue warp of each
+// split-K slice, or of each CTA of a pair.
+static int releases_per_tile(const mlp_chain *h, int b)
+{
+    return (h->pair == 2 ? 2 : h->split[b]) * mlpc::kEpiWarps;
+}
+
 static mlp_status full_reset(mlp_chain *h)
 {
     if (cudaSetDevice(h->device) != cudaSuccess)
@@ -278,8 +286,22 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         d->mode != MLP_MODE_SEQUENTIAL_PDL)
         return MLP_ERR_INVALID_ARG;
     const int bm = d->tile_m == 64 ? 64 : mlpc::kBM;
-    if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < bm || d->microbatch_rows % bm))
+    if (d->cta_pair < 0 || d->cta_pair > 2)
         return MLP_ERR_INVALID_ARG;
+    // CTA pairs run plain stages: no gating, split-K, split accumulators, 64-row tiles, or the
+    // K-granular and Lamport modes; tiles 128 or 256 wide (64 or 128 columns per CTA)
+    bool pair_ok = !d->gated && d->acc_split != 2 && d->tile_m != 64 && d->mode != MLP_MODE_PIPELINED_KWAIT &&
+                   d->mode != MLP_MODE_PIPELINED_LAMPORT;
+    for (int s = 0; s < S && pair_ok; ++s)
+        pair_ok = (d->k_split[s] == 0 || d->k_split[s] == 1) &&
+                  (d->tile_n[s] == 0 || d->tile_n[s] == 128 || d->tile_n[s] == 256);
+    if (d->cta_pair == 2 && !pair_ok)
+        return MLP_ERR_UNSUPPORTED;
+    if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < bm || d->microbatch_rows % bm ||
+                                           (d->cta_pair == 2 && d->microbatch_rows % (2 * bm))))
+        return MLP_ERR_INVALID_ARG;
+    // the library chooses pairs only where micro-batch chunks hold whole pair tiles
+    pair_ok = pair_ok && (d->mode != MLP_MODE_MICROBATCH || d->microbatch_rows % (2 * bm) == 0);
     if (d->gated && (d->acc_split == 2 || (d->tile_n[0] != 0 && d->tile_n[0] > 128) ||
                      (d->k_split[0] != 0 && d->k_split[0] != 1)))
         return MLP_ERR_UNSUPPORTED;   // the gated GEMM keeps gate and up side by side in TMEM, unsplit
@@ -310,10 +332,12 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     }
 
     h->bm = bm;
-    h->tiles_m = static_cast<int>((d->M + bm - 1) / bm);
+    h->tiles_m = static_cast<int>((d->M + bm - 1) / bm);   // single-CTA tiles; pairs are decided below
     // The device maximum, so that handles with different ring depths can share the kernel.
-    if (cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
-        cudaSuccess) {
+    if (cudaFuncSetAttribute(mlpc::chain_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(mlpc::chain_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) !=
+            cudaSuccess) {
         release(h);
         return MLP_ERR_CUDA;
     }
@@ -331,7 +355,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         cfg.dynamicSmemBytes = static_cast<size_t>(smem_optin);
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&clusters[li], mlpc::chain_kernel, &cfg) != cudaSuccess)
+        if (cudaOccupancyMaxActiveClusters(&clusters[li], mlpc::chain_kernel<1>, &cfg) != cudaSuccess)
             clusters[li] = 0;
     }
     cudaGetLastError();
@@ -348,7 +372,10 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         const bool gate_s = d->gated && s == 0;
         const int tn_s = gate_s && tn == 0 ? 128 : tn;
         const int ks_s = gate_s ? 1 : ks;
-        if (choose_tiles(h->tiles_m, bm, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn, &split) >= 1e29) {
+        if (d->cta_pair == 2) {   // a pair tile is 256 rows; 256 wide unless the output is narrow
+            bn = tn ? tn : (d->dims[s + 1] > 128 ? 256 : 128);
+            split = 1;
+        } else if (choose_tiles(h->tiles_m, bm, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn, &split) >= 1e29) {
             release(h);
             return MLP_ERR_UNSUPPORTED;   // no valid tile / split for this request
         }
@@ -361,13 +388,40 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->kb_per_split[s] = (h->k_blocks[s] + split - 1) / split;
         h->cs = std::max(h->cs, split);
     }
+    // CTA pairs: on request, or by default where every stage came out unsplit and 128 or 256 wide
+    // with at least four 128-row panels (pairs measured faster there: prefill -9 %, the GeLU chain
+    // -12 %); fewer rows would leave pair halves empty.
+    bool pair_auto = d->cta_pair == 0 && pair_ok && h->tiles_m >= 4;
+    for (int s = 0; s < S && pair_auto; ++s)
+        pair_auto = h->split[s] == 1 && (h->BN[s] == 128 || h->BN[s] == 256);
+    const int pair = (d->cta_pair == 2 || pair_auto) ? 2 : 1;
+    const int tile_rows = pair * bm;
+    h->pair = pair;
+    if (pair == 2) {
+        h->cs = 2;
+        h->tiles_m = static_cast<int>((d->M + tile_rows - 1) / tile_rows);
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(16, 1, 1);
+        cfg.blockDim = dim3(mlpc::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem_optin);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters[1], mlpc::chain_kernel<2>, &cfg) != cudaSuccess)
+            clusters[1] = 0;
+        cudaGetLastError();
+    }
     for (int s = 0; s < S; ++s) {
-        const int tpi = h->cs / h->split[s];
+        const int tpi = pair == 2 ? 1 : h->cs / h->split[s];
         const int tiles = h->tiles_m * h->tiles_n[s];
         h->items[s] = (tiles + tpi - 1) / tpi;
     }
     const uint32_t a_bytes = static_cast<uint32_t>(bm * mlpc::kBK * 2);
-    h->stage_bytes = a_bytes + static_cast<uint32_t>(mlpc::kBK * h->max_bn * 2);
+    h->stage_bytes = a_bytes + static_cast<uint32_t>(mlpc::kBK * (h->max_bn / pair) * 2);   // a pair's CTA: half of B
     if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles
         h->stage_bytes = std::max(h->stage_bytes, a_bytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
     h->n_w = S + (d->gated ? 1 : 0);
@@ -424,7 +478,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     // dependency arrays (host), then one device block for all library-owned state
     size_t bytes = 8 * sizeof(uint32_t);
     for (int b = 0; b + 1 < S; ++b) {
-        const int64_t nnz = mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], bm, h->BN[b], bm,
+        const int64_t nnz = mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], tile_rows, h->BN[b], tile_rows,
                                            h->BN[b + 1], nullptr, nullptr, 0, nullptr);
         if (nnz < 0) {
             release(h);
@@ -433,7 +487,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->off[b].resize(static_cast<size_t>(h->tiles_m) * h->tiles_n[b] + 1);
         h->tgt[b].resize(static_cast<size_t>(std::max<int64_t>(nnz, 1)));
         h->init[b].resize(static_cast<size_t>(h->tiles_m) * h->tiles_n[b + 1]);
-        mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], bm, h->BN[b], bm, h->BN[b + 1],
+        mlp_deps_build(d->M, d->dims[b + 1], d->dims[b + 2], tile_rows, h->BN[b], tile_rows, h->BN[b + 1],
                        h->off[b].data(), h->tgt[b].data(), nnz, h->init[b].data());
         h->tgt[b].resize(static_cast<size_t>(nnz));
         // The first stage's raster walks groups of rg row panels column by column, so those
@@ -508,10 +562,11 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         up(db.grp_off, G.grp_off);
         up(db.grp_mem, G.grp_mem);
         up(db.cgrp, G.cons_grp);
-        // A producer tile is released by each epilogue warp of each of its S split-K slices.
+        // A producer tile is released by each epilogue warp of each of its S split-K slices (or of
+        // each CTA of its pair).
         std::vector<int32_t> releases(G.grp_init);
         for (int32_t &v : releases)
-            v *= h->split[b] * mlpc::kEpiWarps;
+            v *= releases_per_tile(h, b);
         up(db.grp_init, releases);
     }
     h->meta_bytes = o;
@@ -532,7 +587,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_CUDA;
     }
     if (d->mode == MLP_MODE_MICROBATCH) {
-        const int rows_tiles = d->microbatch_rows / bm;
+        const int rows_tiles = d->microbatch_rows / tile_rows;   // chunk rows in (pair) tiles
         h->chunk_tiles = rows_tiles;
         h->n_chunks = (h->tiles_m + rows_tiles - 1) / rows_tiles;
         h->events.assign(static_cast<size_t>(h->n_chunks) * S, nullptr);
@@ -590,9 +645,10 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         int32_t b_3d = 0, u_3d = 0;
         auto encode_w = [&](CUtensorMap *m, const void *w, int32_t *is_3d) {
             *is_3d = 0;
+            const int bn_cta = h->BN[s] / h->pair;   // the columns one CTA loads
             return d.weight_layout == 1
-                       ? encode_2d(m, w, d.dims[s + 1], d.dims[s], h->BN[s], mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B)
-                       : encode_w_kn(m, w, d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s], h->BN[s], is_3d);
+                       ? encode_2d(m, w, d.dims[s + 1], d.dims[s], bn_cta, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : encode_w_kn(m, w, d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s], bn_cta, is_3d);
         };
         const bool gate_s = d.gated && s == 0;
         if (!encode_w(&P.mapB[s], W[s == 0 ? 0 : s + (d.gated ? 1 : 0)], &b_3d) ||
@@ -615,9 +671,10 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.k_blocks = h->k_blocks[s];
         sp.b_swz = h->b_swz[s];
         sp.b_kmajor = d.weight_layout == 1;
-        sp.split = h->split[s];
-        sp.kb_per_split = h->kb_per_split[s];
-        sp.tiles_per_item = h->cs / h->split[s];
+        // a pair's two CTAs take the same tile (rank r: half r % 2) over the whole k range
+        sp.split = h->pair == 2 ? 2 : h->split[s];
+        sp.kb_per_split = h->pair == 2 ? h->k_blocks[s] : h->kb_per_split[s];
+        sp.tiles_per_item = h->pair == 2 ? 1 : h->cs / h->split[s];
         sp.items = h->items[s];
         sp.partials = h->partials[s];
         sp.dsmem_reduce = h->split[s] > 1 && h->recv_bytes && static_cast<uint32_t>(h->BN[s] * h->bm * 4) <= h->recv_bytes;
@@ -639,7 +696,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.bd[b].tail = h->db[b].tail;
         P.bd[b].slots_per_run = static_cast<uint32_t>(h->db[b].consumers);
         P.bd[b].ready = h->db[b].ready;
-        P.bd[b].ready_quota = static_cast<uint32_t>(h->split[b] * mlpc::kEpiWarps);
+        P.bd[b].ready_quota = static_cast<uint32_t>(releases_per_tile(h, b));
     }
     P.num_stages = h->S;
     for (int s = 0; s <= h->S; ++s) {
@@ -649,6 +706,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     P.cs = h->cs;
     P.partial_floats = h->bm * h->max_bn;
     P.bm = h->bm;
+    P.pair = h->pair;
     P.a_bytes = static_cast<uint32_t>(h->bm * mlpc::kBK * 2);
     P.recv_bytes = h->recv_bytes;
     // Grouped first-stage raster: a weight column slab is reused from L2 by the panels of a group
@@ -682,7 +740,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
 static bool launch(const ChainParams &P, int grid, size_t smem, cudaStream_t st)
 {
     if (P.cs == 1 && !P.pdl_wait) {
-        mlpc::chain_kernel<<<grid, mlpc::kThreads, smem, st>>>(P);
+        mlpc::chain_kernel<1><<<grid, mlpc::kThreads, smem, st>>>(P);
         return cudaGetLastError() == cudaSuccess;
     }
     cudaLaunchConfig_t cfg = {};
@@ -706,7 +764,8 @@ static bool launch(const ChainParams &P, int grid, size_t smem, cudaStream_t st)
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, mlpc::chain_kernel, P) == cudaSuccess && cudaGetLastError() == cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, P.pair == 2 ? mlpc::chain_kernel<2> : mlpc::chain_kernel<1>, P) == cudaSuccess &&
+           cudaGetLastError() == cudaSuccess;
 }
 
 // CTAs of a non-pipelined launch over `items` cluster items.
@@ -871,7 +930,7 @@ extern "C" mlp_status mlp_chain_get_scoreboard(mlp_chain_t h, int32_t b, mlp_sco
     sb->consumers = static_cast<int32_t>(db.consumers);
     sb->groups = static_cast<int32_t>(db.groups);
     sb->edges = static_cast<int32_t>(G.pg_tgt.size());
-    sb->releases_per_producer = h->split[b] * mlpc::kEpiWarps;
+    sb->releases_per_producer = releases_per_tile(h, b);
     if (!sb->pg_off || !sb->pg_tgt || !sb->grp_off || !sb->grp_mem || !sb->grp_target || !sb->cons_grp)
         return MLP_OK;
     // the tables as the kernel reads them: copied back from the device block
@@ -906,7 +965,8 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
         return MLP_ERR_INVALID_ARG;
     std::memset(info, 0, sizeof(*info));
     info->num_gemms = h->S;
-    info->tile_m = h->bm;
+    info->tile_m = h->bm * h->pair;
+    info->cta_pair = h->pair;
     info->tile_k = mlpc::kBK;
     for (int s = 0; s < h->S; ++s) {
         info->tile_n[s] = h->BN[s];
@@ -1063,7 +1123,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     void *scratch_ptr = nullptr;
     if (cudaGetSymbolAddress(&scratch_ptr, g_noalloc_scratch) != cudaSuccess || !scratch_ptr ||
         cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(mlpc::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
+        cudaFuncSetAttribute(mlpc::chain_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
         return MLP_ERR_CUDA;
 
     // Tiling: the same choices mlp_chain_create makes for this shape.
@@ -1138,6 +1198,7 @@ extern "C" mlp_status mlp_chain_run_noalloc(int64_t M, int64_t K, int64_t N1, in
     P_.cs = 1;
     P_.partial_floats = mlpc::kBM * max_bn;
     P_.bm = mlpc::kBM;
+    P_.pair = 1;
     P_.a_bytes = mlpc::kABytes;
     P_.num_pipe = num_pipe;
     P_.stage_bytes = stage_bytes;

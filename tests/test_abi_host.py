@@ -141,6 +141,15 @@ def _desc(**kw):
     ({"gated": 1, "acc_split": 2}, mc.ERR_UNSUPPORTED),
     ({"gated": 1, "k_split": (2, 0)}, mc.ERR_UNSUPPORTED),
     ({"gated": 1, "tile_n": (256, 0)}, mc.ERR_UNSUPPORTED),
+    # CTA pairs run plain stages only: not gated, split, K-granular or Lamport, 128 or 256 wide
+    ({"cta_pair": 3}, mc.ERR_INVALID_ARG),
+    ({"cta_pair": 2, "gated": 1}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "k_split": (2, 0)}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "mode": 3}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "mode": 4}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "tile_n": (64, 0)}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "tile_m": 64}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "mode": 2, "microbatch_rows": 128}, mc.ERR_INVALID_ARG),   # chunks of 256 rows
 ])
 def test_create_rejects_bad_descriptors_before_touching_cuda(lib, kw, expect):
     h = ctypes.c_void_p()

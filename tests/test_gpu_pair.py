@@ -1,0 +1,127 @@
+"""GPU parity of CTA-pair tiles (tcgen05 cta_group::2, `cta_pair=2`) through the C ABI.
+
+A pair computes a 256-row tile: each CTA loads its 128 rows of the activations and half of the
+weight tile's columns, the leader issues every MMA and each CTA's TMEM holds its 128 rows.  Bar:
+within |d| <= 1e-2 (|ref| + 1) of the oracle; bit-exact on integer-valued inputs; bit-identical
+to single-CTA tiles of the same width (the same 16-deep dot products in the same order) and
+across launch modes; the scoreboard equals the one rebuilt from the oracle's enumeration at
+256-row tiles, and the event log shows every dependency respected.
+"""
+import numpy as np
+import pytest
+import torch
+
+import seeded_inputs as si
+from test_gpu_chain import DEV, assert_close_to_oracle, bits, run_chain
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mc():
+    import mlp_latency_gb300
+    mlp_latency_gb300.build()
+    mlp_latency_gb300.load()
+    return mlp_latency_gb300
+
+
+def same(a, b):
+    return torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,dims,tn", [
+    (256, (512, 512, 256), [256, 256]),       # one pair tile per column
+    (300, (320, 264, 520), [256, 128]),       # the second pair tile: 44 rows, the peer's half all past M
+    (640, (1024, 768, 384), [128, 256]),      # 3 pair-row panels, 128-wide tiles (64 columns per CTA)
+    (129, (64, 128, 64), [128, 128]),         # one row past the leader's half; narrow outputs
+])
+def test_pairs_match_oracle_and_single_cta_tiles(mc, oracle_mod, M, dims, tn):
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=41)
+    Yp, Hp, info = run_chain(mc, X, Ws, tile_n=tn, cta_pair=2)
+    assert info["cta_pair"] == 2 and info["tile_m"] == 256 and info["cluster_size"] == 2
+    assert info["tiles_m"][0] == -(-M // 256)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(Hp, Ho)
+    assert_close_to_oracle(Yp, Yo)
+    Ys, _, _ = run_chain(mc, X, Ws, tile_n=tn, k_split=[1, 1])
+    assert same(Yp, Ys)
+
+
+def test_pairs_integer_inputs_are_bit_exact(mc, oracle_mod):
+    X, Ws = si.draw_integer(300, (1024, 1024, 512), seed=42)
+    Y, H, _ = run_chain(mc, X, Ws, tile_n=[256, 256], cta_pair=2)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert np.array_equal(bits(H), Ho)
+    assert np.array_equal(bits(Y), Yo)
+
+
+@pytest.mark.parametrize("M,dims,tn", [(1024, (512, 1024, 512), [256, 256]), (600, (256, 384, 256), [128, 256])])
+def test_pair_modes_are_bit_identical(mc, M, dims, tn):
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=43)
+    kw = dict(tile_n=tn, cta_pair=2)
+    Yp, _, _ = run_chain(mc, X, Ws, **kw)
+    for mode in ("sequential", "sequential_pdl"):
+        Y, _, _ = run_chain(mc, X, Ws, mode=mode, **kw)
+        assert same(Yp, Y), mode
+    for rows in (256, 512):
+        if rows < M:
+            Y, _, info = run_chain(mc, X, Ws, mode="microbatch", microbatch_rows=rows, **kw)
+            assert info["launches_per_run"] == 2 * -(-M // rows)
+            assert same(Yp, Y), rows
+
+
+def test_pairs_gelu_residual_four_gemm_chain(mc, oracle_mod):
+    M, dims = 700, (256, 512, 384, 256, 256)
+    X, Ws = si.draw(si.make_workload("t", M, dims, gelu=True, residual=True), seed=44)
+    Y, _, _ = run_chain(mc, X, Ws, gelu=True, residual=True, cta_pair=2)
+    assert_close_to_oracle(Y, oracle_mod.chain(bits(X), [bits(t) for t in Ws], gelu=True, residual=True))
+    Ys, _, _ = run_chain(mc, X, Ws, gelu=True, residual=True, mode="sequential", cta_pair=2)
+    assert same(Y, Ys)
+
+
+@pytest.mark.parametrize("M,rg", [(1280, 0), (4352, 0), (2304, 3)])
+def test_pair_scoreboard_and_event_log(mc, oracle_mod, M, rg):
+    import expected_scoreboard as es
+    dims, tn = (256, 512, 256), [256, 128]
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=45)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=tn, event_log=True, raster_group=rg, cta_pair=2) as ch:
+        info = ch.info()
+        tm = info["tiles_m"][0]
+        g = rg if rg else (8 if tm >= 16 else (4 if tm >= 8 else 1))
+        es.assert_equal(ch.scoreboard(0), es.expected(oracle_mod, M, dims[1], dims[2], 256, tn[0], tn[1], g, 8))
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        for _ in range(2):
+            ch.run(Xd, Wd, Y, ws)
+            assert ch.check() == 0
+            ev = ch.event_log()
+            off, tgt, _ = ch.deps(0)
+            p_end = {int(e["tile"]): int(e["seq_end"]) for e in ev if e["stage"] == 0}
+            c_start = {int(e["tile"]): int(e["seq_start"]) for e in ev if e["stage"] == 1}
+            assert len(p_end) == tm * info["tiles_n"][0] and len(c_start) == tm * info["tiles_n"][1]
+            for p in range(len(off) - 1):
+                for c in tgt[off[p]:off[p + 1]]:
+                    assert p_end[p] < c_start[int(c)]
+    assert_close_to_oracle(Y.cpu(), oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
+
+
+def test_pairs_many_runs_and_nk_weights(mc, oracle_mod):
+    M, dims = 1100, (512, 768, 512)
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=46)
+    outs, _, _ = run_chain(mc, X, Ws, reps=20, cta_pair=2)
+    for o in outs[1:]:
+        assert same(o, outs[0])
+    Wt = [w.t().contiguous() for w in Ws]   # nn.Linear layout: N x K
+    Yt, _, _ = run_chain(mc, X, Wt, weight_layout="nk", cta_pair=2)
+    assert same(Yt, outs[0])
+    assert_close_to_oracle(outs[0], oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
+
+
+def test_prefill_workload_on_pairs_sampled(mc, oracle_mod):
+    w = si.WORKLOADS["prefill_m2048_d8192"]
+    X, Ws = si.draw(w, seed=0)
+    Y, _, info = run_chain(mc, X, Ws, cta_pair=2)
+    assert info["tile_n"] == [256, 256] and info["cta_pair"] == 2
+    rows = si.sample_rows(w.M, 24, seed=6)
+    assert_close_to_oracle(Y[rows], oracle_mod.chain(bits(X), [bits(t) for t in Ws], rows=rows))
