@@ -354,17 +354,20 @@ def test_split_k_dropped_decrement_times_out_then_recovers(mc):
     (300, (256, 384, 512), [64, 128], [1, 1], 1),            # ragged, unmerged
     (512, (512, 512, 512, 512, 512), [128, 128, 128, 128], [1, 1, 1, 1], 0),   # 3 boundaries
 ])
-def test_device_scoreboard_matches_oracle_enumeration(mc, oracle_mod, M, dims, tn, ks, rg):
+@pytest.mark.parametrize("cp", [1, 0])   # one CTA per tile, and the library's choice (pairs where they apply)
+def test_device_scoreboard_matches_oracle_enumeration(mc, oracle_mod, M, dims, tn, ks, rg, cp):
     """The counters' tables as the kernel reads them (copied back from the device) equal the ones
     rebuilt from the oracle's brute-force enumeration, bit for bit, for every stage boundary."""
     import expected_scoreboard as es
-    with mc.Chain(M, dims, tile_n=tn, k_split=ks, raster_group=rg) as ch:
+    with mc.Chain(M, dims, tile_n=tn, k_split=ks, raster_group=rg, cta_pair=cp) as ch:
         info = ch.info()
         tiles_m = info["tiles_m"][0]
         g = rg if rg else (8 if tiles_m >= 16 else (4 if tiles_m >= 8 else 1))
         for b in range(len(dims) - 2):
+            # releases per producer tile: each epilogue warp of each split-K slice, or of each CTA of a pair
+            rel = (2 if info["cta_pair"] == 2 else info["k_split"][b]) * 4
             want = es.expected(oracle_mod, M, dims[b + 1], dims[b + 2], info["tile_m"], info["tile_n"][b],
-                               info["tile_n"][b + 1], g, info["k_split"][b] * 4)
+                               info["tile_n"][b + 1], g, rel)
             es.assert_equal(ch.scoreboard(b), want)
 
 
