@@ -375,12 +375,15 @@ def run_sweep(args):
         line = {"sweep": "sequence length", "M": M, "dims": [d, d, d], "flops": w.flops,
                 "l2": "flushed between steps", "graph": "one CUDA graph replay per step"}
 
-        def timed(mode, rows=0):
+        def timed(mode, rows=0, cta_pair=0):
             nonlocal ref, tiles
             kw = dict(tile_m=64, tile_n=tiles[0], k_split=tiles[1]) if rows % 128 else {}
+            if cta_pair:
+                kw["cta_pair"] = cta_pair
             with mc.Chain(M, w.dims, mode=mode, microbatch_rows=rows, device=local, **kw) as ch:
                 if tiles is None:
                     tiles = (ch.info()["tile_n"], ch.info()["k_split"])
+                    line["cta_pair"] = ch.info()["cta_pair"]   # the library's choice for this M
                 ws = torch.empty(max(ch.workspace_size(), 256), dtype=torch.uint8, device=dev)
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.stream(stream):
@@ -411,10 +414,11 @@ def run_sweep(args):
         best = None
         rows = 64
         while rows <= M // 2:
-            t = timed("microbatch", rows)
-            line[f"microbatch_{rows}_us"] = t
-            if best is None or t < best[1]:
-                best = (rows, t)
+            for cp in ([0, 2] if rows % 256 == 0 and line["cta_pair"] == 2 else [0]):
+                t = timed("microbatch", rows, cp)
+                line[f"microbatch_{rows}{'_pair' if cp else ''}_us"] = t
+                if best is None or t < best[1]:
+                    best = (rows, t)
             rows *= 2
         line["microbatch_best_us"] = best[1] if best else None
         line["microbatch_best_rows"] = best[0] if best else None
@@ -562,22 +566,29 @@ def main():
                     flush(); g.replay()
                 baselines[f"{mode}_us"] = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
                 ch.close()
+            # Best-tuned micro-batching: every chunk size from 64 rows (64-row tiles below 128), each
+            # on one-CTA tiles and, where the chunk holds whole 256-row tiles, on CTA pairs too.
             best = None
-            rows = 64   # chunks of 64 rows run 64-row tiles (tcgen05 M = 64)
+            rows = 64
             while rows <= w.M // 2:
-                ch = make("microbatch", rows, tile_m=64 if rows % 128 else 0,
-                          cta_pair=args.cta_pair if rows % 256 == 0 else 0)   # pairs need 256-row chunks
-                g = capture(lambda ch=ch: ch.run(Xd, Wd, Y, ws, stream=stream))
-                for _ in range(args.warmup):
-                    flush(); g.replay()
-                t = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
-                baselines[f"microbatch_{rows}_us"] = t
-                if best is None or t < best[1]:
-                    best = (rows, t)
-                ch.close()
+                kinds = [1, 2] if rows % 256 == 0 else [1]
+                for cp in kinds:
+                    try:
+                        ch = make("microbatch", rows, tile_m=64 if rows % 128 else 0, cta_pair=cp)
+                    except mc.MlpChainError:   # a shape pairs cannot run (gating, split-K)
+                        continue
+                    g = capture(lambda ch=ch: ch.run(Xd, Wd, Y, ws, stream=stream))
+                    for _ in range(args.warmup):
+                        flush(); g.replay()
+                    t = statistics.median(time_steps(g.replay, flush, k_base, stream)) * 1e3
+                    baselines[f"microbatch_{rows}{'_pair' if cp == 2 else ''}_us"] = t
+                    if best is None or t < best[1]:
+                        best = (rows, t, cp)
+                    ch.close()
                 rows *= 2
             baselines["microbatch_best_us"] = best[1] if best else None
             baselines["microbatch_best_rows"] = best[0] if best else None
+            baselines["microbatch_best_cta_pair"] = best[2] if best else None
             if not w.gelu and not w.residual:
                 Wd_kn = [t.t() for t in Wd] if args.weight_layout == "nk" else Wd
 
