@@ -443,6 +443,8 @@ def main():
     ap.add_argument("--acc-split", type=int, default=0)
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="0: library choice, 1: one CTA per tile, 2: CTA pairs (256-row tiles, tcgen05 cta_group::2)")
+    ap.add_argument("--splitk-exchange", default="global", choices=["global", "dsmem"],
+                    help="how split-K siblings add partial sums: through L2, or the owners' shared memory")
     ap.add_argument("--weight-layout", default="kn", choices=["kn", "nk"],
                     help="nk: weights stored transposed (nn.Linear layout)")
     ap.add_argument("--no-baselines", action="store_true", help="skip sequential/micro-batch/cuBLAS lines")
@@ -494,7 +496,7 @@ def main():
                         microbatch_rows=rows, device=local, raster_group=args.raster_group,
                         pipe_stages=args.pipe_stages, acc_split=args.acc_split,
                         weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated,
-                        cta_pair=kw.pop("cta_pair", args.cta_pair), **kw)
+                        cta_pair=kw.pop("cta_pair", args.cta_pair), splitk_exchange=args.splitk_exchange, **kw)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()
@@ -665,7 +667,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
                        "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": info["tile_m"], "tile_n": info["tile_n"],
-                       "k_split": info["k_split"], "cluster_size": info["cluster_size"], "cta_pair": info["cta_pair"],
+                       "k_split": info["k_split"], "cluster_size": info["cluster_size"], "cta_pair": info["cta_pair"], "splitk_exchange": args.splitk_exchange,
                        "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",
                        "l2": f"flushed between steps (write of {2 * l2 >> 20} MiB, outside the timed events)",

@@ -168,6 +168,15 @@ typedef struct {
                                            split accumulators, not the K-granular or Lamport
                                            modes (else UNSUPPORTED); micro-batch chunks are
                                            multiples of 256 rows                                 */
+    int32_t splitk_exchange;            /* how split-K siblings add their partial sums (k_split
+                                           > 1), always in sibling order, so both give the same
+                                           bits: 0 or 1 = through global memory (each sibling
+                                           writes the parts other siblings own to its fp32
+                                           buffer, keeps its own part in TMEM, and adds the
+                                           others' parts from L2); 2 = through the owners' shared
+                                           memory (distributed shared memory stores into a 64 KB
+                                           receive buffer per CTA, which takes ring depth; needs
+                                           tile_m * tile_n * 4 <= 65536, else UNSUPPORTED)       */
 } mlp_chain_desc;
 
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG), stage by stage, followed by one

@@ -62,6 +62,7 @@ class ChainDesc(ctypes.Structure):
         ("microbatch_rows", i32), ("device", i32), ("debug_flags", u32), ("drop_tile", i32),
         ("timeout_us", u32), ("grid_ctas", i32), ("raster_group", i32), ("pipe_stages", i32),
         ("weight_layout", i32), ("k_split", i32 * MAX_GEMMS), ("acc_split", i32), ("gated", i32), ("cta_pair", i32),
+        ("splitk_exchange", i32),
     ]
 
 

@@ -61,7 +61,8 @@ class Chain:
       "sequential_pdl"     one launch per GEMM, each a programmatic dependent launch of the one before;
       "microbatch"         row chunks of ``microbatch_rows``, GEMMs of different chunks overlapped.
     ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice).  ``cta_pair=2`` runs 256-row
-    tiles on CTA pairs (tcgen05 cta_group::2).  Errors raise MlpChainError with
+    tiles on CTA pairs (tcgen05 cta_group::2).  ``splitk_exchange`` ("global" or "dsmem") is
+    the path split-K siblings add their partial sums through.  Errors raise MlpChainError with
     the library's status.
     """
 
@@ -71,7 +72,7 @@ class Chain:
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
                  weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False,
-                 force_reload: bool = False, cta_pair: int = 0):
+                 force_reload: bool = False, cta_pair: int = 0, splitk_exchange: str = "global"):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -103,6 +104,7 @@ class Chain:
             d.k_split[i] = int(v)
         d.gated = int(bool(gated))
         d.cta_pair = int(cta_pair)
+        d.splitk_exchange = {"global": 1, "dsmem": 2}[splitk_exchange]
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
         self.n_weights = len(self.dims) - 1 + int(bool(gated))
         self._lib = lib

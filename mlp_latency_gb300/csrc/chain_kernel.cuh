@@ -1459,13 +1459,20 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, pl);
             continue;
         }
-        // Partial layout: [BN/32 chunks][8 vectors][128 rows][4 floats]: for a fixed vector the
-        // warp's 32 lanes (rows) touch 512 contiguous bytes, so stores and loads coalesce.
+        // Through global memory.  Partial layout: [BN/32 chunks][8 vectors][bm rows][4 floats]:
+        // for a fixed vector the warp's lanes (rows) touch 512 contiguous bytes, so stores and
+        // loads coalesce.  Only the chunks other siblings own are written; my own column slice
+        // stays in TMEM until I have added the S parts, so the accumulator is handed back to the
+        // MMA warp after the reduction.
         float *mine = partials + (cbase + rank) * partial_floats;
+        const int32_t slice = BN / S;
+        const int32_t col0 = item.split * slice;
         // my previous partial must have been read by every sibling of that tile
         if (nsplit > 0 && !warp_wait_bar(&c->done_bar, (nsplit - 1) & 1, c, p, true))
             break;
         for (int32_t c0 = 0; c0 < BN; c0 += 32) {
+            if (c0 >= col0 && c0 < col0 + slice)
+                continue;
             uint32_t r[32];
             load_acc(split2, sub_stride, taddr + c0, r);
             float4 *dst = reinterpret_cast<float4 *>(mine) + (c0 / 32) * 8 * bm + row;
@@ -1475,11 +1482,6 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                     dst[v * bm] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&c->tempty[acc]);
-        ++local_tiles;
         fence_acq_rel_cluster();
         __syncwarp();
         if (lane == 0)
@@ -1487,11 +1489,11 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 arrive_rank_relaxed(&c->red_bar, g0 + q, weight);
         if (!warp_wait_bar(&c->red_bar, nsplit & 1, c, p, true))
             break;
-        // Reduce my column slice over the S partials in rank order, then the epilogue.  Loads of
-        // two partials are issued before either is added.
-        const int32_t slice = BN / S;
-        const int32_t col0 = item.split * slice;
+        // Reduce my column slice over the S partials in sibling order (mine from TMEM), then the
+        // epilogue.  Loads of two partials are issued before either is added.
         for (int32_t c0 = col0; c0 < col0 + slice; c0 += 32) {
+            uint32_t own[32];
+            load_acc(split2, sub_stride, taddr + c0, own);
             float acc_v[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -1501,7 +1503,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 float4 v[2][8];
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq)
-                    if (qb + qq < S) {
+                    if (qb + qq < S && qb + qq != item.split) {
                         const float4 *src =
                             reinterpret_cast<const float4 *>(partials + (cbase + g0 + qb + qq) * partial_floats) + off;
 #pragma unroll
@@ -1509,8 +1511,14 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                             v[qq][i] = __ldcg(src + i * bm);
                     }
 #pragma unroll
-                for (int qq = 0; qq < 2; ++qq)
-                    if (qb + qq < S) {
+                for (int qq = 0; qq < 2; ++qq) {
+                    if (qb + qq >= S)
+                        continue;
+                    if (qb + qq == item.split) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            acc_v[e] += __uint_as_float(own[e]);
+                    } else {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             acc_v[4 * i] += v[qq][i].x;
@@ -1519,6 +1527,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                             acc_v[4 * i + 3] += v[qq][i].w;
                         }
                     }
+                }
             }
             uint32_t r[32];
 #pragma unroll
@@ -1526,6 +1535,11 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 r[e] = __float_as_uint(acc_v[e]);
             store_chunk_warp(od, row0, row_lim, n0 + c0, r, stage, lane);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0)   // the MMA warp may reuse this accumulator
+            mbar_arrive(&c->tempty[acc]);
+        ++local_tiles;
         if (lamport)
             fence_acq_rel_cluster();
         else                   // the slice stores, released at gpu scope for the consumers

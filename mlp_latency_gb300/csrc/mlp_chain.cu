@@ -309,7 +309,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_UNSUPPORTED;   // the gated GEMM keeps gate and up side by side in TMEM, unsplit
     if (d->grid_ctas < 0 || d->raster_group < 0 || d->pipe_stages < 0 || d->pipe_stages == 1 ||
         d->pipe_stages > mlpc::kMaxPipe || d->acc_split < 0 || d->acc_split > 2 || d->weight_layout < 0 ||
-        d->weight_layout > 1)
+        d->weight_layout > 1 || d->splitk_exchange < 0 || d->splitk_exchange > 2)
         return MLP_ERR_INVALID_ARG;
 
     mlp_chain *h = new (std::nothrow) mlp_chain();
@@ -427,10 +427,19 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles
         h->stage_bytes = std::max(h->stage_bytes, a_bytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
     h->n_w = S + (d->gated ? 1 : 0);
-    // split tiles up to 128 wide reduce through shared memory (distributed, within the cluster)
-    for (int s = 0; s < S; ++s)
-        if (h->split[s] > 1 && static_cast<uint32_t>(h->BN[s] * bm * 4) <= mlpc::kRecvBytes)
-            h->recv_bytes = mlpc::kRecvBytes;
+    // Split tiles reduce through global memory unless the shared-memory exchange is asked for.
+    // (Distributed shared memory stores measured slower on the decode workload, 43.9 against
+    // 40.2 us with the same ring depth: a warp's st.shared::cluster of 512 bytes costs more than
+    // its global store, and the 64 KB receive buffer takes two ring slots.)
+    if (d->splitk_exchange == 2)
+        for (int s = 0; s < S; ++s)
+            if (h->split[s] > 1) {
+                if (static_cast<uint32_t>(h->BN[s] * bm * 4) > mlpc::kRecvBytes) {
+                    release(h);
+                    return MLP_ERR_UNSUPPORTED;
+                }
+                h->recv_bytes = mlpc::kRecvBytes;
+            }
     const size_t fixed = 1024 + 4 * mlpc::kEpiStageBytes + h->recv_bytes + sizeof(mlpc::Ctrl);
     h->num_pipe = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, (smem_optin - fixed) / h->stage_bytes));
     if (d->pipe_stages)

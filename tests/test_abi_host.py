@@ -143,6 +143,8 @@ def _desc(**kw):
     ({"gated": 1, "tile_n": (256, 0)}, mc.ERR_UNSUPPORTED),
     # CTA pairs run plain stages only: not gated, split, K-granular or Lamport, 128 or 256 wide
     ({"cta_pair": 3}, mc.ERR_INVALID_ARG),
+    ({"splitk_exchange": 3}, mc.ERR_INVALID_ARG),
+    ({"splitk_exchange": -1}, mc.ERR_INVALID_ARG),
     ({"cta_pair": 2, "gated": 1}, mc.ERR_UNSUPPORTED),
     ({"cta_pair": 2, "k_split": (2, 0)}, mc.ERR_UNSUPPORTED),
     ({"cta_pair": 2, "mode": 3}, mc.ERR_UNSUPPORTED),

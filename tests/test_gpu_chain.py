@@ -293,6 +293,10 @@ def test_split_k_matches_oracle_and_modes(mc, oracle_mod, M, dims, tn, ks):
     assert_close_to_oracle(Y, Yo)
     Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=tn, k_split=ks)
     assert torch.equal(Y.view(torch.int16), Ys.view(torch.int16))
+    if ks and max(tn) <= 128:   # the shared-memory exchange adds the same parts in the same order
+        Yd, Hd, _ = run_chain(mc, X, Ws, tile_n=tn, k_split=ks, splitk_exchange="dsmem")
+        assert torch.equal(Y.view(torch.int16), Yd.view(torch.int16))
+        assert torch.equal(H.view(torch.int16), Hd.view(torch.int16))
     if M > 128:
         Ym, _, _ = run_chain(mc, X, Ws, mode="microbatch", microbatch_rows=128, tile_n=tn, k_split=ks)
         assert torch.equal(Y.view(torch.int16), Ym.view(torch.int16))
@@ -399,3 +403,13 @@ def test_many_runs_of_one_handle_without_any_reset(mc, mode):
     outs, _, _ = run_chain(mc, X, Ws, mode=mode, reps=40, tile_n=[64, 128], k_split=[2, 2], raster_group=3)
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+def test_dsmem_exchange_rejects_tiles_wider_than_its_buffer(mc):
+    """The shared-memory exchange holds S parts of a 128-row slice in 64 KB: 256-wide split tiles
+    of 128 rows do not fit and are refused rather than silently sent through global memory."""
+    with pytest.raises(mc.MlpChainError) as e:
+        mc.Chain(256, (1024, 512, 512), tile_n=[256, 256], k_split=[2, 2], splitk_exchange="dsmem")
+    assert e.value.status == mc.ERR_UNSUPPORTED
+    with mc.Chain(256, (1024, 512, 512), tile_n=[256, 256], k_split=[2, 2]) as ch:
+        assert ch.info()["k_split"] == [2, 2]

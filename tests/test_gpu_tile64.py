@@ -69,6 +69,9 @@ def test_modes_are_bit_identical_at_64_rows(mc, oracle_mod, M, dims, tn, ks):
     for mode in ("sequential", "sequential_pdl", "pipelined_kwait", "pipelined_lamport"):
         Y, _, _ = run_chain(mc, X, Ws, mode=mode, **kw)
         assert torch.equal(Yp.view(torch.int16), Y.view(torch.int16)), mode
+    if max(ks) > 1:   # 64-row split tiles up to 256 wide also fit the shared-memory exchange
+        Yd, _, _ = run_chain(mc, X, Ws, splitk_exchange="dsmem", **kw)
+        assert torch.equal(Yp.view(torch.int16), Yd.view(torch.int16))
     for rows in (64, 128):
         if rows < M:
             Ym, _, info = run_chain(mc, X, Ws, mode="microbatch", microbatch_rows=rows, **kw)
