@@ -63,7 +63,8 @@ struct StageParams {
     int32_t b_kmajor;       // 1: weights stored N x K, B tile is K-major (one box of BN rows)
     int32_t b_3d;           // weights K x N with N a multiple of the box width: the map is a 3-D
                             // view (box column, k, box) and one copy loads every box of a B tile
-    int32_t split;          // S: CTAs sharing one tile along k (divides the cluster size)
+    int32_t split;          // CTAs sharing one tile (divides the cluster size): S k-slices, each on
+                            // one CTA, or on a CTA pair (then 2 S, rank 2 q + h: slice q, half h)
     int32_t kb_per_split;   // k blocks of each slice (the last one may get fewer)
     int32_t tiles_per_item; // cluster size / S
     int32_t items;          // cluster items of this stage
@@ -479,6 +480,13 @@ __device__ __forceinline__ int32_t scan_ready(const ChainParams &p, const Ctrl *
     return hi;
 }
 
+// The k-slice of a tile's CTA `split` (see StageParams::split).
+template <int kPair>
+__device__ __forceinline__ int32_t kslice_of(int32_t split)
+{
+    return kPair == 2 ? split >> 1 : split;
+}
+
 __device__ __forceinline__ void slice_range(int32_t k_blocks, int32_t kb_per_split, int32_t split, int32_t &kb0,
                                             int32_t &kb1)
 {
@@ -583,7 +591,7 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const uint32_t b_tile_bytes = static_cast<uint32_t>(kBK * bn_cta * 2);
         const uint32_t bytes = a_bytes + (gated ? 2u : 1u) * b_tile_bytes;
         int32_t kb0, kb1;
-        slice_range(k_blocks, kbps, kPairMode ? 0 : item.split, kb0, kb1);   // a pair's halves run the whole k range
+        slice_range(k_blocks, kbps, kslice_of<kPair>(item.split), kb0, kb1);   // a pair's halves run the same slice
         const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
         // K-granular mode: the A tile of k block kb reads columns [kb*64, kb*64+64) of the
         // previous stage's output, written by producer tiles kb*64/pBN .. (kb*64+63)/pBN of the
@@ -788,7 +796,7 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
         const bool b_kmajor = spr.b_kmajor != 0;
         const uint32_t b_swz = static_cast<uint32_t>(spr.b_swz);
         int32_t kb0, kb1;
-        slice_range(spr.k_blocks, spr.kb_per_split, item.split, kb0, kb1);
+        slice_range(spr.k_blocks, spr.kb_per_split, kslice_of<kPair>(item.split), kb0, kb1);
         const uint32_t acc = local_tiles & 1;
         const uint32_t acc_ph = (local_tiles >> 1) & 1;
         // (a pair's accumulator is released by both CTAs' epilogue warps: remote arrivals)
@@ -1335,7 +1343,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 break;
         }
         const StageParams &spr = p.st[s];
-        const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = kPairMode ? 1 : spr.split;
+        const int32_t BN = spr.BN, tiles_n = spr.tiles_n, S = kPairMode ? spr.split / 2 : spr.split;   // k-slices
         const bool dsmem = spr.dsmem_reduce != 0;
         float *const partials = spr.partials;
         const bool producer = pipelined && s + 1 < num_stages;
@@ -1388,10 +1396,15 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
             continue;
         }
 
-        // ---- split-K tile: S siblings (ranks g0 .. g0+S-1) each hold a k-slice partial ----
-        const uint32_t g0 = rank - static_cast<uint32_t>(item.split);      // first sibling
+        // ---- split-K tile: S siblings each hold a k-slice partial of the same rows: ranks
+        // g0 .. g0+S-1, or with CTA pairs the same half of each slice's pair, g0 + 2 q + half ----
+        const uint32_t g0 = rank - static_cast<uint32_t>(item.split);      // the tile's first rank
         const uint32_t weight = static_cast<uint32_t>(cs / S);             // arrivals per sibling warp
-        if (dsmem) {
+        const int32_t ks = kslice_of<kPair>(item.split);                   // my k-slice
+        auto sibling = [&](int32_t q) {
+            return g0 + static_cast<uint32_t>(kPairMode ? 2 * q + half : q);
+        };
+        if (dsmem && !kPairMode) {
             // Sibling q owns columns [q*BN/S, (q+1)*BN/S).  Every CTA sends each owner its part of
             // that slice straight from TMEM into the owner's receive buffer, laid out
             // [source split][chunk of the slice][vector][128 rows][4 floats] (a warp writes 512
@@ -1466,7 +1479,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         // MMA warp after the reduction.
         float *mine = partials + (cbase + rank) * partial_floats;
         const int32_t slice = BN / S;
-        const int32_t col0 = item.split * slice;
+        const int32_t col0 = ks * slice;
         // my previous partial must have been read by every sibling of that tile
         if (nsplit > 0 && !warp_wait_bar(&c->done_bar, (nsplit - 1) & 1, c, p, true))
             break;
@@ -1486,7 +1499,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         __syncwarp();
         if (lane == 0)
             for (int32_t q = 0; q < S; ++q)
-                arrive_rank_relaxed(&c->red_bar, g0 + q, weight);
+                arrive_rank_relaxed(&c->red_bar, sibling(q), weight);
         if (!warp_wait_bar(&c->red_bar, nsplit & 1, c, p, true))
             break;
         // Reduce my column slice over the S partials in sibling order (mine from TMEM), then the
@@ -1503,9 +1516,9 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 float4 v[2][8];
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq)
-                    if (qb + qq < S && qb + qq != item.split) {
+                    if (qb + qq < S && qb + qq != ks) {
                         const float4 *src =
-                            reinterpret_cast<const float4 *>(partials + (cbase + g0 + qb + qq) * partial_floats) + off;
+                            reinterpret_cast<const float4 *>(partials + (cbase + sibling(qb + qq)) * partial_floats) + off;
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             v[qq][i] = __ldcg(src + i * bm);
@@ -1514,7 +1527,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
                 for (int qq = 0; qq < 2; ++qq) {
                     if (qb + qq >= S)
                         continue;
-                    if (qb + qq == item.split) {
+                    if (qb + qq == ks) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e)
                             acc_v[e] += __uint_as_float(own[e]);
@@ -1537,8 +1550,12 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0)   // the MMA warp may reuse this accumulator
-            mbar_arrive(&c->tempty[acc]);
+        if (lane == 0) {   // the MMA warp may reuse this accumulator
+            if (kPairMode)
+                mbar_arrive_cluster(tempty_lead0 + acc * 8u);
+            else
+                mbar_arrive(&c->tempty[acc]);
+        }
         ++local_tiles;
         if (lamport)
             fence_acq_rel_cluster();
@@ -1547,7 +1564,7 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         __syncwarp();
         if (lane == 0)         // the siblings' partials are read: they may overwrite them
             for (int32_t q = 0; q < S; ++q)
-                arrive_rank_relaxed(&c->done_bar, g0 + q, weight);
+                arrive_rank_relaxed(&c->done_bar, sibling(q), weight);
         ++nsplit;
         if (producer || (pipelined && logging))
             publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, pl);

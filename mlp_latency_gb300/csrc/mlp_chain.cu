@@ -172,11 +172,17 @@ extern "C" const char *mlp_status_str(mlp_status s)
 // Tile width and split-K factor of one stage, from a cost model of this kernel on one SM:
 // one tcgen05.mma (M = 128, K = 16) costs about the same for any N <= 256 (~140 cycles), a TMA
 // box row (64 or 128 bytes) costs ~1.2 ns, a split tile pays ~4 us for its fp32 reduction,
-// and a stage cannot beat the HBM time of its weights.  clusters[i] = co-resident clusters of
-// 2^i CTAs.  Candidates with idle k slices or reduction slices narrower than 32 columns are
-// skipped.  Returns the estimated microseconds.
+// and a stage cannot beat the HBM time of its weights.  With CTA pairs (pair = 2) a tile is
+// 2 bm rows on two SMs, each loading bm activation rows and half of the weight tile; a k-slice
+// of a split tile then takes a pair, and a cluster holds pair x S CTAs.  tiles_m counts row
+// tiles of pair x bm rows; clusters[i] = co-resident clusters of 2^i CTAs.  Candidates with
+// idle k slices or reduction slices narrower than 32 columns are skipped.  Two bounds on a k
+// block that the plain rate misses, used when comparing whole plans: the ring's depth (`slots`
+// fills of ~1.8 us round trip in flight) and `kb_floor`, the per-k-block cost of a pair's
+// leader-to-peer hand-off (~0.33 us measured).  Returns the estimated microseconds.
 static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const int clusters[4], int fixed_bn,
-                           int fixed_split, int *bn_out, int *split_out)
+                           int fixed_split, int *bn_out, int *split_out, int pair = 1, int slots = 0,
+                           double kb_floor = 0.0)
 {
     const int k_blocks = static_cast<int>((K + 63) / 64);
     double best = 1e30;
@@ -186,28 +192,32 @@ static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const 
     for (int bn : bns) {
         if (fixed_bn && bn != fixed_bn)
             continue;
+        if (pair == 2 && bn != 128 && bn != 256)   // a pair's CTA loads 64 or 128 weight columns
+            continue;
         if (!fixed_bn && bn < 128 && N > bn)   // narrow tiles only to cover narrow outputs
             continue;
         if (!fixed_bn && bn > 32 && N <= bn / 2)
             continue;
-        for (int li = 0; li < 4; ++li) {
+        for (int li = 0; li + (pair == 2 ? 1 : 0) < 4; ++li) {
             const int S = 1 << li;
+            const int ci = li + (pair == 2 ? 1 : 0);   // cluster of pair x S CTAs
             if (fixed_split && S != fixed_split)
                 continue;
             const int kbps = (k_blocks + S - 1) / S;
-            if (bn / S < 32 || bn % S || (S - 1) * kbps >= k_blocks || clusters[li] < 1)
+            if (bn / S < 32 || bn % S || (S - 1) * kbps >= k_blocks || clusters[ci] < 1)
                 continue;
             const double tiles = static_cast<double>(tiles_m) * ((N + bn - 1) / bn);
-            const double slots = static_cast<double>(clusters[li]) * S;
-            const double units = tiles * S;
+            const double slots = static_cast<double>(clusters[ci]) * S * pair;
+            const double units = tiles * S * pair;
             // a persistent grid quantises into whole waves only while units are few
             const double waves = units <= 2 * slots ? std::ceil(units / slots) : units / slots;
-            const double rows = bm + (bn >= 64 ? bn : 64);
+            const double rows = bm + (bn / pair >= 64 ? bn / pair : 64);
             // measured on GB300: a 128 x N x 16 MMA takes about max(48, N / 2) cycles; the
             // streaming rate with the MMAs running is about 1.2 ns per 128-byte operand row
             const double t_mma = kbps * 4 * std::max(48.0, bn / 2.0) / 2000.0;   // us
             const double t_tma = kbps * rows * 1.2e-3;                           // us
-            const double t_unit = std::max(t_mma, t_tma) + 1.0 + (S > 1 ? 4.0 : 0.0);
+            const double t_lat = kbps * std::max(kb_floor, slots ? 1.8 / slots : 0.0);
+            const double t_unit = std::max(std::max(t_mma, t_tma), t_lat) + 1.0 + (S > 1 ? 4.0 : 0.0);
             const double t_hbm = static_cast<double>(K) * N * 2 / 6.5e6;
             const double t = std::max(waves * t_unit, t_hbm);
             if (t < best * 0.999) {
@@ -221,10 +231,10 @@ static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const 
 }
 
 // Scoreboard releases one producer tile of stage b makes per run: one per epilogue warp of each
-// split-K slice, or of each CTA of a pair.
+// CTA of the tile (each split-K slice, each CTA of a pair).
 static int releases_per_tile(const mlp_chain *h, int b)
 {
-    return (h->pair == 2 ? 2 : h->split[b]) * mlpc::kEpiWarps;
+    return h->pair * h->split[b] * mlpc::kEpiWarps;
 }
 
 static mlp_status full_reset(mlp_chain *h)
@@ -288,13 +298,13 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     const int bm = d->tile_m == 64 ? 64 : mlpc::kBM;
     if (d->cta_pair < 0 || d->cta_pair > 2)
         return MLP_ERR_INVALID_ARG;
-    // CTA pairs run plain stages: no gating, split-K, split accumulators, 64-row tiles, or the
-    // K-granular and Lamport modes; tiles 128 or 256 wide (64 or 128 columns per CTA)
+    // CTA pairs run plain stages: no gating, split accumulators, 64-row tiles, the K-granular and
+    // Lamport modes or the shared-memory split-K exchange; tiles 128 or 256 wide (64 or 128
+    // columns per CTA)
     bool pair_ok = !d->gated && d->acc_split != 2 && d->tile_m != 64 && d->mode != MLP_MODE_PIPELINED_KWAIT &&
-                   d->mode != MLP_MODE_PIPELINED_LAMPORT;
+                   d->mode != MLP_MODE_PIPELINED_LAMPORT && d->splitk_exchange != 2;
     for (int s = 0; s < S && pair_ok; ++s)
-        pair_ok = (d->k_split[s] == 0 || d->k_split[s] == 1) &&
-                  (d->tile_n[s] == 0 || d->tile_n[s] == 128 || d->tile_n[s] == 256);
+        pair_ok = d->tile_n[s] == 0 || d->tile_n[s] == 128 || d->tile_n[s] == 256;
     if (d->cta_pair == 2 && !pair_ok)
         return MLP_ERR_UNSUPPORTED;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < bm || d->microbatch_rows % bm ||
@@ -303,7 +313,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     // the library does not choose pairs for micro-batching: with concurrent chunk launches they
     // measured slower on the GeLU chain (256-row chunks: 462 against 332 us) and faster on prefill
     // (1024-row chunks: 384 against 441 us), so they stay an explicit option there
-    pair_ok = pair_ok && d->mode != MLP_MODE_MICROBATCH;
+    const bool pair_auto_ok = pair_ok && d->mode != MLP_MODE_MICROBATCH;
     if (d->gated && (d->acc_split == 2 || (d->tile_n[0] != 0 && d->tile_n[0] > 128) ||
                      (d->k_split[0] != 0 && d->k_split[0] != 1)))
         return MLP_ERR_UNSUPPORTED;   // the gated GEMM keeps gate and up side by side in TMEM, unsplit
@@ -361,6 +371,35 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
             clusters[li] = 0;
     }
     cudaGetLastError();
+    // The same for CTA-pair clusters of 2, 4 and 8 CTAs (pair x k-slices).
+    int clusters2[4] = {0, 0, 0, 0};
+    if (pair_ok) {
+        for (int li = 1; li < 4; ++li) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1u << li;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3((1u << li) * 8, 1, 1);
+            cfg.blockDim = dim3(mlpc::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = static_cast<size_t>(smem_optin);
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&clusters2[li], mlpc::chain_kernel<2>, &cfg) != cudaSuccess)
+                clusters2[li] = 0;
+        }
+        cudaGetLastError();
+    }
+    // Two plans, each stage's tile width and split from the cost model: one CTA per tile, and CTA
+    // pairs.  Pairs run where asked for, or by default where the model, with the ring depth each
+    // plan leaves, puts them at least 3 % ahead: prefill and the GeLU chain (a third less fill per
+    // k block), not the Llama MLP (its down-projection would need clusters of 8 for four k-slices
+    // per pair tile, and only 15 of those fit: 120 CTAs) nor decode (a 256-row pair tile over
+    // 128 rows).
+    int bn1[mlpc::kMaxStages] = {}, sp1[mlpc::kMaxStages] = {}, bn2[mlpc::kMaxStages] = {}, sp2[mlpc::kMaxStages] = {};
+    double t1 = 0.0, t2 = pair_ok ? 0.0 : 1e30;
+    const int64_t tiles_m1 = h->tiles_m, tiles_m2 = (d->M + 2 * bm - 1) / (2 * bm);
     for (int s = 0; s < S; ++s) {
         const int tn = d->tile_n[s], ks = d->k_split[s];
         if ((tn != 0 && tn != 32 && tn != 64 && tn != 128 && tn != 256) ||
@@ -369,18 +408,43 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
             return tn != 0 && tn != 32 && tn != 64 && tn != 128 && tn != 256 ? MLP_ERR_UNSUPPORTED
                                                                              : MLP_ERR_INVALID_ARG;
         }
-        int bn = 0, split = 0;
         // a gated GEMM issues two MMAs per k step into two accumulators: unsplit, at most 128 wide
         const bool gate_s = d->gated && s == 0;
         const int tn_s = gate_s && tn == 0 ? 128 : tn;
         const int ks_s = gate_s ? 1 : ks;
-        if (d->cta_pair == 2) {   // a pair tile is 256 rows; 256 wide unless the output is narrow
-            bn = tn ? tn : (d->dims[s + 1] > 128 ? 256 : 128);
-            split = 1;
-        } else if (choose_tiles(h->tiles_m, bm, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn, &split) >= 1e29) {
-            release(h);
-            return MLP_ERR_UNSUPPORTED;   // no valid tile / split for this request
+        t1 += choose_tiles(tiles_m1, bm, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn1[s], &sp1[s]);
+        if (t2 < 1e29)
+            t2 += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2, tn, ks, &bn2[s], &sp2[s], 2, 0, 0.33);
+    }
+    bool pair_auto = false;
+    if (d->cta_pair == 0 && pair_auto_ok && t1 < 1e29 && t2 < 1e29) {
+        const size_t ring_bytes = static_cast<size_t>(smem_optin) - 1024 - 4 * mlpc::kEpiStageBytes - sizeof(mlpc::Ctrl);
+        int mb1 = 0, mb2 = 0;
+        for (int s = 0; s < S; ++s) {
+            mb1 = std::max(mb1, bn1[s]);
+            mb2 = std::max(mb2, bn2[s]);
         }
+        const int slots1 = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, ring_bytes / (bm * 128 + 128 * mb1)));
+        const int slots2 = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, ring_bytes / (bm * 128 + 64 * mb2)));
+        double e1 = 0.0, e2 = 0.0;
+        for (int s = 0; s < S; ++s) {
+            int b, k;
+            e1 += choose_tiles(tiles_m1, bm, d->dims[s], d->dims[s + 1], clusters, bn1[s], sp1[s], &b, &k, 1, slots1);
+            e2 += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2, bn2[s], sp2[s], &b, &k, 2, slots2,
+                               0.33);
+        }
+        pair_auto = e2 < 0.97 * e1;
+    }
+    const int pair = (d->cta_pair == 2 || pair_auto) ? 2 : 1;
+    if ((pair == 2 ? t2 : t1) >= 1e29) {
+        release(h);
+        return MLP_ERR_UNSUPPORTED;   // no valid tile / split for this request
+    }
+    const int tile_rows = pair * bm;
+    h->pair = pair;
+    h->tiles_m = static_cast<int>((d->M + tile_rows - 1) / tile_rows);
+    for (int s = 0; s < S; ++s) {
+        const int bn = pair == 2 ? bn2[s] : bn1[s], split = pair == 2 ? sp2[s] : sp1[s];
         h->BN[s] = bn;
         h->b_swz[s] = bn >= 64 ? 128 : 64;
         h->tiles_n[s] = static_cast<int>((d->dims[s + 1] + bn - 1) / bn);
@@ -388,37 +452,13 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->max_bn = std::max(h->max_bn, bn);
         h->split[s] = split;
         h->kb_per_split[s] = (h->k_blocks[s] + split - 1) / split;
-        h->cs = std::max(h->cs, split);
+        h->cs = std::max(h->cs, pair * split);
     }
-    // CTA pairs: on request, or by default where every stage came out unsplit and 128 or 256 wide
-    // with at least four 128-row panels (pairs measured faster there: prefill -9 %, the GeLU chain
-    // -12 %); fewer rows would leave pair halves empty.
-    bool pair_auto = d->cta_pair == 0 && pair_ok && h->tiles_m >= 4;
-    for (int s = 0; s < S && pair_auto; ++s)
-        pair_auto = h->split[s] == 1 && (h->BN[s] == 128 || h->BN[s] == 256);
-    const int pair = (d->cta_pair == 2 || pair_auto) ? 2 : 1;
-    const int tile_rows = pair * bm;
-    h->pair = pair;
-    if (pair == 2) {
-        h->cs = 2;
-        h->tiles_m = static_cast<int>((d->M + tile_rows - 1) / tile_rows);
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(16, 1, 1);
-        cfg.blockDim = dim3(mlpc::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = static_cast<size_t>(smem_optin);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&clusters[1], mlpc::chain_kernel<2>, &cfg) != cudaSuccess)
-            clusters[1] = 0;
-        cudaGetLastError();
-    }
+    if (pair == 2)
+        for (int li = 1; li < 4; ++li)
+            clusters[li] = clusters2[li];
     for (int s = 0; s < S; ++s) {
-        const int tpi = pair == 2 ? 1 : h->cs / h->split[s];
+        const int tpi = h->cs / (pair * h->split[s]);
         const int tiles = h->tiles_m * h->tiles_n[s];
         h->items[s] = (tiles + tpi - 1) / tpi;
     }
@@ -573,8 +613,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         up(db.grp_off, G.grp_off);
         up(db.grp_mem, G.grp_mem);
         up(db.cgrp, G.cons_grp);
-        // A producer tile is released by each epilogue warp of each of its S split-K slices (or of
-        // each CTA of its pair).
+        // A producer tile is released by each epilogue warp of each of its CTAs (every split-K
+        // slice, both CTAs of a pair).
         std::vector<int32_t> releases(G.grp_init);
         for (int32_t &v : releases)
             v *= releases_per_tile(h, b);
@@ -682,10 +722,10 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.k_blocks = h->k_blocks[s];
         sp.b_swz = h->b_swz[s];
         sp.b_kmajor = d.weight_layout == 1;
-        // a pair's two CTAs take the same tile (rank r: half r % 2) over the whole k range
-        sp.split = h->pair == 2 ? 2 : h->split[s];
-        sp.kb_per_split = h->pair == 2 ? h->k_blocks[s] : h->kb_per_split[s];
-        sp.tiles_per_item = h->pair == 2 ? 1 : h->cs / h->split[s];
+        // the CTAs of one tile: its k-slices, each a pair with CTA pairs (rank 2 q + h: slice q, half h)
+        sp.split = h->pair * h->split[s];
+        sp.kb_per_split = h->kb_per_split[s];
+        sp.tiles_per_item = h->cs / (h->pair * h->split[s]);
         sp.items = h->items[s];
         sp.partials = h->partials[s];
         sp.dsmem_reduce = h->split[s] > 1 && h->recv_bytes && static_cast<uint32_t>(h->BN[s] * h->bm * 4) <= h->recv_bytes;
@@ -861,7 +901,7 @@ extern "C" mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *co
                 return MLP_ERR_CUDA;
             P.first_stage = s;
             const int tiles = (P.m_tile_end - P.m_tile_begin) * h->tiles_n[s];
-            const int tpi = h->cs / h->split[s];
+            const int tpi = h->cs / (h->pair * h->split[s]);
             if (!launch(P, static_grid(h, (tiles + tpi - 1) / tpi), h->smem, ss))
                 return MLP_ERR_CUDA;
             if (cudaEventRecord(h->events[static_cast<size_t>(i) * h->S + s], ss) != cudaSuccess)

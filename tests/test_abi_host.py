@@ -146,7 +146,7 @@ def _desc(**kw):
     ({"splitk_exchange": 3}, mc.ERR_INVALID_ARG),
     ({"splitk_exchange": -1}, mc.ERR_INVALID_ARG),
     ({"cta_pair": 2, "gated": 1}, mc.ERR_UNSUPPORTED),
-    ({"cta_pair": 2, "k_split": (2, 0)}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "splitk_exchange": 2}, mc.ERR_UNSUPPORTED),    # pairs add split-K parts via L2
     ({"cta_pair": 2, "mode": 3}, mc.ERR_UNSUPPORTED),
     ({"cta_pair": 2, "mode": 4}, mc.ERR_UNSUPPORTED),
     ({"cta_pair": 2, "tile_n": (64, 0)}, mc.ERR_UNSUPPORTED),

@@ -287,7 +287,7 @@ def test_split_k_matches_oracle_and_modes(mc, oracle_mod, M, dims, tn, ks):
     X, Ws = si.draw(si.make_workload("t", M, dims), seed=18)
     Y, H, info = run_chain(mc, X, Ws, tile_n=tn, k_split=ks)
     if ks:
-        assert info["k_split"] == ks and info["cluster_size"] == max(ks)
+        assert info["k_split"] == ks and info["cluster_size"] == max(ks) * info["cta_pair"]
     Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
     assert_close_to_oracle(H, Ho)
     assert_close_to_oracle(Y, Yo)
@@ -368,8 +368,8 @@ def test_device_scoreboard_matches_oracle_enumeration(mc, oracle_mod, M, dims, t
         tiles_m = info["tiles_m"][0]
         g = rg if rg else (8 if tiles_m >= 16 else (4 if tiles_m >= 8 else 1))
         for b in range(len(dims) - 2):
-            # releases per producer tile: each epilogue warp of each split-K slice, or of each CTA of a pair
-            rel = (2 if info["cta_pair"] == 2 else info["k_split"][b]) * 4
+            # releases per producer tile: each epilogue warp of each of its CTAs (split-K slices x pair)
+            rel = info["cta_pair"] * info["k_split"][b] * 4
             want = es.expected(oracle_mod, M, dims[b + 1], dims[b + 2], info["tile_m"], info["tile_n"][b],
                                info["tile_n"][b + 1], g, rel)
             es.assert_equal(ch.scoreboard(b), want)

@@ -104,6 +104,8 @@ def test_kwait_withheld_release_times_out_then_recovers(mc):
 def test_kwait_full_size_is_bit_identical_to_queue_protocol(mc, name):
     w = si.WORKLOADS[name]
     X, Ws = si.draw(w, seed=0)
-    Yk, _, _ = run_chain(mc, X, Ws, mode="pipelined_kwait")
-    Yp, _, _ = run_chain(mc, X, Ws, mode="pipelined")
+    Yk, _, info = run_chain(mc, X, Ws, mode="pipelined_kwait")
+    # the same tiles and k-slices (the queue protocol may otherwise run them on CTA pairs, which
+    # compute the same bits: see the pair tests)
+    Yp, _, _ = run_chain(mc, X, Ws, mode="pipelined", tile_n=info["tile_n"], k_split=info["k_split"])
     assert same(Yk, Yp)

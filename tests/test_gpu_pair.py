@@ -1,7 +1,9 @@
 """GPU parity of CTA-pair tiles (tcgen05 cta_group::2, `cta_pair=2`) through the C ABI.
 
 A pair computes a 256-row tile: each CTA loads its 128 rows of the activations and half of the
-weight tile's columns, the leader issues every MMA and each CTA's TMEM holds its 128 rows.  Bar:
+weight tile's columns, the leader issues every MMA and each CTA's TMEM holds its 128 rows.  A
+split-K tile takes one pair per k-slice; each CTA adds the slices of its own rows with the
+same-half CTAs of the other pairs, through global memory.  Bar:
 within |d| <= 1e-2 (|ref| + 1) of the oracle; bit-exact on integer-valued inputs; bit-identical
 to single-CTA tiles of the same width (the same 16-deep dot products in the same order) and
 across launch modes; the scoreboard equals the one rebuilt from the oracle's enumeration at
@@ -37,7 +39,7 @@ def same(a, b):
 ])
 def test_pairs_match_oracle_and_single_cta_tiles(mc, oracle_mod, M, dims, tn):
     X, Ws = si.draw(si.make_workload("t", M, dims), seed=41)
-    Yp, Hp, info = run_chain(mc, X, Ws, tile_n=tn, cta_pair=2)
+    Yp, Hp, info = run_chain(mc, X, Ws, tile_n=tn, cta_pair=2, k_split=[1, 1])
     assert info["cta_pair"] == 2 and info["tile_m"] == 256 and info["cluster_size"] == 2
     assert info["tiles_m"][0] == -(-M // 256)
     Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
@@ -85,7 +87,7 @@ def test_pair_scoreboard_and_event_log(mc, oracle_mod, M, rg):
     dims, tn = (256, 512, 256), [256, 128]
     X, Ws = si.draw(si.make_workload("t", M, dims), seed=45)
     Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
-    with mc.Chain(M, dims, tile_n=tn, event_log=True, raster_group=rg, cta_pair=2) as ch:
+    with mc.Chain(M, dims, tile_n=tn, event_log=True, raster_group=rg, cta_pair=2, k_split=[1, 1]) as ch:
         info = ch.info()
         tm = info["tiles_m"][0]
         g = rg if rg else (8 if tm >= 16 else (4 if tm >= 8 else 1))
@@ -125,3 +127,84 @@ def test_prefill_workload_on_pairs_sampled(mc, oracle_mod):
     assert info["tile_n"] == [256, 256] and info["cta_pair"] == 2
     rows = si.sample_rows(w.M, 24, seed=6)
     assert_close_to_oracle(Y[rows], oracle_mod.chain(bits(X), [bits(t) for t in Ws], rows=rows))
+
+
+@pytest.mark.parametrize("M,dims,tn,ks", [
+    (256, (2048, 1024, 512), [256, 256], [4, 4]),    # clusters of 8: four pairs per tile
+    (300, (1024, 512, 264), [128, 256], [2, 1]),     # ragged rows and columns, mixed splits
+    (700, (3072, 640, 384), [256, 128], [2, 4]),     # three pair-row panels, ragged N, the last k-slice 1 block
+])
+def test_pairs_with_split_k_match_oracle_and_single_cta_tiles(mc, oracle_mod, M, dims, tn, ks):
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=47)
+    Yp, Hp, info = run_chain(mc, X, Ws, tile_n=tn, k_split=ks, cta_pair=2)
+    assert info["cta_pair"] == 2 and info["k_split"] == ks and info["cluster_size"] == 2 * max(ks)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert_close_to_oracle(Hp, Ho)
+    assert_close_to_oracle(Yp, Yo)
+    # the same k-slices added in the same order: bit-identical to one CTA per tile
+    Ys, Hs, info1 = run_chain(mc, X, Ws, tile_n=tn, k_split=ks, cta_pair=1)
+    assert info1["cta_pair"] == 1
+    assert same(Hp, Hs) and same(Yp, Ys)
+    for mode in ("sequential", "sequential_pdl"):
+        Y, _, _ = run_chain(mc, X, Ws, mode=mode, tile_n=tn, k_split=ks, cta_pair=2)
+        assert same(Yp, Y), mode
+    Ym, _, _ = run_chain(mc, X, Ws, mode="microbatch", microbatch_rows=256, tile_n=tn, k_split=ks, cta_pair=2)
+    assert same(Yp, Ym)
+    outs, _, _ = run_chain(mc, X, Ws, reps=6, tile_n=tn, k_split=ks, cta_pair=2)
+    for o in outs:
+        assert same(o, Yp)
+
+
+def test_pair_split_k_integer_inputs_are_bit_exact(mc, oracle_mod):
+    X, Ws = si.draw_integer(256, (2048, 512, 1024), seed=48)
+    Y, H, _ = run_chain(mc, X, Ws, tile_n=[256, 128], k_split=[4, 2], cta_pair=2)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(t) for t in Ws], return_h=True)
+    assert np.array_equal(bits(H), Ho)
+    assert np.array_equal(bits(Y), Yo)
+
+
+def test_pair_split_k_scoreboard_and_event_log(mc, oracle_mod):
+    """Each CTA of a split pair tile releases its rows once per epilogue warp: 2 x S x 4 releases
+    per producer tile, against the groups rebuilt from the oracle's enumeration."""
+    import expected_scoreboard as es
+    M, dims, tn, ks = 1024, (1024, 512, 1024), [256, 128], [2, 4]
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=49)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=tn, k_split=ks, event_log=True, cta_pair=2) as ch:
+        info = ch.info()
+        tm = info["tiles_m"][0]
+        g = 8 if tm >= 16 else (4 if tm >= 8 else 1)
+        es.assert_equal(ch.scoreboard(0), es.expected(oracle_mod, M, dims[1], dims[2], 256, tn[0], tn[1], g, 2 * ks[0] * 4))
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        for _ in range(2):
+            ch.run(Xd, Wd, Y, ws)
+            assert ch.check() == 0
+            ev = ch.event_log()
+            off, tgt, _ = ch.deps(0)
+            p_end = {int(e["tile"]): int(e["seq_end"]) for e in ev if e["stage"] == 0}
+            c_start = {int(e["tile"]): int(e["seq_start"]) for e in ev if e["stage"] == 1}
+            assert len(p_end) == tm * info["tiles_n"][0] and len(c_start) == tm * info["tiles_n"][1]
+            for p in range(len(off) - 1):
+                for c in tgt[off[p]:off[p + 1]]:
+                    assert p_end[p] < c_start[int(c)]
+    assert_close_to_oracle(Y.cpu(), oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
+
+
+def test_pairs_refuse_more_than_four_k_slices(mc):
+    """A split pair tile takes 2 x k_split CTAs of one cluster, at most 8."""
+    with pytest.raises(mc.MlpChainError) as e:
+        mc.Chain(256, (4096, 512, 512), tile_n=[256, 256], k_split=[8, 1], cta_pair=2)
+    assert e.value.status == mc.ERR_UNSUPPORTED
+
+
+def test_llama_workload_library_choice_sampled(mc, oracle_mod):
+    """The Llama MLP (one 256-row panel) with the library's tiling, on sampled rows."""
+    w = si.WORKLOADS["llama_m256_4096_14336"]
+    X, Ws = si.draw(w, seed=0)
+    Y, _, info = run_chain(mc, X, Ws)
+    rows = si.sample_rows(w.M, 16, seed=7)
+    assert_close_to_oracle(Y[rows], oracle_mod.chain(bits(X), [bits(t) for t in Ws], rows=rows))
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=info["tile_n"], k_split=info["k_split"],
+                         cta_pair=info["cta_pair"])
+    assert same(Y, Ys)
