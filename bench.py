@@ -371,13 +371,17 @@ def run_sweep(args):
         Xd, Wd = X.to(dev), [t.to(dev) for t in Ws]
         Y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
         ref = None
-        tiles = None     # the first handle's tile widths and splits, kept by the 64-row handles
+        tiles = None     # the first handle's tile widths and splits, kept by every later handle
         line = {"sweep": "sequence length", "M": M, "dims": [d, d, d], "flops": w.flops,
                 "l2": "flushed between steps", "graph": "one CUDA graph replay per step"}
 
         def timed(mode, rows=0, cta_pair=0):
             nonlocal ref, tiles
-            kw = dict(tile_m=64, tile_n=tiles[0], k_split=tiles[1]) if rows % 128 else {}
+            # every handle after the first keeps its tile widths and splits, so that all modes add the
+            # same k-slices and the bit-identity check holds (the K-granular mode has no CTA pairs)
+            kw = dict(tile_n=tiles[0], k_split=tiles[1]) if tiles else {}
+            if rows % 128:
+                kw["tile_m"] = 64
             if cta_pair:
                 kw["cta_pair"] = cta_pair
             with mc.Chain(M, w.dims, mode=mode, microbatch_rows=rows, device=local, **kw) as ch:

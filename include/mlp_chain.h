@@ -136,7 +136,9 @@ typedef struct {
     int32_t grid_ctas;                  /* 0 = one CTA per SM                                    */
     int32_t raster_group;               /* first-stage raster: 1 = row panels in order; g > 1 =
                                            groups of g row panels, column-major inside a group;
-                                           0 = library choice (8 from 16 panels, 4 from 8);
+                                           0 = library choice (8 from 16 panels, 4 from 8;
+                                           below 8 all panels when the first stage takes more
+                                           than one wave, else 1; see mlp_chain_info);
                                            pipelined consumers are grouped the same way         */
     int32_t pipe_stages;                /* shared-memory ring depth: 0 = as deep as fits         */
     int32_t weight_layout;              /* 0: W_s stored dims[s] x dims[s+1] row-major (K x N);
@@ -207,6 +209,8 @@ typedef struct {
     int32_t cluster_size;               /* CTAs per thread-block cluster                          */
     int32_t k_split[MLP_MAX_GEMMS];
     int32_t cta_pair;                   /* 2: CTA pairs (tile_m is then the pair's 256 rows)      */
+    int32_t raster_group;               /* row panels per first-stage raster group (the caller's
+                                           or the library's choice)                              */
 } mlp_chain_info;
 
 typedef struct mlp_chain *mlp_chain_t;

@@ -207,7 +207,8 @@ class Chain:
                 "tiles_m": list(i.tiles_m[:S]), "tiles_n": list(i.tiles_n[:S]), "grid_ctas": i.grid_ctas,
                 "num_sms": i.num_sms, "pipe_stages": i.pipe_stages, "smem_bytes": i.smem_bytes,
                 "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run,
-                "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S]), "cta_pair": i.cta_pair}
+                "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S]), "cta_pair": i.cta_pair,
+                "raster_group": i.raster_group}
 
 
 def deps_build(M: int, n_out: int, n_next: int, bm_p: int, bn_p: int, bm_c: int, bn_c: int):

@@ -96,8 +96,20 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // First-stage raster (and consumer grouping) when the caller leaves it to the library: groups of
 // 8 row panels from 16 panels up, of 4 from 8 (measured best on GB300 for 16 and 64 panels; a
-// group of all panels serialises the stages), none below.
-int default_raster_group(int tiles_m) { return tiles_m >= 16 ? 8 : (tiles_m >= 8 ? 4 : 1); }
+// group of all panels serialises the stages).  Below 8 panels, one group of all of them when the
+// first stage takes more than one wave of cluster items: a later wave then reads each weight slab
+// together with the other panels' tiles instead of re-reading the slabs an earlier wave streamed
+// (SwiGLU MLP, 2 panels: 126 -> 103 us; 3, 4 and 6 panels of 256 rows at d = 8192: 5-7 %
+// faster); a single wave reads every slab together in either order (Llama MLP: 77 us row by
+// row against 78 grouped).
+int default_raster_group(int tiles_m, int first_stage_items, int clusters)
+{
+    if (tiles_m >= 16)
+        return 8;
+    if (tiles_m >= 8)
+        return 4;
+    return first_stage_items > clusters ? tiles_m : 1;
+}
 
 // Both pipelined modes run one persistent, co-resident grid over all stages.
 bool is_pipelined(int mode)
@@ -121,6 +133,7 @@ struct mlp_chain {
     int device = 0, num_sms = 0, S = 0;
     int bm = mlpc::kBM;      // rows per CTA's tile: 128, or 64 (tcgen05 M = 64)
     int pair = 1;            // 2: CTA pairs, each tile pair x bm rows (chain_kernel<2>)
+    int raster_group = 1;    // first-stage raster and consumer grouping (row panels per group)
     int BN[MLP_MAX_GEMMS] = {}, tiles_m = 0, tiles_n[MLP_MAX_GEMMS] = {}, k_blocks[MLP_MAX_GEMMS] = {};
     int b_swz[MLP_MAX_GEMMS] = {};
     int num_pipe = 0, max_bn = 0, grid = 0, acc_split = 1;
@@ -525,6 +538,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         release(h);  // the pipelined grid must be co-resident
         return MLP_ERR_INVALID_ARG;
     }
+    h->raster_group = d->raster_group ? d->raster_group : default_raster_group(h->tiles_m, h->items[0], h->grid / h->cs);
 
     // dependency arrays (host), then one device block for all library-owned state
     size_t bytes = 8 * sizeof(uint32_t);
@@ -544,7 +558,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         // The first stage's raster walks groups of rg row panels column by column, so those
         // panels' consumers become ready together: one scoreboard group per rg panels, pushed
         // column by column so that neighbouring queue slots share a weight slab in L2.
-        const int rg = d->raster_group ? d->raster_group : default_raster_group(h->tiles_m);
+        const int rg = h->raster_group;
         h->grp[b] = mlpc::scoreboard_groups(h->off[b].data(), h->tgt[b].data(), static_cast<int32_t>(h->off[b].size() - 1),
                                             static_cast<int32_t>(h->init[b].size()), h->tiles_n[b + 1], rg);
         const mlpc::DepGroups &G = h->grp[b];
@@ -762,7 +776,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
     P.recv_bytes = h->recv_bytes;
     // Grouped first-stage raster: a weight column slab is reused from L2 by the panels of a group
     // instead of being streamed again per panel.
-    P.raster_group = d.raster_group ? d.raster_group : default_raster_group(h->tiles_m);
+    P.raster_group = h->raster_group;
     P.num_pipe = h->num_pipe;
     P.stage_bytes = h->stage_bytes;
     P.tmem_cols = h->tmem_cols;
@@ -1018,6 +1032,7 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->num_gemms = h->S;
     info->tile_m = h->bm * h->pair;
     info->cta_pair = h->pair;
+    info->raster_group = h->raster_group;
     info->tile_k = mlpc::kBK;
     for (int s = 0; s < h->S; ++s) {
         info->tile_n[s] = h->BN[s];

@@ -366,7 +366,8 @@ def test_device_scoreboard_matches_oracle_enumeration(mc, oracle_mod, M, dims, t
     with mc.Chain(M, dims, tile_n=tn, k_split=ks, raster_group=rg, cta_pair=cp) as ch:
         info = ch.info()
         tiles_m = info["tiles_m"][0]
-        g = rg if rg else (8 if tiles_m >= 16 else (4 if tiles_m >= 8 else 1))
+        g = info["raster_group"]
+        assert (g == rg) if rg else (g == 8 if tiles_m >= 16 else g == 4 if tiles_m >= 8 else g in (1, tiles_m))
         for b in range(len(dims) - 2):
             # releases per producer tile: each epilogue warp of each of its CTAs (split-K slices x pair)
             rel = info["cta_pair"] * info["k_split"][b] * 4
@@ -413,3 +414,19 @@ def test_dsmem_exchange_rejects_tiles_wider_than_its_buffer(mc):
     assert e.value.status == mc.ERR_UNSUPPORTED
     with mc.Chain(256, (1024, 512, 512), tile_n=[256, 256], k_split=[2, 2]) as ch:
         assert ch.info()["k_split"] == [2, 2]
+
+
+def test_library_raster_group_choice(mc):
+    """Below 8 row panels the library groups all panels when the first stage takes more than one
+    wave of cluster items, and none otherwise; from 8 panels up, groups of 4, then 8."""
+    with mc.Chain(256, (4096, 14336, 4096), gated=True) as ch:   # SwiGLU MLP: 224 tiles, 36 clusters of 4
+        assert ch.info()["raster_group"] == 2
+    with mc.Chain(256, (4096, 14336, 4096)) as ch:               # Llama MLP: 112 tiles in one wave
+        assert ch.info()["raster_group"] == 1
+    with mc.Chain(1024, (8192, 8192, 8192)) as ch:               # 4 pair panels, 128 pair tiles on 76 pairs
+        info = ch.info()
+        assert info["cta_pair"] == 2 and info["raster_group"] == 4
+    with mc.Chain(4096, (1024, 1024, 1024), cta_pair=1) as ch:    # 32 panels
+        assert ch.info()["raster_group"] == 8
+    with mc.Chain(4096, (1024, 1024, 1024), cta_pair=1, raster_group=3) as ch:
+        assert ch.info()["raster_group"] == 3

@@ -90,7 +90,8 @@ def test_pair_scoreboard_and_event_log(mc, oracle_mod, M, rg):
     with mc.Chain(M, dims, tile_n=tn, event_log=True, raster_group=rg, cta_pair=2, k_split=[1, 1]) as ch:
         info = ch.info()
         tm = info["tiles_m"][0]
-        g = rg if rg else (8 if tm >= 16 else (4 if tm >= 8 else 1))
+        g = info["raster_group"]
+        assert (g == rg) if rg else (g == 8 if tm >= 16 else g == 4 if tm >= 8 else g in (1, tm))
         es.assert_equal(ch.scoreboard(0), es.expected(oracle_mod, M, dims[1], dims[2], 256, tn[0], tn[1], g, 8))
         ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
         Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
@@ -173,7 +174,7 @@ def test_pair_split_k_scoreboard_and_event_log(mc, oracle_mod):
     with mc.Chain(M, dims, tile_n=tn, k_split=ks, event_log=True, cta_pair=2) as ch:
         info = ch.info()
         tm = info["tiles_m"][0]
-        g = 8 if tm >= 16 else (4 if tm >= 8 else 1)
+        g = info["raster_group"]
         es.assert_equal(ch.scoreboard(0), es.expected(oracle_mod, M, dims[1], dims[2], 256, tn[0], tn[1], g, 2 * ks[0] * 4))
         ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
         Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)

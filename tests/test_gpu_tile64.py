@@ -108,7 +108,8 @@ def test_scoreboard_and_event_log_at_64_rows(mc, oracle_mod, M, rg):
     with mc.Chain(M, dims, tile_m=64, tile_n=tn, event_log=True, raster_group=rg) as ch:
         info = ch.info()
         tm = info["tiles_m"][0]
-        g = rg if rg else (8 if tm >= 16 else (4 if tm >= 8 else 1))
+        g = info["raster_group"]
+        assert (g == rg) if rg else (g == 8 if tm >= 16 else g == 4 if tm >= 8 else g in (1, tm))
         es.assert_equal(ch.scoreboard(0), es.expected(oracle_mod, M, dims[1], dims[2], 64, tn[0], tn[1], g, 4))
         ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
         Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
