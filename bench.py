@@ -672,6 +672,7 @@ def main():
             "config": {"workload": w.name, "M": w.M, "dims": list(w.dims), "gelu": w.gelu,
                        "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": info["tile_m"], "tile_n": info["tile_n"],
                        "k_split": info["k_split"], "cluster_size": info["cluster_size"], "cta_pair": info["cta_pair"], "splitk_exchange": args.splitk_exchange,
+                       "raster_group": info["raster_group"],
                        "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",
                        "l2": f"flushed between steps (write of {2 * l2 >> 20} MiB, outside the timed events)",
