@@ -237,10 +237,13 @@ __device__ __forceinline__ bool warp_wait_bar_all(uint64_t *bar, uint32_t parity
 
 __device__ __forceinline__ float gelu_tanh_f32(float x)
 {
-    const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
-    const float k1 = 0.044715f;
-    // the epilogue's critical path on one-wave stages: one MUFU tanh instead of a tanhf call
-    return 0.5f * x * (1.0f + tanh_approx(k0 * (x + k1 * x * x * x)));
+    const float k0 = 0.7978845608028654f;             // sqrt(2 / pi)
+    const float k01 = 0.7978845608028654f * 0.044715f;
+    // the epilogue's critical path on one-wave stages: one MUFU tanh instead of a tanhf call,
+    // and the polynomial as x (k0 + k0 k1 x^2), then h + h t with h = x / 2: six instructions
+    const float t = tanh_approx(x * fmaf(k01, x * x, k0));
+    const float h = 0.5f * x;
+    return fmaf(h, t, h);
 }
 
 // Arrive on the same mbarrier in CTA `rank` of this cluster, `count` times, without release
@@ -1028,15 +1031,15 @@ __device__ __forceinline__ void role_validate(const ChainParams &p, Ctrl *c, uin
 }
 
 // -------------------------------------------------------------------------------- epilogue --
-// Two fp32 values to packed bf16 (lo in the low half), round to nearest even on the bit
-// pattern: add half an ulp of the kept part plus its lowest kept bit, keep the upper 16 bits;
-// NaN stays a (quiet) NaN.
+// Two fp32 values to packed bf16 (lo in the low half), rounded to nearest even by one
+// cvt.rn.bf16x2.f32 (its first source fills the upper half); NaN stays a (quiet) NaN.  A
+// bit-pattern rounding in integer arithmetic took ten instructions per pair on the epilogue's
+// critical path.
 __device__ __forceinline__ uint32_t pack_bf16x2_rne(float lo, float hi)
 {
-    uint32_t a = __float_as_uint(lo), b = __float_as_uint(hi);
-    const uint32_t ra = ((a & 0x7fffffffu) > 0x7f800000u) ? (a | 0x00400000u) : a + 0x7fffu + ((a >> 16) & 1u);
-    const uint32_t rb = ((b & 0x7fffffffu) > 0x7f800000u) ? (b | 0x00400000u) : b + 0x7fffu + ((b >> 16) & 1u);
-    return __byte_perm(ra, rb, 0x7632);   // high halves: ra[31:16] low, rb[31:16] high
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // Byte offset of 16-byte segment `seg` (0..3) of row `row` (0..31) in a warp's staging buffer;
