@@ -144,11 +144,12 @@ typedef struct {
     int32_t weight_layout;              /* 0: W_s stored dims[s] x dims[s+1] row-major (K x N);
                                            1: stored transposed, dims[s+1] x dims[s] row-major
                                            (N x K, the layout of nn.Linear.weight)             */
-    int32_t k_split[MLP_MAX_GEMMS];     /* per GEMM: CTAs sharing one tile along its reduction
-                                           dimension (split-K inside a thread-block cluster):
-                                           0 = library choice, else 1, 2, 4 or 8 with
-                                           tile_n / k_split >= 32; partial sums are added in a
-                                           fixed order, so results stay deterministic            */
+    int32_t k_split[MLP_MAX_GEMMS];     /* per GEMM: k-slices sharing one tile along its reduction
+                                           dimension (split-K inside a thread-block cluster; each
+                                           slice one CTA, or one CTA pair): 0 = library choice,
+                                           else 1, 2, 4 or 8 with tile_n / k_split >= 32; partial
+                                           sums are added in a fixed order, so results stay
+                                           deterministic                                         */
     int32_t acc_split;                  /* 0/1: one fp32 accumulator per tile; 2: 16-deep k steps
                                            alternate between two accumulators that the epilogue
                                            adds (even + odd), so consecutive MMAs do not depend on
@@ -161,15 +162,19 @@ typedef struct {
                                            the weight of GEMM s >= 1.  The gated GEMM runs
                                            unsplit with tile_n <= 128 and acc_split 1; epilogue
                                            (GeLU) applies to the later GEMMs only                 */
-    int32_t cta_pair;                   /* 0 or 1: one CTA per tile; 2: CTA pairs (tcgen05
+    int32_t cta_pair;                   /* 0: library choice (one CTA per tile, or CTA pairs where
+                                           its cost model puts them ahead; never for micro-batch
+                                           chunks); 1: one CTA per tile; 2: CTA pairs (tcgen05
                                            cta_group::2), each pair computing a 256-row tile, each
                                            CTA loading its 128 rows of the activations and half of
                                            the weight tile's columns (tiles 128 or 256 wide), so a
                                            k block's fill per SM shrinks by a third and the ring
-                                           gets deeper.  Plain stages only: no gating, split-K or
-                                           split accumulators, not the K-granular or Lamport
-                                           modes (else UNSUPPORTED); micro-batch chunks are
-                                           multiples of 256 rows                                 */
+                                           gets deeper.  With k_split S a tile takes S pairs in
+                                           one cluster of 2 S <= 8 CTAs.  No gating, split
+                                           accumulators, 64-row tiles, K-granular or Lamport
+                                           modes, or shared-memory split-K exchange (else
+                                           UNSUPPORTED); micro-batch chunks are multiples of 256
+                                           rows                                                  */
     int32_t splitk_exchange;            /* how split-K siblings add their partial sums (k_split
                                            > 1), always in sibling order, so both give the same
                                            bits: 0 or 1 = through global memory (each sibling
