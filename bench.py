@@ -686,7 +686,7 @@ def main():
             "parity_vs_oracle_sample": parity,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": X.numel() * 2,
                     "d2h_bytes_per_step": Y.numel() * 2, "latency_us": statistics.median(e2e_ms) * 1e3,
-                    "what": "mlp_chain_run_host: pinned X -> device, chain, Y -> pinned host, per step"},
+                    "what": "mlp_chain_run_host: pinned X -> device, chain whose last GEMM stores into pinned Y on the host, per step"},
             "gpu_launches": args.steps * launches,
             "clocks": {**clocks, "remeasured": remeasured},
             "kernel_source_sha256": kernel_source_hash(),

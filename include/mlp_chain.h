@@ -236,8 +236,12 @@ mlp_status mlp_chain_run(mlp_chain_t h, const void *X, const void *const *W, voi
                          void *workspace, void *stream);
 
 /* As mlp_chain_run, but X and Y are HOST buffers: enqueue the copy of X into the device
- * staging buffer X_dev, the chain, and the copy of the result from Y_dev back into Y_host, all
- * on `stream` (asynchronous; synchronise the stream before reading Y_host). */
+ * staging buffer X_dev, the chain, and the transfer of the result into Y_host, all on `stream`
+ * (asynchronous; synchronise the stream before reading Y_host).  When Y_host is page-locked
+ * memory the device can address (cudaHostAlloc, or cudaHostRegister with mapping; with unified
+ * addressing every page-locked allocation qualifies, cudaPointerGetAttributes decides), the last
+ * GEMM's epilogue stores its tiles straight into it as they complete, so the transfer overlaps the
+ * chain and Y_dev is not written; otherwise Y_dev receives the result and is copied to Y_host. */
 mlp_status mlp_chain_run_host(mlp_chain_t h, const void *X_host, const void *const *W,
                               void *Y_host, void *X_dev, void *Y_dev, void *workspace,
                               void *stream);

@@ -151,7 +151,8 @@ class Chain:
                                        _stream_ptr(stream)), "mlp_chain_run")
 
     def run_host(self, X_host, Ws, Y_host, X_dev, Y_dev, workspace, stream=None):
-        """Enqueue H2D copy of X_host, the chain, and D2H copy into Y_host (pinned host tensors)."""
+        """Enqueue the H2D copy of X_host, the chain, and the transfer into Y_host (page-locked Y_host:
+        stored directly by the last GEMM; otherwise through Y_dev and a copy)."""
         ptr = lambda t: t.data_ptr() if hasattr(t, "data_ptr") else int(t)
         _check(self._lib.mlp_chain_run_host(self._h, ptr(X_host), self._wptrs(Ws), ptr(Y_host), ptr(X_dev),
                                             ptr(Y_dev), ptr(workspace) if workspace is not None else None,

@@ -937,11 +937,20 @@ extern "C" mlp_status mlp_chain_run_host(mlp_chain_t h, const void *X_host, cons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t xb = static_cast<size_t>(h->desc.M) * h->desc.dims[0] * 2;
     const size_t yb = static_cast<size_t>(h->desc.M) * h->desc.dims[h->S] * 2;
-    if (cudaSetDevice(h->device) != cudaSuccess ||
-        cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    if (cudaSetDevice(h->device) != cudaSuccess)
         return MLP_ERR_CUDA;
-    const mlp_status r = mlp_chain_run(h, X_dev, W, Y_dev, workspace, stream);
-    if (r != MLP_OK)
+    // Page-locked host memory the device can address: the last GEMM's epilogue stores into it
+    // directly, tile by tile as the tiles complete, so the transfer runs under the chain.
+    void *y_direct = nullptr;
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, Y_host) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+        attr.devicePointer && (reinterpret_cast<uintptr_t>(attr.devicePointer) & 15u) == 0)
+        y_direct = attr.devicePointer;
+    cudaGetLastError();   // a pageable pointer is not an error here
+    if (cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return MLP_ERR_CUDA;
+    const mlp_status r = mlp_chain_run(h, X_dev, W, y_direct ? y_direct : Y_dev, workspace, stream);
+    if (r != MLP_OK || y_direct)
         return r;
     return cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, st) == cudaSuccess ? MLP_OK : MLP_ERR_CUDA;
 }
