@@ -91,6 +91,11 @@ struct BoundaryParams {
     // accumulated over the handle's runs and compared against the run's epoch).
     uint32_t *ready;
     uint32_t ready_quota;      // releases of one producer tile in one run: split x kEpiWarps
+    // One scoreboard group for the whole boundary (a single row panel, or one raster group of all
+    // panels): the queue would carry no order, so consumer slot q takes member q of the group and
+    // acquires its counter directly, and the completing release pushes nothing.  Queue protocol
+    // only (the Lamport mode keeps its queue entries).
+    int32_t single_group;
 };
 
 struct EventRec {
@@ -358,8 +363,10 @@ __device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl
                                                       bool acquire)
 {
     // Relaxed polls: the entry only names the tile (the acquire is on the group counter below).
+    // A boundary of one group names its members in the queue's order: slot q is member q.
+    const bool single = p.bd[s - 1].single_group != 0;
     const unsigned long long *q = p.bd[s - 1].queue + qslot;
-    uint64_t v = ld_relaxed_gpu_u64(q);
+    uint64_t v = single ? queue_entry(c->epoch, p.bd[s - 1].grp_mem[qslot]) : ld_relaxed_gpu_u64(q);
     if (!queue_entry_ready(v, c->epoch)) {
         const uint64_t t0 = globaltimer_ns();
         uint32_t backoff = 32;
@@ -1196,6 +1203,11 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
                                              const ReleasePlan &pl)
 {
     const BoundaryParams &bd = p.bd[s];
+    if (bd.single_group) {   // the caller's fence and this relaxed add are the release; no push
+        if (lane == 0)
+            red_add_relaxed_gpu(bd.count + pl.g, 1u);
+        return;
+    }
     if (pl.ne == 1) {
         // One group: lane 0 counts this release (the caller's fence and this relaxed add are the
         // release); the add that completes the run's count reserves the group's queue slots.

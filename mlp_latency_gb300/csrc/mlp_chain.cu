@@ -762,6 +762,8 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.bd[b].slots_per_run = static_cast<uint32_t>(h->db[b].consumers);
         P.bd[b].ready = h->db[b].ready;
         P.bd[b].ready_quota = static_cast<uint32_t>(releases_per_tile(h, b));
+        // one group for the whole boundary: consumers skip the queue (queue protocol only)
+        P.bd[b].single_group = h->desc.mode == MLP_MODE_PIPELINED && h->grp[b].grp_init.size() == 1 ? 1 : 0;
     }
     P.num_stages = h->S;
     for (int s = 0; s <= h->S; ++s) {
