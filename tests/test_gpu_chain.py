@@ -184,8 +184,9 @@ def test_event_log_respects_every_dependency(mc, oracle_mod, M, rg):
     assert torch.equal(Y.cpu().view(torch.int16), Ys.view(torch.int16))
 
 
-def test_dropped_decrement_times_out_then_recovers(mc):
-    M, dims = 256, (256, 256, 256)
+@pytest.mark.parametrize("M", [256, 128])   # two scoreboard groups (queue), one group (no queue)
+def test_dropped_decrement_times_out_then_recovers(mc, M):
+    dims = (256, 256, 256)
     X, Ws = si.draw(si.make_workload("t", M, dims), seed=12)
     Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
     with mc.Chain(M, dims, tile_n=[64, 64], drop_tile=1, timeout_us=20000) as ch:
@@ -430,3 +431,32 @@ def test_library_raster_group_choice(mc):
         assert ch.info()["raster_group"] == 8
     with mc.Chain(4096, (1024, 1024, 1024), cta_pair=1, raster_group=3) as ch:
         assert ch.info()["raster_group"] == 3
+
+
+@pytest.mark.parametrize("ks", [[1, 1], [2, 4]])
+def test_single_group_boundary_skips_the_queue(mc, oracle_mod, ks):
+    """One row panel: every consumer waits on the same group, so consumer slot q takes member q
+    and acquires the counter directly.  Every dependency is still respected (event log, two runs)
+    and Y matches the sequential launches bit for bit and the oracle within tolerance."""
+    M, dims, tn = 128, (1024, 1024, 512), [128, 128]
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=19)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=tn, k_split=ks, event_log=True, cta_pair=1) as ch:
+        assert ch.scoreboard(0)["groups"] == 1
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        for _ in range(2):
+            ch.run(Xd, Wd, Y, ws)
+            assert ch.check() == 0
+            ev = ch.event_log()
+            off, tgt, _ = ch.deps(0)
+            p_end = {int(e["tile"]): int(e["seq_end"]) for e in ev if e["stage"] == 0}
+            c_start = {int(e["tile"]): int(e["seq_start"]) for e in ev if e["stage"] == 1}
+            assert len(c_start) == 4
+            for p in range(len(off) - 1):
+                for c in tgt[off[p]:off[p + 1]]:
+                    assert p_end[p] < c_start[int(c)]
+        Yp = Y.cpu()
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=tn, k_split=ks)
+    assert torch.equal(Yp.view(torch.int16), Ys.view(torch.int16))
+    assert_close_to_oracle(Yp, oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
