@@ -123,7 +123,11 @@ typedef struct {
     int32_t tile_m;                     /* rows per tile: 0 (= 128), 128, or 64 (tcgen05 MMAs of
                                            M = 64: half the activation bytes per tile, twice the
                                            row panels; micro-batch chunks of 64 rows)           */
-    int32_t tile_n[MLP_MAX_GEMMS];      /* per GEMM: 0 (library choice), 32, 64, 128 or 256     */
+    int32_t tile_n[MLP_MAX_GEMMS];      /* per GEMM: 0 (library choice) or a multiple of 32 up to
+                                           256 (a gated GEMM: 32, 64 or 128); a width that is not
+                                           a multiple of 64 loads its last 64-column weight box
+                                           whole, one copy per box; the library chooses among
+                                           32, 64, 128 and 256                                   */
     int32_t tile_k;                     /* 0 or 64                                               */
     mlp_epilogue epilogue;              /* applied after every GEMM                              */
     int32_t residual;                   /* nonzero: last stage adds X (needs dims[S] == dims[0]) */

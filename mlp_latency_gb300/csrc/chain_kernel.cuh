@@ -596,9 +596,9 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t n0 = (tile % tiles_n) * BN + static_cast<int32_t>(half) * bn_cta;
         const int32_t box_cols = b_swz / 2;
         const uint32_t box_bytes = kBK * b_swz;
-        const int32_t nbox = bn_cta / box_cols;
+        const int32_t nbox = (bn_cta + box_cols - 1) / box_cols;   // a ragged last box is loaded whole
         const bool gated = spr.gated != 0;
-        const uint32_t b_tile_bytes = static_cast<uint32_t>(kBK * bn_cta * 2);
+        const uint32_t b_tile_bytes = b_kmajor ? static_cast<uint32_t>(kBK * bn_cta * 2) : static_cast<uint32_t>(nbox) * box_bytes;
         const uint32_t bytes = a_bytes + (gated ? 2u : 1u) * b_tile_bytes;
         int32_t kb0, kb1;
         slice_range(k_blocks, kbps, kslice_of<kPair>(item.split), kb0, kb1);   // a pair's halves run the same slice

@@ -65,7 +65,7 @@ bool encode_w_kn(CUtensorMap *map, const void *ptr, int64_t K, int64_t N, int k_
     const int box_cols = b_swz / 2;
     const CUtensorMapSwizzle swz = b_swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     *is_3d = 0;
-    if (bn <= box_cols || N % box_cols != 0)
+    if (bn <= box_cols || N % box_cols != 0 || bn % box_cols != 0)   // (tiles must start on a box)
         return encode_2d(map, ptr, K, N, k_rows, box_cols, swz);
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -190,22 +190,30 @@ extern "C" const char *mlp_status_str(mlp_status s)
 // of a split tile then takes a pair, and a cluster holds pair x S CTAs.  tiles_m counts row
 // tiles of pair x bm rows; clusters[i] = co-resident clusters of 2^i CTAs.  Candidates with
 // idle k slices or reduction slices narrower than 32 columns are skipped.  Two bounds on a k
-// block that the plain rate misses, used when comparing whole plans: the ring's depth (`slots`
-// fills of ~1.8 us round trip in flight) and `kb_floor`, the per-k-block cost of a pair's
-// leader-to-peer hand-off (~0.33 us measured).  Returns the estimated microseconds.
+// block that the plain rate misses, used when comparing whole plans: the ring's depth
+// (`ring_slots` fills of ~1.8 us round trip in flight) and `kb_floor`, the per-k-block cost of a
+// 256-wide pair tile (~0.33 us measured).  Widths that are not powers of two (96 to 224 columns:
+// their last 64-column box of weights is loaded whole, one copy per box) run only where asked
+// for: 224-wide pair tiles put the GeLU chain's 74 tiles on 76 pairs instead of 64, and still
+// measured slower (216 against 203 us; the 2-GEMM chain at M = 512: 108 against 101 us), the
+// extra copies per k block costing more than the smaller MMAs save.  Returns the estimated
+// microseconds.
 static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const int clusters[4], int fixed_bn,
-                           int fixed_split, int *bn_out, int *split_out, int pair = 1, int slots = 0,
+                           int fixed_split, int *bn_out, int *split_out, int pair = 1, int ring_slots = 0,
                            double kb_floor = 0.0)
 {
     const int k_blocks = static_cast<int>((K + 63) / 64);
     double best = 1e30;
     *bn_out = 256;
     *split_out = 1;
-    const int bns[4] = {256, 128, 64, 32};
+    const int bns[8] = {256, 224, 192, 160, 128, 96, 64, 32};
     for (int bn : bns) {
+        const bool pow2 = (bn & (bn - 1)) == 0;
         if (fixed_bn && bn != fixed_bn)
             continue;
-        if (pair == 2 && bn != 128 && bn != 256)   // a pair's CTA loads 64 or 128 weight columns
+        if (pair == 2 && bn < 128)   // a pair's CTA loads at least 64 weight columns
+            continue;
+        if (!pow2 && !fixed_bn)
             continue;
         if (!fixed_bn && bn < 128 && N > bn)   // narrow tiles only to cover narrow outputs
             continue;
@@ -217,19 +225,20 @@ static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const 
             if (fixed_split && S != fixed_split)
                 continue;
             const int kbps = (k_blocks + S - 1) / S;
-            if (bn / S < 32 || bn % S || (S - 1) * kbps >= k_blocks || clusters[ci] < 1)
+            if (bn / S < 32 || bn % S || (bn / S) % 32 || (S - 1) * kbps >= k_blocks || clusters[ci] < 1)
                 continue;
             const double tiles = static_cast<double>(tiles_m) * ((N + bn - 1) / bn);
-            const double slots = static_cast<double>(clusters[ci]) * S * pair;
+            const double cap = static_cast<double>(clusters[ci]) * S * pair;   // CTAs resident at once
             const double units = tiles * S * pair;
             // a persistent grid quantises into whole waves only while units are few
-            const double waves = units <= 2 * slots ? std::ceil(units / slots) : units / slots;
-            const double rows = bm + (bn / pair >= 64 ? bn / pair : 64);
+            const double waves = units <= 2 * cap ? std::ceil(units / cap) : units / cap;
+            const int b_cols = (bn / pair + 63) / 64 * 64;   // weight columns one CTA loads per k block
+            const double rows = bm + (bn / pair >= 64 ? b_cols : 64);
             // measured on GB300: a 128 x N x 16 MMA takes about max(48, N / 2) cycles; the
             // streaming rate with the MMAs running is about 1.2 ns per 128-byte operand row
             const double t_mma = kbps * 4 * std::max(48.0, bn / 2.0) / 2000.0;   // us
             const double t_tma = kbps * rows * 1.2e-3;                           // us
-            const double t_lat = kbps * std::max(kb_floor, slots ? 1.8 / slots : 0.0);
+            const double t_lat = kbps * std::max(kb_floor, ring_slots ? 1.8 / ring_slots : 0.0);
             const double t_unit = std::max(std::max(t_mma, t_tma), t_lat) + 1.0 + (S > 1 ? 4.0 : 0.0);
             const double t_hbm = static_cast<double>(K) * N * 2 / 6.5e6;
             const double t = std::max(waves * t_unit, t_hbm);
@@ -317,7 +326,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     bool pair_ok = !d->gated && d->acc_split != 2 && d->tile_m != 64 && d->mode != MLP_MODE_PIPELINED_KWAIT &&
                    d->mode != MLP_MODE_PIPELINED_LAMPORT && d->splitk_exchange != 2;
     for (int s = 0; s < S && pair_ok; ++s)
-        pair_ok = d->tile_n[s] == 0 || d->tile_n[s] == 128 || d->tile_n[s] == 256;
+        pair_ok = d->tile_n[s] == 0 || d->tile_n[s] >= 128;
     if (d->cta_pair == 2 && !pair_ok)
         return MLP_ERR_UNSUPPORTED;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < bm || d->microbatch_rows % bm ||
@@ -415,11 +424,13 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     const int64_t tiles_m1 = h->tiles_m, tiles_m2 = (d->M + 2 * bm - 1) / (2 * bm);
     for (int s = 0; s < S; ++s) {
         const int tn = d->tile_n[s], ks = d->k_split[s];
-        if ((tn != 0 && tn != 32 && tn != 64 && tn != 128 && tn != 256) ||
-            (ks != 0 && ks != 1 && ks != 2 && ks != 4 && ks != 8)) {
+        // tile widths: multiples of 32 up to 256 (a gated GEMM: 32, 64 or 128, its gate and up tiles
+        // lying back to back as one tile twice as wide)
+        const bool tn_ok = tn == 0 || (tn % 32 == 0 && tn <= 256 &&
+                                       (!(d->gated && s == 0) || tn == 32 || tn == 64 || tn == 128));
+        if (!tn_ok || (ks != 0 && ks != 1 && ks != 2 && ks != 4 && ks != 8)) {
             release(h);
-            return tn != 0 && tn != 32 && tn != 64 && tn != 128 && tn != 256 ? MLP_ERR_UNSUPPORTED
-                                                                             : MLP_ERR_INVALID_ARG;
+            return !tn_ok ? MLP_ERR_UNSUPPORTED : MLP_ERR_INVALID_ARG;
         }
         // a gated GEMM issues two MMAs per k step into two accumulators: unsplit, at most 128 wide
         const bool gate_s = d->gated && s == 0;
@@ -476,7 +487,10 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->items[s] = (tiles + tpi - 1) / tpi;
     }
     const uint32_t a_bytes = static_cast<uint32_t>(bm * mlpc::kBK * 2);
-    h->stage_bytes = a_bytes + static_cast<uint32_t>(mlpc::kBK * (h->max_bn / pair) * 2);   // a pair's CTA: half of B
+    // a pair's CTA loads half of B; a width that is not a multiple of the 64-column weight box
+    // loads its last box whole
+    const int b_cols = h->max_bn / pair >= 64 ? (h->max_bn / pair + 63) / 64 * 64 : h->max_bn / pair;
+    h->stage_bytes = a_bytes + static_cast<uint32_t>(mlpc::kBK * b_cols * 2);
     if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles
         h->stage_bytes = std::max(h->stage_bytes, a_bytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
     h->n_w = S + (d->gated ? 1 : 0);
@@ -499,6 +513,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->num_pipe = std::min(h->num_pipe, d->pipe_stages);
     h->acc_split = d->acc_split == 2 ? 2 : 1;
     h->acc_cols = std::max(h->acc_split * h->max_bn, d->gated ? 2 * h->BN[0] : 0);
+    if (h->acc_cols & (h->acc_cols - 1))   // the second accumulator starts on a power-of-two column, as for the other widths
+        h->acc_cols = (h->acc_cols + 127) / 128 * 128;
     if (2 * h->acc_cols > 512) {
         release(h);
         return MLP_ERR_UNSUPPORTED;
