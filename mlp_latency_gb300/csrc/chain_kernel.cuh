@@ -1605,25 +1605,42 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     if (cta_rec && threadIdx.x == 0)
         cta_rec->t_start = globaltimer_ns();
 
-    if (threadIdx.x == 0) {
-        // The status read goes out first, so its latency overlaps the barrier set-up below.
-        const uint32_t status0 = ld_relaxed_gpu_u32(p.status);
-        for (int i = 0; i < p.num_pipe; ++i) {
+    if (warp == 3 && lane == 0) {   // (otherwise idle now) the tensor maps, while warp 0 sets up
+        for (int i = 0; i < p.num_stages; ++i) {
+            prefetch_tensormap(&p.mapA[i]);
+            prefetch_tensormap(&p.mapB[i]);
+        }
+        if (p.st[0].gated)
+            prefetch_tensormap(&p.mapU);
+    }
+    if (warp == 0) {
+        // The status read goes out first, so its latency overlaps the barrier set-up below; the
+        // warp's lanes initialise the ring's barriers side by side.
+        const uint32_t status0 = lane == 0 ? ld_relaxed_gpu_u32(p.status) : 0u;
+        for (int i = lane; i < p.num_pipe; i += 32) {
             mbar_init(&c->full[i], 1);
             mbar_init(&c->empty[i], 1);
             mbar_init(&c->valid[i], 1);
             mbar_init(&c->reload[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&c->tfull[i], 1);
-            mbar_init(&c->tempty[i], 4 * kPair);   // a pair's: both CTAs' epilogue warps
+        if (lane < 2) {
+            mbar_init(&c->tfull[lane], 1);
+            mbar_init(&c->tempty[lane], 4 * kPair);   // a pair's: both CTAs' epilogue warps
         }
-        for (int i = 0; i < kSchedDepth; ++i) {
+        for (int i = lane; i < kSchedDepth; i += 32) {
             mbar_init(&c->sfull[i], 1);
             // TMA + MMA + 4 epilogue warps of every rank (+ the Lamport validator)
             mbar_init(&c->sempty[i], (p.pipelined && p.lamport ? 7 : 6) * p.cs);
         }
-        {   // the cluster's first item needs no ticket and no broadcast: write it into slot 0 here
+        if (lane == 2) {
+            mbar_init(&c->drain, 1);
+            mbar_init(&c->want_next, 1);
+            mbar_init(&c->red_bar, 4 * p.cs);          // 4 warps x S siblings, each arriving cs/S times
+            mbar_init(&c->done_bar, 4 * p.cs);
+            mbar_init(&c->epoch_bar, 1);
+        }
+        if (lane == 0) {
+            // the cluster's first item needs no ticket and no broadcast: write it into slot 0 here
             int32_t ntiles = 0;
             int32_t tiles[kMaxCluster];
             const int32_t stage = item_tiles(p, static_cast<int32_t>(cluster_id_x()), ntiles, tiles);
@@ -1632,25 +1649,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             c->item_stage[0] = stage;
             c->item_tile[0] = (stage >= 0 && j < ntiles) ? tiles[j] : -1;
             c->item_split[0] = static_cast<int32_t>(rank) % S;
+            c->abort_flag = 0;
+            c->skip = status0 != 0;   // sticky error: do nothing
+            c->epoch = 0;
         }
-        mbar_init(&c->drain, 1);
-        mbar_init(&c->want_next, 1);
-        mbar_init(&c->red_bar, 4 * p.cs);          // 4 warps x S siblings, each arriving cs/S times
-        mbar_init(&c->done_bar, 4 * p.cs);
-        c->abort_flag = 0;
-        mbar_init(&c->epoch_bar, 1);
-        c->skip = status0 != 0;   // sticky error: do nothing
-        c->epoch = 0;
-        fence_barrier_init();
-        mbar_arrive(&c->sfull[0]);   // item 0 is in place (a local arrival, before any remote one)
-    }
-    if (warp == 0 && lane == 0) {
-        for (int i = 0; i < p.num_stages; ++i) {
-            prefetch_tensormap(&p.mapA[i]);
-            prefetch_tensormap(&p.mapB[i]);
-        }
-        if (p.st[0].gated)
-            prefetch_tensormap(&p.mapU);
+        fence_barrier_init();   // (each lane orders its own initialisations)
+        if (lane == 0)
+            mbar_arrive(&c->sfull[0]);   // item 0 is in place (a local arrival, before any remote one)
     }
     if (warp == 1) {
         tmem_alloc_g<kPair>(&c->tmem_base, p.tmem_cols);   // with a pair: one warp in each CTA, together
