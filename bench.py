@@ -445,6 +445,8 @@ def main():
     ap.add_argument("--raster-group", type=int, default=0)
     ap.add_argument("--pipe-stages", type=int, default=0)
     ap.add_argument("--acc-split", type=int, default=0)
+    ap.add_argument("--tile-k", type=int, default=0, choices=[0, 64, 128],
+                    help="k depth of one ring fill (0 = library choice; 128 = two 64-deep blocks per fill)")
     ap.add_argument("--cta-pair", type=int, default=0, choices=[0, 1, 2],
                     help="0: library choice, 1: one CTA per tile, 2: CTA pairs (256-row tiles, tcgen05 cta_group::2)")
     ap.add_argument("--splitk-exchange", default="global", choices=["global", "dsmem"],
@@ -496,11 +498,14 @@ def main():
     stream = torch.cuda.Stream(device=dev)
 
     def make(mode, rows=0, **kw):
+        cta_pair = kw.pop("cta_pair", args.cta_pair)
+        # two-block ring fills run with one CTA per tile, outside the K-granular and Lamport modes
+        tile_k = 0 if mode in ("pipelined_kwait", "pipelined_lamport") or cta_pair == 2 else args.tile_k
         return mc.Chain(w.M, w.dims, tile_n=tiles, gelu=w.gelu, residual=w.residual, mode=mode,
                         microbatch_rows=rows, device=local, raster_group=args.raster_group,
                         pipe_stages=args.pipe_stages, acc_split=args.acc_split,
                         weight_layout=args.weight_layout, k_split=ksplit, gated=w.gated,
-                        cta_pair=kw.pop("cta_pair", args.cta_pair), splitk_exchange=args.splitk_exchange, **kw)
+                        cta_pair=cta_pair, splitk_exchange=args.splitk_exchange, tile_k=tile_k, **kw)
 
     chain = make(args.mode, args.microbatch_rows)
     info = chain.info()
@@ -673,7 +678,7 @@ def main():
                        "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": info["tile_m"], "tile_n": info["tile_n"],
                        "k_split": info["k_split"], "cluster_size": info["cluster_size"], "cta_pair": info["cta_pair"], "splitk_exchange": args.splitk_exchange,
                        "raster_group": info["raster_group"],
-                       "tile_k": 64, "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
+                       "tile_k": info["tile_k"], "fill_k": info["fill_k"], "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",
                        "l2": f"flushed between steps (write of {2 * l2 >> 20} MiB, outside the timed events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

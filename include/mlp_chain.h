@@ -128,7 +128,15 @@ typedef struct {
                                            a multiple of 64 loads its last 64-column weight box
                                            whole, one copy per box; the library chooses among
                                            32, 64, 128 and 256                                   */
-    int32_t tile_k;                     /* 0 or 64                                               */
+    int32_t tile_k;                     /* k depth of one shared-memory ring fill: 0 or 64, or 128
+                                           (two 64-deep blocks per fill, one copy per operand and
+                                           one barrier phase for twice the bytes; fewer, larger
+                                           ring slots).  128 applies to the GEMMs with K a multiple
+                                           of 128, k-slices of an even number of 64-deep blocks,
+                                           whole weight boxes per tile and no gate; the others
+                                           fill 64 deep (mlp_chain_info.fill_k).  With CTA pairs,
+                                           split accumulators or the K-granular and Lamport modes:
+                                           UNSUPPORTED                                           */
     mlp_epilogue epilogue;              /* applied after every GEMM                              */
     int32_t residual;                   /* nonzero: last stage adds X (needs dims[S] == dims[0]) */
     mlp_mode mode;
@@ -220,6 +228,8 @@ typedef struct {
     int32_t cta_pair;                   /* 2: CTA pairs (tile_m is then the pair's 256 rows)      */
     int32_t raster_group;               /* row panels per first-stage raster group (the caller's
                                            or the library's choice)                              */
+    int32_t fill_k[MLP_MAX_GEMMS];      /* per GEMM: k depth of one ring fill (64 or 128);
+                                           tile_k is the largest                                 */
 } mlp_chain_info;
 
 typedef struct mlp_chain *mlp_chain_t;

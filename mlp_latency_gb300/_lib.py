@@ -77,7 +77,7 @@ class ChainInfo(ctypes.Structure):
         ("tiles_m", i32 * MAX_GEMMS), ("tiles_n", i32 * MAX_GEMMS), ("grid_ctas", i32),
         ("num_sms", i32), ("pipe_stages", i32), ("smem_bytes", i32), ("tmem_cols", i32),
         ("launches_per_run", i32), ("cluster_size", i32), ("k_split", i32 * MAX_GEMMS), ("cta_pair", i32),
-        ("raster_group", i32),
+        ("raster_group", i32), ("fill_k", i32 * MAX_GEMMS),
     ]
 
 

@@ -62,7 +62,8 @@ class Chain:
       "microbatch"         row chunks of ``microbatch_rows``, GEMMs of different chunks overlapped.
     ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice).  ``cta_pair=2`` runs 256-row
     tiles on CTA pairs (tcgen05 cta_group::2).  ``splitk_exchange`` ("global" or "dsmem") is
-    the path split-K siblings add their partial sums through.  Errors raise MlpChainError with
+    the path split-K siblings add their partial sums through.  ``tile_k=128`` fills the ring with
+    two 64-deep k blocks at a time where a GEMM allows it (``info()["fill_k"]``).  Errors raise MlpChainError with
     the library's status.
     """
 
@@ -72,7 +73,8 @@ class Chain:
                  drop_tile: Optional[int] = None, timeout_us: int = 0, grid_ctas: int = 0,
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
                  weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False,
-                 force_reload: bool = False, cta_pair: int = 0, splitk_exchange: str = "global"):
+                 force_reload: bool = False, cta_pair: int = 0, splitk_exchange: str = "global",
+                 tile_k: int = 0):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -83,7 +85,7 @@ class Chain:
         d.tile_m = int(tile_m)
         for i, v in enumerate(tile_n or []):
             d.tile_n[i] = int(v)
-        d.tile_k = 0
+        d.tile_k = int(tile_k)
         d.epilogue = 1 if gelu else 0
         d.residual = int(bool(residual))
         d.mode = MODES[mode]
@@ -209,7 +211,7 @@ class Chain:
                 "num_sms": i.num_sms, "pipe_stages": i.pipe_stages, "smem_bytes": i.smem_bytes,
                 "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run,
                 "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S]), "cta_pair": i.cta_pair,
-                "raster_group": i.raster_group}
+                "raster_group": i.raster_group, "fill_k": list(i.fill_k[:S])}
 
 
 def deps_build(M: int, n_out: int, n_next: int, bm_p: int, bn_p: int, bm_c: int, bn_c: int):

@@ -72,6 +72,10 @@ struct StageParams {
     int32_t dsmem_reduce;   // split-K through the owners' shared memory (BN * 512 <= recv_bytes)
     int32_t gated;          // SwiGLU: B tiles of gate (mapB) and up (mapU) weights, accumulators
                             // side by side in TMEM, output SiLU(gate) * up; unsplit
+    int32_t kpf;            // 64-deep k blocks per ring fill: 0 or 1, or 2 (one CTA per tile, plain
+                            // stage, even k blocks per slice): mapA is then a 3-D view (column, row,
+                            // k block) and mapB a 3-D (K-major) or 4-D (column in box, k, box,
+                            // k block) one, so each operand of a fill is still one copy
 };
 
 // Stage boundary s -> s+1.  The scoreboard holds one counter per group of consumer tiles with
@@ -649,6 +653,35 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                     pph ^= 1;
                 }
             }
+        } else if (spr.kpf == 2) {
+            // Two k blocks per fill (never K-granular or gated): the slot holds the A tiles of k
+            // blocks kb and kb + 1, then their B tiles, each laid out as in a one-block fill; one
+            // copy per operand, one barrier phase, twice the bytes.  A fill's issue and completion
+            // cost little more than a one-block fill's, so a slice of short k blocks streams
+            // nearer the memory system's rate.  (Slices hold an even number of blocks, so
+            // lead_kb - kb0 is even and kb meets it.)
+            const int32_t by = b_kmajor ? n0 : n0 / box_cols;
+            const uint32_t fill_bytes = 2u * bytes;
+            for (int32_t kb = kb0; kb < kb1; kb += 2) {
+                if (leader && kb == lead_kb)
+                    mbar_arrive(&c->want_next);
+                if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
+                mbar_arrive_expect_tx(&c->full[ps], fill_bytes);
+                if (b_kmajor)
+                    tma_load_3d(a + 2u * a_bytes, mapB, &c->full[ps], 0, by, kb, pol_w);
+                else
+                    tma_load_4d(a + 2u * a_bytes, mapB, &c->full[ps], 0, 0, by, kb, pol_w);
+                tma_load_3d(a, mapA, &c->full[ps], 0, m0, kb, pol_act);
+                ++issued;
+                if (++ps == num_pipe) {
+                    ps = 0;
+                    pph ^= 1;
+                }
+            }
         } else if (!kwait_s && (b_kmajor || b_3d || nbox == 1)) {
             // The common case: two copies per k block (three for a gated stage: gate and up
             // weights), the B tile in one copy whatever its layout, no per-k-block mode
@@ -833,6 +866,36 @@ __device__ __forceinline__ void role_mma(const ChainParams &p, Ctrl *c, uint8_t 
             const uint64_t bstep = b_kmajor ? 2u : b_swz;   // 16-byte units per 16-deep k step
             const uint64_t slot16 = stage_bytes >> 4;
             uint32_t accum = 0;
+            if (spr.kpf == 2) {
+                // Two k blocks per fill: A tiles of blocks kb, kb + 1, then their B tiles (role_tma).
+                const uint32_t box_cols = b_swz / 2u;
+                const uint32_t b_tile = b_kmajor ? static_cast<uint32_t>(kBK) * BN * 2u
+                                                 : (BN + box_cols - 1u) / box_cols * static_cast<uint32_t>(kBK) * b_swz;
+                const uint64_t bd2 = b_kmajor ? smem_desc(ring_base + 2u * a_bytes, 16u, 1024u, 2u)
+                                              : smem_desc(ring_base + 2u * a_bytes, kBK * b_swz, 8u * b_swz, b_code);
+                const uint64_t a16 = a_bytes >> 4, b16 = b_tile >> 4;
+                for (int32_t kb = kb0; kb < kb1; kb += 2) {
+                    if (!wait_bar(&c->full[ps], pph, c, p, true, kPairMode)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t off = static_cast<uint64_t>(ps) * slot16;
+#pragma unroll
+                    for (uint32_t f = 0; f < 2; ++f)
+#pragma unroll
+                        for (uint32_t kk = 0; kk < kBK / 16; ++kk) {
+                            mma_bf16_ss_g<kPair>(d_tmem, ad0 + off + f * a16 + 2u * kk, bd2 + off + f * b16 + bstep * kk,
+                                                 idesc, accum);
+                            accum = 1u;
+                        }
+                    issued = true;
+                    mma_commit_g<kPair>(smem_u32(&c->empty[ps]));
+                    if (++ps == num_pipe) {
+                        ps = 0;
+                        pph ^= 1;
+                    }
+                }
+            } else
             for (int32_t kb = kb0; kb < kb1; ++kb) {
                 // (a pair's fill also completes through the peer's copies: acquire at cluster scope)
                 if (!wait_bar(&c->full[ps], pph, c, p, true, kPairMode)) {

@@ -84,6 +84,44 @@ bool encode_w_kn(CUtensorMap *map, const void *ptr, int64_t K, int64_t N, int k_
     return true;
 }
 
+// Views whose outermost coordinate is the 64-deep k block, for fills of two k blocks: one copy
+// then lands both blocks' tiles one after the other, each in the layout of a one-block copy.
+//   activations (rows x K, row-major), or weights stored N x K: (k in block, row, k block);
+//   weights stored K x N: (column in box, k in block, box, k block).
+bool encode_kblocks(CUtensorMap *map, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                    const cuuint32_t *box, CUtensorMapSwizzle swz)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void *>(ptr), dims,
+              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_rows_kblocks(CUtensorMap *map, const void *ptr, int64_t rows, int64_t K, int box_rows)
+{
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(mlpc::kBK), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(K / mlpc::kBK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(mlpc::kBK) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(mlpc::kBK), static_cast<cuuint32_t>(box_rows), 2};
+    return encode_kblocks(map, ptr, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool encode_w_kn_kblocks(CUtensorMap *map, const void *ptr, int64_t K, int64_t N, int b_swz, int bn)
+{
+    const int box_cols = b_swz / 2;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(box_cols), static_cast<cuuint64_t>(mlpc::kBK),
+                                static_cast<cuuint64_t>(N / box_cols), static_cast<cuuint64_t>(K / mlpc::kBK)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(b_swz),
+                                   static_cast<cuuint64_t>(N) * 2 * mlpc::kBK};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(mlpc::kBK),
+                               static_cast<cuuint32_t>(bn / box_cols), 2};
+    return encode_kblocks(map, ptr, 4, dims, strides, box,
+                          b_swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 struct DeviceBoundary {
     int32_t *pg_off = nullptr, *pg_tgt = nullptr, *grp_off = nullptr, *grp_mem = nullptr, *grp_init = nullptr;
     int32_t *cgrp = nullptr;
@@ -141,6 +179,7 @@ struct mlp_chain {
     int cs = 1, max_clusters = 0;
     uint32_t recv_bytes = 0;
     int split[MLP_MAX_GEMMS] = {}, kb_per_split[MLP_MAX_GEMMS] = {}, items[MLP_MAX_GEMMS] = {};
+    int kpf[MLP_MAX_GEMMS] = {};   // 64-deep k blocks per ring fill (1 or 2)
     int32_t tile_base[MLP_MAX_GEMMS + 1] = {};
     float *partials[MLP_MAX_GEMMS] = {};
     uint32_t stage_bytes = 0, tmem_cols = 0;
@@ -308,7 +347,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     if (d->in_dtype != MLP_DT_BF16 || d->acc_dtype != MLP_DT_F32 || d->h_dtype != MLP_DT_BF16 ||
         d->out_dtype != MLP_DT_BF16)
         return MLP_ERR_UNSUPPORTED;
-    if (!(d->tile_m == 0 || d->tile_m == 64 || d->tile_m == 128) || !(d->tile_k == 0 || d->tile_k == 64))
+    if (!(d->tile_m == 0 || d->tile_m == 64 || d->tile_m == 128) ||
+        !(d->tile_k == 0 || d->tile_k == 64 || d->tile_k == 128))
         return MLP_ERR_UNSUPPORTED;
     if (d->epilogue != MLP_EPI_NONE && d->epilogue != MLP_EPI_GELU_TANH)
         return MLP_ERR_INVALID_ARG;
@@ -324,7 +364,12 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     // Lamport modes or the shared-memory split-K exchange; tiles 128 or 256 wide (64 or 128
     // columns per CTA)
     bool pair_ok = !d->gated && d->acc_split != 2 && d->tile_m != 64 && d->mode != MLP_MODE_PIPELINED_KWAIT &&
-                   d->mode != MLP_MODE_PIPELINED_LAMPORT && d->splitk_exchange != 2;
+                   d->mode != MLP_MODE_PIPELINED_LAMPORT && d->splitk_exchange != 2 && d->tile_k != 128;
+    // Fills of two k blocks: one CTA per tile, one accumulator, and no per-k-block consumer work
+    // (the K-granular waits and the Lamport scan are per 64-deep block)
+    const bool deep_ok = d->acc_split != 2 && d->mode != MLP_MODE_PIPELINED_KWAIT && d->mode != MLP_MODE_PIPELINED_LAMPORT;
+    if (d->tile_k == 128 && (!deep_ok || d->cta_pair == 2))
+        return MLP_ERR_UNSUPPORTED;
     for (int s = 0; s < S && pair_ok; ++s)
         pair_ok = d->tile_n[s] == 0 || d->tile_n[s] >= 128;
     if (d->cta_pair == 2 && !pair_ok)
@@ -489,8 +534,21 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     const uint32_t a_bytes = static_cast<uint32_t>(bm * mlpc::kBK * 2);
     // a pair's CTA loads half of B; a width that is not a multiple of the 64-column weight box
     // loads its last box whole
-    const int b_cols = h->max_bn / pair >= 64 ? (h->max_bn / pair + 63) / 64 * 64 : h->max_bn / pair;
+    auto padded_cols = [](int bn) { return bn >= 64 ? (bn + 63) / 64 * 64 : bn; };
+    const int b_cols = padded_cols(h->max_bn / pair);
     h->stage_bytes = a_bytes + static_cast<uint32_t>(mlpc::kBK * b_cols * 2);
+    // Two k blocks per fill where asked for (tile_k = 128) and the GEMM allows it: one CTA per tile,
+    // a plain stage, K a multiple of 128 with every k-slice an even number of blocks, and a B tile
+    // of whole weight boxes (the copy views need them).
+    for (int s = 0; s < S; ++s) {
+        const int box_cols = h->b_swz[s] / 2;
+        const bool boxes = d->weight_layout == 1 || (d->dims[s + 1] % box_cols == 0 && h->BN[s] % box_cols == 0);
+        const bool ok = pair == 1 && deep_ok && !(d->gated && s == 0) && d->dims[s] % 128 == 0 &&
+                        h->kb_per_split[s] % 2 == 0 && boxes;
+        h->kpf[s] = d->tile_k == 128 && ok ? 2 : 1;
+        if (h->kpf[s] == 2)
+            h->stage_bytes = std::max(h->stage_bytes, 2u * (a_bytes + static_cast<uint32_t>(mlpc::kBK * padded_cols(h->BN[s]) * 2)));
+    }
     if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles
         h->stage_bytes = std::max(h->stage_bytes, a_bytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
     h->n_w = S + (d->gated ? 1 : 0);
@@ -721,12 +779,17 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         } else {
             out_ptr = Y;
         }
-        if (!encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], h->bm, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+        const bool deep = h->kpf[s] == 2;
+        if (!(deep ? encode_rows_kblocks(&P.mapA[s], a_ptr, d.M, d.dims[s], h->bm)
+                   : encode_2d(&P.mapA[s], a_ptr, d.M, d.dims[s], h->bm, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B)))
             return MLP_ERR_CUDA;
         int32_t b_3d = 0, u_3d = 0;
         auto encode_w = [&](CUtensorMap *m, const void *w, int32_t *is_3d) {
             *is_3d = 0;
             const int bn_cta = h->BN[s] / h->pair;   // the columns one CTA loads
+            if (deep)
+                return d.weight_layout == 1 ? encode_rows_kblocks(m, w, d.dims[s + 1], d.dims[s], bn_cta)
+                                            : encode_w_kn_kblocks(m, w, d.dims[s], d.dims[s + 1], h->b_swz[s], bn_cta);
             return d.weight_layout == 1
                        ? encode_2d(m, w, d.dims[s + 1], d.dims[s], bn_cta, mlpc::kBK, CU_TENSOR_MAP_SWIZZLE_128B)
                        : encode_w_kn(m, w, d.dims[s], d.dims[s + 1], mlpc::kBK, h->b_swz[s], bn_cta, is_3d);
@@ -762,6 +825,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
         sp.gelu = d.epilogue == MLP_EPI_GELU_TANH && !gate_s;
         sp.gated = gate_s;
+        sp.kpf = h->kpf[s];
         sp.residual = (d.residual && s + 1 == h->S) ? static_cast<const __nv_bfloat16 *>(X) : nullptr;
         a_ptr = out_ptr;
     }
@@ -1062,6 +1126,8 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->raster_group = h->raster_group;
     info->tile_k = mlpc::kBK;
     for (int s = 0; s < h->S; ++s) {
+        info->fill_k[s] = mlpc::kBK * h->kpf[s];
+        info->tile_k = std::max(info->tile_k, info->fill_k[s]);
         info->tile_n[s] = h->BN[s];
         info->tiles_m[s] = h->tiles_m;
         info->tiles_n[s] = h->tiles_n[s];

@@ -152,6 +152,14 @@ def _desc(**kw):
     ({"cta_pair": 2, "tile_n": (64, 0)}, mc.ERR_UNSUPPORTED),
     ({"cta_pair": 2, "tile_m": 64}, mc.ERR_UNSUPPORTED),
     ({"cta_pair": 2, "mode": 2, "microbatch_rows": 128}, mc.ERR_INVALID_ARG),   # chunks of 256 rows
+    # ring fills 64 or 128 deep; two-block fills need one CTA per tile, one accumulator, no
+    # per-block consumer work (K-granular waits, Lamport scans)
+    ({"tile_k": 96}, mc.ERR_UNSUPPORTED),
+    ({"tile_k": 256}, mc.ERR_UNSUPPORTED),
+    ({"tile_k": 128, "cta_pair": 2}, mc.ERR_UNSUPPORTED),
+    ({"tile_k": 128, "mode": 3}, mc.ERR_UNSUPPORTED),
+    ({"tile_k": 128, "mode": 4}, mc.ERR_UNSUPPORTED),
+    ({"tile_k": 128, "acc_split": 2}, mc.ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_descriptors_before_touching_cuda(lib, kw, expect):
     h = ctypes.c_void_p()
