@@ -230,6 +230,13 @@ typedef struct {
                                            or the library's choice)                              */
     int32_t fill_k[MLP_MAX_GEMMS];      /* per GEMM: k depth of one ring fill (64 or 128);
                                            tile_k is the largest                                 */
+    int32_t queue_free[MLP_MAX_GEMMS];  /* per stage boundary b (GEMM b -> b + 1), pipelined mode
+                                           with the work-queue: 1 when its consumers skip the
+                                           queue (one scoreboard group, or no more consumer
+                                           items than co-resident clusters): consumer slot q
+                                           takes the q-th member of the groups in group order
+                                           and acquires its group's counter, and no release
+                                           pushes; 0 when consumers poll queue entries           */
 } mlp_chain_info;
 
 typedef struct mlp_chain *mlp_chain_t;
@@ -337,7 +344,9 @@ int64_t mlp_deps_build(int64_t M, int64_t n_out, int64_t n_next, int32_t bm_p, i
  * (protocol.h): first-stage raster and scoreboard groups of `raster_group` row panels (0 or 1:
  * none), releases_per_tile releases per finished tile (the kernel's split-K slices x epilogue
  * warps), counters that count up and accumulate over three back-to-back runs against the run's
- * epoch-scaled target, the completing release pushing the group's members column by column,
+ * epoch-scaled target, the completing release pushing the group's members column by column
+ * (a boundary of one group, or of no more consumer tiles than threads, has no queue: consumer
+ * slot q takes the q-th member of the groups in group order, as on the device),
  * relaxed queue polls followed by an acquire of the group counter before a consumer reads its
  * producers' output (plain reads: a missing happens-before edge is a data race for
  * ThreadSanitizer, a stale value fails the run), and seeded random delays.  order_out (optional,

@@ -78,6 +78,7 @@ class ChainInfo(ctypes.Structure):
         ("num_sms", i32), ("pipe_stages", i32), ("smem_bytes", i32), ("tmem_cols", i32),
         ("launches_per_run", i32), ("cluster_size", i32), ("k_split", i32 * MAX_GEMMS), ("cta_pair", i32),
         ("raster_group", i32), ("fill_k", i32 * MAX_GEMMS),
+        ("queue_free", i32 * MAX_GEMMS),
     ]
 
 

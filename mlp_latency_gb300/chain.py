@@ -211,7 +211,8 @@ class Chain:
                 "num_sms": i.num_sms, "pipe_stages": i.pipe_stages, "smem_bytes": i.smem_bytes,
                 "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run,
                 "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S]), "cta_pair": i.cta_pair,
-                "raster_group": i.raster_group, "fill_k": list(i.fill_k[:S])}
+                "raster_group": i.raster_group, "fill_k": list(i.fill_k[:S]),
+                "queue_free": list(i.queue_free[:max(S - 1, 0)])}
 
 
 def deps_build(M: int, n_out: int, n_next: int, bm_p: int, bn_p: int, bm_c: int, bn_c: int):

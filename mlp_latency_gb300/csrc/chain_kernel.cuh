@@ -95,11 +95,13 @@ struct BoundaryParams {
     // accumulated over the handle's runs and compared against the run's epoch).
     uint32_t *ready;
     uint32_t ready_quota;      // releases of one producer tile in one run: split x kEpiWarps
-    // One scoreboard group for the whole boundary (a single row panel, or one raster group of all
-    // panels): the queue would carry no order, so consumer slot q takes member q of the group and
-    // acquires its counter directly, and the completing release pushes nothing.  Queue protocol
-    // only (the Lamport mode keeps its queue entries).
-    int32_t single_group;
+    // Queue-free boundary: one scoreboard group for the whole boundary (a single row panel, or one
+    // raster group of all panels), or no more consumer items than co-resident clusters (every
+    // consumer item gets a cluster of its own, so no CTA could run a ready tile in place of one it
+    // waits for).  The queue would carry no order that matters: consumer slot q takes member q of
+    // the groups in group order (grp_mem as stored) and acquires its group's counter directly, and
+    // releases push nothing.  Queue protocol only (the Lamport mode keeps its queue entries).
+    int32_t queue_free;
 };
 
 struct EventRec {
@@ -367,10 +369,10 @@ __device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl
                                                       bool acquire)
 {
     // Relaxed polls: the entry only names the tile (the acquire is on the group counter below).
-    // A boundary of one group names its members in the queue's order: slot q is member q.
-    const bool single = p.bd[s - 1].single_group != 0;
+    // A queue-free boundary names the members in group order: slot q is grp_mem[q].
+    const bool queue_free = p.bd[s - 1].queue_free != 0;
     const unsigned long long *q = p.bd[s - 1].queue + qslot;
-    uint64_t v = single ? queue_entry(c->epoch, p.bd[s - 1].grp_mem[qslot]) : ld_relaxed_gpu_u64(q);
+    uint64_t v = queue_free ? queue_entry(c->epoch, p.bd[s - 1].grp_mem[qslot]) : ld_relaxed_gpu_u64(q);
     if (!queue_entry_ready(v, c->epoch)) {
         const uint64_t t0 = globaltimer_ns();
         uint32_t backoff = 32;
@@ -1266,9 +1268,14 @@ __device__ __forceinline__ void release_tile(const ChainParams &p, Ctrl *c, int3
                                              const ReleasePlan &pl)
 {
     const BoundaryParams &bd = p.bd[s];
-    if (bd.single_group) {   // the caller's fence and this relaxed add are the release; no push
-        if (lane == 0)
-            red_add_relaxed_gpu(bd.count + pl.g, 1u);
+    if (bd.queue_free) {   // the caller's fence and these relaxed adds are the release; no push
+        if (pl.ne == 1) {
+            if (lane == 0)
+                red_add_relaxed_gpu(bd.count + pl.g, 1u);
+        } else {
+            for (int32_t e = bd.pg_off[tile] + lane; e < bd.pg_off[tile + 1]; e += 32)
+                red_add_relaxed_gpu(bd.count + bd.pg_tgt[e], 1u);
+        }
         return;
     }
     if (pl.ne == 1) {

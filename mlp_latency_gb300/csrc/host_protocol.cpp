@@ -198,8 +198,9 @@ extern "C" mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_n
 //     one acq_rel add of +1 on every group it feeds (on the device: fence.acq_rel.gpu + a
 //     relaxed add, the PTX form of a release RMW); the add that completes the run's target,
 //     run_target(init, epoch), reserves the group's queue slots on the tail and stores the
-//     members there with relaxed stores, tagged with the epoch (a boundary of one group pushes
-//     nothing: its consumer slot q is member q, as on the device);
+//     members there with relaxed stores, tagged with the epoch (a queue-free boundary, one group
+//     or no more consumer tiles than threads, pushes nothing: its consumer slot q is the q-th
+//     member of the groups in group order, as on the device);
 //   - a consumer ticket polls its queue slot with relaxed loads until this run's entry lands,
 //     then acquires the named tile's group counter until it reaches the run's target, and only
 //     then reads the producers' output (plain, non-atomic reads: a missing happens-before edge is
@@ -219,6 +220,7 @@ struct ModelBoundary {
     std::vector<std::atomic<uint64_t>> queue;
     std::atomic<uint32_t> tail{0};
     std::vector<uint32_t> data;                  // producer output: R parts per producer tile
+    bool queue_free = false;                     // consumers skip the queue (as on the device)
 };
 
 }  // namespace
@@ -265,6 +267,8 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
         for (auto &q : B.queue)
             q.store(0);
         B.data.assign(static_cast<size_t>(P) * R, 0u);
+        // one group, or no more consumer tiles than threads (each consumer gets a thread of its own)
+        B.queue_free = B.grp.grp_init.size() == 1 || C <= threads;
     }
 
     std::atomic<uint32_t> ticket{0}, seq{0}, status{0};
@@ -313,10 +317,10 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                         std::this_thread::yield();
                         return false;
                     };
-                    // relaxed polls of the queue slot: the entry only names the tile (a boundary of one
-                    // group has no queue: slot q is member q of the group)
+                    // relaxed polls of the queue slot: the entry only names the tile (a queue-free
+                    // boundary has none: slot q is the q-th member of the groups in group order)
                     uint64_t v;
-                    if (B.grp.grp_init.size() == 1)
+                    if (B.queue_free)
                         v = mlpc::queue_entry(epoch, B.grp.grp_mem[static_cast<size_t>(local)]);
                     else
                         while (!mlpc::queue_entry_ready(v = B.queue[local].load(std::memory_order_relaxed), epoch))
@@ -360,9 +364,9 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                     for (int32_t e = G.pg_off[tile]; e < G.pg_off[tile + 1]; ++e) {
                         const int32_t g = G.pg_tgt[e];
                         const uint32_t old = B.count[static_cast<size_t>(g)].fetch_add(1, std::memory_order_acq_rel);
-                        if (G.grp_init.size() == 1 ||
+                        if (B.queue_free ||
                             !mlpc::release_completes(old, mlpc::run_target(B.target[static_cast<size_t>(g)], epoch)))
-                            continue;   // (one group: nothing is pushed)
+                            continue;   // (a queue-free boundary pushes nothing)
                         const int32_t m0 = G.grp_off[g], n = G.grp_off[g + 1] - m0;
                         const uint32_t q0 = mlpc::run_relative(B.tail.fetch_add(static_cast<uint32_t>(n), std::memory_order_relaxed),
                                                                run, static_cast<uint32_t>(B.queue.size()));

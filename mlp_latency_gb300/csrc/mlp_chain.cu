@@ -758,6 +758,17 @@ extern "C" mlp_status mlp_chain_workspace_size(mlp_chain_t h, size_t *bytes)
     return MLP_OK;
 }
 
+// Consumers of boundary b skip the work-queue (queue protocol only): one scoreboard group, whose
+// queue would list its members in a fixed order anyway, or no more consumer items than
+// co-resident clusters, where every consumer item gets a cluster of its own and readiness order
+// cannot give any cluster a better tile.
+static bool queue_free(const mlp_chain *h, int b)
+{
+    if (h->desc.mode != MLP_MODE_PIPELINED)
+        return false;
+    return h->grp[b].grp_init.size() == 1 || h->items[b + 1] <= h->grid / h->cs;
+}
+
 static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const *W, void *Y, void *ws)
 {
     bool same = h->params_valid && X == h->c_X && Y == h->c_Y && ws == h->c_ws;
@@ -842,8 +853,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         P.bd[b].slots_per_run = static_cast<uint32_t>(h->db[b].consumers);
         P.bd[b].ready = h->db[b].ready;
         P.bd[b].ready_quota = static_cast<uint32_t>(releases_per_tile(h, b));
-        // one group for the whole boundary: consumers skip the queue (queue protocol only)
-        P.bd[b].single_group = h->desc.mode == MLP_MODE_PIPELINED && h->grp[b].grp_init.size() == 1 ? 1 : 0;
+        P.bd[b].queue_free = queue_free(h, b) ? 1 : 0;
     }
     P.num_stages = h->S;
     for (int s = 0; s <= h->S; ++s) {
@@ -1125,6 +1135,8 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->cta_pair = h->pair;
     info->raster_group = h->raster_group;
     info->tile_k = mlpc::kBK;
+    for (int b = 0; b + 1 < h->S; ++b)
+        info->queue_free[b] = queue_free(h, b) ? 1 : 0;
     for (int s = 0; s < h->S; ++s) {
         info->fill_k[s] = mlpc::kBK * h->kpf[s];
         info->tile_k = std::max(info->tile_k, info->fill_k[s]);

@@ -25,12 +25,13 @@ int main()
                                            static_cast<int32_t>(d[5]), static_cast<int32_t>(d[6]), off.data(), tgt.data(),
                                            nnz, init.data()) != nnz;
     }
-    const int32_t tn2[2] = {4, 4}, tn4[4] = {3, 5, 2, 4}, tn3[3] = {3, 2, 3};
+    const int32_t tn2[2] = {4, 4}, tn4[4] = {3, 5, 2, 4}, tn3[3] = {3, 2, 3}, tn5[2] = {3, 2};
     for (uint64_t seed = 1; seed <= 3; ++seed) {
         std::vector<int32_t> order(64 * 16);
         fails += mlp_protocol_model(2, 4, tn2, 1, 4, 8, seed, -1, 2000, order.data()) != MLP_OK;
         fails += mlp_protocol_model(4, 3, tn4, 1, 16, 6, seed, -1, 2000, order.data()) != MLP_OK;
         fails += mlp_protocol_model(3, 17, tn3, 8, 8, 12, seed, -1, 2000, order.data()) != MLP_OK;   // merged groups
+        fails += mlp_protocol_model(2, 4, tn5, 1, 4, 8, seed, -1, 2000, order.data()) != MLP_OK;    // queue-free groups
     }
     fails += mlp_protocol_model(2, 2, tn2, 1, 4, 4, 5, 1, 200, nullptr) != MLP_ERR_TIMEOUT;   // withheld release
     for (int32_t rg : {1, 3, 8}) {   // the grouped scoreboard tables, sizes first

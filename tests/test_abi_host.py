@@ -93,6 +93,8 @@ def test_tiny_config_has_four_producers_per_consumer(lib):
 @pytest.mark.parametrize("tiles_m,tiles_n,threads,seed,rg,rel", [
     (1, [4, 4], 4, 0, 1, 4), (4, [8, 3], 8, 1, 1, 16), (3, [5, 7, 2, 4], 6, 2, 1, 4), (6, [2, 9], 16, 3, 1, 8),
     (2, [1, 1], 3, 4, 1, 4), (9, [4, 5], 8, 5, 4, 8), (17, [3, 2, 3], 12, 6, 8, 4), (7, [2, 6], 6, 7, 3, 32),
+    # no more consumer tiles than threads: queue-free boundaries of several groups
+    (4, [3, 2], 8, 8, 1, 4), (3, [4, 3, 2], 9, 9, 1, 8), (4, [2, 4], 16, 10, 2, 4),
 ])
 def test_protocol_model_orders_every_tile(lib, tiles_m, tiles_n, threads, seed, rg, rel):
     """Merged raster groups, several releases per tile, counters accumulating over three runs."""
@@ -108,6 +110,13 @@ def test_protocol_model_orders_every_tile(lib, tiles_m, tiles_n, threads, seed, 
 def test_protocol_model_dropped_decrement_times_out(lib, rg):
     st, _ = mc.protocol_model(8 if rg > 1 else 2, [4, 4], threads=4, seed=5, drop_tile=1, timeout_ms=200,
                               raster_group=rg)
+    assert st == mc.ERR_TIMEOUT
+
+
+def test_protocol_model_dropped_decrement_times_out_without_queue(lib):
+    # 8 consumer tiles on 8 threads in 4 groups: the consumers skip the queue and wait on their
+    # group's counter, which the dropped releases keep short
+    st, _ = mc.protocol_model(4, [2, 2], threads=8, seed=6, drop_tile=1, timeout_ms=200)
     assert st == mc.ERR_TIMEOUT
 
 

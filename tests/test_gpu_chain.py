@@ -184,12 +184,18 @@ def test_event_log_respects_every_dependency(mc, oracle_mod, M, rg):
     assert torch.equal(Y.cpu().view(torch.int16), Ys.view(torch.int16))
 
 
-@pytest.mark.parametrize("M", [256, 128])   # two scoreboard groups (queue), one group (no queue)
-def test_dropped_decrement_times_out_then_recovers(mc, M):
+@pytest.mark.parametrize("M,grid,queue_free", [
+    (256, 0, 1),    # two scoreboard groups, a cluster for every consumer: no queue
+    (256, 4, 0),    # two groups, 8 consumer tiles on 4 CTAs: the queue
+    (128, 0, 1),    # one group: no queue
+])
+def test_dropped_decrement_times_out_then_recovers(mc, M, grid, queue_free):
     dims = (256, 256, 256)
     X, Ws = si.draw(si.make_workload("t", M, dims), seed=12)
     Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
-    with mc.Chain(M, dims, tile_n=[64, 64], drop_tile=1, timeout_us=20000) as ch:
+    with mc.Chain(M, dims, tile_n=[64, 64], k_split=[1, 1], drop_tile=1, timeout_us=20000, grid_ctas=grid,
+                  raster_group=1) as ch:
+        assert ch.info()["queue_free"] == [queue_free]
         ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
         Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
         ch.run(Xd, Wd, Y, ws)                    # tile 1 withholds its decrements
@@ -197,7 +203,7 @@ def test_dropped_decrement_times_out_then_recovers(mc, M):
         ch.run(Xd, Wd, Y, ws)                    # the fault fires once; check() re-armed the handle
         assert ch.check() == 0
         Y2 = Y.cpu()
-    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=[64, 64])
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=[64, 64], k_split=[1, 1])
     assert torch.equal(Y2.view(torch.int16), Ys.view(torch.int16))
 
 
@@ -442,7 +448,7 @@ def test_single_group_boundary_skips_the_queue(mc, oracle_mod, ks):
     X, Ws = si.draw(si.make_workload("t", M, dims), seed=19)
     Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
     with mc.Chain(M, dims, tile_n=tn, k_split=ks, event_log=True, cta_pair=1) as ch:
-        assert ch.scoreboard(0)["groups"] == 1
+        assert ch.scoreboard(0)["groups"] == 1 and ch.info()["queue_free"] == [1]
         ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
         Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
         for _ in range(2):
@@ -458,5 +464,36 @@ def test_single_group_boundary_skips_the_queue(mc, oracle_mod, ks):
                     assert p_end[p] < c_start[int(c)]
         Yp = Y.cpu()
     Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=tn, k_split=ks)
+    assert torch.equal(Yp.view(torch.int16), Ys.view(torch.int16))
+    assert_close_to_oracle(Yp, oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
+
+
+@pytest.mark.parametrize("grid,queue_free", [(0, 1), (8, 0)])
+def test_one_wave_boundary_of_several_groups_skips_the_queue(mc, oracle_mod, grid, queue_free):
+    """Four row panels (four scoreboard groups) and 16 consumer tiles: with a cluster for every
+    consumer item the consumers take the groups' members in group order and acquire their group's
+    counter (no queue); on 8 CTAs they poll the queue.  Both respect every dependency (event log,
+    two runs) and give the sequential launches' bits."""
+    M, dims, tn = 512, (1024, 1024, 512), [128, 128]
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=20)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    with mc.Chain(M, dims, tile_n=tn, k_split=[1, 1], event_log=True, cta_pair=1, grid_ctas=grid,
+                  raster_group=1) as ch:
+        assert ch.scoreboard(0)["groups"] == 4 and ch.info()["queue_free"] == [queue_free]
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        for _ in range(2):
+            ch.run(Xd, Wd, Y, ws)
+            assert ch.check() == 0
+            ev = ch.event_log()
+            off, tgt, _ = ch.deps(0)
+            p_end = {int(e["tile"]): int(e["seq_end"]) for e in ev if e["stage"] == 0}
+            c_start = {int(e["tile"]): int(e["seq_start"]) for e in ev if e["stage"] == 1}
+            assert len(p_end) == 32 and len(c_start) == 16
+            for p in range(len(off) - 1):
+                for c in tgt[off[p]:off[p + 1]]:
+                    assert p_end[p] < c_start[int(c)]
+        Yp = Y.cpu()
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=tn, k_split=[1, 1])
     assert torch.equal(Yp.view(torch.int16), Ys.view(torch.int16))
     assert_close_to_oracle(Yp, oracle_mod.chain(bits(X), [bits(t) for t in Ws]))
