@@ -361,6 +361,29 @@ struct Item {
     int32_t stage, tile, split;
 };
 
+// The queue entry names the tile; the synchronisation with the producers is an acquire of the
+// tile's group counter, which every producer warp incremented with a release (fence + relaxed
+// add): reading the run's final count makes all of their stores visible.  The pusher therefore
+// stores the entries without a fence of its own.  False after an error (status recorded, abort
+// raised).
+__device__ __forceinline__ bool acquire_group(const ChainParams &p, Ctrl *c, int32_t s, int32_t tile)
+{
+    const BoundaryParams &bd = p.bd[s - 1];
+    const int32_t g = bd.cgrp[tile];
+    const uint32_t want = run_target(bd.grp_init[g], c->epoch);
+    const uint64_t t0 = globaltimer_ns();
+    while (!count_reached(ld_acquire_gpu_u32(bd.count + g), want)) {
+        if (c->abort_flag)
+            return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            atomicCAS(p.status, 0u, kStatusTimeout);
+            c->abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Consumer prologue (the injected prologue of section III-A, Fig. 1): poll work-queue slot
 // `qslot` of the boundary before stage s until this run's entry lands, with back-off and a
 // deadline.  Returns the consumer tile it names, or -1 after an error (status recorded, this
@@ -401,25 +424,8 @@ __device__ __forceinline__ int32_t resolve_queue_slot(const ChainParams &p, Ctrl
         c->abort_flag = 1;
         return -1;
     }
-    if (acquire) {
-        // The queue entry names the tile; the synchronisation with the producers is an acquire
-        // of the tile's group counter, which every producer warp incremented with a release
-        // (fence + relaxed add): reading the run's final count makes all of their stores
-        // visible.  The pusher therefore stores the entries without a fence of its own.
-        const BoundaryParams &bd = p.bd[s - 1];
-        const int32_t g = bd.cgrp[tile];
-        const uint32_t want = run_target(bd.grp_init[g], c->epoch);
-        const uint64_t t0 = globaltimer_ns();
-        while (!count_reached(ld_acquire_gpu_u32(bd.count + g), want)) {
-            if (c->abort_flag)
-                return -1;
-            if (globaltimer_ns() - t0 > p.timeout_ns) {
-                atomicCAS(p.status, 0u, kStatusTimeout);
-                c->abort_flag = 1;
-                return -1;
-            }
-        }
-    }
+    if (acquire && !acquire_group(p, c, s, tile))
+        return -1;
     return tile;
 }
 
@@ -572,24 +578,26 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             }
             have_epoch = true;
         }
+        // At a queue-free boundary the slot names its tile without a wait (the acquire follows).
+        const bool queue_free = pipelined && s > 0 && !kwait && !p.lamport && p.bd[s - 1].queue_free != 0;
         if (pipelined && s > 0 && !kwait) {
-            tile = resolve_queue_slot(p, c, s, item.tile, !p.lamport);   // Lamport: validated instead
+            tile = resolve_queue_slot(p, c, s, item.tile, !p.lamport && !queue_free);   // Lamport: validated instead
             if (tile < 0) {
                 free_item_slot(c, slot);
                 break;
             }
         }
-        if (s > 0 && !kwait_s)   // TMA (async proxy) reads of a producer's output come after the acquire
-            fence_proxy_async_global();
-        if (events && item.split == 0) {
-            EventRec *e = events + p.tile_base[s] + tile;
-            e->stage = s;
-            e->tile = tile;
-            e->smid = static_cast<int32_t>(smid());
-            e->cta = static_cast<int32_t>(blockIdx.x);
-            e->seq_start = atom_add_relaxed_gpu(p.seq, 1u);
-            e->t_start = globaltimer_ns();
-        }
+        auto log_start = [&]() {   // (a consumer's start is taken after its acquire)
+            if (events && item.split == 0) {
+                EventRec *e = events + p.tile_base[s] + tile;
+                e->stage = s;
+                e->tile = tile;
+                e->smid = static_cast<int32_t>(smid());
+                e->cta = static_cast<int32_t>(blockIdx.x);
+                e->seq_start = atom_add_relaxed_gpu(p.seq, 1u);
+                e->t_start = globaltimer_ns();
+            }
+        };
         const StageParams &spr = p.st[s];
         const int32_t tiles_n = spr.tiles_n, BN = spr.BN, b_swz = spr.b_swz, b_kmajor = spr.b_kmajor;
         const bool b_3d = spr.b_3d != 0;
@@ -617,6 +625,19 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t pbase = kwait_s ? (tile / tiles_n) * ptn : 0;
         int32_t ready_hi = -1;
         const int32_t slice_last = kwait_s ? min(((kb1 - 1) * kBK + kBK - 1) / pBN, ptn - 1) : 0;
+        // Weights before the acquire (queue-free boundary, one CTA per tile, one-block fills, the
+        // B tile in one copy): the first ring-full of weight copies goes out while the producers
+        // finish, the activation copies of those fills after the acquire (see the common loop).
+        const bool early = queue_free && !kPairMode && spr.kpf != 2 && (b_kmajor || b_3d || nbox == 1);
+        if (queue_free && !early && !acquire_group(p, c, s, tile)) {
+            free_item_slot(c, slot);
+            break;
+        }
+        if (!early) {
+            if (s > 0 && !kwait_s)   // TMA (async proxy) reads of a producer's output come after the acquire
+                fence_proxy_async_global();
+            log_start();
+        }
         bool ok = true;
         if constexpr (kPairMode) {
             // Pair stages are plain (no K-granular waits, gating or Lamport): the B tile's half is
@@ -692,10 +713,57 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             const int32_t by = b_kmajor ? n0 : (b_3d ? n0 / box_cols : 0);
             const int32_t b_form = b_kmajor ? 0 : (b_3d ? 1 : 2);
             const CUtensorMap *mapU = &p.mapU;
+            int32_t kb_first = kb0;
+            if (early) {
+                // Arm the first ring-full of fills with their weight copies, acquire the producers'
+                // output, then send the activation copies of the armed fills (also after a failed
+                // wait: every armed fill's transaction count must complete, so that the drain
+                // below accounts for its copies).
+                const int32_t n_early = min(num_pipe, kb1 - kb0);
+                const int32_t ps0 = ps;
+                int32_t armed = 0;
+                for (; armed < n_early; ++armed) {
+                    const int32_t kb = kb0 + armed;
+                    if (leader && kb == lead_kb)
+                        mbar_arrive(&c->want_next);
+                    if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
+                    mbar_arrive_expect_tx(&c->full[ps], bytes);
+                    for (int32_t u = 0; u < (gated ? 2 : 1); ++u) {
+                        const CUtensorMap *mb = u ? mapU : mapB;
+                        uint8_t *bt = a + a_bytes + u * b_tile_bytes;
+                        if (b_form == 0)
+                            tma_load_2d(bt, mb, &c->full[ps], kb * kBK, by, pol_w);
+                        else if (b_form == 1)
+                            tma_load_3d(bt, mb, &c->full[ps], 0, kb * kBK, by, pol_w);
+                        else
+                            tma_load_2d(bt, mb, &c->full[ps], bx, kb * kBK, pol_w);
+                    }
+                    if (++ps == num_pipe) {
+                        ps = 0;
+                        pph ^= 1;
+                    }
+                }
+                if (ok && !acquire_group(p, c, s, tile))
+                    ok = false;
+                fence_proxy_async_global();
+                if (ok)
+                    log_start();
+                for (int32_t i = 0; i < armed; ++i) {
+                    const int32_t sl = ps0 + i < num_pipe ? ps0 + i : ps0 + i - num_pipe;
+                    tma_load_2d(ring + static_cast<size_t>(sl) * stage_bytes, mapA, &c->full[sl], (kb0 + i) * kBK, m0,
+                                pol_act);
+                    ++issued;
+                }
+                kb_first = kb0 + armed;
+            }
             // One loop per stage kind, so the plain loop carries no test for the gated copy.
             auto k_loop = [&](auto gated_kind) {
                 constexpr bool kGated = decltype(gated_kind)::value;
-                for (int32_t kb = kb0; kb < kb1; ++kb) {
+                for (int32_t kb = kb_first; kb < kb1; ++kb) {
                     if (leader && kb == lead_kb)
                         mbar_arrive(&c->want_next);
                     if (!wait_bar(&c->empty[ps], pph ^ 1, c, p)) {
@@ -724,10 +792,12 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                     }
                 }
             };
-            if (gated)
-                k_loop(std::true_type{});
-            else
-                k_loop(std::false_type{});
+            if (ok) {
+                if (gated)
+                    k_loop(std::true_type{});
+                else
+                    k_loop(std::false_type{});
+            }
         } else
         for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (leader && kb == lead_kb)
