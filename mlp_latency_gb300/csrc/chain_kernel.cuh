@@ -625,10 +625,10 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t pbase = kwait_s ? (tile / tiles_n) * ptn : 0;
         int32_t ready_hi = -1;
         const int32_t slice_last = kwait_s ? min(((kb1 - 1) * kBK + kBK - 1) / pBN, ptn - 1) : 0;
-        // Weights before the acquire (queue-free boundary, one CTA per tile, one-block fills, the
-        // B tile in one copy): the first ring-full of weight copies goes out while the producers
-        // finish, the activation copies of those fills after the acquire (see the common loop).
-        const bool early = queue_free && !kPairMode && spr.kpf != 2 && (b_kmajor || b_3d || nbox == 1);
+        // Weights before the acquire (queue-free boundary, one-block fills; one CTA per tile with
+        // the B tile in one copy, or a CTA pair): the first ring-full of weight copies goes out
+        // while the producers finish, the activation copies of those fills after the acquire.
+        const bool early = queue_free && spr.kpf != 2 && (kPairMode || b_kmajor || b_3d || nbox == 1);
         if (queue_free && !early && !acquire_group(p, c, s, tile)) {
             free_item_slot(c, slot);
             break;
@@ -646,15 +646,14 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
             const int32_t by = b_kmajor ? n0 : (b_3d ? n0 / box_cols : 0);
             const int32_t b_form = b_kmajor ? 0 : (b_3d ? 1 : 2);
             const uint32_t pair_bytes = 2u * bytes;
-            for (int32_t kb = kb0; kb < kb1; ++kb) {
+            // Wait for the slot of k block kb (the leader for its MMA's release of the slot's
+            // previous fill, the peer for the leader's go-ahead for this fill), arm it (leader) and
+            // send this CTA's half of the B tile.
+            auto arm_fill_b = [&](int32_t kb) {
                 if (leader && kb == lead_kb)
                     mbar_arrive(&c->want_next);
-                // the leader waits for its MMA's release of the slot's previous fill; the peer for
-                // the leader's go-ahead for this fill
-                if (!wait_bar(&c->empty[ps], half ? pph : pph ^ 1, c, p, true, half != 0)) {
-                    ok = false;
-                    break;
-                }
+                if (!wait_bar(&c->empty[ps], half ? pph : pph ^ 1, c, p, true, half != 0))
+                    return false;
                 uint8_t *a = ring + static_cast<size_t>(ps) * stage_bytes;
                 const uint32_t fb = full_lead0 + static_cast<uint32_t>(ps) * 8u;
                 if (!half) {
@@ -669,7 +668,43 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                 else   // a ragged N keeps the 2-D map: one copy per 64-column box of the half
                     for (int32_t j = 0; j < nbox; ++j)
                         tma_load_2d_pair(a + a_bytes + j * box_bytes, mapB, fb, bx + j * box_cols, k, pol_w);
-                tma_load_2d_pair(a, mapA, fb, k, m0, pol_act);
+                return true;
+            };
+            int32_t kb_first = kb0;
+            if (early) {   // as in the one-CTA loop below: weights, the acquire, then activations
+                const int32_t n_early = min(num_pipe, kb1 - kb0);
+                const int32_t ps0 = ps;
+                int32_t armed = 0;
+                for (; armed < n_early; ++armed) {
+                    if (!arm_fill_b(kb0 + armed)) {
+                        ok = false;
+                        break;
+                    }
+                    if (++ps == num_pipe) {
+                        ps = 0;
+                        pph ^= 1;
+                    }
+                }
+                if (ok && !acquire_group(p, c, s, tile))
+                    ok = false;
+                fence_proxy_async_global();
+                if (ok)
+                    log_start();
+                for (int32_t i = 0; i < armed; ++i) {
+                    const int32_t sl = ps0 + i < num_pipe ? ps0 + i : ps0 + i - num_pipe;
+                    tma_load_2d_pair(ring + static_cast<size_t>(sl) * stage_bytes, mapA,
+                                     full_lead0 + static_cast<uint32_t>(sl) * 8u, (kb0 + i) * kBK, m0, pol_act);
+                    ++issued;
+                }
+                kb_first = kb0 + armed;
+            }
+            for (int32_t kb = kb_first; kb < kb1 && ok; ++kb) {
+                if (!arm_fill_b(kb)) {
+                    ok = false;
+                    break;
+                }
+                tma_load_2d_pair(ring + static_cast<size_t>(ps) * stage_bytes, mapA,
+                                 full_lead0 + static_cast<uint32_t>(ps) * 8u, kb * kBK, m0, pol_act);
                 ++issued;
                 if (++ps == num_pipe) {
                     ps = 0;
@@ -679,10 +714,8 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         } else if (spr.kpf == 2) {
             // Two k blocks per fill (never K-granular or gated): the slot holds the A tiles of k
             // blocks kb and kb + 1, then their B tiles, each laid out as in a one-block fill; one
-            // copy per operand, one barrier phase, twice the bytes.  A fill's issue and completion
-            // cost little more than a one-block fill's, so a slice of short k blocks streams
-            // nearer the memory system's rate.  (Slices hold an even number of blocks, so
-            // lead_kb - kb0 is even and kb meets it.)
+            // copy per operand, one barrier phase, twice the bytes, half the ring slots.  (Slices
+            // hold an even number of blocks, so lead_kb - kb0 is even and kb meets it.)
             const int32_t by = b_kmajor ? n0 : n0 / box_cols;
             const uint32_t fill_bytes = 2u * bytes;
             for (int32_t kb = kb0; kb < kb1; kb += 2) {
