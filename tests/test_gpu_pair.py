@@ -209,3 +209,27 @@ def test_llama_workload_library_choice_sampled(mc, oracle_mod):
     Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", tile_n=info["tile_n"], k_split=info["k_split"],
                          cta_pair=info["cta_pair"])
     assert same(Y, Ys)
+
+
+@pytest.mark.parametrize("ks", [[1, 1], [1, 2]])
+def test_pair_dropped_release_times_out_then_recovers(mc, ks):
+    """Two pair panels, a pair for every consumer item (a queue-free boundary: the consumer pairs
+    send their first weight copies, then wait on their group's counter).  Producer tile 1 withholds
+    its releases, so the consumers of its panel run out of time: both CTAs of each such pair send
+    the activation copies of their armed fills anyway, the run ends in TIMEOUT, and the next run
+    (the fault fires once) gives the sequential launches' bits."""
+    M, dims = 512, (1024, 1024, 512)
+    X, Ws = si.draw(si.make_workload("t", M, dims), seed=23)
+    Xd, Wd = X.to(DEV), [w.to(DEV) for w in Ws]
+    kw = dict(tile_n=[128, 128], k_split=ks, cta_pair=2, raster_group=1)
+    with mc.Chain(M, dims, drop_tile=1, timeout_us=20000, **kw) as ch:
+        assert ch.info()["queue_free"] == [1] and ch.info()["cta_pair"] == 2
+        ws = torch.empty(ch.workspace_size(), dtype=torch.uint8, device=DEV)
+        Y = torch.empty(M, dims[-1], dtype=torch.bfloat16, device=DEV)
+        ch.run(Xd, Wd, Y, ws)
+        assert ch.check() == mc.ERR_TIMEOUT
+        ch.run(Xd, Wd, Y, ws)
+        assert ch.check() == 0
+        Y2 = Y.cpu()
+    Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", **kw)
+    assert same(Y2, Ys)
