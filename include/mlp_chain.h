@@ -196,6 +196,18 @@ typedef struct {
                                            memory (distributed shared memory stores into a 64 KB
                                            receive buffer per CTA, which takes ring depth; needs
                                            tile_m * tile_n * 4 <= 65536, else UNSUPPORTED)       */
+    int32_t split_clusters;             /* where the k-slices of a split tile run: 0 = library
+                                           choice; 1 = in one cluster (the tile's CTAs are one
+                                           cluster item); 2 = on separate clusters of a CTA pair
+                                           each (every slice its own cluster item, partial sums
+                                           exchanged through global memory with a per-tile count,
+                                           in the same fixed order, so results are the same bits).
+                                           2 needs MLP_MODE_PIPELINED, CTA pairs (cta_pair 0 or
+                                           2), M <= 256 (one 256-row panel, so each stage
+                                           boundary is one scoreboard group) and a grid with a
+                                           cluster for every item of each split stage (a cluster
+                                           then never holds two slices of one stage); else
+                                           UNSUPPORTED                                           */
 } mlp_chain_desc;
 
 /* One record per tile of a pipelined run (MLP_DEBUG_EVENT_LOG), stage by stage, followed by one
@@ -230,6 +242,8 @@ typedef struct {
                                            or the library's choice)                              */
     int32_t fill_k[MLP_MAX_GEMMS];      /* per GEMM: k depth of one ring fill (64 or 128);
                                            tile_k is the largest                                 */
+    int32_t split_across[MLP_MAX_GEMMS]; /* per GEMM: 1 when its k-slices run on separate clusters
+                                           (split_clusters)                                      */
     int32_t queue_free[MLP_MAX_GEMMS];  /* per stage boundary b (GEMM b -> b + 1), pipelined mode
                                            with the work-queue: 1 when its consumers skip the
                                            queue (one scoreboard group, or no more consumer

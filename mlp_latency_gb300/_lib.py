@@ -62,7 +62,7 @@ class ChainDesc(ctypes.Structure):
         ("microbatch_rows", i32), ("device", i32), ("debug_flags", u32), ("drop_tile", i32),
         ("timeout_us", u32), ("grid_ctas", i32), ("raster_group", i32), ("pipe_stages", i32),
         ("weight_layout", i32), ("k_split", i32 * MAX_GEMMS), ("acc_split", i32), ("gated", i32), ("cta_pair", i32),
-        ("splitk_exchange", i32),
+        ("splitk_exchange", i32), ("split_clusters", i32),
     ]
 
 
@@ -78,7 +78,7 @@ class ChainInfo(ctypes.Structure):
         ("num_sms", i32), ("pipe_stages", i32), ("smem_bytes", i32), ("tmem_cols", i32),
         ("launches_per_run", i32), ("cluster_size", i32), ("k_split", i32 * MAX_GEMMS), ("cta_pair", i32),
         ("raster_group", i32), ("fill_k", i32 * MAX_GEMMS),
-        ("queue_free", i32 * MAX_GEMMS),
+        ("split_across", i32 * MAX_GEMMS), ("queue_free", i32 * MAX_GEMMS),
     ]
 
 

@@ -63,7 +63,8 @@ class Chain:
     ``tile_n`` / ``k_split`` per GEMM (0 or None: library choice).  ``cta_pair=2`` runs 256-row
     tiles on CTA pairs (tcgen05 cta_group::2).  ``splitk_exchange`` ("global" or "dsmem") is
     the path split-K siblings add their partial sums through.  ``tile_k=128`` fills the ring with
-    two 64-deep k blocks at a time where a GEMM allows it (``info()["fill_k"]``).  Errors raise MlpChainError with
+    two 64-deep k blocks at a time where a GEMM allows it (``info()["fill_k"]``).  ``split_clusters``
+    (0 library, 1 one cluster per tile, 2 a cluster per k-slice) places a split tile's k-slices.  Errors raise MlpChainError with
     the library's status.
     """
 
@@ -74,7 +75,7 @@ class Chain:
                  raster_group: int = 0, tile_m: int = 0, pipe_stages: int = 0, acc_split: int = 0,
                  weight_layout: str = "kn", k_split: Optional[Sequence[int]] = None, gated: bool = False,
                  force_reload: bool = False, cta_pair: int = 0, splitk_exchange: str = "global",
-                 tile_k: int = 0):
+                 tile_k: int = 0, split_clusters: int = 0):
         lib = _lib.load()
         d = ChainDesc()
         d.M = int(M)
@@ -107,6 +108,7 @@ class Chain:
         d.gated = int(bool(gated))
         d.cta_pair = int(cta_pair)
         d.splitk_exchange = {"global": 1, "dsmem": 2}[splitk_exchange]
+        d.split_clusters = int(split_clusters)
         self.M, self.dims, self.mode = int(M), tuple(int(v) for v in dims), mode
         self.n_weights = len(self.dims) - 1 + int(bool(gated))
         self._lib = lib
@@ -211,7 +213,7 @@ class Chain:
                 "num_sms": i.num_sms, "pipe_stages": i.pipe_stages, "smem_bytes": i.smem_bytes,
                 "tmem_cols": i.tmem_cols, "launches_per_run": i.launches_per_run,
                 "cluster_size": i.cluster_size, "k_split": list(i.k_split[:S]), "cta_pair": i.cta_pair,
-                "raster_group": i.raster_group, "fill_k": list(i.fill_k[:S]),
+                "raster_group": i.raster_group, "fill_k": list(i.fill_k[:S]), "split_across": list(i.split_across[:S]),
                 "queue_free": list(i.queue_free[:max(S - 1, 0)])}
 
 

@@ -72,6 +72,11 @@ struct StageParams {
     int32_t dsmem_reduce;   // split-K through the owners' shared memory (BN * 512 <= recv_bytes)
     int32_t gated;          // SwiGLU: B tiles of gate (mapB) and up (mapU) weights, accumulators
                             // side by side in TMEM, output SiLU(gate) * up; unsplit
+    int32_t xsplit;         // split-K slices on separate clusters (pipelined CTA pairs, a one-wave stage
+                            // after a one-group boundary): a cluster item is one slice of one tile,
+                            // siblings exchange partial sums through their own buffers and count on
+                            // xcount (per tile and pair half) instead of the cluster's barriers
+    uint32_t *xcount;       // xsplit: releases of the slices' partials, accumulating over runs
     int32_t kpf;            // 64-deep k blocks per ring fill: 0 or 1, or 2 (one CTA per tile, plain
                             // stage, even k blocks per slice): mapA is then a 3-D view (column, row,
                             // k block) and mapB a 3-D (K-major) or 4-D (column in box, k, box,
@@ -279,15 +284,25 @@ __device__ __forceinline__ void arrive_rank(uint64_t *bar, uint32_t rank, uint32
 // The tiles of one cluster item: pipelined ticket t, or the `item`-th static item of a
 // non-pipelined launch.  Returns the stage (-1: no work left) and fills tiles[0 .. ntiles).
 __device__ __forceinline__ int32_t item_tiles(const ChainParams &p, int32_t t, int32_t &ntiles,
-                                              int32_t (&tiles)[kMaxCluster])
+                                              int32_t (&tiles)[kMaxCluster], int32_t &slice)
 {
     ntiles = 0;
+    slice = -1;
     if (p.pipelined) {
         if (t >= p.stage_base[p.num_stages])
             return -1;
         const int32_t s = stage_of_ticket(p.stage_base, t);
         const StageParams &sp = p.st[s];
         const int32_t ntile_stage = sp.tiles_m * sp.tiles_n;
+        if (sp.xsplit) {   // one k-slice of one tile (or work-queue slot); its siblings are the neighbouring tickets
+            const int32_t slices = sp.split / p.pair;
+            const int32_t local = t - p.stage_base[s];
+            const int32_t first = local / slices;
+            slice = local % slices;
+            ntiles = 1;
+            tiles[0] = s == 0 ? raster_tile(first, sp.tiles_m, sp.tiles_n, p.raster_group) : first;
+            return s;
+        }
         const int32_t first = (t - p.stage_base[s]) * sp.tiles_per_item;
         ntiles = min(sp.tiles_per_item, ntile_stage - first);
         // Stage 0 tiles (and every stage's in the K-granular mode) follow the raster order; a
@@ -307,6 +322,21 @@ __device__ __forceinline__ int32_t item_tiles(const ChainParams &p, int32_t t, i
     for (int32_t j = 0; j < ntiles; ++j)
         tiles[j] = p.m_tile_begin * sp.tiles_n + first + j;
     return p.first_stage;
+}
+
+// The tile and split index of cluster rank r in an item (see StageParams::split, ::xsplit).
+__device__ __forceinline__ void item_member(const ChainParams &p, int32_t stage, int32_t ntiles,
+                                            const int32_t (&tiles)[kMaxCluster], int32_t slice, int32_t S, int32_t r,
+                                            int32_t &tile, int32_t &split)
+{
+    if (slice >= 0) {
+        tile = tiles[0];
+        split = slice * p.pair + r;
+        return;
+    }
+    const int32_t j = r / S;
+    tile = (stage >= 0 && j < ntiles) ? tiles[j] : -1;
+    split = r % S;
 }
 
 // Rank 0 of each cluster: obtain the cluster's next items and broadcast them.  Item 0 is
@@ -333,19 +363,20 @@ __device__ __forceinline__ void role_scheduler(const ChainParams &p, Ctrl *c)
         const int32_t t = p.pipelined ? nclusters + static_cast<int32_t>(run_relative(
                                                         atom_add_relaxed_gpu(p.ticket, 1u), c->epoch, p.tickets_per_run))
                                       : static_cast<int32_t>(cluster_id_x()) + it * nclusters;
-        int32_t ntiles = 0;
+        int32_t ntiles = 0, slice = -1;
         int32_t tiles[kMaxCluster];
-        const int32_t stage = item_tiles(p, t, ntiles, tiles);
-        // Broadcast: rank r gets tile r / S of the item (or none) and k-slice r % S.  All items
-        // are written first and released by one fence: a release arrive per rank would cost a
-        // round trip each and start the last rank's slice that much later than the first's.
+        const int32_t stage = item_tiles(p, t, ntiles, tiles, slice);
+        // Broadcast: rank r gets tile r / S of the item (or none) and k-slice r % S (a slice item
+        // of a cross-cluster split: the tile, and CTA r of the slice's pair).  All items are
+        // written first and released by one fence: a release arrive per rank would cost a round
+        // trip each and start the last rank's slice that much later than the first's.
         const int32_t S = stage >= 0 ? p.st[stage].split : 1;
         for (int32_t r = 0; r < cs; ++r) {
-            const int32_t j = r / S;
-            const int32_t tile = (stage >= 0 && j < ntiles) ? tiles[j] : -1;
+            int32_t tile, split;
+            item_member(p, stage, ntiles, tiles, slice, S, r, tile, split);
             st_cluster_s32(map_to_rank(&c->item_stage[slot], r), stage);
             st_cluster_s32(map_to_rank(&c->item_tile[slot], r), tile);
-            st_cluster_s32(map_to_rank(&c->item_split[slot], r), r % S);
+            st_cluster_s32(map_to_rank(&c->item_split[slot], r), split);
         }
         fence_acq_rel_cluster();
         for (int32_t r = 0; r < cs; ++r)
@@ -1592,6 +1623,98 @@ __device__ __forceinline__ void role_epilogue(const ChainParams &p, Ctrl *c, uin
         auto sibling = [&](int32_t q) {
             return g0 + static_cast<uint32_t>(kPairMode ? 2 * q + half : q);
         };
+        if (spr.xsplit) {
+            // The slices run on separate clusters.  Each keeps its partial in a buffer of its own
+            // (tile, slice, half), written once per run, so no sibling waits before overwriting
+            // one; the same halves of the tile's slices count their releases on one counter.
+            // Layout and order of the sum as below.
+            const size_t tile_buf = static_cast<size_t>(tile) * S * kPair;
+            auto buf = [&](int32_t q) { return partials + (tile_buf + static_cast<size_t>(q) * kPair + half) * partial_floats; };
+            const int32_t slice = BN / S;
+            const int32_t col0 = ks * slice;
+            float *mine = buf(ks);
+            for (int32_t c0 = 0; c0 < BN; c0 += 32) {
+                if (c0 >= col0 && c0 < col0 + slice)
+                    continue;
+                uint32_t r[32];
+                load_acc(split2, sub_stride, taddr + c0, r);
+                float4 *dst = reinterpret_cast<float4 *>(mine) + (c0 / 32) * 8 * bm + row;
+                if (row_ok)
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        dst[v * bm] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            }
+            fence_acq_rel_gpu();   // these stores, released at gpu scope by the add below
+            __syncwarp();
+            uint32_t *cnt = spr.xcount + static_cast<size_t>(tile) * kPair + half;
+            uint32_t ok = 1;
+            if (lane == 0) {
+                red_add_relaxed_gpu(cnt, 1u);
+                // every epilogue warp of every slice of this half: S x kEpiWarps releases per run
+                const uint32_t want = run_target(S * kEpiWarps, c->epoch);
+                const uint64_t t0 = globaltimer_ns();
+                while (!count_reached(ld_acquire_gpu_u32(cnt), want)) {
+                    if (c->abort_flag || globaltimer_ns() - t0 > p.timeout_ns) {
+                        if (!c->abort_flag)
+                            atomicCAS(p.status, 0u, kStatusTimeout);
+                        c->abort_flag = 1;
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0))
+                break;
+            for (int32_t c0 = col0; c0 < col0 + slice; c0 += 32) {
+                uint32_t own[32];
+                load_acc(split2, sub_stride, taddr + c0, own);
+                float acc_v[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    acc_v[e] = 0.0f;
+                const size_t off = static_cast<size_t>((c0 / 32) * 8 * bm + row);   // in float4
+                for (int32_t q = 0; q < S && row_ok; ++q) {
+                    if (q == ks) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            acc_v[e] += __uint_as_float(own[e]);
+                        continue;
+                    }
+                    const float4 *src = reinterpret_cast<const float4 *>(buf(q)) + off;
+                    float4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v[i] = __ldcg(src + i * bm);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        acc_v[4 * i] += v[i].x;
+                        acc_v[4 * i + 1] += v[i].y;
+                        acc_v[4 * i + 2] += v[i].z;
+                        acc_v[4 * i + 3] += v[i].w;
+                    }
+                }
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    r[e] = __float_as_uint(acc_v[e]);
+                store_chunk_warp(od, row0, row_lim, n0 + c0, r, stage, lane);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {   // the MMA warp may reuse this accumulator
+                if (kPairMode)
+                    mbar_arrive_cluster(tempty_lead0 + acc * 8u);
+                else
+                    mbar_arrive(&c->tempty[acc]);
+            }
+            ++local_tiles;
+            fence_acq_rel_gpu();   // the slice stores, released at gpu scope for the consumers
+            __syncwarp();
+            if (producer || (pipelined && logging))
+                publish(p, c, s, tile, logging && item.split == 0, producer, warp, lane, pl);
+            continue;
+        }
         if (dsmem && !kPairMode) {
             // Sibling q owns columns [q*BN/S, (q+1)*BN/S).  Every CTA sends each owner its part of
             // that slice straight from TMEM into the owner's receive buffer, laid out
@@ -1814,14 +1937,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
         if (lane == 0) {
             // the cluster's first item needs no ticket and no broadcast: write it into slot 0 here
-            int32_t ntiles = 0;
+            int32_t ntiles = 0, slice = -1;
             int32_t tiles[kMaxCluster];
-            const int32_t stage = item_tiles(p, static_cast<int32_t>(cluster_id_x()), ntiles, tiles);
-            const int32_t S = stage >= 0 ? p.st[stage].split : 1;
-            const int32_t j = static_cast<int32_t>(rank) / S;
+            const int32_t stage = item_tiles(p, static_cast<int32_t>(cluster_id_x()), ntiles, tiles, slice);
+            int32_t tile0, split0;
+            item_member(p, stage, ntiles, tiles, slice, stage >= 0 ? p.st[stage].split : 1, static_cast<int32_t>(rank),
+                        tile0, split0);
             c->item_stage[0] = stage;
-            c->item_tile[0] = (stage >= 0 && j < ntiles) ? tiles[j] : -1;
-            c->item_split[0] = static_cast<int32_t>(rank) % S;
+            c->item_tile[0] = tile0;
+            c->item_split[0] = split0;
             c->abort_flag = 0;
             c->skip = status0 != 0;   // sticky error: do nothing
             c->epoch = 0;

@@ -180,6 +180,8 @@ struct mlp_chain {
     uint32_t recv_bytes = 0;
     int split[MLP_MAX_GEMMS] = {}, kb_per_split[MLP_MAX_GEMMS] = {}, items[MLP_MAX_GEMMS] = {};
     int kpf[MLP_MAX_GEMMS] = {};   // 64-deep k blocks per ring fill (1 or 2)
+    bool xsplit[MLP_MAX_GEMMS] = {};   // k-slices on separate clusters (StageParams::xsplit)
+    uint32_t *xcount[MLP_MAX_GEMMS] = {};
     int32_t tile_base[MLP_MAX_GEMMS + 1] = {};
     float *partials[MLP_MAX_GEMMS] = {};
     uint32_t stage_bytes = 0, tmem_cols = 0;
@@ -239,7 +241,7 @@ extern "C" const char *mlp_status_str(mlp_status s)
 // microseconds.
 static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const int clusters[4], int fixed_bn,
                            int fixed_split, int *bn_out, int *split_out, int pair = 1, int ring_slots = 0,
-                           double kb_floor = 0.0)
+                           double kb_floor = 0.0, bool split_one_wave = false)
 {
     const int k_blocks = static_cast<int>((K + 63) / 64);
     double best = 1e30;
@@ -269,6 +271,8 @@ static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const 
             const double tiles = static_cast<double>(tiles_m) * ((N + bn - 1) / bn);
             const double cap = static_cast<double>(clusters[ci]) * S * pair;   // CTAs resident at once
             const double units = tiles * S * pair;
+            if (split_one_wave && S > 1 && units > cap)   // slices on separate clusters: one wave only
+                continue;
             // a persistent grid quantises into whole waves only while units are few
             const double waves = units <= 2 * cap ? std::ceil(units / cap) : units / cap;
             const int b_cols = (bn / pair + 63) / 64 * 64;   // weight columns one CTA loads per k block
@@ -278,7 +282,11 @@ static double choose_tiles(int64_t tiles_m, int bm, int64_t K, int64_t N, const 
             const double t_mma = kbps * 4 * std::max(48.0, bn / 2.0) / 2000.0;   // us
             const double t_tma = kbps * rows * 1.2e-3;                           // us
             const double t_lat = kbps * std::max(kb_floor, ring_slots ? 1.8 / ring_slots : 0.0);
-            const double t_unit = std::max(std::max(t_mma, t_tma), t_lat) + 1.0 + (S > 1 ? 4.0 : 0.0);
+            // a split tile's exchange: ~4 us in a cluster; slices on separate clusters exchange through
+            // a gpu-scope fence, counter and acquire, measured ~3 us more per split stage (M = 256,
+            // two 4096^2 GEMMs split four ways: 45.6 against 43.5 us for one CTA per tile)
+            const double t_split = S > 1 ? (split_one_wave ? 7.0 : 4.0) : 0.0;
+            const double t_unit = std::max(std::max(t_mma, t_tma), t_lat) + 1.0 + t_split;
             const double t_hbm = static_cast<double>(K) * N * 2 / 6.5e6;
             const double t = std::max(waves * t_unit, t_hbm);
             if (t < best * 0.999) {
@@ -312,6 +320,10 @@ static mlp_status full_reset(mlp_chain *h)
             cudaMemset(db.ready, 0, db.producers * sizeof(uint32_t)) != cudaSuccess)
             return MLP_ERR_CUDA;
     }
+    for (int s = 0; s < h->S; ++s)
+        if (h->xcount[s] &&
+            cudaMemset(h->xcount[s], 0, static_cast<size_t>(h->tiles_m) * h->tiles_n[s] * h->pair * 4) != cudaSuccess)
+            return MLP_ERR_CUDA;
     return cudaDeviceSynchronize() == cudaSuccess ? MLP_OK : MLP_ERR_CUDA;
 }
 
@@ -386,8 +398,12 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         return MLP_ERR_UNSUPPORTED;   // the gated GEMM keeps gate and up side by side in TMEM, unsplit
     if (d->grid_ctas < 0 || d->raster_group < 0 || d->pipe_stages < 0 || d->pipe_stages == 1 ||
         d->pipe_stages > mlpc::kMaxPipe || d->acc_split < 0 || d->acc_split > 2 || d->weight_layout < 0 ||
-        d->weight_layout > 1 || d->splitk_exchange < 0 || d->splitk_exchange > 2)
+        d->weight_layout > 1 || d->splitk_exchange < 0 || d->splitk_exchange > 2 || d->split_clusters < 0 ||
+        d->split_clusters > 2)
         return MLP_ERR_INVALID_ARG;
+    // k-slices on separate clusters: the queue protocol on CTA pairs over one 256-row panel
+    if (d->split_clusters == 2 && (d->mode != MLP_MODE_PIPELINED || d->cta_pair == 1 || !pair_ok || d->M > 2 * bm))
+        return MLP_ERR_UNSUPPORTED;
 
     mlp_chain *h = new (std::nothrow) mlp_chain();
     if (!h)
@@ -465,8 +481,20 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     // per pair tile, and only 15 of those fit: 120 CTAs) nor decode (a 256-row pair tile over
     // 128 rows).
     int bn1[mlpc::kMaxStages] = {}, sp1[mlpc::kMaxStages] = {}, bn2[mlpc::kMaxStages] = {}, sp2[mlpc::kMaxStages] = {};
+    int bn2x[mlpc::kMaxStages] = {}, sp2x[mlpc::kMaxStages] = {};
     double t1 = 0.0, t2 = pair_ok ? 0.0 : 1e30;
     const int64_t tiles_m1 = h->tiles_m, tiles_m2 = (d->M + 2 * bm - 1) / (2 * bm);
+    // A third plan for pairs: k-slices on separate clusters of two (each a cluster item of its
+    // own), which lifts the cluster-size limit on split pair tiles.  Only where a cluster can hold
+    // no more than one item of such a stage (see StageParams::xsplit): the queue protocol, one
+    // 256-row panel (every boundary one scoreboard group), a one-wave split stage.
+    const bool xs_ok = pair_ok && d->mode == MLP_MODE_PIPELINED && tiles_m2 == 1 && d->split_clusters != 1;
+    if (d->split_clusters == 2 && (!xs_ok || d->cta_pair == 1)) {
+        release(h);
+        return MLP_ERR_UNSUPPORTED;
+    }
+    int clusters2x[4] = {0, 0, 0, 0};   // pair x S CTAs per tile, all resident as clusters of two
+    double t2x = xs_ok ? 0.0 : 1e30;
     for (int s = 0; s < S; ++s) {
         const int tn = d->tile_n[s], ks = d->k_split[s];
         // tile widths: multiples of 32 up to 256 (a gated GEMM: 32, 64 or 128, its gate and up tiles
@@ -484,6 +512,34 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         t1 += choose_tiles(tiles_m1, bm, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn1[s], &sp1[s]);
         if (t2 < 1e29)
             t2 += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2, tn, ks, &bn2[s], &sp2[s], 2, 0, 0.33);
+        if (t2x < 1e29) {
+            for (int li = 1; li < 4; ++li)
+                clusters2x[li] = clusters2[1] >> (li - 1);
+            t2x += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2x, tn, ks, &bn2x[s], &sp2x[s], 2, 0,
+                                0.33, true);
+        }
+    }
+    // slices on separate clusters where asked for, or where that plan is better than the other
+    // pair plan (it can only differ where a stage splits)
+    bool use_x = false;
+    if (t2x < 1e29) {
+        bool splits = false;
+        for (int s = 0; s < S; ++s)
+            splits = splits || sp2x[s] > 1;
+        use_x = d->split_clusters == 2 ? true : (splits && t2x < 0.999 * t2);
+    }
+    if (d->split_clusters == 2 && t2x >= 1e29) {
+        release(h);
+        return MLP_ERR_UNSUPPORTED;
+    }
+    if (use_x) {
+        for (int s = 0; s < S; ++s) {
+            bn2[s] = bn2x[s];
+            sp2[s] = sp2x[s];
+        }
+        t2 = t2x;
+        for (int li = 1; li < 4; ++li)
+            clusters2[li] = clusters2x[li];
     }
     bool pair_auto = false;
     if (d->cta_pair == 0 && pair_auto_ok && t1 < 1e29 && t2 < 1e29) {
@@ -500,11 +556,11 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
             int b, k;
             e1 += choose_tiles(tiles_m1, bm, d->dims[s], d->dims[s + 1], clusters, bn1[s], sp1[s], &b, &k, 1, slots1);
             e2 += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2, bn2[s], sp2[s], &b, &k, 2, slots2,
-                               0.33);
+                               0.33, use_x);
         }
         pair_auto = e2 < 0.97 * e1;
     }
-    const int pair = (d->cta_pair == 2 || pair_auto) ? 2 : 1;
+    const int pair = (d->cta_pair == 2 || pair_auto || (use_x && d->split_clusters == 2)) ? 2 : 1;
     if ((pair == 2 ? t2 : t1) >= 1e29) {
         release(h);
         return MLP_ERR_UNSUPPORTED;   // no valid tile / split for this request
@@ -521,14 +577,19 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         h->max_bn = std::max(h->max_bn, bn);
         h->split[s] = split;
         h->kb_per_split[s] = (h->k_blocks[s] + split - 1) / split;
-        h->cs = std::max(h->cs, pair * split);
+        h->xsplit[s] = pair == 2 && use_x && split > 1;
+        h->cs = std::max(h->cs, pair * (h->xsplit[s] ? 1 : split));
     }
     if (pair == 2)
         for (int li = 1; li < 4; ++li)
             clusters[li] = clusters2[li];
     for (int s = 0; s < S; ++s) {
-        const int tpi = h->cs / (pair * h->split[s]);
         const int tiles = h->tiles_m * h->tiles_n[s];
+        if (h->xsplit[s]) {   // a cluster item is one slice of one tile
+            h->items[s] = tiles * h->split[s];
+            continue;
+        }
+        const int tpi = h->cs / (pair * h->split[s]);
         h->items[s] = (tiles + tpi - 1) / tpi;
     }
     const uint32_t a_bytes = static_cast<uint32_t>(bm * mlpc::kBK * 2);
@@ -612,6 +673,11 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         release(h);  // the pipelined grid must be co-resident
         return MLP_ERR_INVALID_ARG;
     }
+    for (int s = 0; s < S; ++s)
+        if (h->xsplit[s] && h->items[s] > h->grid / h->cs) {
+            release(h);  // slices on separate clusters need a cluster for every item of their stage
+            return MLP_ERR_UNSUPPORTED;
+        }
     h->raster_group = d->raster_group ? d->raster_group : default_raster_group(h->tiles_m, h->items[0], h->grid / h->cs);
 
     // dependency arrays (host), then one device block for all library-owned state
@@ -647,19 +713,27 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         bytes = align_up(bytes, 256) + 4;                          // tail
         bytes = align_up(bytes, 256) + (h->off[b].size() - 1) * 4; // ready (K-granular mode)
     }
+    for (int s = 0; s < S; ++s)   // slices on separate clusters: release counters per tile and half
+        if (h->xsplit[s])
+            bytes = align_up(bytes, 256) + static_cast<size_t>(h->tiles_m) * h->tiles_n[s] * pair * 4;
     if (d->debug_flags & MLP_DEBUG_EVENT_LOG) {
         h->n_events = static_cast<size_t>(total) + static_cast<size_t>(h->grid);   // tiles, then CTAs
         bytes = align_up(bytes, 256) + h->n_events * sizeof(mlpc::EventRec);
     }
-    // split-K partial sums: per stage that splits, one 128 x max_bn fp32 buffer per CTA slot
+    // split-K partial sums: per stage that splits, one 128 x max_bn fp32 buffer per CTA slot, or
+    // with slices on separate clusters one per slice of every tile (written once per run)
     const int cta_slots = std::max(h->grid, h->max_clusters * h->cs);
-    const size_t partial_bytes = static_cast<size_t>(cta_slots) * bm * h->max_bn * sizeof(float);
+    auto partial_bytes = [&](int s) {
+        const size_t bufs = h->xsplit[s] ? static_cast<size_t>(h->tiles_m) * h->tiles_n[s] * h->split[s] * pair
+                                         : static_cast<size_t>(cta_slots);
+        return bufs * bm * h->max_bn * sizeof(float);
+    };
     auto global_partials = [&](int s) {
         return h->split[s] > 1 && !(h->recv_bytes && static_cast<uint32_t>(h->BN[s] * bm * 4) <= h->recv_bytes);
     };
     for (int s = 0; s < S; ++s)
         if (global_partials(s))
-            bytes = align_up(bytes, 256) + partial_bytes;
+            bytes = align_up(bytes, 256) + partial_bytes(s);
     if (cudaMalloc(&h->dev_block, bytes) != cudaSuccess) {
         h->dev_block = nullptr;
         release(h);
@@ -708,6 +782,12 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
             v *= releases_per_tile(h, b);
         up(db.grp_init, releases);
     }
+    for (int s = 0; s < S; ++s)
+        if (h->xsplit[s]) {
+            o = align_up(o, 256);
+            h->xcount[s] = reinterpret_cast<uint32_t *>(p + o);
+            o += static_cast<size_t>(h->tiles_m) * h->tiles_n[s] * pair * 4;
+        }
     h->meta_bytes = o;
     if (h->n_events) {
         o = align_up(o, 256);
@@ -719,7 +799,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         if (global_partials(s)) {
             o = align_up(o, 256);
             h->partials[s] = reinterpret_cast<float *>(p + o);
-            o += partial_bytes;
+            o += partial_bytes(s);
         }
     if (!ok || full_reset(h) != MLP_OK) {
         release(h);
@@ -829,8 +909,10 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         // the CTAs of one tile: its k-slices, each a pair with CTA pairs (rank 2 q + h: slice q, half h)
         sp.split = h->pair * h->split[s];
         sp.kb_per_split = h->kb_per_split[s];
-        sp.tiles_per_item = h->cs / (h->pair * h->split[s]);
+        sp.tiles_per_item = h->xsplit[s] ? 1 : h->cs / (h->pair * h->split[s]);
         sp.items = h->items[s];
+        sp.xsplit = h->xsplit[s] ? 1 : 0;
+        sp.xcount = h->xcount[s];
         sp.partials = h->partials[s];
         sp.dsmem_reduce = h->split[s] > 1 && h->recv_bytes && static_cast<uint32_t>(h->BN[s] * h->bm * 4) <= h->recv_bytes;
         sp.out = static_cast<__nv_bfloat16 *>(out_ptr);
@@ -1137,6 +1219,8 @@ extern "C" mlp_status mlp_chain_get_info(mlp_chain_t h, mlp_chain_info *info)
     info->tile_k = mlpc::kBK;
     for (int b = 0; b + 1 < h->S; ++b)
         info->queue_free[b] = queue_free(h, b) ? 1 : 0;
+    for (int s = 0; s < h->S; ++s)
+        info->split_across[s] = h->xsplit[s] ? 1 : 0;
     for (int s = 0; s < h->S; ++s) {
         info->fill_k[s] = mlpc::kBK * h->kpf[s];
         info->tile_k = std::max(info->tile_k, info->fill_k[s]);

@@ -169,6 +169,14 @@ def _desc(**kw):
     ({"tile_k": 128, "mode": 3}, mc.ERR_UNSUPPORTED),
     ({"tile_k": 128, "mode": 4}, mc.ERR_UNSUPPORTED),
     ({"tile_k": 128, "acc_split": 2}, mc.ERR_UNSUPPORTED),
+    # k-slices on separate clusters: the queue protocol on CTA pairs over one 256-row panel
+    ({"split_clusters": 3}, mc.ERR_INVALID_ARG),
+    ({"split_clusters": -1}, mc.ERR_INVALID_ARG),
+    ({"split_clusters": 2, "mode": 1}, mc.ERR_UNSUPPORTED),
+    ({"split_clusters": 2, "mode": 3}, mc.ERR_UNSUPPORTED),
+    ({"split_clusters": 2, "cta_pair": 1}, mc.ERR_UNSUPPORTED),
+    ({"split_clusters": 2, "gated": 1}, mc.ERR_UNSUPPORTED),
+    ({"split_clusters": 2, "M": 257}, mc.ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_descriptors_before_touching_cuda(lib, kw, expect):
     h = ctypes.c_void_p()
