@@ -678,7 +678,8 @@ def main():
                        "residual": w.residual, "gated": w.gated, "mode": args.mode, "tile_m": info["tile_m"], "tile_n": info["tile_n"],
                        "k_split": info["k_split"], "cluster_size": info["cluster_size"], "cta_pair": info["cta_pair"], "splitk_exchange": args.splitk_exchange,
                        "raster_group": info["raster_group"],
-                       "tile_k": info["tile_k"], "fill_k": info["fill_k"], "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
+                       "tile_k": info["tile_k"], "fill_k": info["fill_k"], "split_across": info["split_across"],
+                       "queue_free": info["queue_free"], "grid_ctas": info["grid_ctas"], "pipe_stages": info["pipe_stages"],
                        "graph": "one CUDA graph replay per step",
                        "l2": f"flushed between steps (write of {2 * l2 >> 20} MiB, outside the timed events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

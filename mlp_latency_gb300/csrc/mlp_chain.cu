@@ -477,9 +477,9 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     // Two plans, each stage's tile width and split from the cost model: one CTA per tile, and CTA
     // pairs.  Pairs run where asked for, or by default where the model, with the ring depth each
     // plan leaves, puts them at least 3 % ahead: prefill and the GeLU chain (a third less fill per
-    // k block), not the Llama MLP (its down-projection would need clusters of 8 for four k-slices
-    // per pair tile, and only 15 of those fit: 120 CTAs) nor decode (a 256-row pair tile over
-    // 128 rows).
+    // k block) and the Llama MLP with its down-projection's four k-slices on separate clusters
+    // (in one cluster they would need clusters of 8, and only 15 of those fit: 120 CTAs), not
+    // decode (a 256-row pair tile over 128 rows).
     int bn1[mlpc::kMaxStages] = {}, sp1[mlpc::kMaxStages] = {}, bn2[mlpc::kMaxStages] = {}, sp2[mlpc::kMaxStages] = {};
     int bn2x[mlpc::kMaxStages] = {}, sp2x[mlpc::kMaxStages] = {};
     double t1 = 0.0, t2 = pair_ok ? 0.0 : 1e30;
