@@ -635,16 +635,19 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         const int32_t k_blocks = spr.k_blocks, kbps = spr.kb_per_split;
         const CUtensorMap *mapA = &p.mapA[s];
         const CUtensorMap *mapB = &p.mapB[s];
-        // a pair's tile is 2 bm rows: this CTA's rows and its half of the tile's columns
-        const int32_t bn_cta = BN / kPair;
+        const bool gated = spr.gated != 0;
+        // a pair's tile is 2 bm rows: this CTA's rows and its half of the tile's columns (of a gated
+        // tile, whose MMA is twice as wide, the leader's half is the gate tile and the peer's the up
+        // tile, both at the tile's columns)
+        const bool gated_pair = kPairMode && gated;
+        const int32_t bn_cta = gated_pair ? BN : BN / kPair;
         const int32_t m0 = (tile / tiles_n) * (kPair * bm) + static_cast<int32_t>(half) * bm;
-        const int32_t n0 = (tile % tiles_n) * BN + static_cast<int32_t>(half) * bn_cta;
+        const int32_t n0 = (tile % tiles_n) * BN + (gated_pair ? 0 : static_cast<int32_t>(half) * bn_cta);
         const int32_t box_cols = b_swz / 2;
         const uint32_t box_bytes = kBK * b_swz;
         const int32_t nbox = (bn_cta + box_cols - 1) / box_cols;   // a ragged last box is loaded whole
-        const bool gated = spr.gated != 0;
         const uint32_t b_tile_bytes = b_kmajor ? static_cast<uint32_t>(kBK * bn_cta * 2) : static_cast<uint32_t>(nbox) * box_bytes;
-        const uint32_t bytes = a_bytes + (gated ? 2u : 1u) * b_tile_bytes;
+        const uint32_t bytes = a_bytes + (gated && !kPairMode ? 2u : 1u) * b_tile_bytes;
         int32_t kb0, kb1;
         slice_range(k_blocks, kbps, kslice_of<kPair>(item.split), kb0, kb1);   // a pair's halves run the same slice
         const int32_t lead_kb = kb1 - kb0 > kTicketLead ? kb1 - kTicketLead : kb0;
@@ -671,8 +674,10 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
         }
         bool ok = true;
         if constexpr (kPairMode) {
-            // Pair stages are plain (no K-granular waits, gating or Lamport): the B tile's half is
-            // one copy (N x K weights, or a 3-D view of K x N ones), or one per box (ragged N).
+            // Pair stages have no K-granular waits or Lamport: the B tile's half is one copy (N x K
+            // weights, or a 3-D view of K x N ones), or one per box (ragged N); of a gated stage,
+            // the gate tile (leader) or the up tile (peer).
+            const CUtensorMap *mapBh = gated_pair && half ? &p.mapU : mapB;
             const int32_t bx = b_kmajor ? 0 : (b_3d ? 0 : n0);
             const int32_t by = b_kmajor ? n0 : (b_3d ? n0 / box_cols : 0);
             const int32_t b_form = b_kmajor ? 0 : (b_3d ? 1 : 2);
@@ -693,12 +698,12 @@ __device__ __forceinline__ void role_tma(const ChainParams &p, Ctrl *c, uint8_t 
                 }
                 const int32_t k = kb * kBK;
                 if (b_form == 0)
-                    tma_load_2d_pair(a + a_bytes, mapB, fb, k, by, pol_w);
+                    tma_load_2d_pair(a + a_bytes, mapBh, fb, k, by, pol_w);
                 else if (b_form == 1)
-                    tma_load_3d_pair(a + a_bytes, mapB, fb, 0, k, by, pol_w);
+                    tma_load_3d_pair(a + a_bytes, mapBh, fb, 0, k, by, pol_w);
                 else   // a ragged N keeps the 2-D map: one copy per 64-column box of the half
                     for (int32_t j = 0; j < nbox; ++j)
-                        tma_load_2d_pair(a + a_bytes + j * box_bytes, mapB, fb, bx + j * box_cols, k, pol_w);
+                        tma_load_2d_pair(a + a_bytes + j * box_bytes, mapBh, fb, bx + j * box_cols, k, pol_w);
                 return true;
             };
             int32_t kb_first = kb0;

@@ -372,10 +372,10 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     const int bm = d->tile_m == 64 ? 64 : mlpc::kBM;
     if (d->cta_pair < 0 || d->cta_pair > 2)
         return MLP_ERR_INVALID_ARG;
-    // CTA pairs run plain stages: no gating, split accumulators, 64-row tiles, the K-granular and
-    // Lamport modes or the shared-memory split-K exchange; tiles 128 or 256 wide (64 or 128
-    // columns per CTA)
-    bool pair_ok = !d->gated && d->acc_split != 2 && d->tile_m != 64 && d->mode != MLP_MODE_PIPELINED_KWAIT &&
+    // CTA pairs run no split accumulators, 64-row tiles, K-granular or Lamport modes or
+    // shared-memory split-K exchange; tiles 128 or 256 wide (64 or 128 columns per CTA), a gated
+    // GEMM's 64 or 128 wide (one CTA loads the gate tile, the other the up tile)
+    bool pair_ok = d->acc_split != 2 && d->tile_m != 64 && d->mode != MLP_MODE_PIPELINED_KWAIT &&
                    d->mode != MLP_MODE_PIPELINED_LAMPORT && d->splitk_exchange != 2 && d->tile_k != 128;
     // Fills of two k blocks: one CTA per tile, one accumulator, and no per-k-block consumer work
     // (the K-granular waits and the Lamport scan are per 64-deep block)
@@ -383,7 +383,7 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     if (d->tile_k == 128 && (!deep_ok || d->cta_pair == 2))
         return MLP_ERR_UNSUPPORTED;
     for (int s = 0; s < S && pair_ok; ++s)
-        pair_ok = d->tile_n[s] == 0 || d->tile_n[s] >= 128;
+        pair_ok = d->tile_n[s] == 0 || d->tile_n[s] >= (d->gated && s == 0 ? 64 : 128);
     if (d->cta_pair == 2 && !pair_ok)
         return MLP_ERR_UNSUPPORTED;
     if (d->mode == MLP_MODE_MICROBATCH && (d->microbatch_rows < bm || d->microbatch_rows % bm ||
@@ -510,13 +510,21 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         const int tn_s = gate_s && tn == 0 ? 128 : tn;
         const int ks_s = gate_s ? 1 : ks;
         t1 += choose_tiles(tiles_m1, bm, d->dims[s], d->dims[s + 1], clusters, tn_s, ks_s, &bn1[s], &sp1[s]);
-        if (t2 < 1e29)
-            t2 += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2, tn, ks, &bn2[s], &sp2[s], 2, 0, 0.33);
+        // a gated GEMM on pairs is costed as a plain pair GEMM twice as wide over the gate and up
+        // columns side by side (the MMA's width), unsplit, and its tile is half that width
+        const int64_t n2 = gate_s ? 2 * d->dims[s + 1] : d->dims[s + 1];
+        const int tn2 = gate_s ? 2 * (tn ? tn : 128) : tn, ks2 = gate_s ? 1 : ks;
+        if (t2 < 1e29) {
+            t2 += choose_tiles(tiles_m2, bm, d->dims[s], n2, clusters2, tn2, ks2, &bn2[s], &sp2[s], 2, 0, 0.33);
+            if (gate_s)
+                bn2[s] /= 2;
+        }
         if (t2x < 1e29) {
             for (int li = 1; li < 4; ++li)
                 clusters2x[li] = clusters2[1] >> (li - 1);
-            t2x += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2x, tn, ks, &bn2x[s], &sp2x[s], 2, 0,
-                                0.33, true);
+            t2x += choose_tiles(tiles_m2, bm, d->dims[s], n2, clusters2x, tn2, ks2, &bn2x[s], &sp2x[s], 2, 0, 0.33, true);
+            if (gate_s)
+                bn2x[s] /= 2;
         }
     }
     // slices on separate clusters where asked for, or where that plan is better than the other
@@ -544,19 +552,21 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
     bool pair_auto = false;
     if (d->cta_pair == 0 && pair_auto_ok && t1 < 1e29 && t2 < 1e29) {
         const size_t ring_bytes = static_cast<size_t>(smem_optin) - 1024 - 4 * mlpc::kEpiStageBytes - sizeof(mlpc::Ctrl);
-        int mb1 = 0, mb2 = 0;
+        int mb1 = 0, mb2 = 0;   // widest B tile of a ring slot (a gated GEMM's: gate and up)
         for (int s = 0; s < S; ++s) {
-            mb1 = std::max(mb1, bn1[s]);
-            mb2 = std::max(mb2, bn2[s]);
+            const int g = d->gated && s == 0 ? 2 : 1;
+            mb1 = std::max(mb1, g * bn1[s]);
+            mb2 = std::max(mb2, g * bn2[s]);
         }
         const int slots1 = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, ring_bytes / (bm * 128 + 128 * mb1)));
         const int slots2 = static_cast<int>(std::min<size_t>(mlpc::kMaxPipe, ring_bytes / (bm * 128 + 64 * mb2)));
         double e1 = 0.0, e2 = 0.0;
         for (int s = 0; s < S; ++s) {
             int b, k;
+            const int g = d->gated && s == 0 ? 2 : 1;
             e1 += choose_tiles(tiles_m1, bm, d->dims[s], d->dims[s + 1], clusters, bn1[s], sp1[s], &b, &k, 1, slots1);
-            e2 += choose_tiles(tiles_m2, bm, d->dims[s], d->dims[s + 1], clusters2, bn2[s], sp2[s], &b, &k, 2, slots2,
-                               0.33, use_x);
+            e2 += choose_tiles(tiles_m2, bm, d->dims[s], g * d->dims[s + 1], clusters2, g * bn2[s], sp2[s], &b, &k, 2,
+                               slots2, 0.33, use_x);
         }
         pair_auto = e2 < 0.97 * e1;
     }
@@ -610,8 +620,8 @@ extern "C" mlp_status mlp_chain_create(const mlp_chain_desc *d, mlp_chain_t *out
         if (h->kpf[s] == 2)
             h->stage_bytes = std::max(h->stage_bytes, 2u * (a_bytes + static_cast<uint32_t>(mlpc::kBK * padded_cols(h->BN[s]) * 2)));
     }
-    if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles
-        h->stage_bytes = std::max(h->stage_bytes, a_bytes + static_cast<uint32_t>(2 * mlpc::kBK * h->BN[0] * 2));
+    if (d->gated)   // the gated stage's ring slot holds gate and up weight tiles (a pair's CTA: one of them)
+        h->stage_bytes = std::max(h->stage_bytes, a_bytes + static_cast<uint32_t>((pair == 2 ? 1 : 2) * mlpc::kBK * h->BN[0] * 2));
     h->n_w = S + (d->gated ? 1 : 0);
     // Split tiles reduce through global memory unless the shared-memory exchange is asked for.
     // (Distributed shared memory stores measured slower on the decode workload, 43.9 against
@@ -877,7 +887,7 @@ static mlp_status prepare_params(mlp_chain *h, const void *X, const void *const 
         int32_t b_3d = 0, u_3d = 0;
         auto encode_w = [&](CUtensorMap *m, const void *w, int32_t *is_3d) {
             *is_3d = 0;
-            const int bn_cta = h->BN[s] / h->pair;   // the columns one CTA loads
+            const int bn_cta = d.gated && s == 0 ? h->BN[s] : h->BN[s] / h->pair;   // the columns one CTA loads
             if (deep)
                 return d.weight_layout == 1 ? encode_rows_kblocks(m, w, d.dims[s + 1], d.dims[s], bn_cta)
                                             : encode_w_kn_kblocks(m, w, d.dims[s], d.dims[s + 1], h->b_swz[s], bn_cta);

@@ -150,11 +150,11 @@ def _desc(**kw):
     ({"gated": 1, "acc_split": 2}, mc.ERR_UNSUPPORTED),
     ({"gated": 1, "k_split": (2, 0)}, mc.ERR_UNSUPPORTED),
     ({"gated": 1, "tile_n": (256, 0)}, mc.ERR_UNSUPPORTED),
-    # CTA pairs run plain stages only: not gated, split, K-granular or Lamport, 128 or 256 wide
+    # CTA pairs: no split accumulators, K-granular or Lamport modes; 128 or 256 wide (gated: 64 or 128)
     ({"cta_pair": 3}, mc.ERR_INVALID_ARG),
     ({"splitk_exchange": 3}, mc.ERR_INVALID_ARG),
     ({"splitk_exchange": -1}, mc.ERR_INVALID_ARG),
-    ({"cta_pair": 2, "gated": 1}, mc.ERR_UNSUPPORTED),
+    ({"cta_pair": 2, "gated": 1, "tile_n": (32, 0)}, mc.ERR_UNSUPPORTED),   # a gated pair tile: 64 or 128 wide
     ({"cta_pair": 2, "splitk_exchange": 2}, mc.ERR_UNSUPPORTED),    # pairs add split-K parts via L2
     ({"cta_pair": 2, "mode": 3}, mc.ERR_UNSUPPORTED),
     ({"cta_pair": 2, "mode": 4}, mc.ERR_UNSUPPORTED),
@@ -175,7 +175,7 @@ def _desc(**kw):
     ({"split_clusters": 2, "mode": 1}, mc.ERR_UNSUPPORTED),
     ({"split_clusters": 2, "mode": 3}, mc.ERR_UNSUPPORTED),
     ({"split_clusters": 2, "cta_pair": 1}, mc.ERR_UNSUPPORTED),
-    ({"split_clusters": 2, "gated": 1}, mc.ERR_UNSUPPORTED),
+    ({"split_clusters": 2, "acc_split": 2}, mc.ERR_UNSUPPORTED),
     ({"split_clusters": 2, "M": 257}, mc.ERR_UNSUPPORTED),
 ])
 def test_create_rejects_bad_descriptors_before_touching_cuda(lib, kw, expect):

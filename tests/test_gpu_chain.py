@@ -426,7 +426,7 @@ def test_dsmem_exchange_rejects_tiles_wider_than_its_buffer(mc):
 def test_library_raster_group_choice(mc):
     """Below 8 row panels the library groups all panels when the first stage takes more than one
     wave of cluster items, and none otherwise; from 8 panels up, groups of 4, then 8."""
-    with mc.Chain(256, (4096, 14336, 4096), gated=True) as ch:   # SwiGLU MLP: 224 tiles, 36 clusters of 4
+    with mc.Chain(256, (4096, 14336, 4096), gated=True, cta_pair=1) as ch:   # SwiGLU MLP: 224 tiles, 36 clusters of 4
         assert ch.info()["raster_group"] == 2
     with mc.Chain(256, (4096, 14336, 4096)) as ch:               # Llama MLP: 112 tiles in one wave
         assert ch.info()["raster_group"] == 1

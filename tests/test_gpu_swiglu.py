@@ -107,3 +107,39 @@ def test_gated_llama_full_size_sampled_rows(mc, oracle_mod):
     assert_close_to_oracle(Y[torch.as_tensor(rows)], Yo)
     Yk, _ = run_gated(mc, X, Ws, w.dims, mode="pipelined_kwait")
     assert same(Y, Yk)
+
+
+@pytest.mark.parametrize("M,dims,tn,ks", [
+    (256, (1024, 1536, 1024), [128, 256], [1, 4]),     # the down-projection's slices on separate clusters
+    (200, (512, 640, 512), [64, 128], [1, 2]),         # 64-wide gated pair tiles, ragged rows
+    (512, (1024, 1024, 512), [128, 128], [1, 1]),      # two pair panels
+])
+def test_gated_pairs_match_oracle_and_one_cta_tiles(mc, oracle_mod, M, dims, tn, ks):
+    """On a CTA pair the leader loads the gate tile and the peer the up tile; the pair's MMA is as
+    wide as both and each CTA's accumulator holds its rows of gate and up side by side.  Same bits
+    as one CTA per tile."""
+    X, Ws = si.draw(si.make_workload("t", M, dims, gated=True), seed=45)
+    Yp, Hp = run_gated(mc, X, Ws, dims, tile_n=tn, k_split=ks, cta_pair=2)
+    Yo, Ho = oracle_mod.chain(bits(X), [bits(w) for w in Ws], gated=True, return_h=True)
+    assert_close_to_oracle(Hp, Ho)
+    assert_close_to_oracle(Yp, Yo)
+    Y1, H1 = run_gated(mc, X, Ws, dims, tile_n=tn, k_split=ks, cta_pair=1)
+    assert same(Yp, Y1) and same(Hp, H1)
+    Ys, _ = run_gated(mc, X, Ws, dims, mode="sequential", tile_n=tn, k_split=ks, cta_pair=2)
+    assert same(Yp, Ys)
+
+
+def test_gated_llama_library_choice_sampled(mc, oracle_mod):
+    """The SwiGLU Llama MLP with the library's plan (CTA pairs, the down-projection's slices on
+    separate clusters where the model puts them ahead), on sampled rows, and the same bits as the
+    sequential launches of the same tiles."""
+    w = si.WORKLOADS["llama_swiglu_m256_4096_14336"]
+    X, Ws = si.draw(w, seed=0)
+    with mc.Chain(w.M, w.dims, gated=True) as ch:
+        info = ch.info()
+    Y, _ = run_gated(mc, X, Ws, w.dims)
+    rows = si.sample_rows(w.M, 12, seed=5)
+    assert_close_to_oracle(Y[rows], oracle_mod.chain(bits(X), [bits(t) for t in Ws], gated=True, rows=rows))
+    Ys, _ = run_gated(mc, X, Ws, w.dims, mode="sequential", tile_n=info["tile_n"], k_split=info["k_split"],
+                      cta_pair=info["cta_pair"])
+    assert same(Y, Ys)
