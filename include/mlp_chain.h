@@ -179,11 +179,13 @@ typedef struct {
                                            chunks); 1: one CTA per tile; 2: CTA pairs (tcgen05
                                            cta_group::2), each pair computing a 256-row tile, each
                                            CTA loading its 128 rows of the activations and half of
-                                           the weight tile's columns (tiles 128 or 256 wide), so a
-                                           k block's fill per SM shrinks by a third and the ring
-                                           gets deeper.  With k_split S a tile takes S pairs in
-                                           one cluster of 2 S <= 8 CTAs.  No gating, split
-                                           accumulators, 64-row tiles, K-granular or Lamport
+                                           the weight tile's columns (tiles 128 or 256 wide; of a
+                                           gated GEMM's tile, 64 or 128 wide, the leader loads the
+                                           gate tile and the peer the up tile), so a k block's fill
+                                           per SM shrinks by a third and the ring gets deeper.
+                                           With k_split S a tile takes S pairs in one cluster of
+                                           2 S <= 8 CTAs, or S clusters of 2 (split_clusters).  No
+                                           split accumulators, 64-row tiles, K-granular or Lamport
                                            modes, or shared-memory split-K exchange (else
                                            UNSUPPORTED); micro-batch chunks are multiples of 256
                                            rows                                                  */
