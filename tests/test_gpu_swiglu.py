@@ -127,6 +127,9 @@ def test_gated_pairs_match_oracle_and_one_cta_tiles(mc, oracle_mod, M, dims, tn,
     assert same(Yp, Y1) and same(Hp, H1)
     Ys, _ = run_gated(mc, X, Ws, dims, mode="sequential", tile_n=tn, k_split=ks, cta_pair=2)
     assert same(Yp, Ys)
+    if M % 256 == 0 and M > 256:   # pair micro-batch chunks hold whole 256-row tiles
+        Ym, _ = run_gated(mc, X, Ws, dims, mode="microbatch", microbatch_rows=256, tile_n=tn, k_split=ks, cta_pair=2)
+        assert same(Yp, Ym)
 
 
 def test_gated_llama_library_choice_sampled(mc, oracle_mod):
