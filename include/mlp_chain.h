@@ -374,6 +374,24 @@ mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t 
                               int32_t raster_group, int32_t releases_per_tile, int32_t threads,
                               uint64_t seed, int32_t drop_tile, uint32_t timeout_ms, int32_t *order_out);
 
+/* As mlp_protocol_model, with k-slices on separate items (the kernel's split-K slices on separate
+ * clusters of a CTA pair each, ChainDesc.split_clusters = 2).  slices (NULL: all 1) gives per stage
+ * the number of slices S of each tile; S must divide releases_per_tile, and a stage with S > 1
+ * must fit one wave: tiles_m * tiles_n[s] * S <= threads (siblings wait on one another).  Slice j
+ * of a tile is the ticket after slice j-1 (first stage: the tile of raster position ticket / S;
+ * later stages: work-queue slot ticket / S), makes releases_per_tile / S of the tile's releases
+ * and, before them, exchanges partials with its siblings: each of its releases writes its own
+ * partial and adds 1 to the tile's exchange counter, then the slice acquires that counter until it
+ * reaches the run's target of releases_per_tile adds and reads its siblings' partials.  The
+ * exchange counters accumulate over the three runs like the scoreboard's.  order_out (optional)
+ * receives one entry per item, so a tile of a sliced stage appears S times.  drop_exchange >= 0
+ * (a first-stage tile; the first stage must be sliced) makes that tile's last slice withhold its
+ * exchange adds: the run must end in MLP_ERR_TIMEOUT.  Invalid sizes give MLP_ERR_INVALID_ARG. */
+mlp_status mlp_protocol_model_slices(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
+                                     const int32_t *slices, int32_t raster_group, int32_t releases_per_tile,
+                                     int32_t threads, uint64_t seed, int32_t drop_tile, int32_t drop_exchange,
+                                     uint32_t timeout_ms, int32_t *order_out);
+
 /* Allocation-free run of the two-GEMM chain (the paper has no counterpart to this entry point).
  *
  * For callers that cannot allocate device memory when they run the chain: code running inside

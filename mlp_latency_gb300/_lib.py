@@ -104,6 +104,7 @@ SIGNATURES = {
     "mlp_chain_destroy": (ctypes.c_int, [vp]),
     "mlp_deps_build": (i64, [i64, i64, i64, i32, i32, i32, i32, vp, vp, i64, vp]),
     "mlp_protocol_model": (ctypes.c_int, [i32, i32, vp, i32, i32, i32, u64, i32, u32, vp]),
+    "mlp_protocol_model_slices": (ctypes.c_int, [i32, i32, vp, vp, i32, i32, i32, u64, i32, i32, u32, vp]),
     "mlp_chain_run_noalloc": (ctypes.c_int, [i64, i64, i64, i64, vp, vp, vp, vp, i32, vp]),
     "mlp_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }

@@ -264,14 +264,26 @@ def scoreboard_build(M: int, n_out: int, n_next: int, bm: int, bn_p: int, bn_c: 
 
 def protocol_model(tiles_m: int, tiles_n: Sequence[int], threads: int = 8, seed: int = 0,
                    drop_tile: int = -1, timeout_ms: int = 2000, return_order: bool = False,
-                   raster_group: int = 1, releases_per_tile: int = 4):
-    """Run the host-thread protocol model (mlp_protocol_model); returns (status, order)."""
+                   raster_group: int = 1, releases_per_tile: int = 4, slices: Optional[Sequence[int]] = None,
+                   drop_exchange: int = -1):
+    """Run the host-thread protocol model (mlp_protocol_model, or mlp_protocol_model_slices when
+    `slices` gives per-stage k-slice counts); returns (status, order), one order entry per item."""
     lib = _lib.load()
     tn = np.ascontiguousarray(tiles_n, dtype=np.int32)
-    total = int(tiles_m * tn.sum())
-    order = np.full(total, -1, dtype=np.int32) if return_order else None
-    st = lib.mlp_protocol_model(len(tn), tiles_m, tn.ctypes.data, raster_group, releases_per_tile, threads, seed,
-                                drop_tile, timeout_ms, order.ctypes.data if order is not None else None)
+    if slices is None and drop_exchange < 0:
+        order = np.full(int(tiles_m * tn.sum()), -1, dtype=np.int32) if return_order else None
+        order_ptr = order.ctypes.data if order is not None else None
+        st = lib.mlp_protocol_model(len(tn), tiles_m, tn.ctypes.data, raster_group, releases_per_tile, threads, seed,
+                                    drop_tile, timeout_ms, order_ptr)
+        return int(st), order
+    sl = np.ascontiguousarray(slices if slices is not None else [1] * len(tn), dtype=np.int32)
+    if sl.shape != tn.shape:
+        raise ValueError("slices needs one entry per stage")
+    order = np.full(int(tiles_m * (tn * sl).sum()), -1, dtype=np.int32) if return_order else None
+    order_ptr = order.ctypes.data if order is not None else None
+    st = lib.mlp_protocol_model_slices(len(tn), tiles_m, tn.ctypes.data, sl.ctypes.data, raster_group,
+                                       releases_per_tile, threads, seed, drop_tile, drop_exchange, timeout_ms,
+                                       order_ptr)
     return int(st), order
 
 

@@ -205,9 +205,16 @@ extern "C" mlp_status mlp_scoreboard_build(int64_t M, int64_t n_out, int64_t n_n
 //     then acquires the named tile's group counter until it reaches the run's target, and only
 //     then reads the producers' output (plain, non-atomic reads: a missing happens-before edge is
 //     a data race that ThreadSanitizer reports, and a stale value fails the run);
+//   - a stage may split each tile into k-slices that run as items of their own (the device's
+//     slices on separate clusters): slice j of a tile is the ticket after slice j-1, makes R / S
+//     of the tile's releases, and first exchanges partial sums with its siblings: each of its
+//     releases writes its own partial rows and adds 1 to the tile's exchange counter (acq_rel),
+//     then the slice acquires that counter until it holds this run's S x R/S adds and reads the
+//     siblings' rows (plain reads again).  Siblings wait on one another, so such a stage must fit
+//     one wave (items <= threads), as on the device;
 //   - nothing is reset between three back-to-back runs (epochs 0, 1, 2): scoreboard counters,
-//     the ticket, the queue tails and the launch counter accumulate, and each run reads its own
-//     share of them relative to its epoch (protocol.h).
+//     the exchange counters, the ticket, the queue tails and the launch counter accumulate, and
+//     each run reads its own share of them relative to its epoch (protocol.h).
 // ------------------------------------------------------------------------------------------
 namespace {
 
@@ -225,23 +232,45 @@ struct ModelBoundary {
 
 }  // namespace
 
-extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
-                                         int32_t raster_group, int32_t releases_per_tile, int32_t threads,
-                                         uint64_t seed, int32_t drop_tile, uint32_t timeout_ms, int32_t *order_out)
+extern "C" mlp_status mlp_protocol_model_slices(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
+                                                const int32_t *slices, int32_t raster_group,
+                                                int32_t releases_per_tile, int32_t threads, uint64_t seed,
+                                                int32_t drop_tile, int32_t drop_exchange, uint32_t timeout_ms,
+                                                int32_t *order_out)
 {
     if (num_gemms < 1 || num_gemms > MLP_MAX_GEMMS || tiles_m < 1 || !tiles_n || threads < 1 || threads > 512 ||
         raster_group < 0 || releases_per_tile < 1 || releases_per_tile > 64)
         return MLP_ERR_INVALID_ARG;
-    for (int s = 0; s < num_gemms; ++s)
-        if (tiles_n[s] < 1)
-            return MLP_ERR_INVALID_ARG;
     const int S = num_gemms;
     const int32_t R = releases_per_tile;
-    int32_t base[MLP_MAX_GEMMS + 1];
-    base[0] = 0;
-    for (int s = 0; s < S; ++s)
+    int32_t X[MLP_MAX_GEMMS];   // k-slices per tile, each an item of its own
+    for (int s = 0; s < S; ++s) {
+        X[s] = slices ? slices[s] : 1;
+        if (tiles_n[s] < 1 || X[s] < 1 || R % X[s] != 0)
+            return MLP_ERR_INVALID_ARG;
+        // siblings wait on one another, so a sliced stage must fit one wave of threads
+        if (X[s] > 1 && static_cast<int64_t>(tiles_m) * tiles_n[s] * X[s] > threads)
+            return MLP_ERR_INVALID_ARG;
+    }
+    if (drop_exchange >= 0 && (X[0] == 1 || drop_exchange >= tiles_m * tiles_n[0]))
+        return MLP_ERR_INVALID_ARG;
+    int32_t base[MLP_MAX_GEMMS + 1], ibase[MLP_MAX_GEMMS + 1];   // per stage: first tile, first item (ticket)
+    base[0] = ibase[0] = 0;
+    for (int s = 0; s < S; ++s) {
         base[s + 1] = base[s] + tiles_m * tiles_n[s];
-    const int32_t total = base[S];
+        ibase[s + 1] = ibase[s] + tiles_m * tiles_n[s] * X[s];
+    }
+    const int32_t total = base[S], items = ibase[S];
+    // the slices' exchange: one partial per (tile, slice, release) and one counter per tile
+    std::vector<std::vector<uint32_t>> part(static_cast<size_t>(S));
+    std::vector<std::vector<std::atomic<uint32_t>>> xcount(static_cast<size_t>(S));
+    for (int s = 0; s < S; ++s)
+        if (X[s] > 1) {
+            part[s].assign(static_cast<size_t>(tiles_m) * tiles_n[s] * R, 0u);
+            xcount[s] = std::vector<std::atomic<uint32_t>>(static_cast<size_t>(tiles_m) * tiles_n[s]);
+            for (auto &c : xcount[s])
+                c.store(0);
+        }
 
     std::vector<ModelBoundary> bd(S > 1 ? S - 1 : 0);
     for (int b = 0; b + 1 < S; ++b) {
@@ -273,6 +302,7 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
 
     std::atomic<uint32_t> ticket{0}, seq{0}, status{0};
     std::atomic<uint64_t> launches{0};
+    // per tile: the first start and the last end over its slices, and how many slices ran
     std::vector<std::atomic<uint32_t>> start_seq(total), end_seq(total), runs(total);
     std::atomic<int32_t> order_pos{0};
     const auto timeout = std::chrono::milliseconds(timeout_ms ? timeout_ms : 2000);
@@ -283,7 +313,7 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
 
     for (uint32_t epoch = 0; epoch < 3; ++epoch) {
         for (int32_t i = 0; i < total; ++i) {
-            start_seq[i].store(0);
+            start_seq[i].store(UINT32_MAX);
             end_seq[i].store(0);
             runs[i].store(0);
         }
@@ -296,27 +326,28 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                 fail(MLP_ERR_DEVICE_STATE);
                 return;
             }
-            for (int32_t t = tid; t < total;
+            for (int32_t t = tid; t < items;
                  t = threads + static_cast<int32_t>(mlpc::run_relative(ticket.fetch_add(1, std::memory_order_relaxed),
-                                                                       run, static_cast<uint32_t>(total)))) {
-                const int32_t s = mlpc::stage_of_ticket(base, t);
-                const int32_t local = t - base[s];
+                                                                       run, static_cast<uint32_t>(items)))) {
+                const int32_t s = mlpc::stage_of_ticket(ibase, t);
+                // a sliced stage's item is one k-slice of one tile; its siblings are the neighbouring tickets
+                const int32_t local = (t - ibase[s]) / X[s], slice = (t - ibase[s]) % X[s];
+                const auto t0 = std::chrono::steady_clock::now();
+                auto expired = [&]() {
+                    if (status.load(std::memory_order_relaxed) != 0)
+                        return true;
+                    if (std::chrono::steady_clock::now() - t0 > timeout) {
+                        fail(MLP_ERR_TIMEOUT);
+                        return true;
+                    }
+                    std::this_thread::yield();
+                    return false;
+                };
                 int32_t tile;
                 if (s == 0) {
                     tile = mlpc::raster_tile(local, tiles_m, tiles_n[0], raster_group);
                 } else {
                     ModelBoundary &B = bd[s - 1];
-                    const auto t0 = std::chrono::steady_clock::now();
-                    auto expired = [&]() {
-                        if (status.load(std::memory_order_relaxed) != 0)
-                            return true;
-                        if (std::chrono::steady_clock::now() - t0 > timeout) {
-                            fail(MLP_ERR_TIMEOUT);
-                            return true;
-                        }
-                        std::this_thread::yield();
-                        return false;
-                    };
                     // relaxed polls of the queue slot: the entry only names the tile (a queue-free
                     // boundary has none: slot q is the q-th member of the groups in group order)
                     uint64_t v;
@@ -345,17 +376,45 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                             }
                 }
                 const int32_t id = base[s] + tile;
-                start_seq[id].store(seq.fetch_add(1) + 1);
+                uint32_t st = seq.fetch_add(1) + 1, cur = start_seq[id].load();
+                while (st < cur && !start_seq[id].compare_exchange_weak(cur, st)) {
+                }
                 std::this_thread::sleep_for(std::chrono::microseconds(delay(rng)));
+                const int32_t Rs = R / X[s];   // releases this item makes (its epilogue warps)
+                if (X[s] > 1) {
+                    // the slices' exchange: each release writes its own partial rows, then adds 1 to the
+                    // tile's counter (on the device: fence.acq_rel.gpu + a relaxed add); every slice waits
+                    // for all S x Rs adds of this run and reads its siblings' rows of the same release
+                    std::vector<uint32_t> &P = part[s];
+                    for (int32_t w = 0; w < Rs; ++w) {
+                        P[(static_cast<size_t>(tile) * X[s] + slice) * Rs + w] = epoch + 1u;
+                        if (s == 0 && tile == drop_exchange && slice == X[s] - 1)
+                            continue;   // fault injection: the partial lands, its add never comes
+                        xcount[s][static_cast<size_t>(tile)].fetch_add(1, std::memory_order_acq_rel);
+                    }
+                    const uint32_t want = mlpc::run_target(static_cast<uint32_t>(R), epoch);
+                    while (!mlpc::count_reached(xcount[s][static_cast<size_t>(tile)].load(std::memory_order_acquire), want))
+                        if (expired())
+                            return;
+                    for (int32_t w = 0; w < Rs; ++w)
+                        for (int32_t q = 0; q < X[s]; ++q)
+                            if (q != slice && P[(static_cast<size_t>(tile) * X[s] + q) * Rs + w] != epoch + 1u) {
+                                fail(MLP_ERR_DEVICE_STATE);
+                                return;
+                            }
+                }
                 runs[id].fetch_add(1);
-                end_seq[id].store(seq.fetch_add(1) + 1);
+                const uint32_t en = seq.fetch_add(1) + 1;
+                cur = end_seq[id].load();
+                while (en > cur && !end_seq[id].compare_exchange_weak(cur, en)) {
+                }
                 if (order_out && epoch == 0)
                     order_out[order_pos.fetch_add(1)] = (s << 24) | tile;
                 if (s + 1 >= S)
                     continue;
                 ModelBoundary &B = bd[s];
                 const mlpc::DepGroups &G = B.grp;
-                for (int32_t r = 0; r < R; ++r) {   // the epilogue warps of the split-K slices
+                for (int32_t r = slice * Rs; r < (slice + 1) * Rs; ++r) {   // this item's epilogue warps
                     B.data[static_cast<size_t>(tile) * R + r] = epoch + 1u;   // this release's rows
                     if (s == 0 && tile == drop_tile)
                         continue;   // fault injection: the stores land, the releases never come
@@ -383,10 +442,11 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
             th.join();
         if (status.load() != 0)
             return static_cast<mlp_status>(status.load());
-        // every tile ran once, after all of its producers had finished
-        for (int32_t i = 0; i < total; ++i)
-            if (runs[i].load() != 1)
-                return MLP_ERR_DEVICE_STATE;
+        // every slice of every tile ran once, after all of its producers' slices had finished
+        for (int s = 0; s < S; ++s)
+            for (int32_t i = base[s]; i < base[s + 1]; ++i)
+                if (runs[i].load() != static_cast<uint32_t>(X[s]))
+                    return MLP_ERR_DEVICE_STATE;
         for (int b = 0; b + 1 < S; ++b) {
             for (int32_t p = 0; p + 1 < static_cast<int32_t>(bd[b].off.size()); ++p)
                 for (int32_t e = bd[b].off[p]; e < bd[b].off[p + 1]; ++e)
@@ -397,6 +457,18 @@ extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, con
                 if (bd[b].count[g].load() != mlpc::run_target(bd[b].target[g], epoch))
                     return MLP_ERR_DEVICE_STATE;
         }
+        for (int s = 0; s < S; ++s)
+            for (auto &c : xcount[s])
+                if (c.load() != mlpc::run_target(static_cast<uint32_t>(R), epoch))
+                    return MLP_ERR_DEVICE_STATE;
     }
     return MLP_OK;
+}
+
+extern "C" mlp_status mlp_protocol_model(int32_t num_gemms, int32_t tiles_m, const int32_t *tiles_n,
+                                         int32_t raster_group, int32_t releases_per_tile, int32_t threads,
+                                         uint64_t seed, int32_t drop_tile, uint32_t timeout_ms, int32_t *order_out)
+{
+    return mlp_protocol_model_slices(num_gemms, tiles_m, tiles_n, nullptr, raster_group, releases_per_tile, threads,
+                                     seed, drop_tile, -1, timeout_ms, order_out);
 }

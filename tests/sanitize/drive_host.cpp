@@ -34,6 +34,17 @@ int main()
         fails += mlp_protocol_model(2, 4, tn5, 1, 4, 8, seed, -1, 2000, order.data()) != MLP_OK;    // queue-free groups
     }
     fails += mlp_protocol_model(2, 2, tn2, 1, 4, 4, 5, 1, 200, nullptr) != MLP_ERR_TIMEOUT;   // withheld release
+    // k-slices on separate threads: each slice exchanges its partials with its siblings through a
+    // per-tile counter before its own releases
+    const int32_t sl_first[2] = {2, 1}, sl_cons[2] = {1, 4}, sl3[3] = {2, 4, 1}, tn8[2] = {8, 4}, tn3b[3] = {4, 2, 4};
+    for (uint64_t seed = 1; seed <= 3; ++seed) {
+        std::vector<int32_t> order(64 * 16);
+        fails += mlp_protocol_model_slices(2, 2, tn2, sl_first, 1, 8, 16, seed, -1, -1, 2000, order.data()) != MLP_OK;
+        fails += mlp_protocol_model_slices(2, 1, tn8, sl_cons, 1, 8, 16, seed, -1, -1, 2000, order.data()) != MLP_OK;
+        fails += mlp_protocol_model_slices(3, 2, tn3b, sl3, 2, 8, 16, seed, -1, -1, 2000, order.data()) != MLP_OK;
+    }
+    fails += mlp_protocol_model_slices(2, 2, tn2, sl_first, 1, 8, 16, 7, -1, 3, 200, nullptr) !=
+             MLP_ERR_TIMEOUT;   // withheld exchange add
     for (int32_t rg : {1, 3, 8}) {   // the grouped scoreboard tables, sizes first
         mlp_scoreboard sb{};
         fails += mlp_scoreboard_build(1000, 512, 384, 128, 128, 64, rg, 4, &sb) != MLP_OK;

@@ -120,6 +120,52 @@ def test_protocol_model_dropped_decrement_times_out_without_queue(lib):
     assert st == mc.ERR_TIMEOUT
 
 
+@pytest.mark.parametrize("tiles_m,tiles_n,slices,threads,seed,rg,rel", [
+    (2, [4, 4], [2, 1], 16, 11, 1, 8),         # a sliced first stage (static tickets)
+    (1, [8, 4], [1, 4], 16, 12, 1, 8),         # a sliced consumer stage after a one-group boundary
+    (2, [4, 2, 4], [2, 4, 1], 16, 13, 2, 8),   # both, with merged raster groups
+    (4, [3, 2], [1, 2], 16, 14, 1, 4),         # a sliced consumer stage at a queue-free boundary of 4 groups
+    (1, [4, 4], [4, 4], 16, 15, 1, 16),        # every stage sliced, 4 releases per slice
+    (2, [3, 3], [1, 1], 6, 16, 1, 4),          # no slices through the same entry point
+])
+def test_protocol_model_slices_on_separate_items(lib, tiles_m, tiles_n, slices, threads, seed, rg, rel):
+    """k-slices as items of their own (the device's slices on separate clusters): every slice of
+    every tile runs once per run, the exchange counters land on each run's target, and each tile
+    appears once per slice in the completion order."""
+    st, order = mc.protocol_model(tiles_m, tiles_n, threads=threads, seed=seed, return_order=True,
+                                  raster_group=rg, releases_per_tile=rel, slices=slices)
+    assert st == mc.OK
+    assert sorted(order.tolist()) == sorted((s << 24) | t for s in range(len(tiles_n))
+                                            for t in range(tiles_m * tiles_n[s]) for _ in range(slices[s]))
+
+
+def test_protocol_model_withheld_exchange_times_out(lib):
+    # first-stage tile 3's last slice writes its partials but never adds to the tile's exchange
+    # counter: its siblings (and it) wait until the deadline
+    st, _ = mc.protocol_model(2, [4, 4], threads=16, seed=17, slices=[2, 1], releases_per_tile=8,
+                              drop_exchange=3, timeout_ms=200)
+    assert st == mc.ERR_TIMEOUT
+
+
+def test_protocol_model_sliced_tile_withheld_releases_time_out(lib):
+    st, _ = mc.protocol_model(2, [4, 4], threads=16, seed=18, slices=[2, 1], releases_per_tile=8,
+                              drop_tile=3, timeout_ms=200)
+    assert st == mc.ERR_TIMEOUT
+
+
+@pytest.mark.parametrize("tiles_n,slices,threads,rel,drop_exchange", [
+    ([4, 4], [2, 1], 15, 8, -1),   # 16 sliced items on 15 threads: more than one wave
+    ([4, 4], [3, 1], 16, 8, -1),   # 3 slices do not divide 8 releases
+    ([4, 4], [1, 2], 16, 8, 0),    # a withheld exchange on an unsliced first stage
+    ([4, 4], [2, 1], 16, 8, 8),    # ... or on a tile that does not exist
+    ([4, 4], [0, 1], 16, 8, -1),
+])
+def test_protocol_model_slices_rejects_bad_arguments(lib, tiles_n, slices, threads, rel, drop_exchange):
+    st, _ = mc.protocol_model(2, tiles_n, threads=threads, slices=slices, releases_per_tile=rel,
+                              drop_exchange=drop_exchange)
+    assert st == mc.ERR_INVALID_ARG
+
+
 def _desc(**kw):
     d = _lib.ChainDesc()
     d.M, d.num_gemms = 128, 2
