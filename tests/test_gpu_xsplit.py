@@ -4,8 +4,9 @@ Every k-slice of a split pair tile is a cluster item of its own (a pair); the sl
 partial sums through buffers of their own in global memory, count their releases on one counter
 per tile and half, and add the parts in slice order, as the in-cluster exchange does.  Bar: within
 |d| <= 1e-2 (|ref| + 1) of the oracle; bit-exact on integer-valued inputs; bit-identical to the
-same tiles and slices in one cluster and to the sequential launches; every dependency respected in
-the event log; forty runs of one handle give the same bits.
+same tiles and slices in one cluster and to the sequential launches; the device scoreboard equal to
+the tables rebuilt from the oracle's enumeration; every dependency respected in the event log;
+forty runs of one handle give the same bits.
 """
 import numpy as np
 import pytest
@@ -49,6 +50,22 @@ def test_separate_cluster_slices_match_oracle_and_one_cluster(mc, oracle_mod, M,
     assert same(Y, Y1) and same(H, H1)
     Ys, _, _ = run_chain(mc, X, Ws, mode="sequential", **kw)
     assert same(Y, Ys)
+
+
+@pytest.mark.parametrize("M,dims,tn,ks", [
+    (256, (1024, 1536, 768), [128, 256], [2, 2]),   # the producer's slices on separate clusters
+    (256, (2048, 2048, 1024), [256, 256], [1, 4]),  # only the consumer's
+])
+def test_scoreboard_matches_oracle_enumeration(mc, oracle_mod, M, dims, tn, ks):
+    """Each slice's pair releases its rows once per epilogue warp, wherever the slices run:
+    2 x S x 4 releases per producer tile, against the groups rebuilt from the oracle's
+    enumeration of overlapping tiles."""
+    import expected_scoreboard as es
+    with mc.Chain(M, dims, tile_n=tn, k_split=ks, cta_pair=2, split_clusters=2) as ch:
+        info = ch.info()
+        assert info["split_across"] == [int(k > 1) for k in ks]
+        es.assert_equal(ch.scoreboard(0), es.expected(oracle_mod, M, dims[1], dims[2], 256, tn[0], tn[1],
+                                                      info["raster_group"], 2 * ks[0] * 4))
 
 
 def test_integer_inputs_are_bit_exact(mc, oracle_mod):
