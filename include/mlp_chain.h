@@ -81,7 +81,7 @@ extern "C" {
 typedef enum {
     MLP_OK = 0,
     MLP_ERR_INVALID_ARG = 1,  /* a size, pointer, alignment or option is not acceptable      */
-    MLP_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (dtype, tile)    */
+    MLP_ERR_UNSUPPORTED = 2,  /* valid request the library does not implement (dtype, tile) */
     MLP_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                             */
     MLP_ERR_OOM = 4,          /* device allocation failed                                      */
     MLP_ERR_TIMEOUT = 5,      /* a bounded device wait ran out (dependency never satisfied)    */
